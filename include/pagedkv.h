@@ -1,0 +1,349 @@
+/*
+ * pagedkv.h - C ABI of the GB300 paged / block-sparse grouped-query attention library.
+ *
+ * Operations (each names the page and passage that defines it):
+ *
+ *   pkv_paged_attention        "com.microsoft.PagedAttention manifest.json": operator
+ *                              inputs/outputs/attributes, the derive table and the
+ *                              ScatterKV -> AttendSplitK -> AttendSplitKMerge passes.
+ *   pkv_paged_scatter_kv       the ScatterKV pass of the same manifest on its own.
+ *   pkv_kv_append_rotary       "com.microsoft.SparseAttention sparse-kv-append.wgsl.jinja":
+ *                              sparse_schedule, sparse_rotary and the KV-append main.
+ *   pkv_sparse_attention_partials
+ *                              "alice-llm src/shaders/sparse_attention_forward.wgsl":
+ *                              sparse_forward and its layout comment block.
+ *   pkv_combine_partials       log-sum-exp merge of (o, m, l) partials: the manifest's
+ *                              AttendSplitKMerge pass and the merge of sparse partials.
+ *
+ * Conventions for every call:
+ *   - Tensor pointers are DEVICE pointers owned by the caller; the library never frees
+ *     or retains them. Scratch memory is a caller-provided device workspace whose size
+ *     the matching *_workspace_size call returns; the library allocates nothing.
+ *   - `stream` is a cudaStream_t (CUstream) handle passed as void*; NULL is the legacy
+ *     default stream. Calls enqueue work and return without synchronising.
+ *   - Host-side argument errors return a pkv_status before anything is enqueued.
+ *     Invalid DATA found on the device (a block id outside the pool, a slot past the
+ *     pool, ...) never traps: the offending row is skipped or masked as documented and
+ *     a PKV_DEV_* bit is OR-ed into the optional `device_status` int32 word.
+ *   - All layouts are row-major and dense; sizes are element counts.
+ *   - fp16 tensors and every row stride must be 16-byte aligned (head_size % 8 == 0).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_ABI_VERSION 1
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_NULL = 1,        /* a required pointer is NULL */
+  PKV_ERR_SHAPE = 2,       /* a size breaks the contract (cacheShapeOk, ioShapeOk,
+                              scheduleShapeOk or slotShapeOk of the manifest) */
+  PKV_ERR_HEADS = 3,       /* num_heads or kv_num_heads <= 0, or not divisible */
+  PKV_ERR_DTYPE = 4,       /* dtype other than the operation's type constraint */
+  PKV_ERR_KV_MODE = 5,     /* exactly one of key / value given (neither separateKv
+                              nor packedKv holds) */
+  PKV_ERR_CAUSAL = 6,      /* is_causal != 1 (the manifest admits only 1) */
+  PKV_ERR_WORKSPACE = 7,   /* workspace NULL, too small or not 256-byte aligned */
+  PKV_ERR_ALIGN = 8,       /* a tensor pointer is not 16-byte aligned */
+  PKV_ERR_UNSUPPORTED = 9, /* a size outside what this build compiles (see each call) */
+  PKV_ERR_LAUNCH = 10      /* a CUDA launch or API call failed */
+} pkv_status;
+
+/* Bits OR-ed into *device_status by kernels that meet invalid data. */
+#define PKV_DEV_BAD_BLOCK 1u     /* block-table entry outside [0, num_blocks), or a key
+                                    position past max_blocks * block_size: key masked,
+                                    row not written */
+#define PKV_DEV_BAD_SLOT 2u      /* slot_mapping entry >= num_blocks * block_size: the
+                                    token's K/V are not written (negative = padding,
+                                    skipped without a flag) */
+#define PKV_DEV_BAD_POSITION 4u  /* KV-append position >= max_cache_seq: row skipped */
+#define PKV_DEV_BAD_SEQUENCE 8u  /* cumulative_sequence_length / past_seqlens
+                                    inconsistent for a sequence: its tokens get zero
+                                    output and are not scattered */
+#define PKV_DEV_BAD_EDGE 16u     /* edge_meta field out of range: block_len clipped to
+                                    block_size, or a page slot / page id treated as
+                                    unmapped; an edge whose q_idx, head, batch or
+                                    block lies outside the tensors gets the empty
+                                    partial */
+
+typedef enum pkv_dtype { PKV_F16 = 1, PKV_BF16 = 2, PKV_F32 = 3, PKV_I32 = 4 } pkv_dtype;
+
+/* ---------------------------------------------------------------------------------
+ * Paged attention (PagedAttention manifest)
+ * ------------------------------------------------------------------------------- */
+
+/* Split policy for the attention pass. */
+#define PKV_SPLIT_AUTO 0   /* per-sequence split count chosen on the device: up to
+                              max_splits splits of >= split_min_keys keys, sized so the
+                              whole batch covers the GPU several times over */
+#define PKV_SPLIT_PAGES 1  /* every decoding sequence uses the manifest's numSplits */
+#define PKV_SPLIT_FIXED 2  /* every decoding sequence uses fixed_splits (tests) */
+
+typedef struct pkv_paged_attention_args {
+  /* query  fp16 [num_tokens, query_hidden]. query_hidden = num_heads*head_size when
+            key/value are given (separateKv); (num_heads + 2*kv_num_heads)*head_size for
+            packed [Q | K | V] rows when key == value == NULL (packedKv). */
+  const void* query;
+  /* key, value  fp16 [num_tokens, kv_num_heads*head_size] or both NULL. */
+  const void* key;
+  const void* value;
+  /* key_cache, value_cache  fp16 [num_blocks, block_size, kv_num_heads, head_size];
+            updated in place by the scatter pass (the manifest's optional outputs). */
+  void* key_cache;
+  void* value_cache;
+  /* cumulative_sequence_length int32 [batch + 1]: tokens of sequence b are rows
+            [cu[b], cu[b+1]) of query. past_seqlens int32 [batch]: tokens already in
+            the cache. block_table int32 [batch, max_blocks]: physical block of each
+            16.. block_size-token column; -1 (or any id outside the pool) = unmapped. */
+  const int32_t* cumulative_sequence_length;
+  const int32_t* past_seqlens;
+  const int32_t* block_table;
+  /* slot_mapping int32 [num_tokens] or NULL: flat pool row blk*block_size + offset of
+            each new token (negative = padding, not written). When NULL the scatter
+            destination comes from block_table at the token's absolute position. The
+            attention pass always reads keys through block_table. */
+  const int32_t* slot_mapping;
+  /* output fp16 [num_tokens, num_heads*head_size]. */
+  void* output;
+  /* optional int32 word that kernels OR PKV_DEV_* bits into (may be NULL). */
+  int32_t* device_status;
+  /* optional rotary of the new keys before they enter the cache (NULL = none):
+            fp16 [rotary_positions, rotary_dim/2] cos / sin tables, rotation rule of the
+            SparseAttention append page at the token's absolute position. */
+  const void* cos_cache;
+  const void* sin_cache;
+
+  int64_t num_tokens;
+  int64_t query_hidden;
+  int64_t batch;
+  int64_t num_heads;
+  int64_t kv_num_heads;
+  int64_t head_size;
+  int64_t block_size;
+  int64_t num_blocks;
+  int64_t max_blocks;
+  int64_t rotary_dim;        /* 0 = no rotary; else even and <= head_size */
+  int64_t rotary_positions;  /* rows of cos_cache / sin_cache */
+  int32_t rotary_interleaved;/* 0 = NeoX split pairs, 1 = interleaved pairs */
+  int32_t is_causal;         /* must be 1 */
+  int32_t dtype;             /* must be PKV_F16 (type constraint T = float16) */
+  float scale;               /* softmax scale; 0 means 1/sqrt(head_size) */
+  int32_t split_policy;      /* PKV_SPLIT_* */
+  int32_t fixed_splits;      /* for PKV_SPLIT_FIXED */
+  int32_t max_splits;        /* 0 = 16 (manifest MAX_SPLITS) */
+  int32_t split_min_keys;    /* 0 = 128 (manifest SPLIT_MIN_KEYS) */
+} pkv_paged_attention_args;
+
+typedef struct pkv_paged_plan {
+  int32_t mode;              /* 1 = separate K/V, 2 = packed QKV */
+  int32_t group_size;        /* num_heads / kv_num_heads */
+  int32_t pages_num_splits;  /* the manifest's derive.numSplits for these shapes */
+  int32_t max_splits;        /* per-sequence split bound used by this call */
+  int64_t pages_partial_bytes; /* the manifest's pagedSplitScratchBytes at its numSplits */
+  int64_t pages_stats_bytes;   /* the manifest's pagedSplitStatsBytes */
+  int64_t workspace_bytes;     /* bytes pkv_paged_attention needs */
+  int64_t decode_item_bound;   /* grid bound of the split-KV decode pass */
+  int64_t prefill_item_bound;  /* grid bound of the tiled prefill pass */
+  int64_t partial_slot_bound;  /* tokens that may need split partials */
+} pkv_paged_plan;
+
+/* Host only (no CUDA call): validates the arguments against the contract and fills
+ * *plan. Returns PKV_OK or the first failing status. Pointers are checked for NULL /
+ * alignment only if non-NULL values are required by the chosen mode. */
+int pkv_paged_attention_plan(const pkv_paged_attention_args* args, pkv_paged_plan* plan);
+
+/* Host only: workspace bytes pkv_paged_attention needs for these sizes. */
+int pkv_paged_attention_workspace_size(const pkv_paged_attention_args* args,
+                                       size_t* bytes);
+
+/* ScatterKV + AttendSplitK + AttendSplitKMerge of the manifest, GB300 form:
+ *   1. scatter: new K/V rows (rotated first when cos/sin are given) -> caches;
+ *   2. plan (device): per-sequence work items; multi-token sequences become query
+ *      tiles, short sequences become split-KV items;
+ *   3. attention: causal GQA, token at absolute position pos sees keys 0..pos, query
+ *      head hq uses kv head hq / (num_heads / kv_num_heads); tiles write the output
+ *      directly, split items write fp32 (o, m, l) partials to the workspace;
+ *   4. combine: LSE merge of the partials into output.
+ * workspace: device memory of at least pkv_paged_attention_workspace_size bytes,
+ * 256-byte aligned, owned by the caller, contents need not be initialised and are
+ * scratch after the call. Supported: head_size in {64, 128}; num_heads/kv_num_heads
+ * <= 16; any block_size >= 1. Otherwise PKV_ERR_UNSUPPORTED. */
+int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* The ScatterKV pass alone (same argument block; query is read only in packed mode,
+ * output and the attention fields are ignored). Bit-exact copy when rotary_dim == 0. */
+int pkv_paged_scatter_kv(const pkv_paged_attention_args* args, void* stream);
+
+/* Shape-level contract check of the manifest (host only). Each tensor is described
+ * by presence, rank, dtype (pkv_dtype) and up to 4 dims. On return *failed holds
+ * PKV_PRED_* bits of the predicates that are false and *mode is 1 (separate),
+ * 2 (packed) or 0 (neither). Returns PKV_OK when pagedContractOk holds, a mode
+ * exists and is_causal == 1; else the status of the first failure. */
+typedef struct pkv_tensor_desc {
+  int32_t present;
+  int32_t rank;
+  int32_t dtype;
+  int32_t reserved;
+  int64_t dims[4];
+} pkv_tensor_desc;
+
+typedef struct pkv_paged_shapes {
+  pkv_tensor_desc query, key, value, key_cache, value_cache;
+  pkv_tensor_desc cumulative_sequence_length, past_seqlens, block_table, slot_mapping;
+  pkv_tensor_desc output;
+  int64_t num_heads;
+  int64_t kv_num_heads;
+  int32_t is_causal;
+  int32_t reserved;
+} pkv_paged_shapes;
+
+#define PKV_PRED_CACHE_SHAPE 1u
+#define PKV_PRED_HEAD_LAYOUT 2u
+#define PKV_PRED_SCHEDULE_SHAPE 4u
+#define PKV_PRED_IO_SHAPE 8u
+#define PKV_PRED_SEPARATE_KV 16u
+#define PKV_PRED_PACKED_KV 32u
+#define PKV_PRED_SLOT_SHAPE 64u
+
+int pkv_paged_contract_check(const pkv_paged_shapes* shapes, uint32_t* failed,
+                             int32_t* mode);
+
+/* ---------------------------------------------------------------------------------
+ * KV append + RoPE into a [batch, kv_heads, max_cache_seq, head] cache
+ * (SparseAttention append page)
+ * ------------------------------------------------------------------------------- */
+typedef struct pkv_kv_append_args {
+  /* source fp16: packed [batch*seq_len, (num_heads + 2*kv_num_heads)*head_size] rows
+     [Q | K | V] when packed != 0, else key rows [batch*seq_len, kv_num_heads*head_size]. */
+  const void* source;
+  const void* value;                         /* separate mode: [batch*seq_len, kv*head] */
+  const int32_t* total_sequence_length;      /* device scalar: == seq_len -> prompt mode */
+  const int32_t* key_total_sequence_lengths; /* [batch]: history = total - seq_len */
+  const void* cos_cache;                     /* fp16 [rotary_positions, rotary_dim/2] */
+  const void* sin_cache;
+  void* present_key;                         /* fp16 [batch, kv, max_cache_seq, head] */
+  void* present_value;
+  int32_t* device_status;                    /* optional */
+  int64_t batch;
+  int64_t seq_len;
+  int64_t num_heads;
+  int64_t kv_num_heads;
+  int64_t head_size;
+  int64_t max_cache_seq;
+  int64_t rotary_dim;                        /* 0 = plain copy; else even, <= head_size */
+  int64_t rotary_positions;
+  int32_t packed;
+  int32_t interleaved;
+  int32_t dtype;                             /* PKV_F16 */
+  int32_t reserved;
+} pkv_kv_append_args;
+
+/* For each (batch b, kv head h, new token t): position = history(b) + t with the
+ * sparse_schedule rule (both totals read as u32); K rotated at that position when
+ * rotary_dim > 0 (leading member own*cos - partner*sin, trailing own*cos +
+ * partner*sin, fp32 math, fp16 round-to-nearest-even), V copied; written to row
+ * `position` of (b, h). Rows no new token lands on are untouched. position >=
+ * max_cache_seq (or >= rotary_positions when rotating) skips the row and sets
+ * PKV_DEV_BAD_POSITION. */
+int pkv_kv_append_rotary(const pkv_kv_append_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Block-sparse partials (sparse_attention_forward.wgsl)
+ * ------------------------------------------------------------------------------- */
+typedef struct pkv_sparse_args {
+  const float* q;              /* [num_queries, hq, head_dim] */
+  const float* k_pages;        /* [num_pages, hkv, page_size, head_dim] */
+  const float* v_pages;
+  const int32_t* edge_meta;    /* [num_edges, 5]: q_idx, h (kv head), blk, batch, block_len */
+  const int32_t* block_tables; /* [num_seqs, max_pages]: page id or -1 (unmapped) */
+  float* o_partial;            /* [num_edges*qhead, head_dim] */
+  float* m_partial;            /* [num_edges*qhead] */
+  float* l_partial;            /* [num_edges*qhead] */
+  int32_t* device_status;      /* optional */
+  int64_t num_queries;
+  int64_t num_edges;
+  int64_t num_seqs;
+  int64_t max_pages;
+  int64_t num_pages;
+  int64_t qhead;               /* query heads per kv head; hq = hkv * qhead */
+  int64_t hq;
+  int64_t hkv;
+  int64_t head_dim;
+  int64_t block_size;          /* keys per block (<= page_size * pages_per_block) */
+  int64_t page_size;
+  int64_t pages_per_block;
+  float softmax_scale;
+  int32_t reserved;
+} pkv_sparse_args;
+
+/* Host only: workspace bytes for the edge grouping of pkv_sparse_attention_partials. */
+int pkv_sparse_attention_partials_workspace_size(const pkv_sparse_args* args,
+                                                 size_t* bytes);
+
+/* One partial per (edge e, lane qh), index e*qhead + qh: query row q[q_idx, h*qhead+qh];
+ * key t < block_len of block blk lives in page slot blk*pages_per_block + t/page_size
+ * of the sequence's table row, row t % page_size; unmapped page -> score -1e30.
+ * s = softmax_scale * <q, k>; m = max s (>= -1e30); weights exp(s - m) for s > -5e29
+ * else 0; l = sum of weights; o = weighted sum of value rows (unnormalised).
+ * block_len <= 0 -> (o = 0, m = -1e30, l = 0). No causal mask. fp32 throughout.
+ * The GPU form groups edges by (batch, kv head, block) so each K/V block is read
+ * once for all edges that name it. Supported: head_dim in {64, 128}, block_size
+ * <= 128, qhead <= 64. */
+int pkv_sparse_attention_partials(const pkv_sparse_args* args, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Combine of (o, m, l) partials
+ * ------------------------------------------------------------------------------- */
+typedef struct pkv_combine_args {
+  const float* o;              /* [num_partials, head_dim] unnormalised */
+  const float* m;              /* [num_partials] running max (natural-log units) */
+  const float* l;              /* [num_partials] sum of exp(s - m) */
+  const int32_t* segment_offsets; /* [num_segments + 1] CSR over partial groups, or NULL */
+  void* out;                   /* [num_segments*lanes, head_dim], dtype out_dtype */
+  float* lse;                  /* optional [num_segments*lanes]: M + ln L, -inf if empty */
+  int64_t num_segments;
+  int64_t lanes;               /* partials per group (e.g. query heads per kv head) */
+  int64_t head_dim;
+  int64_t uniform_count;       /* groups per segment when segment_offsets == NULL */
+  int32_t out_dtype;           /* PKV_F16 or PKV_F32 */
+  int32_t reserved;
+} pkv_combine_args;
+
+/* Output row s*lanes + c merges partial rows e*lanes + c for groups e in
+ * [off[s], off[s+1]) (or [s*uniform_count, (s+1)*uniform_count)): over partials with
+ * l > 0, M = max m, w = exp(m - M), L = sum w*l, out = sum w*o / L, lse = M + ln L.
+ * A partial with l == 0 is empty and its o row is not read. No non-empty partial:
+ * out = 0, lse = -inf. Supported: head_dim in {64, 128}. */
+int pkv_combine_partials(const pkv_combine_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------------
+ * Runtime utilities
+ * ------------------------------------------------------------------------------- */
+int pkv_abi_version(void);
+const char* pkv_status_string(int status);
+/* sizeof of each argument struct, so a binding can check its layout. */
+size_t pkv_sizeof_struct(const char* name);
+/* Kernels this library has launched since load (all entry points, all streams). */
+int64_t pkv_launch_count(void);
+/* Per-kernel timing: when enabled, every launch is bracketed by CUDA events on its own
+ * stream; pkv_profiler_query synchronises those events and returns the summed device
+ * time (ms) and launch count of `kernel` ("scatter", "append", "plan", "decode",
+ * "prefill", "combine", "sparse_group", "sparse_partials"). Not thread-safe. */
+void pkv_profiler_enable(int on);
+void pkv_profiler_reset(void);
+int pkv_profiler_query(const char* kernel, double* total_ms, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -282,18 +282,28 @@ def paged_contract(*, query_shape, key_shape, value_shape, key_cache_shape,
     return r
 
 
-def sequence_map(cu_seqlens, past_seqlens):
+def sequence_map(cu_seqlens, past_seqlens, num_tokens: Optional[int] = None):
     """Token i in [cu[b], cu[b+1]) belongs to sequence b as new token t = i - cu[b]
-    at absolute position past[b] + t. Returns a list of (b, t, pos) per token.
-    Sequences with a negative new-token count or negative past contribute nothing."""
+    at absolute position past[b] + t. Returns (entries, status): entries[i] is
+    (b, t, pos) or None for a token no valid sequence covers.
+
+    Reading for data the manifest does not check: sequence b is valid when
+    0 <= cu[b] <= cu[b+1] <= num_tokens and past[b] >= 0; an invalid sequence
+    contributes no tokens and sets ST_BAD_SEQUENCE. Uncovered tokens (e.g. padding
+    after cu[batch]) are not an error."""
     cu = [int(x) for x in cu_seqlens]
     past = [int(x) for x in past_seqlens]
-    out = [None] * (cu[-1] if cu else 0)
+    T = cu[-1] if num_tokens is None else int(num_tokens)
+    out = [None] * T
+    status = 0
     for b in range(len(past)):
         lo, hi = cu[b], cu[b + 1]
+        if not (0 <= lo <= hi <= T and past[b] >= 0):
+            status |= ST_BAD_SEQUENCE
+            continue
         for i in range(lo, hi):
             out[i] = (b, i - lo, past[b] + i - lo)
-    return out
+    return out, status
 
 
 def split_new_kv(case_query, case_key, case_value, num_heads, kv_num_heads, head_size):
@@ -321,14 +331,16 @@ def paged_scatter(k_new, v_new, key_cache, value_cache, cu_seqlens, past_seqlens
     (blk = block_table[b, pos // block_size], offset = pos % block_size). When
     rotary_dim > 0 the key row is first rotated at its absolute position with the
     append page's rotation rule and rounded once to fp16. Returns (key_cache,
-    value_cache, status) as new fp16 arrays.
+    value_cache, status) as new fp16 arrays. Readings for unchecked data: a slot past
+    the pool, a table column past max_blocks or a block id outside the pool skips the
+    token (status bit); with rotation, a position past the cos/sin table skips it.
     """
     kc = np.array(key_cache, copy=True)
     vc = np.array(value_cache, copy=True)
     NB, BS = kc.shape[0], kc.shape[1]
     MB = block_table.shape[1]
-    status = 0
-    for i, entry in enumerate(sequence_map(cu_seqlens, past_seqlens)):
+    smap, status = sequence_map(cu_seqlens, past_seqlens, k_new.shape[0])
+    for i, entry in enumerate(smap):
         if entry is None:
             continue
         b, t, pos = entry
@@ -350,6 +362,9 @@ def paged_scatter(k_new, v_new, key_cache, value_cache, cu_seqlens, past_seqlens
                 status |= ST_BAD_BLOCK
                 continue
         k_row = k_new[i]
+        if rotary_dim > 0 and pos >= cos_cache.shape[0]:
+            status |= ST_BAD_POSITION      # no cos/sin row for this position
+            continue
         if rotary_dim > 0:
             k_row = rotate_rows(k_new[i], [pos] * k_new.shape[1], cos_cache, sin_cache,
                                 rotary_dim, rotary_interleaved).astype(np.float16)
@@ -436,7 +451,7 @@ def paged_attention(query, key, value, key_cache, value_cache, cu_seqlens,
                                    sin_cache, rotary_dim, rotary_interleaved)
     T = q_all.shape[0]
     out = np.zeros((T, Hq, D), dtype=np.float64)
-    smap = sequence_map(cu_seqlens, past_seqlens)
+    smap, _ = sequence_map(cu_seqlens, past_seqlens, T)
     wanted = range(T) if tokens is None else tokens
     by_seq = {}
     for i in wanted:
@@ -491,7 +506,9 @@ def sparse_partial(q_buf, k_pages, v_pages, meta, block_tables, qh: int, *, qhea
 
     Readings for data the page leaves unchecked: block_len above block_size is
     clipped to block_size, and a page slot past the table row or a page id past
-    the pool counts as unmapped; each sets a status bit.
+    the pool counts as unmapped; each sets a status bit. An edge with block_len > 0
+    whose q_idx, head, batch or block lies outside the tensors gets the empty
+    partial and a status bit.
     """
     q_idx, h, blk, batch, block_len = (int(x) for x in meta)
     status = 0
@@ -501,6 +518,10 @@ def sparse_partial(q_buf, k_pages, v_pages, meta, block_tables, qh: int, *, qhea
         status |= ST_BAD_EDGE
     if block_len <= 0:
         return np.zeros(D), NEG_LARGE, 0.0, status
+    if not (0 <= q_idx < q_buf.shape[0] and 0 <= h * qhead + qh < q_buf.shape[1]
+            and 0 <= batch < block_tables.shape[0] and blk >= 0
+            and blk * pages_per_block < block_tables.shape[1]):
+        return np.zeros(D), NEG_LARGE, 0.0, status | ST_BAD_EDGE
     q = _f64(q_buf[q_idx, h * qhead + qh])
     num_pages = k_pages.shape[0]
     max_pages = block_tables.shape[1]

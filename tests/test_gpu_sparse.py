@@ -1,0 +1,143 @@
+"""GPU parity of pkv_sparse_attention_partials and pkv_combine_partials."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import pagedkv_oracle as orc
+from paged_kv_cache_231_gb300 import binding as B
+from paged_kv_cache_231_gb300 import workloads as wl
+
+from .gpu_util import DEV, assert_f16_close, assert_f32_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(c):
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, m, l = B.pkv_sparse_attention_partials(
+        dev(c.q), dev(c.k_pages), dev(c.v_pages), dev(c.edge_meta), dev(c.block_tables),
+        qhead=c.qhead, block_size=c.block_size, page_size=c.page_size,
+        pages_per_block=c.pages_per_block, softmax_scale=c.softmax_scale,
+        device_status=status)
+    nseg = c.seg_offsets.shape[0] - 1
+    lse = torch.empty(nseg * c.qhead, dtype=torch.float32, device=DEV)
+    out, _ = B.pkv_combine_partials(o, m, l, dev(c.seg_offsets), num_segments=nseg,
+                                    lanes=c.qhead, lse=lse)
+    torch.cuda.synchronize()
+    return host(o), host(m), host(l), host(out), host(lse), int(status.item())
+
+
+def oracle_partials(c, edges=None):
+    return orc.sparse_attention_partials(
+        c.q, c.k_pages, c.v_pages, c.edge_meta, c.block_tables, qhead=c.qhead, hq=c.hq,
+        head_dim=c.head_dim, block_size=c.block_size, page_size=c.page_size,
+        pages_per_block=c.pages_per_block, softmax_scale=c.softmax_scale, edges=edges)
+
+
+def compare_partials(go, gm, gl, ro, rm, rl, rows):
+    np.testing.assert_array_equal(gl[rows] == 0, rl[rows] == 0)
+    empty = rl[rows] == 0
+    assert (gm[rows][empty] == -1e30).all() and (go[rows][empty] == 0).all()
+    live = rows[~empty]
+    assert_f32_close(go[live], ro[live], "o partial")
+    assert_f32_close(gm[live], rm[live], "m partial")
+    assert_f32_close(gl[live], rl[live], "l partial")
+
+
+@pytest.mark.parametrize("head_dim,pages_per_block,qhead", [(128, 4, 4), (64, 2, 2),
+                                                            (128, 8, 1)])
+def test_small_full_parity(head_dim, pages_per_block, qhead):
+    c = wl.block_sparse(51, n_seqs=3, kv_len=1024, queries_per_seq=24, hq=4 * qhead,
+                        hkv=4, head_dim=head_dim, pages_per_block=pages_per_block,
+                        blocks_per_query=5, n_empty_edges=6, unmapped_frac=0.05)
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    ro, rm, rl, rst = oracle_partials(c)
+    assert gst == rst
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]))
+    rout, rlse = orc.combine_partials(ro, rm, rl, c.seg_offsets, c.qhead)
+    assert_f32_close(gout, rout, "combined output")
+    fin = np.isfinite(rlse)
+    np.testing.assert_array_equal(np.isfinite(glse), fin)
+    assert_f32_close(glse[fin], rlse[fin], "lse")
+
+
+def test_bad_edges_and_pages_are_flagged():
+    c = wl.block_sparse(52, n_seqs=2, kv_len=512, queries_per_seq=8, hq=8, hkv=2,
+                        head_dim=128, blocks_per_query=3, unmapped_frac=0.0)
+    c.edge_meta[0, 4] = 1000          # block_len past the block: clipped, flagged
+    c.edge_meta[1, 0] = 9999          # q_idx out of range: empty partial, flagged
+    c.block_tables[0, 3] = c.num_pages + 2   # page id past the pool: unmapped, flagged
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    ro, rm, rl, rst = oracle_partials(c)
+    assert gst == rst == orc.ST_BAD_EDGE
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]))
+
+
+def test_block_sparse_full_size_sampled():
+    """The full block-sparse workload (524 288 edges, 2 097 152 partials) in the same
+    launch configuration as the benchmark; the oracle checks 1500 sampled edges plus
+    every edge of 40 sampled (query, head) segments, whose combined rows are checked
+    too."""
+    c = wl.block_sparse(5, n_empty_edges=16)
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    rng = np.random.default_rng(7)
+    segs = rng.choice(c.seg_offsets.shape[0] - 1, size=40, replace=False)
+    edges = set(rng.choice(c.num_edges, size=1500, replace=False).tolist())
+    for s in segs:
+        edges |= set(range(int(c.seg_offsets[s]), int(c.seg_offsets[s + 1])))
+    edges |= set(np.nonzero(c.edge_meta[:, 4] <= 0)[0].tolist())
+    edges = sorted(edges)
+    ro, rm, rl, rst = oracle_partials(c, edges)
+    rows = (np.asarray(edges)[:, None] * c.qhead + np.arange(c.qhead)[None, :]).reshape(-1)
+    compare_partials(go, gm, gl, ro, rm, rl, rows)
+    for s in segs:
+        e0, e1 = int(c.seg_offsets[s]), int(c.seg_offsets[s + 1])
+        for qh in range(c.qhead):
+            pr = [e * c.qhead + qh for e in range(e0, e1)]
+            ref, rlse = orc.combine_rows(ro[pr], rm[pr], rl[pr])
+            assert_f32_close(gout[s * c.qhead + qh], ref, "combined row")
+
+
+def _random_partials(rng, n, D, empty_frac=0.2):
+    o = rng.standard_normal((n, D)).astype(np.float32) * 3
+    m = (rng.standard_normal(n) * 4).astype(np.float32)
+    l = rng.uniform(0.5, 40, size=n).astype(np.float32)
+    e = rng.random(n) < empty_frac
+    o[e], m[e], l[e] = 0, -1e30, 0
+    return o, m, l
+
+
+@pytest.mark.parametrize("D,lanes,out_f16", [(128, 4, False), (64, 1, True), (128, 2, True)])
+def test_combine_csr(D, lanes, out_f16):
+    rng = np.random.default_rng(D + lanes)
+    counts = rng.integers(0, 20, size=300)
+    counts[:3] = [0, 1, 17]
+    off = np.zeros(301, dtype=np.int32)
+    off[1:] = np.cumsum(counts)
+    o, m, l = _random_partials(rng, int(off[-1]) * lanes, D)
+    lse = torch.empty(300 * lanes, dtype=torch.float32, device=DEV)
+    out, _ = B.pkv_combine_partials(dev(o), dev(m), dev(l), dev(off), num_segments=300,
+                                    lanes=lanes, lse=lse,
+                                    out_dtype=torch.float16 if out_f16 else torch.float32)
+    torch.cuda.synchronize()
+    ref, rlse = orc.combine_partials(o, m, l, off, lanes)
+    got = host(out).astype(np.float64)
+    if out_f16:
+        assert_f16_close(got, ref, "combine fp16")
+    else:
+        assert_f32_close(got, ref, "combine fp32")
+    g = host(lse)
+    fin = np.isfinite(rlse)
+    np.testing.assert_array_equal(np.isfinite(g), fin)
+    assert_f32_close(g[fin], rlse[fin], "lse")
+
+
+def test_combine_uniform_segments():
+    rng = np.random.default_rng(9)
+    o, m, l = _random_partials(rng, 50 * 16, 128)
+    out, _ = B.pkv_combine_partials(dev(o), dev(m), dev(l), None, num_segments=50, lanes=1,
+                                    uniform_count=16)
+    torch.cuda.synchronize()
+    off = np.arange(0, 50 * 16 + 1, 16)
+    ref, _ = orc.combine_partials(o, m, l, off, 1)
+    assert_f32_close(host(out), ref, "uniform combine")

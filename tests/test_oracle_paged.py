@@ -258,7 +258,7 @@ def test_rotary_on_append_rotates_new_keys_at_absolute_position():
                       past=[6, 2], new_tokens=[2, 3], rotary_dim=8)
     out, kc, vc, st = run(c)
     k_new, v_new, _ = orc.split_new_kv(c.query, c.key, c.value, 4, 2, 16)
-    smap = orc.sequence_map(c.cu_seqlens, c.past_seqlens)
+    smap, _ = orc.sequence_map(c.cu_seqlens, c.past_seqlens)
     for i, (b, t, pos) in enumerate(smap):
         blk = c.block_table[b, pos // 4]
         expect = orc.rotate_rows(k_new[i], [pos, pos], c.cos_cache, c.sin_cache, 8, False)
@@ -298,3 +298,40 @@ def test_llama8b_workload_shape():
     assert (np.diff(c.cu_seqlens) == 1).all()
     used = c.block_table[c.block_table >= 0]
     assert len(set(used.tolist())) == used.size == c.num_blocks
+
+
+def test_invalid_sequence_and_uncovered_tokens():
+    c = wl.paged_case(20, num_heads=2, kv_num_heads=1, head_size=8, block_size=4,
+                      past=[3, 2, 5], new_tokens=[2, 1, 2])
+    good = run(c)
+    # sequence 1 gets a negative past: its token is neither scattered nor attended
+    c.past_seqlens = c.past_seqlens.copy()
+    c.past_seqlens[1] = -1
+    out, kc, vc, st = run(c)
+    assert st & orc.ST_BAD_SEQUENCE
+    assert (out[2] == 0).all()
+    np.testing.assert_array_equal(out[[0, 1, 3, 4]], good[0][[0, 1, 3, 4]])
+    # cu ends before the last token: that token is padding (zero output, no flag)
+    c2 = wl.paged_case(20, num_heads=2, kv_num_heads=1, head_size=8, block_size=4,
+                       past=[3, 2, 5], new_tokens=[2, 1, 2])
+    c2.cu_seqlens = c2.cu_seqlens.copy()
+    c2.cu_seqlens[3] = 4
+    out2, _, _, st2 = run(c2)
+    assert st2 == 0 and (out2[4] == 0).all()
+    np.testing.assert_array_equal(out2[:4], good[0][:4])
+
+
+def test_rotary_position_past_table_skips_token():
+    c = wl.paged_case(21, num_heads=2, kv_num_heads=1, head_size=8, block_size=4,
+                      past=[5], new_tokens=[2], rotary_dim=8)
+    c.cos_cache = c.cos_cache[:6]
+    c.sin_cache = c.sin_cache[:6]
+    k_new, v_new, _ = orc.split_new_kv(c.query, c.key, c.value, 2, 1, 8)
+    kc, vc, st = orc.paged_scatter(k_new, v_new, c.key_cache, c.value_cache, c.cu_seqlens,
+                                   c.past_seqlens, c.block_table, None, c.cos_cache,
+                                   c.sin_cache, 8, False)
+    assert st == orc.ST_BAD_POSITION
+    blk6 = c.block_table[0, 6 // 4]
+    np.testing.assert_array_equal(kc[blk6, 6 % 4], c.key_cache[blk6, 6 % 4])   # skipped
+    blk5 = c.block_table[0, 5 // 4]
+    assert not np.array_equal(kc[blk5, 5 % 4], c.key_cache[blk5, 5 % 4])       # written

@@ -182,3 +182,14 @@ def test_block_sparse_workload_structure():
             assert pos // BSZ in blks
             assert blks.max() <= (c.used_kv_lens[b] - 1) // BSZ
     assert (em[:, 4] <= 0).sum() == 4
+
+
+def test_out_of_range_edge_fields_give_flagged_sentinel():
+    q, kp, vp, bt = tiny_pages()
+    for meta in ([1, 0, 0, 0, 3], [0, 1, 0, 0, 3], [0, 0, 0, 1, 3], [0, 0, -1, 0, 3],
+                 [0, 0, 1, 0, 3]):
+        o, m, l, st = sp(q, kp, vp, meta, bt)
+        assert m == -1e30 and l == 0.0 and (o == 0).all() and st == orc.ST_BAD_EDGE, meta
+    # an empty edge is never flagged, whatever its other fields hold
+    o, m, l, st = sp(q, kp, vp, [9, 9, 9, 9, 0], bt)
+    assert st == 0 and l == 0.0
