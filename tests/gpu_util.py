@@ -38,10 +38,16 @@ def assert_f16_close(got, ref, what=""):
     return float(err.max()) if err.size else 0.0
 
 
-def assert_f32_close(got, ref, what=""):
+def assert_f32_close(got, ref, what="", scalars=False):
+    """Rows are the last axis (a 1-D array is one row) unless ``scalars`` is set, in
+    which case every element is its own row: then the floor is 1e-4 * max(|ref|, 1),
+    the scale of a softmax statistic such as m."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    row_scale = np.max(np.abs(ref), axis=-1, keepdims=True) if ref.ndim > 1 else np.abs(ref)
+    if scalars:
+        row_scale = np.maximum(np.abs(ref), 1.0)
+    else:
+        row_scale = np.max(np.abs(ref), axis=-1, keepdims=True)
     err = np.abs(got - ref)
     tol = F32_RTOL * (np.abs(ref) + row_scale) + 1e-30
     bad = ~(err <= tol)

@@ -40,8 +40,8 @@ def compare_partials(go, gm, gl, ro, rm, rl, rows):
     assert (gm[rows][empty] == -1e30).all() and (go[rows][empty] == 0).all()
     live = rows[~empty]
     assert_f32_close(go[live], ro[live], "o partial")
-    assert_f32_close(gm[live], rm[live], "m partial")
-    assert_f32_close(gl[live], rl[live], "l partial")
+    assert_f32_close(gm[live], rm[live], "m partial", scalars=True)
+    assert_f32_close(gl[live], rl[live], "l partial", scalars=True)
 
 
 @pytest.mark.parametrize("head_dim,pages_per_block,qhead", [(128, 4, 4), (64, 2, 2),
@@ -58,7 +58,7 @@ def test_small_full_parity(head_dim, pages_per_block, qhead):
     assert_f32_close(gout, rout, "combined output")
     fin = np.isfinite(rlse)
     np.testing.assert_array_equal(np.isfinite(glse), fin)
-    assert_f32_close(glse[fin], rlse[fin], "lse")
+    assert_f32_close(glse[fin], rlse[fin], "lse", scalars=True)
 
 
 def test_bad_edges_and_pages_are_flagged():
@@ -129,7 +129,7 @@ def test_combine_csr(D, lanes, out_f16):
     g = host(lse)
     fin = np.isfinite(rlse)
     np.testing.assert_array_equal(np.isfinite(g), fin)
-    assert_f32_close(g[fin], rlse[fin], "lse")
+    assert_f32_close(g[fin], rlse[fin], "lse", scalars=True)
 
 
 def test_combine_uniform_segments():
