@@ -51,6 +51,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps")
+    ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer leg")
     return ap.parse_args()
 
 
@@ -192,6 +193,7 @@ def timed_loop(fn, steps, world):
 # ----------------------------------------------------------------------------- workloads
 ATTN_SOURCES = ["paged_kv_cache_231_gb300/csrc/attention.cu",
                 "paged_kv_cache_231_gb300/csrc/device_common.cuh",
+                "paged_kv_cache_231_gb300/csrc/scatter_dev.cuh",
                 "paged_kv_cache_231_gb300/csrc/internal.h"]
 SPARSE_SOURCES = ["paged_kv_cache_231_gb300/csrc/sparse.cu",
                   "paged_kv_cache_231_gb300/csrc/device_common.cuh",
@@ -272,9 +274,10 @@ def setup_paged(name, args):
         kvb, qb, ob = decode_bytes(case)
         w.metric, w.unit, w.work, w.dtype = METRIC, "GB/s", (kvb + qb + ob) / 1e9, "f16"
         w.tokens = case.num_tokens
-        w.dominant, w.dom_work, w.bound = "decode", (kvb + qb) / 1e9, "hbm"
+        # the persistent attention kernel reads K/V and Q and writes O (fused combine)
+        w.dominant, w.dom_work, w.bound = "attention", (kvb + qb + ob) / 1e9, "hbm"
         w.dom_unit = "GB/s"
-        w.traffic_summary, w.traffic_sources = "decode_llama8b.md", ATTN_SOURCES
+        w.traffic_summary, w.traffic_sources = "attention_llama8b_decode.md", ATTN_SOURCES
         w.config = {"workload": "llama8b_decode", "batch": case.batch, "tokens": case.num_tokens,
                     "num_heads": 32, "kv_num_heads": 8, "head_size": 128, "block_size": 16,
                     "context": "U[512,8192]", "mean_context": float(case.context_lengths().mean()),
@@ -286,7 +289,7 @@ def setup_paged(name, args):
         w.metric = "varlen prefill+decode attention TFLOP/s (causal pairs)"
         w.unit, w.work, w.dtype = "TFLOP/s", fl / 1e12, "f16"
         w.tokens = case.num_tokens
-        w.dominant, w.dom_work, w.bound, w.dom_unit = "prefill", fl / 1e12, "tensor", "TFLOP/s"
+        w.dominant, w.dom_work, w.bound, w.dom_unit = "attention", fl / 1e12, "tensor", "TFLOP/s"
         w.traffic_summary, w.traffic_sources = None, ATTN_SOURCES
         w.config = {"workload": "varlen_mixed", "batch": case.batch, "tokens": case.num_tokens,
                     "num_heads": 32, "kv_num_heads": 8, "head_size": 128, "block_size": 32,
@@ -539,12 +542,12 @@ def main():
     B.pkv_profiler_enable(False)
     dom_ms, dom_n = B.pkv_profiler_query(w.dominant)
     kernel_ms = {k: B.pkv_profiler_query(k) for k in
-                 ("scatter", "plan", "decode", "prefill", "combine", "sparse_group",
-                  "sparse_partials", "append")}
+                 ("prologue", "attention", "decode_split", "combine", "scatter",
+                  "sparse_group", "sparse_partials", "append")}
     B.pkv_profiler_reset()
 
     e2e = None
-    if w.e2e_step is not None:
+    if w.e2e_step is not None and not args.skip_e2e:
         for _ in range(3):
             w.e2e_step()
         e2e_ms = timed_loop(w.e2e_step, args.e2e_steps or args.steps, world)
@@ -584,7 +587,7 @@ def main():
     line["gpu_launches"] = launches
     line["clocks"] = clk
     line["e2e"] = e2e
-    if world == 1:
+    if world == 1 and args.cpu_seconds > 0:
         v, tps, desc = oracle_sample(args.workload, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": w.unit, "cores": cpu_cores(),
                                 "kind": "oracle", "sample": desc}

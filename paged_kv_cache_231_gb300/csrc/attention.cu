@@ -1,38 +1,38 @@
-// Paged causal GQA attention: device planner, split-KV decode kernel and tiled
-// varlen prefill kernel.
+// Paged causal GQA attention: prologue (device planner + ScatterKV), persistent
+// attention kernel (stream-K split-KV decode with a fused LSE combine, then tiled
+// varlen prefill), and a per-split decode kernel for fixed split policies.
 //
-// Operator: "com.microsoft.PagedAttention manifest.json" - AttendSplitK (one
-// workgroup per (token, kv head, split) covering that kv head's query heads, fp32
-// partials) and Attend (one workgroup per (token, kv head), whole causal key range).
-// The GB300 form keeps the manifest's sharing of one K/V read across the qPerKv query
-// heads of a kv head, but:
-//   * a sequence with few new tokens (decode) is one row tile of (new tokens x query
-//     heads) per kv head and is split along its keys; each split writes an fp32
-//     (o, m, l) partial and a combine pass merges them;
-//   * a sequence with many new tokens (prefill) is tiled over its query positions, so
-//     K/V is read once per (tile, kv head) instead of once per token;
-//   * K/V rows are gathered through block_table with 16-byte cp.async copies into a
-//     multi-stage shared-memory ring, and QK^T / PV run on tensor cores
-//     (mma.sync m16n8k16, fp16 in, fp32 accumulate) with the score accumulators
-//     reused in registers as the A operand of PV.
+// Operator: "com.microsoft.PagedAttention manifest.json" - ScatterKV, AttendSplitK
+// (one workgroup per (token, kv head, split) covering that kv head's query heads, fp32
+// partials), AttendSplitKMerge, and Attend (one workgroup per (token, kv head)). The
+// GB300 form keeps the manifest's sharing of one K/V read across the qPerKv query heads
+// of a kv head, and changes the schedule:
+//   * decode (a sequence with few new tokens): the (sequence, kv head) key ranges of
+//     the whole batch are cut into 16-key stages and laid end to end; every warp of a
+//     persistent grid takes an equal run of stages ("stream-K"), streams them through
+//     its own cp.async ring and writes an fp32 (o, m, l) partial wherever its run ends
+//     inside a (sequence, kv head) range. The warp that completes a range last (atomic
+//     ticket, no waiting) merges its partials into the fp16 output, so the split count
+//     adapts per sequence and the load is balanced to one stage;
+//   * prefill (many new tokens): tiles of query positions x query heads, taken by the
+//     same persistent CTAs from an atomic counter, so K/V is read once per tile;
+//   * QK^T and PV run on tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate),
+//     the score accumulators are reused in registers as the A operand of PV, and the
+//     online softmax works in base 2 (scores pre-scaled by log2 e).
 #include <limits.h>
 #include <math.h>
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "scatter_dev.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 128;  // 4 warps per CTA for both attention kernels
+constexpr int kThreads = 128;  // 4 warps per CTA
 constexpr int kWarps = 4;
-
-template <int D>
-struct Tile {
-  static constexpr int CPR = D / 8;  // 16-byte chunks per head row
-  // XOR swizzle so that 8 rows read at the same logical chunk hit 8 distinct bank groups
-  static __device__ __forceinline__ int chunk(int r, int c) { return r * CPR + (c ^ (r & 7)); }
-};
+constexpr int kCtasPerSm = 2;
+constexpr int kPrologueThreads = 256;
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
@@ -42,6 +42,13 @@ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? 
 __device__ __forceinline__ int seq_keys(const AttnParams& p, int P, int N) {
   return (int)min64((int64_t)P + N, (int64_t)p.MB * p.BS);
 }
+
+template <int D>
+struct Tile {
+  static constexpr int CPR = D / 8;  // 16-byte chunks per head row
+  // XOR swizzle so that 8 rows read at the same logical chunk hit 8 distinct bank groups
+  static __device__ __forceinline__ int chunk(int r, int c) { return r * CPR + (c ^ (r & 7)); }
+};
 
 // Element offset of key j of (sequence b, kv head h) in the cache, or -1 if unmapped.
 __device__ __forceinline__ int64_t key_row_offset(const AttnParams& p, int b, int h, int j) {
@@ -59,8 +66,8 @@ __device__ __forceinline__ int64_t key_row_offset(const AttnParams& p, int b, in
   return (((int64_t)blk * p.BS + off) * p.Hkv + h) * p.D;
 }
 
-// Stage keys [k0, k0 + kStageKeys) of (b, h) into shared memory; keys at or past kend
-// and unmapped keys are zero-filled and marked invalid.
+// CTA-wide: stage keys [k0, k0 + kStageKeys) of (b, h); keys at or past kend and
+// unmapped keys are zero-filled and marked invalid.
 template <int D>
 __device__ __forceinline__ void load_stage(const AttnParams& p, int b, int h, int k0,
                                            int kend, __half* sK, __half* sV,
@@ -92,6 +99,34 @@ __device__ __forceinline__ void load_stage(const AttnParams& p, int b, int h, in
     cp_async_16(sV + sidx, gv, nbytes);
     if (c == 0) sValid[r] = off >= 0 ? 1 : 0;
   }
+}
+
+// Warp-wide: stage 16 keys [k0, k0 + 16) of (b, h) into this warp's ring slot. Two
+// lanes per key row, each copying half of the K row and half of the V row.
+template <int D>
+__device__ __forceinline__ void warp_load16(const AttnParams& p, int b, int h, int k0,
+                                            int kend, __half* sK, __half* sV,
+                                            uint8_t* sValid, int lane, bool& bad) {
+  constexpr int CPL = D / 16;  // chunks per lane
+  const int r = lane >> 1;
+  const int c0 = (lane & 1) * CPL;
+  const int j = k0 + r;
+  int64_t off = -1;
+  if (j < kend) {
+    off = key_row_offset(p, b, h, j);
+    if (off < 0) bad = true;
+  }
+  const int nb = off >= 0 ? 16 : 0;
+  const __half* gk = off >= 0 ? p.kc + off : p.kc;
+  const __half* gv = off >= 0 ? p.vc + off : p.vc;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const int cc = c0 + c;
+    const int sidx = Tile<D>::chunk(r, cc) * 8;
+    cp_async_16(sK + sidx, nb ? gk + cc * 8 : gk, nb);
+    cp_async_16(sV + sidx, nb ? gv + cc * 8 : gv, nb);
+  }
+  if ((lane & 1) == 0) sValid[r] = off >= 0 ? 1 : 0;
 }
 
 __device__ __forceinline__ uint32_t ld_half2(const __half* ptr) {
@@ -145,205 +180,311 @@ __device__ __forceinline__ void pv_16(float (&o)[D / 8][4], const uint32_t (&pa)
   }
 }
 
+// Online-softmax update of the two rows (g, g+8) held by this lane for 16 new scores
+// s[2][4] (already scaled to log2 units, -inf where masked); turns s into weights.
+template <int DN>
+__device__ __forceinline__ void softmax_16(float (&s)[2][4], float (&m_run)[2],
+                                           float (&l_run)[2], float (&o)[DN][4]) {
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    float mx = fmaxf(fmaxf(s[0][2 * hr], s[0][2 * hr + 1]),
+                     fmaxf(s[1][2 * hr], s[1][2 * hr + 1]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mnew = fmaxf(m_run[hr], mx);
+    const float base = mnew == -INFINITY ? 0.f : mnew;
+    const float alpha = ex2(m_run[hr] - base);
+    m_run[hr] = mnew;
+    float sum = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const float pv = ex2(s[nt][2 * hr + x] - base);
+        s[nt][2 * hr + x] = pv;
+        sum += pv;
+      }
+    l_run[hr] = l_run[hr] * alpha + sum;
+#pragma unroll
+    for (int d = 0; d < DN; ++d) {
+      o[d][2 * hr] *= alpha;
+      o[d][2 * hr + 1] *= alpha;
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------------
-// Split-KV decode: CTA = one split of one short sequence for one kv head; the 4 warps
-// take 16 keys each of every 64-key stage and merge their softmax states at the end.
+// Stream-K decode (phase 1 of the persistent kernel)
 // ----------------------------------------------------------------------------------
-template <int D, int NSTAGE>
-__global__ void __launch_bounds__(kThreads) decode_kernel(AttnParams p) {
-  constexpr int SK = kStageKeys;
+__device__ __forceinline__ DecSeq load_seq(const AttnParams& p, int i) {
+  const int4* q = reinterpret_cast<const int4*>(p.dec_seqs + i);
+  const int4 a = q[0], b = q[1];
+  DecSeq d;
+  d.b = a.x;
+  d.n = a.y;
+  d.st = a.z;
+  d.base = a.w;
+  d.nq = b.x;
+  d.cu0 = b.y;
+  d.P = b.z;
+  d.slot = b.w;
+  return d;
+}
+
+struct Cursor {
+  int i, h, s;  // decode sequence, kv head, stage within the (sequence, kv head) range
+  DecSeq d;
+};
+
+// cursor at global stage g: the last decode sequence whose range starts at or before g
+__device__ __forceinline__ Cursor locate(const AttnParams& p, int g, int ndec) {
+  int lo = 0, hi = ndec - 1, i = 0;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if (p.dec_seqs[mid].base <= g) {
+      i = mid;
+      lo = mid + 1;
+    } else {
+      hi = mid - 1;
+    }
+  }
+  Cursor c;
+  c.i = i;
+  c.d = load_seq(p, i);
+  const int off = g - c.d.base;
+  c.h = off / c.d.st;
+  c.s = off - c.h * c.d.st;
+  return c;
+}
+
+__device__ __forceinline__ void advance(const AttnParams& p, Cursor& c, int ndec) {
+  if (++c.s < c.d.st) return;
+  c.s = 0;
+  if (++c.h < p.Hkv) return;
+  c.h = 0;
+  if (++c.i < ndec) c.d = load_seq(p, c.i);
+}
+
+template <int D>
+__device__ __forceinline__ void decode_rows(const AttnParams& p, const Cursor& c, int g,
+                                            int t4, uint32_t (&qa)[D / 16][4],
+                                            int (&lim)[2]) {
+  const int R = c.d.nq * p.G;
+  const __half* rows[2];
+  bool ok[2];
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int r = g + 8 * hr;
+    ok[hr] = r < R;
+    const int pos = ok[hr] ? r / p.G : 0;
+    const int gg = ok[hr] ? r % p.G : 0;
+    rows[hr] = p.q + (int64_t)(c.d.cu0 + pos) * p.q_stride + (int64_t)(c.h * p.G + gg) * D;
+    lim[hr] = ok[hr] ? (int)min64((int64_t)c.d.P + pos, INT32_MAX) : -1;
+  }
+  load_q_frags<D>(qa, rows[0], rows[1], ok[0], ok[1], t4);
+}
+
+// End of this warp's piece of the (sequence, kv head) range under cursor c: write the
+// piece's partial (or the final output if the range is a single piece) and, if this
+// warp finished the range last, merge all pieces into the output.
+template <int D>
+__device__ void flush_piece(const AttnParams& p, const Cursor& c, int gw, int W,
+                            float (&m_run)[2], float (&l_run)[2], float (&o)[D / 8][4],
+                            int lane) {
   constexpr int DN = D / 8;
-  extern __shared__ __align__(128) unsigned char smem[];
-  __half* sK = reinterpret_cast<__half*>(smem);
-  __half* sV = sK + NSTAGE * SK * D;
-  uint8_t* sValid = reinterpret_cast<uint8_t*>(sV + NSTAGE * SK * D);
-
-  const int h = blockIdx.x % p.Hkv;
-  const int64_t item_idx = blockIdx.x / p.Hkv;
-  if (item_idx >= p.counts[0]) return;
-  const DecodeItem it = p.dec_items[item_idx];
-  const int b = it.b;
-  const int cu0 = p.cu[b];
-  const int P = p.past[b];
-  const int n = seq_keys(p, P, it.nq);
-  const int kb = it.split * it.chunk;
-  const int ke = min(n, kb + it.chunk);
-  const int R = it.nq * p.G;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int V = D / 32;
   const int g = lane >> 2, t4 = lane & 3;
-
-  int lim[2];
-  uint32_t qa[D / 16][4];
-  {
-    const __half* rows[2];
-    bool ok[2];
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int r = g + 8 * hr;
-      ok[hr] = r < R;
-      const int pos = ok[hr] ? r / p.G : 0;
-      const int gg = ok[hr] ? r % p.G : 0;
-      rows[hr] = p.q + (int64_t)(cu0 + pos) * p.q_stride + (int64_t)(h * p.G + gg) * D;
-      lim[hr] = ok[hr] ? (int)min64((int64_t)P + pos, INT32_MAX) : -1;
-    }
-    load_q_frags<D>(qa, rows[0], rows[1], ok[0], ok[1], t4);
-  }
-
-  const int nst = ke > kb ? (ke - kb + SK - 1) / SK : 0;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
-  float o[DN][4];
-#pragma unroll
-  for (int i = 0; i < DN; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  bool bad = false;
-
-#pragma unroll
-  for (int s = 0; s < NSTAGE - 1; ++s) {
-    if (s < nst)
-      load_stage<D>(p, b, h, kb + s * SK, ke, sK + s * SK * D, sV + s * SK * D,
-                    sValid + s * SK, bad);
-    cp_async_commit();
-  }
-  for (int i = 0; i < nst; ++i) {
-    cp_async_wait<NSTAGE - 2>();
-    __syncthreads();
-    {
-      const int nx = i + NSTAGE - 1;
-      if (nx < nst) {
-        const int bf = nx % NSTAGE;
-        load_stage<D>(p, b, h, kb + nx * SK, ke, sK + bf * SK * D, sV + bf * SK * D,
-                      sValid + bf * SK, bad);
-      }
-      cp_async_commit();
-    }
-    const int bf = i % NSTAGE;
-    const __half* K = sK + bf * SK * D;
-    const __half* V = sV + bf * SK * D;
-    const uint8_t* vld = sValid + bf * SK;
-    const int kw = warp * 16;
-    const int kstage = kb + i * SK;
-    if (kstage + kw < ke) {
-      float s[2][4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[0][e] = s[1][e] = 0.f;
-      qk_16<D>(s[0], s[1], qa, K, kw, lane);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int kk = kw + nt * 8 + 2 * t4 + (e & 1);
-          const bool ok = vld[kk] && (kstage + kk <= lim[e >> 1]);
-          s[nt][e] = ok ? s[nt][e] * p.scale_log2 : -INFINITY;
-        }
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        float mx = fmaxf(fmaxf(s[0][2 * hr], s[0][2 * hr + 1]),
-                         fmaxf(s[1][2 * hr], s[1][2 * hr + 1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mnew = fmaxf(m_run[hr], mx);
-        const float base = mnew == -INFINITY ? 0.f : mnew;
-        const float alpha = ex2(m_run[hr] - base);
-        m_run[hr] = mnew;
-        float sum = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const float pv = ex2(s[nt][2 * hr + x] - base);
-            s[nt][2 * hr + x] = pv;
-            sum += pv;
-          }
-        l_run[hr] = l_run[hr] * alpha + sum;
-#pragma unroll
-        for (int d = 0; d < DN; ++d) {
-          o[d][2 * hr] *= alpha;
-          o[d][2 * hr + 1] *= alpha;
-        }
-      }
-      uint32_t pa[4] = {pack_half2(s[0][0], s[0][1]), pack_half2(s[0][2], s[0][3]),
-                        pack_half2(s[1][0], s[1][1]), pack_half2(s[1][2], s[1][3])};
-      pv_16<D>(o, pa, V, kw, lane);
-    }
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-
-  // merge the 4 warps' states (stage buffers are free now)
+  const int R = c.d.nq * p.G;
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
     l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
     l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
   }
-  float* sO = reinterpret_cast<float*>(smem);  // [kWarps][16][D]
-  float* sM = sO + kWarps * 16 * D;            // [kWarps][16]
-  float* sL = sM + kWarps * 16;
+  const int seg0 = c.d.base + c.h * c.d.st;
+  const int first_w = seg0 / W;
+  const int pieces = (seg0 + c.d.st - 1) / W - first_w + 1;
+  if (pieces == 1) {
 #pragma unroll
-  for (int d = 0; d < DN; ++d) {
-    const int c = d * 8 + 2 * t4;
-    *reinterpret_cast<float2*>(&sO[(warp * 16 + g) * D + c]) = make_float2(o[d][0], o[d][1]);
-    *reinterpret_cast<float2*>(&sO[(warp * 16 + g + 8) * D + c]) =
-        make_float2(o[d][2], o[d][3]);
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = g + 8 * hr;
+      if (r >= R) continue;
+      const float inv = l_run[hr] > 0.f ? 1.f / l_run[hr] : 0.f;
+      __half* orow = p.out + ((int64_t)(c.d.cu0 + r / p.G) * p.Hq + c.h * p.G + r % p.G) * D;
+#pragma unroll
+      for (int d = 0; d < DN; ++d)
+        *reinterpret_cast<__half2*>(orow + d * 8 + 2 * t4) =
+            __floats2half2_rn(o[d][2 * hr] * inv, o[d][2 * hr + 1] * inv);
+    }
+    return;
   }
-  if (t4 == 0) {
-    sM[warp * 16 + g] = m_run[0];
-    sM[warp * 16 + g + 8] = m_run[1];
-    sL[warp * 16 + g] = l_run[0];
-    sL[warp * 16 + g + 8] = l_run[1];
+  const int piece = gw - first_w;
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int r = g + 8 * hr;
+    if (r >= R) continue;
+    const int64_t prow =
+        ((int64_t)(c.d.slot + r / p.G) * p.Hq + c.h * p.G + r % p.G) * p.max_splits + piece;
+    const bool live = l_run[hr] > 0.f;
+#pragma unroll
+    for (int d = 0; d < DN; ++d)
+      *reinterpret_cast<float2*>(p.part_o + prow * D + d * 8 + 2 * t4) =
+          live ? make_float2(o[d][2 * hr], o[d][2 * hr + 1]) : make_float2(0.f, 0.f);
+    if (t4 == 0) {
+      p.part_m[prow] = live ? m_run[hr] * kLn2 : kNegLarge;
+      p.part_l[prow] = l_run[hr];
+    }
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < R * D; e += kThreads) {
-    const int r = e / D, d = e % D;
-    float M = -INFINITY;
+  __threadfence();
+  __syncwarp();
+  int done = 0;
+  if (lane == 0) done = atomicAdd(&p.seg_done[c.i * p.Hkv + c.h], 1);
+  done = __shfl_sync(0xffffffffu, done, 0);
+  if (done != pieces - 1) return;
+  __threadfence();
+  for (int r = 0; r < R; ++r) {
+    const int64_t prow0 =
+        ((int64_t)(c.d.slot + r / p.G) * p.Hq + c.h * p.G + r % p.G) * p.max_splits;
+    float lp = 0.f, mp = -INFINITY;
+    if (lane < pieces) {
+      lp = __ldcg(p.part_l + prow0 + lane);
+      if (lp > 0.f) mp = __ldcg(p.part_m + prow0 + lane);
+    }
+    const float M = warp_max(mp);
+    const float w = lp > 0.f ? ex2((mp - M) * kLog2e) : 0.f;
+    const float L = warp_sum(w * lp);
+    float acc[V];
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sM[w * 16 + r]);
-    float num = 0.f, L = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float wt = ex2(sM[w * 16 + r] - M);
-        num += wt * sO[(w * 16 + r) * D + d];
-        L += wt * sL[w * 16 + r];
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    for (int q = 0; q < pieces; ++q) {
+      const float wq = __shfl_sync(0xffffffffu, w, q);
+      if (wq > 0.f) {
+        const float* src = p.part_o + (prow0 + q) * D + lane * V;
+        if constexpr (V == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+          acc[0] += wq * x.x;
+          acc[1] += wq * x.y;
+          acc[2] += wq * x.z;
+          acc[3] += wq * x.w;
+        } else {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+          acc[0] += wq * x.x;
+          acc[1] += wq * x.y;
+        }
       }
     }
-    const int pos = r / p.G, gg = r % p.G;
-    const int64_t prow =
-        ((int64_t)(it.slot_base + pos) * p.Hq + h * p.G + gg) * p.max_splits + it.split;
-    p.part_o[prow * D + d] = L > 0.f ? num : 0.f;
-    if (d == 0) {
-      p.part_m[prow] = L > 0.f ? M * kLn2 : kNegLarge;
-      p.part_l[prow] = L;
-    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __half* orow = p.out + ((int64_t)(c.d.cu0 + r / p.G) * p.Hq + c.h * p.G + r % p.G) * D +
+                   lane * V;
+#pragma unroll
+    for (int v = 0; v < V; v += 2)
+      *reinterpret_cast<__half2*>(orow + v) = __floats2half2_rn(acc[v] * inv, acc[v + 1] * inv);
   }
-  if (bad) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+}
+
+template <int D, int NS>
+__device__ void decode_phase(const AttnParams& p, unsigned char* wsm, int gw, int lane,
+                             bool& bad) {
+  constexpr int DN = D / 8;
+  const int ndec = p.counts[kCntDecSeqs];
+  const int total = p.counts[kCntStages];
+  const int W = p.counts[kCntW];
+  if (ndec == 0 || W <= 0) return;
+  const int64_t g0 = (int64_t)gw * W;
+  if (g0 >= total) return;
+  const int nst = (int)(min64(total, g0 + W) - g0);
+  __half* rK = reinterpret_cast<__half*>(wsm);
+  __half* rV = rK + NS * 16 * D;
+  uint8_t* rValid = reinterpret_cast<uint8_t*>(rV + NS * 16 * D);
+
+  Cursor pc = locate(p, (int)g0, ndec);
+  Cursor cc = pc;
+#pragma unroll
+  for (int k = 0; k < NS - 1; ++k) {
+    if (k < nst) {
+      warp_load16<D>(p, pc.d.b, pc.h, pc.s * 16, pc.d.n, rK + k * 16 * D, rV + k * 16 * D,
+                     rValid + k * 16, lane, bad);
+      advance(p, pc, ndec);
+    }
+    cp_async_commit();
+  }
+  const int g = lane >> 2, t4 = lane & 3;
+  uint32_t qa[D / 16][4];
+  int lim[2];
+  decode_rows<D>(p, cc, g, t4, qa, lim);
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  float o[DN][4];
+#pragma unroll
+  for (int i = 0; i < DN; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  for (int k = 0; k < nst; ++k) {
+    cp_async_wait<NS - 2>();
+    __syncwarp();
+    if (k + NS - 1 < nst) {
+      const int bf = (k + NS - 1) % NS;
+      warp_load16<D>(p, pc.d.b, pc.h, pc.s * 16, pc.d.n, rK + bf * 16 * D, rV + bf * 16 * D,
+                     rValid + bf * 16, lane, bad);
+      advance(p, pc, ndec);
+    }
+    cp_async_commit();
+    const int bf = k % NS;
+    const uint8_t* vld = rValid + bf * 16;
+    const int kstage = cc.s * 16;
+    float s[2][4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[0][e] = s[1][e] = 0.f;
+    qk_16<D>(s[0], s[1], qa, rK + bf * 16 * D, 0, lane);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int kk = nt * 8 + 2 * t4 + (e & 1);
+        const bool ok = vld[kk] && (kstage + kk <= lim[e >> 1]);
+        s[nt][e] = ok ? s[nt][e] * p.scale_log2 : -INFINITY;
+      }
+    softmax_16<DN>(s, m_run, l_run, o);
+    uint32_t pa[4] = {pack_half2(s[0][0], s[0][1]), pack_half2(s[0][2], s[0][3]),
+                      pack_half2(s[1][0], s[1][1]), pack_half2(s[1][2], s[1][3])};
+    pv_16<D>(o, pa, rV + bf * 16 * D, 0, lane);
+
+    const bool seg_last = cc.s == cc.d.st - 1;
+    if (seg_last || k == nst - 1) {
+      flush_piece<D>(p, cc, gw, W, m_run, l_run, o, lane);
+      m_run[0] = m_run[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+      for (int i = 0; i < DN; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    }
+    advance(p, cc, ndec);
+    if (seg_last && k < nst - 1) decode_rows<D>(p, cc, g, t4, qa, lim);
+  }
+  cp_async_wait<0>();
+  __syncwarp();
 }
 
 // ----------------------------------------------------------------------------------
-// Tiled prefill: CTA = one tile of query positions of one sequence for one kv head;
-// warp w owns 16 rows = (16 / G) positions x G query heads; all warps stream the
-// same K/V stages up to the tile's causal limit. Output is written directly.
+// Prefill tile (phase 2 of the persistent kernel): one tile of query positions of one
+// sequence for one kv head; warp w owns 16 rows = (16 / G) positions x G query heads;
+// all warps stream the same 64-key stages up to the tile's causal limit.
 // ----------------------------------------------------------------------------------
 template <int D, int NSTAGE>
-__global__ void __launch_bounds__(kThreads) prefill_kernel(AttnParams p) {
+__device__ void prefill_tile(const AttnParams& p, unsigned char* smem, int item_idx, int h,
+                             bool& bad) {
   constexpr int SK = kStageKeys;
   constexpr int DN = D / 8;
-  extern __shared__ __align__(128) unsigned char smem[];
   __half* sK = reinterpret_cast<__half*>(smem);
   __half* sV = sK + NSTAGE * SK * D;
   uint8_t* sValid = reinterpret_cast<uint8_t*>(sV + NSTAGE * SK * D);
 
-  const int h = blockIdx.x % p.Hkv;
-  const int64_t item_idx = blockIdx.x / p.Hkv;
-  if (item_idx >= p.counts[1]) return;
   const PrefillItem it = p.pre_items[item_idx];
   const int b = it.b;
   const int cu0 = p.cu[b];
   const int P = p.past[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
-  const int ppw = 16 / p.G;                 // positions per warp
-  const int wpos0 = warp * ppw;             // first tile position of this warp
-  const int wn = max(0, min(ppw, it.nq - wpos0));  // valid positions of this warp
+  const int ppw = 16 / p.G;
+  const int wpos0 = warp * ppw;
+  const int wn = (int)max64(0, min64(ppw, it.nq - wpos0));
   const int warp_lim =
       wn > 0 ? (int)min64((int64_t)P + it.q0 + wpos0 + wn - 1, INT32_MAX) : -1;
   const int kend = seq_keys(p, P, it.q0 + it.nq);
@@ -375,13 +516,12 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnParams p) {
   float o[DN][4];
 #pragma unroll
   for (int i = 0; i < DN; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  bool bad = false;
 
 #pragma unroll
   for (int s = 0; s < NSTAGE - 1; ++s) {
     if (s < nst)
-      load_stage<D>(p, b, h, s * SK, kend, sK + s * SK * D, sV + s * SK * D,
-                    sValid + s * SK, bad);
+      load_stage<D>(p, b, h, s * SK, kend, sK + s * SK * D, sV + s * SK * D, sValid + s * SK,
+                    bad);
     cp_async_commit();
   }
   for (int i = 0; i < nst; ++i) {
@@ -398,7 +538,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnParams p) {
     }
     const int bf = i % NSTAGE;
     const __half* K = sK + bf * SK * D;
-    const __half* V = sV + bf * SK * D;
+    const __half* Vt = sV + bf * SK * D;
     const uint8_t* vld = sValid + bf * SK;
     const int kstage = i * SK;
     if (kstage > warp_lim) continue;   // warp-uniform: everything here is in the future
@@ -453,7 +593,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnParams p) {
                         pack_half2(s[2 * sub][2], s[2 * sub][3]),
                         pack_half2(s[2 * sub + 1][0], s[2 * sub + 1][1]),
                         pack_half2(s[2 * sub + 1][2], s[2 * sub + 1][3])};
-      pv_16<D>(o, pa, V, sub * 16, lane);
+      pv_16<D>(o, pa, Vt, sub * 16, lane);
     }
   }
   cp_async_wait<0>();
@@ -474,16 +614,192 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnParams p) {
       *reinterpret_cast<__half2*>(orow + d * 8 + 2 * t4) = v;
     }
   }
+}
+
+// ring sizes (bytes) of the two phases; the dynamic shared memory is their maximum
+template <int D, int NS>
+struct DecodeRing {
+  static constexpr size_t kWarpBytes =
+      ((size_t)NS * 16 * D * 2 * 2 + NS * 16 + 127) / 128 * 128;
+  static constexpr size_t kBytes = kWarpBytes * kWarps;
+};
+template <int D, int NSTAGE>
+struct TileRing {
+  static constexpr size_t kBytes =
+      (size_t)NSTAGE * kStageKeys * D * 2 * 2 + NSTAGE * kStageKeys;
+};
+
+template <int D, int NS, int NSTAGE>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) attention_kernel(AttnParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int s_tile;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool bad = false;
+  decode_phase<D, NS>(p, smem + warp * DecodeRing<D, NS>::kWarpBytes,
+                      blockIdx.x * kWarps + warp, lane, bad);
+  __syncthreads();
+  const int ntiles = p.counts[kCntTiles];
+  while (true) {
+    if (threadIdx.x == 0) s_tile = atomicAdd(&p.counts[kCntTileNext], 1);
+    __syncthreads();
+    const int t = s_tile;
+    __syncthreads();
+    if (t >= ntiles) break;
+    prefill_tile<D, NSTAGE>(p, smem, t / p.Hkv, t % p.Hkv, bad);
+  }
   if (bad) flag_status(p.status, PKV_DEV_BAD_BLOCK);
 }
 
 // ----------------------------------------------------------------------------------
-// Planner: one CTA. Reads cu / past, decides per sequence between split-KV decode
-// (new tokens <= dec_rows) and prefill tiles, and writes the work lists, the partial
-// slot map and zero output rows for tokens no valid sequence covers.
+// Split mode (fixed split counts): CTA = one split of one short sequence for one kv
+// head; the 4 warps take 16 keys each of every 64-key stage and merge at the end. The
+// partials are merged by the combine kernel.
 // ----------------------------------------------------------------------------------
-constexpr int kPlanThreads = 1024;
+template <int D, int NSTAGE>
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(AttnParams p) {
+  constexpr int SK = kStageKeys;
+  constexpr int DN = D / 8;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __half* sK = reinterpret_cast<__half*>(smem);
+  __half* sV = sK + NSTAGE * SK * D;
+  uint8_t* sValid = reinterpret_cast<uint8_t*>(sV + NSTAGE * SK * D);
 
+  const int h = blockIdx.x % p.Hkv;
+  const int64_t item_idx = blockIdx.x / p.Hkv;
+  if (item_idx >= p.counts[kCntSplitItems]) return;
+  const DecodeItem it = p.dec_items[item_idx];
+  const int b = it.b;
+  const int cu0 = p.cu[b];
+  const int P = p.past[b];
+  const int n = seq_keys(p, P, it.nq);
+  const int kb = it.split * it.chunk;
+  const int ke = (int)min64(n, (int64_t)kb + it.chunk);
+  const int R = it.nq * p.G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+
+  int lim[2];
+  uint32_t qa[D / 16][4];
+  {
+    const __half* rows[2];
+    bool ok[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = g + 8 * hr;
+      ok[hr] = r < R;
+      const int pos = ok[hr] ? r / p.G : 0;
+      const int gg = ok[hr] ? r % p.G : 0;
+      rows[hr] = p.q + (int64_t)(cu0 + pos) * p.q_stride + (int64_t)(h * p.G + gg) * D;
+      lim[hr] = ok[hr] ? (int)min64((int64_t)P + pos, INT32_MAX) : -1;
+    }
+    load_q_frags<D>(qa, rows[0], rows[1], ok[0], ok[1], t4);
+  }
+
+  const int nst = ke > kb ? (ke - kb + SK - 1) / SK : 0;
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  float o[DN][4];
+#pragma unroll
+  for (int i = 0; i < DN; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  bool bad = false;
+
+#pragma unroll
+  for (int s = 0; s < NSTAGE - 1; ++s) {
+    if (s < nst)
+      load_stage<D>(p, b, h, kb + s * SK, ke, sK + s * SK * D, sV + s * SK * D,
+                    sValid + s * SK, bad);
+    cp_async_commit();
+  }
+  for (int i = 0; i < nst; ++i) {
+    cp_async_wait<NSTAGE - 2>();
+    __syncthreads();
+    {
+      const int nx = i + NSTAGE - 1;
+      if (nx < nst) {
+        const int bf = nx % NSTAGE;
+        load_stage<D>(p, b, h, kb + nx * SK, ke, sK + bf * SK * D, sV + bf * SK * D,
+                      sValid + bf * SK, bad);
+      }
+      cp_async_commit();
+    }
+    const int bf = i % NSTAGE;
+    const int kw = warp * 16;
+    const int kstage = kb + i * SK;
+    if (kstage + kw < ke) {
+      const uint8_t* vld = sValid + bf * SK;
+      float s[2][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[0][e] = s[1][e] = 0.f;
+      qk_16<D>(s[0], s[1], qa, sK + bf * SK * D, kw, lane);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kk = kw + nt * 8 + 2 * t4 + (e & 1);
+          const bool ok = vld[kk] && (kstage + kk <= lim[e >> 1]);
+          s[nt][e] = ok ? s[nt][e] * p.scale_log2 : -INFINITY;
+        }
+      softmax_16<DN>(s, m_run, l_run, o);
+      uint32_t pa[4] = {pack_half2(s[0][0], s[0][1]), pack_half2(s[0][2], s[0][3]),
+                        pack_half2(s[1][0], s[1][1]), pack_half2(s[1][2], s[1][3])};
+      pv_16<D>(o, pa, sV + bf * SK * D, kw, lane);
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
+    l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
+  }
+  float* sO = reinterpret_cast<float*>(smem);  // [kWarps][16][D]
+  float* sM = sO + kWarps * 16 * D;            // [kWarps][16]
+  float* sL = sM + kWarps * 16;
+#pragma unroll
+  for (int d = 0; d < DN; ++d) {
+    const int c = d * 8 + 2 * t4;
+    *reinterpret_cast<float2*>(&sO[(warp * 16 + g) * D + c]) = make_float2(o[d][0], o[d][1]);
+    *reinterpret_cast<float2*>(&sO[(warp * 16 + g + 8) * D + c]) =
+        make_float2(o[d][2], o[d][3]);
+  }
+  if (t4 == 0) {
+    sM[warp * 16 + g] = m_run[0];
+    sM[warp * 16 + g + 8] = m_run[1];
+    sL[warp * 16 + g] = l_run[0];
+    sL[warp * 16 + g + 8] = l_run[1];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < R * D; e += kThreads) {
+    const int r = e / D, d = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sM[w * 16 + r]);
+    float num = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float wt = ex2(sM[w * 16 + r] - M);
+        num += wt * sO[(w * 16 + r) * D + d];
+        L += wt * sL[w * 16 + r];
+      }
+    }
+    const int pos = r / p.G, gg = r % p.G;
+    const int64_t prow =
+        ((int64_t)(it.slot_base + pos) * p.Hq + h * p.G + gg) * p.max_splits + it.split;
+    p.part_o[prow * D + d] = L > 0.f ? num : 0.f;
+    if (d == 0) {
+      p.part_m[prow] = L > 0.f ? M * kLn2 : kNegLarge;
+      p.part_l[prow] = L;
+    }
+  }
+  if (bad) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+}
+
+// ----------------------------------------------------------------------------------
+// Prologue: block 0 plans (one pass over the sequences), the other blocks run the
+// ScatterKV pass. The attention kernels run after it on the same stream.
+// ----------------------------------------------------------------------------------
 __device__ __forceinline__ bool seq_valid(const AttnParams& p, int b, int& lo, int& hi,
                                           int& P) {
   lo = p.cu[b];
@@ -492,137 +808,147 @@ __device__ __forceinline__ bool seq_valid(const AttnParams& p, int b, int& lo, i
   return lo >= 0 && hi >= lo && hi <= p.T && P >= 0;
 }
 
-// inclusive block scan of three counters
-__device__ void block_scan3(int& a, int& b, int& c, int& ta, int& tb, int& tc) {
-  __shared__ int sa[kPlanThreads], sb[kPlanThreads], sc[kPlanThreads];
-  const int tid = threadIdx.x;
-  sa[tid] = a;
-  sb[tid] = b;
-  sc[tid] = c;
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    int xa = 0, xb = 0, xc = 0;
-    if (tid >= off) {
-      xa = sa[tid - off];
-      xb = sb[tid - off];
-      xc = sc[tid - off];
-    }
-    __syncthreads();
-    sa[tid] += xa;
-    sb[tid] += xb;
-    sc[tid] += xc;
-    __syncthreads();
+// exclusive scan over the 256 threads of the block; *total gets the block sum
+__device__ int block_scan(int v, int* total) {
+  __shared__ int warp_tot[kPrologueThreads / 32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  a = sa[tid];
-  b = sb[tid];
-  c = sc[tid];
-  ta = sa[kPlanThreads - 1];
-  tb = sb[kPlanThreads - 1];
-  tc = sc[kPlanThreads - 1];
+  if (lane == 31) warp_tot[w] = x;
   __syncthreads();
+  if (w == 0) {
+    int t = lane < kPrologueThreads / 32 ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < kPrologueThreads / 32) warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const int base = w > 0 ? warp_tot[w - 1] : 0;
+  *total = warp_tot[kPrologueThreads / 32 - 1];
+  __syncthreads();
+  return base + x - v;
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnParams p) {
+__device__ void plan_block(const AttnParams& p) {
   const int tid = threadIdx.x;
-  __shared__ unsigned long long s_keys;
-  __shared__ int s_bad, s_bad_block;
+  __shared__ int s_maxst, s_bad, s_badblk;
   if (tid == 0) {
-    s_keys = 0ull;
+    s_maxst = 0;
     s_bad = 0;
-    s_bad_block = 0;
+    s_badblk = 0;
   }
   __syncthreads();
-  // total keys of the split-KV sequences, for the automatic split size
-  unsigned long long keys = 0;
-  for (int b = tid; b < p.B; b += kPlanThreads) {
-    int lo, hi, P;
-    if (seq_valid(p, b, lo, hi, P)) {
-      const int N = hi - lo;
-      if (N >= 1 && N <= p.dec_rows) keys += (unsigned long long)seq_keys(p, P, N);
-      if (N >= 1 && (int64_t)P + N > (int64_t)p.MB * p.BS) s_bad_block = 1;
-    } else {
-      s_bad = 1;
-    }
-  }
-  atomicAdd(&s_keys, keys);
-  __syncthreads();
-  int target = p.split_min_keys;
-  if (p.split_policy == PKV_SPLIT_AUTO) {
-    // aim for ~16 waves of 2 CTAs per SM over all (split, kv head) items
-    const unsigned long long denom = (unsigned long long)p.num_sms * 2ull * 16ull;
-    const unsigned long long want = (s_keys * (unsigned long long)p.Hkv + denom - 1) / denom;
-    if (want > (unsigned long long)target) target = (int)min(want, 1ull << 30);
-  }
-
-  int base_dec = 0, base_pre = 0, base_slot = 0;
-  for (int c0 = 0; c0 < p.B; c0 += kPlanThreads) {
+  const bool sk = p.streamk != 0;
+  int run_dec = 0, run_st = 0, run_slot = 0, run_pre = 0, run_items = 0;
+  for (int c0 = 0; c0 < p.B; c0 += kPrologueThreads) {
     const int b = c0 + tid;
-    int nd = 0, np = 0, ns = 0, S = 0, chunk = 0, N = 0, lo = 0, hi = 0, P = 0;
-    if (b < p.B && seq_valid(p, b, lo, hi, P)) {
-      N = hi - lo;
-      if (N >= 1 && N <= p.dec_rows) {
-        const int n = seq_keys(p, P, N);
-        if (p.split_policy == PKV_SPLIT_AUTO)
-          S = (n + target - 1) / target;
-        else
-          S = p.fixed_splits;
-        S = max(1, min(S, p.max_splits));
-        chunk = (n + S - 1) / S;
-        chunk = (chunk + kStageKeys - 1) / kStageKeys * kStageKeys;
-        S = (n + chunk - 1) / chunk;
-        nd = S;
-        ns = N;
-      } else if (N > p.dec_rows) {
-        np = (N + p.pre_rows - 1) / p.pre_rows;
+    int lo = 0, hi = 0, P = 0, N = 0;
+    int is_dec = 0, st = 0, nslot = 0, tiles = 0, S = 0, chunk = 0, n = 0;
+    if (b < p.B) {
+      if (seq_valid(p, b, lo, hi, P)) {
+        N = hi - lo;
+        if (N >= 1 && (int64_t)P + N > (int64_t)p.MB * p.BS) s_badblk = 1;
+        if (N >= 1 && N <= p.dec_rows) {
+          is_dec = 1;
+          n = seq_keys(p, P, N);
+          nslot = N;
+          if (sk) {
+            st = (n + 15) / 16;
+          } else {
+            S = max(1, min(p.fixed_splits, p.max_splits));
+            chunk = (n + S - 1) / S;
+            chunk = (chunk + kStageKeys - 1) / kStageKeys * kStageKeys;
+            S = (n + chunk - 1) / chunk;
+          }
+        } else if (N > p.dec_rows) {
+          tiles = (N + p.pre_rows - 1) / p.pre_rows;
+        }
+      } else {
+        s_bad = 1;
       }
     }
-    int od = nd, op = np, os = ns, td, tp, ts;
-    block_scan3(od, op, os, td, tp, ts);
-    od -= nd;
-    op -= np;
-    os -= ns;
-    // writes stay inside the host-computed bounds even when overlapping (invalid) cu
-    // ranges claim more tokens than exist
-    nd = (int)max64(0, min64(nd, p.dec_bound - base_dec - od));
-    np = (int)max64(0, min64(np, p.pre_bound - base_pre - op));
-    ns = (int)max64(0, min64(ns, p.slot_bound - base_slot - os));
-    if (nd > 0 && ns < N) nd = 0;   // a decode item needs all its partial slots
-    for (int s = 0; s < nd; ++s) {
-      DecodeItem itm;
-      itm.b = b;
-      itm.nq = N;
-      itm.split = s;
-      itm.nsplit = S;
-      itm.chunk = chunk;
-      itm.slot_base = base_slot + os;
-      itm.pad0 = itm.pad1 = 0;
-      p.dec_items[base_dec + od + s] = itm;
+    int t_dec, t_st, t_slot, t_pre, t_items;
+    const int o_dec = block_scan(is_dec, &t_dec);
+    const int o_st = block_scan(st, &t_st);
+    const int o_slot = block_scan(nslot, &t_slot);
+    const int o_pre = block_scan(tiles, &t_pre);
+    const int o_items = block_scan(S, &t_items);
+    // every index below stays inside its host-computed bound, even when overlapping
+    // (invalid) cu ranges claim more tokens than exist
+    const bool slot_ok = (int64_t)run_slot + o_slot + nslot <= p.slot_bound;
+    if (is_dec && slot_ok && sk && run_dec + o_dec < p.B) {
+      DecSeq d;
+      d.b = b;
+      d.n = n;
+      d.st = st;
+      d.base = p.Hkv * (run_st + o_st);
+      d.nq = N;
+      d.cu0 = lo;
+      d.P = P;
+      d.slot = run_slot + o_slot;
+      p.dec_seqs[run_dec + o_dec] = d;
+      atomicMax(&s_maxst, st);
     }
-    for (int k = 0; k < np; ++k) {   // the heaviest (latest) tile first
-      PrefillItem itm;
-      itm.b = b;
-      itm.q0 = (np - 1 - k) * p.pre_rows;
-      itm.nq = min(p.pre_rows, N - itm.q0);
-      itm.pad = 0;
-      p.pre_items[base_pre + op + k] = itm;
+    if (is_dec && slot_ok && !sk && (int64_t)run_items + o_items + S <= p.dec_bound) {
+      for (int s = 0; s < S; ++s) {
+        DecodeItem itm;
+        itm.b = b;
+        itm.nq = N;
+        itm.split = s;
+        itm.nsplit = S;
+        itm.chunk = chunk;
+        itm.slot_base = run_slot + o_slot;
+        itm.pad0 = itm.pad1 = 0;
+        p.dec_items[run_items + o_items + s] = itm;
+      }
+      for (int t = 0; t < N; ++t) {
+        p.slot_token[run_slot + o_slot + t] = lo + t;
+        p.slot_splits[run_slot + o_slot + t] = S;
+      }
     }
-    for (int t = 0; t < ns; ++t) {
-      p.slot_token[base_slot + os + t] = lo + t;
-      p.slot_splits[base_slot + os + t] = S;
+    if (tiles > 0 && (int64_t)run_pre + o_pre + tiles <= p.pre_bound) {
+      for (int k = 0; k < tiles; ++k) {   // the heaviest (latest) tile first
+        PrefillItem itm;
+        itm.b = b;
+        itm.q0 = (tiles - 1 - k) * p.pre_rows;
+        itm.nq = min(p.pre_rows, N - itm.q0);
+        itm.pad = 0;
+        p.pre_items[run_pre + o_pre + k] = itm;
+      }
     }
-    base_dec += td;
-    base_pre += tp;
-    base_slot += ts;
+    run_dec += t_dec;
+    run_st += t_st;
+    run_slot += t_slot;
+    run_pre += t_pre;
+    run_items += t_items;
   }
+  __syncthreads();
+  const int ndec = sk ? min(run_dec, p.B) : 0;
   if (tid == 0) {
-    p.counts[0] = (int)min64(base_dec, p.dec_bound);
-    p.counts[1] = (int)min64(base_pre, p.pre_bound);
-    p.counts[2] = (int)min64(base_slot, p.slot_bound);
+    const int64_t total = (int64_t)p.Hkv * run_st;
+    int64_t W = (total + p.total_warps - 1) / max(1, p.total_warps);
+    W = max64(W, kSplitMinKeysDefault / 16);
+    if (p.max_splits >= 2) W = max64(W, (s_maxst + p.max_splits - 2) / (p.max_splits - 1));
+    p.counts[kCntDecSeqs] = ndec;
+    p.counts[kCntTiles] = (int)min64(run_pre, p.pre_bound) * p.Hkv;
+    p.counts[kCntStages] = sk ? (int)total : 0;
+    p.counts[kCntTileNext] = 0;
+    p.counts[kCntW] = (int)W;
+    p.counts[kCntSplitItems] = sk ? 0 : (int)min64(run_items, p.dec_bound);
+    p.counts[kCntSlots] = (int)min64(run_slot, p.slot_bound);
     if (s_bad) flag_status(p.status, PKV_DEV_BAD_SEQUENCE);
-    if (s_bad_block) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+    if (s_badblk) flag_status(p.status, PKV_DEV_BAD_BLOCK);
   }
+  for (int i = tid; i < ndec * p.Hkv; i += kPrologueThreads) p.seg_done[i] = 0;
   // tokens that no valid sequence covers get zero output
-  for (int i = tid; i < p.T; i += kPlanThreads) {
+  for (int i = tid; i < p.T; i += kPrologueThreads) {
     int lo = 0, hi = p.B - 1, b = -1;
     while (lo <= hi) {
       const int mid = (lo + hi) >> 1;
@@ -645,48 +971,66 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(AttnParams p) {
   }
 }
 
-template <int D, int NSTAGE>
-cudaError_t launch_attention_d(const AttnParams& p, cudaStream_t s) {
-  const size_t smem = (size_t)NSTAGE * kStageKeys * D * 2 * sizeof(__half) +
-                      (size_t)NSTAGE * kStageKeys;
+__global__ void __launch_bounds__(kPrologueThreads) prologue_kernel(AttnParams p,
+                                                                    ScatterParams sp) {
+  if (blockIdx.x == 0) {
+    plan_block(p);
+    return;
+  }
+  paged_scatter_thread(sp, (int64_t)(blockIdx.x - 1) * kPrologueThreads + threadIdx.x);
+}
+
+template <int D, int NS, int NSTAGE>
+cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cudaStream_t s) {
+  constexpr size_t smem = DecodeRing<D, NS>::kBytes > TileRing<D, NSTAGE>::kBytes
+                              ? DecodeRing<D, NS>::kBytes
+                              : TileRing<D, NSTAGE>::kBytes;
+  constexpr size_t split_smem = TileRing<D, NSTAGE>::kBytes;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NSTAGE>,
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, NS, NSTAGE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prefill_kernel<D, NSTAGE>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(decode_split_kernel<D, NSTAGE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)split_smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  const int64_t scatter_threads = (int64_t)sp.T * sp.Hkv * (sp.D / 8);
   {
-    ProfScope ps("plan", s);
-    plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+    ProfScope ps("prologue", s);
+    prologue_kernel<<<(unsigned)(1 + (scatter_threads + kPrologueThreads - 1) /
+                                         kPrologueThreads),
+                      kPrologueThreads, 0, s>>>(p, sp);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (p.dec_bound > 0) {
-    ProfScope ps("decode", s);
-    decode_kernel<D, NSTAGE><<<(unsigned)(p.dec_bound * p.Hkv), kThreads, smem, s>>>(p);
+  if (!p.streamk && p.dec_bound > 0) {
+    ProfScope ps("decode_split", s);
+    decode_split_kernel<D, NSTAGE>
+        <<<(unsigned)(p.dec_bound * p.Hkv), kThreads, split_smem, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (p.pre_bound > 0) {
-    ProfScope ps("prefill", s);
-    prefill_kernel<D, NSTAGE><<<(unsigned)(p.pre_bound * p.Hkv), kThreads, smem, s>>>(p);
+  {
+    ProfScope ps("attention", s);
+    attention_kernel<D, NS, NSTAGE>
+        <<<(unsigned)(p.total_warps / kWarps), kThreads, smem, s>>>(p);
   }
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attention(const AttnParams& p, cudaStream_t s) {
+int attention_ctas_per_sm() { return kCtasPerSm; }
+
+cudaError_t launch_attention(const AttnParams& p, const ScatterParams& sp, cudaStream_t s) {
   switch (p.D) {
     case 64:
-      return launch_attention_d<64, 4>(p, s);
+      return launch_attention_d<64, 6, 4>(p, sp, s);
     case 128:
-      return launch_attention_d<128, 3>(p, s);
+      return launch_attention_d<128, 3, 3>(p, sp, s);
     default:
       return cudaErrorInvalidValue;
   }

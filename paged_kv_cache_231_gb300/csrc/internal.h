@@ -51,12 +51,32 @@ struct AppendParams {
 };
 
 // ---- attention (AttendSplitK / Attend) ----------------------------------------------
-struct DecodeItem {   // one split of one short (decoding) sequence
+struct DecodeItem {   // split mode: one split of one short (decoding) sequence
   int b, nq, split, nsplit, chunk, slot_base, pad0, pad1;
 };
 struct PrefillItem {  // one query tile of one multi-token sequence
   int b, q0, nq, pad;
 };
+struct DecSeq {       // stream-K mode: one short (decoding) sequence
+  int b;              // batch row
+  int n;              // keys its last new token sees (clamped to the block table)
+  int st;             // 16-key stages per kv head = ceil(n / 16)
+  int base;           // first global stage of (this sequence, kv head 0)
+  int nq;             // new tokens
+  int cu0;            // first token row
+  int P;              // past length
+  int slot;           // first partial slot
+};
+
+// counts[] words written by the planner
+constexpr int kCntDecSeqs = 0;    // stream-K decode sequences
+constexpr int kCntTiles = 1;      // prefill tiles = prefill items x kv heads
+constexpr int kCntStages = 2;     // total 16-key stages of the stream-K decode
+constexpr int kCntTileNext = 3;   // tile counter of the persistent kernel (zeroed)
+constexpr int kCntW = 4;          // stages per warp
+constexpr int kCntSplitItems = 5; // split mode: decode items
+constexpr int kCntSlots = 6;      // split mode: partial slots
+constexpr int kCntWords = 8;
 
 struct AttnParams {
   const __half* q;         // query head row of (token, hq) at q + token*q_stride + hq*D
@@ -73,16 +93,20 @@ struct AttnParams {
   int bs_shift;            // log2(BS) when BS is a power of two, else -1
   float scale_log2;        // softmax scale * log2(e)
   // planning
-  int split_policy, fixed_splits, max_splits, split_min_keys, num_sms;
-  int dec_rows;            // max new tokens of a sequence handled as split-KV decode
+  int streamk;             // 1: stream-K decode with fused combine; 0: split items
+  int split_policy, fixed_splits, max_splits, split_min_keys;
+  int dec_rows;            // max new tokens of a sequence handled as decode
   int pre_rows;            // query positions per prefill tile
+  int total_warps;         // warps of the persistent kernel
   // workspace
-  int32_t* counts;         // [0] decode items, [1] prefill items, [2] partial slots
-  DecodeItem* dec_items;
+  int32_t* counts;         // kCnt* words
+  DecSeq* dec_seqs;        // stream-K
+  int32_t* seg_done;       // stream-K: finished pieces per (decode sequence, kv head)
+  DecodeItem* dec_items;   // split mode
   PrefillItem* pre_items;
-  int32_t* slot_token;     // partial slot -> token
-  int32_t* slot_splits;    // partial slot -> split count
-  float* part_o;           // [(slot*Hq + hq)*max_splits + s][D]
+  int32_t* slot_token;     // split mode: partial slot -> token
+  int32_t* slot_splits;    // split mode: partial slot -> split count
+  float* part_o;           // [(slot*Hq + hq)*max_splits + piece][D]
   float* part_m;
   float* part_l;
   int64_t dec_bound, pre_bound, slot_bound;
@@ -135,7 +159,8 @@ struct SparseParams {
 // launchers (return cudaSuccess or the launch error)
 cudaError_t launch_paged_scatter(const ScatterParams& p, cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
-cudaError_t launch_attention(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_attention(const AttnParams& p, const ScatterParams& sp, cudaStream_t s);
+int attention_ctas_per_sm();
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s);
 

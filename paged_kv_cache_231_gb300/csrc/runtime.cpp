@@ -86,9 +86,10 @@ struct PagedLayout {
   int dec_rows = 1, pre_rows = 4;
   int max_splits = 1;
   int fixed_splits = 1;
+  int streamk = 0;
   int64_t dec_bound = 0, pre_bound = 0, slot_bound = 0;
-  size_t off_counts = 0, off_dec = 0, off_pre = 0, off_slot_tok = 0, off_slot_spl = 0,
-         off_po = 0, off_pm = 0, off_pl = 0, total = 0;
+  size_t off_counts = 0, off_seqs = 0, off_done = 0, off_dec = 0, off_pre = 0,
+         off_slot_tok = 0, off_slot_spl = 0, off_po = 0, off_pm = 0, off_pl = 0, total = 0;
   int pages_splits = 1;
 };
 
@@ -164,6 +165,8 @@ int check_paged(const pkv_paged_attention_args* a, bool attention, PagedLayout* 
     L->max_splits = (int)std::max<int64_t>(
         1, std::min<int64_t>(cap, ceil_div(a->max_blocks * a->block_size, min_keys)));
     L->fixed_splits = 1;
+    // stream-K decode needs room for at least two pieces per (sequence, kv head)
+    L->streamk = L->max_splits >= 2 ? 1 : 0;
   } else if (a->split_policy == PKV_SPLIT_PAGES) {
     L->max_splits = L->pages_splits;
     L->fixed_splits = L->pages_splits;
@@ -174,23 +177,29 @@ int check_paged(const pkv_paged_attention_args* a, bool attention, PagedLayout* 
   L->dec_rows = (int)(16 / G);
   L->pre_rows = 4 * L->dec_rows;
   const int64_t T = a->num_tokens, B = a->batch;
-  L->dec_bound = B * L->max_splits;
+  L->dec_bound = L->streamk ? 0 : B * L->max_splits;
   L->pre_bound = ceil_div(T, L->pre_rows) + std::min<int64_t>(B, T / (L->dec_rows + 1));
   L->slot_bound = std::min<int64_t>(T, B * L->dec_rows);
-  if (L->dec_bound * a->kv_num_heads > INT32_MAX || L->pre_bound * a->kv_num_heads > INT32_MAX)
+  // stage indices and grid sizes must fit in int32
+  if (a->kv_num_heads * B * ceil_div(a->max_blocks * a->block_size, 16) > INT32_MAX / 2 ||
+      L->dec_bound * a->kv_num_heads > INT32_MAX || L->pre_bound * a->kv_num_heads > INT32_MAX)
     return PKV_ERR_UNSUPPORTED;
   const int64_t prow = L->slot_bound * a->num_heads * L->max_splits;
   size_t off = 0;
   L->off_counts = off;
-  off += align_up(16);
+  off += align_up(4 * kCntWords);
+  L->off_seqs = off;
+  off += align_up(L->streamk ? sizeof(DecSeq) * (size_t)B : 0);
+  L->off_done = off;
+  off += align_up(L->streamk ? 4 * (size_t)B * a->kv_num_heads : 0);
   L->off_dec = off;
   off += align_up(sizeof(DecodeItem) * (size_t)L->dec_bound);
   L->off_pre = off;
   off += align_up(sizeof(PrefillItem) * (size_t)L->pre_bound);
   L->off_slot_tok = off;
-  off += align_up(4 * (size_t)L->slot_bound);
+  off += align_up(L->streamk ? 0 : 4 * (size_t)L->slot_bound);
   L->off_slot_spl = off;
-  off += align_up(4 * (size_t)L->slot_bound);
+  off += align_up(L->streamk ? 0 : 4 * (size_t)L->slot_bound);
   L->off_po = off;
   off += align_up(4 * (size_t)prow * a->head_size);
   L->off_pm = off;
@@ -368,8 +377,6 @@ int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
 
   ScatterParams sp{};
   fill_scatter(args, L.mode, sp);
-  cudaError_t e = launch_paged_scatter(sp, s);
-  if (e != cudaSuccess) return PKV_ERR_LAUNCH;
 
   AttnParams ap{};
   ap.q = static_cast<const __half*>(args->query);
@@ -394,14 +401,17 @@ int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
   const double scale = args->scale != 0.f ? (double)args->scale
                                           : 1.0 / std::sqrt((double)args->head_size);
   ap.scale_log2 = (float)(scale * 1.4426950408889634);
+  ap.streamk = L.streamk;
   ap.split_policy = args->split_policy;
   ap.fixed_splits = L.fixed_splits;
   ap.max_splits = L.max_splits;
   ap.split_min_keys = args->split_min_keys > 0 ? args->split_min_keys : kSplitMinKeysDefault;
-  ap.num_sms = num_sms_current();
   ap.dec_rows = L.dec_rows;
   ap.pre_rows = L.pre_rows;
+  ap.total_warps = num_sms_current() * attention_ctas_per_sm() * 4;
   ap.counts = reinterpret_cast<int32_t*>(ws + L.off_counts);
+  ap.dec_seqs = reinterpret_cast<DecSeq*>(ws + L.off_seqs);
+  ap.seg_done = reinterpret_cast<int32_t*>(ws + L.off_done);
   ap.dec_items = reinterpret_cast<DecodeItem*>(ws + L.off_dec);
   ap.pre_items = reinterpret_cast<PrefillItem*>(ws + L.off_pre);
   ap.slot_token = reinterpret_cast<int32_t*>(ws + L.off_slot_tok);
@@ -412,10 +422,10 @@ int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
   ap.dec_bound = L.dec_bound;
   ap.pre_bound = L.pre_bound;
   ap.slot_bound = L.slot_bound;
-  e = launch_attention(ap, s);
+  cudaError_t e = launch_attention(ap, sp, s);
   if (e != cudaSuccess) return PKV_ERR_LAUNCH;
 
-  if (L.slot_bound > 0) {
+  if (!L.streamk && L.slot_bound > 0) {
     CombineParams cp{};
     cp.o = ap.part_o;
     cp.m = ap.part_m;
@@ -430,7 +440,7 @@ int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
     cp.out_f16 = 1;
     cp.slot_token = ap.slot_token;
     cp.slot_splits = ap.slot_splits;
-    cp.slot_count = ap.counts + 2;
+    cp.slot_count = ap.counts + kCntSlots;
     cp.Hq = ap.Hq;
     e = launch_combine(cp, s);
     if (e != cudaSuccess) return PKV_ERR_LAUNCH;

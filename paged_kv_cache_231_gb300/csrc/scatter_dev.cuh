@@ -1,0 +1,127 @@
+// Device code of the ScatterKV pass, shared by the standalone scatter kernel and the
+// attention prologue kernel (which plans in block 0 and scatters in the others).
+//
+// "com.microsoft.PagedAttention manifest.json", ScatterKV: each new token's K and V
+// rows go to the paged cache [num_blocks, block_size, kv_heads, head] at the row
+// slot_mapping names, or at the block-table row of the token's absolute position
+// past + t. Optionally the key is first rotated at that position with the rotation
+// rule of "com.microsoft.SparseAttention sparse-kv-append.wgsl.jinja" (sparse_rotary).
+#pragma once
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+// rotated value of component d of a head row held as 8-element chunk `own` starting at
+// d0, reading a partner outside the chunk from `row` (global memory).
+__device__ __forceinline__ void rotate_chunk(__half (&x)[8], const __half* row, int d0,
+                                             int64_t pos, const __half* cos_t,
+                                             const __half* sin_t, int rotary_dim,
+                                             int interleaved) {
+  const int half = rotary_dim / 2;
+  float out[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int d = d0 + e;
+    const float own = __half2float(x[e]);
+    out[e] = own;
+    if (d < rotary_dim) {
+      int slot, partner;
+      bool first;
+      if (interleaved) {
+        slot = d >> 1;
+        first = (d & 1) == 0;
+        partner = first ? d + 1 : d - 1;
+      } else {
+        first = d < half;
+        slot = first ? d : d - half;
+        partner = first ? d + half : d - half;
+      }
+      const float pv = (partner >= d0 && partner < d0 + 8)
+                           ? __half2float(x[partner - d0])
+                           : __half2float(row[partner]);
+      const float cs = __half2float(cos_t[pos * half + slot]);
+      const float sn = __half2float(sin_t[pos * half + slot]);
+      out[e] = first ? own * cs - pv * sn : own * cs + pv * sn;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) x[e] = __float2half_rn(out[e]);
+}
+
+// One thread of the ScatterKV pass: 16-byte chunk `gid` of the (token, kv head, chunk)
+// grid moves K (rotated when asked) and V into the paged cache.
+__device__ __forceinline__ void paged_scatter_thread(const ScatterParams& p, int64_t gid) {
+  const int CPR = p.D / 8;
+  const int64_t total = (int64_t)p.T * p.Hkv * CPR;
+  if (gid >= total) return;
+  const int c = (int)(gid % CPR);
+  const int64_t rh = gid / CPR;
+  const int h = (int)(rh % p.Hkv);
+  const int i = (int)(rh / p.Hkv);
+
+  // sequence of token i: the last b with cu[b] <= i
+  int lo = 0, hi = p.B - 1, b = -1;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if (p.cu[mid] <= i) {
+      b = mid;
+      lo = mid + 1;
+    } else {
+      hi = mid - 1;
+    }
+  }
+  if (b < 0) return;
+  const int s0 = p.cu[b], s1 = p.cu[b + 1], P = p.past[b];
+  const bool valid = s0 >= 0 && s1 >= s0 && s1 <= p.T && P >= 0;
+  if (!valid) {
+    if (c == 0 && h == 0) flag_status(p.status, PKV_DEV_BAD_SEQUENCE);
+    return;
+  }
+  if (i >= s1) return;  // token past the last sequence: not part of the batch
+  const int64_t pos = (int64_t)P + (i - s0);
+
+  int64_t blk, off;
+  if (p.slot_mapping) {
+    const int slot = p.slot_mapping[i];
+    if (slot < 0) return;  // padding
+    blk = slot / p.BS;
+    off = slot % p.BS;
+    if (blk >= p.NB) {
+      if (c == 0) flag_status(p.status, PKV_DEV_BAD_SLOT);
+      return;
+    }
+  } else {
+    const int64_t col = pos / p.BS;
+    if (col >= p.MB) {
+      if (c == 0) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+      return;
+    }
+    blk = p.block_table[(int64_t)b * p.MB + col];
+    off = pos % p.BS;
+    if (blk < 0 || blk >= p.NB) {
+      if (c == 0) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+      return;
+    }
+  }
+  if (p.rotary_dim > 0 && pos >= p.rotary_positions) {
+    if (c == 0) flag_status(p.status, PKV_DEV_BAD_POSITION);
+    return;
+  }
+  const __half* krow = p.k_src + (int64_t)i * p.src_stride + (int64_t)h * p.D;
+  const __half* vrow = p.v_src + (int64_t)i * p.src_stride + (int64_t)h * p.D;
+  const int64_t dst = ((blk * p.BS + off) * p.Hkv + h) * p.D + c * 8;
+  uint4 kv = *reinterpret_cast<const uint4*>(krow + c * 8);
+  const uint4 vv = *reinterpret_cast<const uint4*>(vrow + c * 8);
+  if (p.rotary_dim > 0 && c * 8 < p.rotary_dim) {
+    __half x[8];
+    *reinterpret_cast<uint4*>(x) = kv;
+    rotate_chunk(x, krow, c * 8, pos, p.cos, p.sin, p.rotary_dim, p.interleaved);
+    kv = *reinterpret_cast<uint4*>(x);
+  }
+  *reinterpret_cast<uint4*>(p.kc + dst) = kv;
+  *reinterpret_cast<uint4*>(p.vc + dst) = vv;
+}
+
+}  // namespace pkv

@@ -232,12 +232,15 @@ def test_workspace_bounds(lib):
                              num_heads=32, kv_num_heads=8)
     plan = B.pkv_paged_attention_plan(args)
     assert plan.max_splits == 16 and plan.group_size == 4
-    assert plan.partial_slot_bound == 64 and plan.decode_item_bound == 64 * 16
+    # the automatic policy runs the stream-K decode: no per-split items, partial rows
+    # for up to 16 pieces of every (token, query head)
+    assert plan.partial_slot_bound == 64 and plan.decode_item_bound == 0
     assert plan.workspace_bytes >= 64 * 32 * 16 * (128 + 2) * 4
     assert B.pkv_paged_attention_workspace_size(args) == plan.workspace_bytes
     # fixed split policy bounds the splits
     args.split_policy, args.fixed_splits = B.PKV_SPLIT_FIXED, 3
-    assert B.pkv_paged_attention_plan(args).max_splits == 3
+    plan = B.pkv_paged_attention_plan(args)
+    assert plan.max_splits == 3 and plan.decode_item_bound == 64 * 3
     args.split_policy = B.PKV_SPLIT_PAGES
     assert B.pkv_paged_attention_plan(args).max_splits == orc.pages_num_splits(64, 8, 512, 16)
 
