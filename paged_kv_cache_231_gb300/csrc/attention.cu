@@ -838,11 +838,14 @@ __device__ int block_scan(int v, int* total) {
 
 __device__ void plan_block(const AttnParams& p) {
   const int tid = threadIdx.x;
-  __shared__ int s_maxst, s_bad, s_badblk;
+  // s_w*: extent of what was actually written. Every write condition below is monotone
+  // in the scan offsets, so the written entries form a prefix of each array.
+  __shared__ int s_maxst, s_bad, s_badblk, s_wdec, s_wst, s_witems, s_wslot, s_wpre;
   if (tid == 0) {
     s_maxst = 0;
     s_bad = 0;
     s_badblk = 0;
+    s_wdec = s_wst = s_witems = s_wslot = s_wpre = 0;
   }
   __syncthreads();
   const bool sk = p.streamk != 0;
@@ -883,7 +886,19 @@ __device__ void plan_block(const AttnParams& p) {
     // every index below stays inside its host-computed bound, even when overlapping
     // (invalid) cu ranges claim more tokens than exist
     const bool slot_ok = (int64_t)run_slot + o_slot + nslot <= p.slot_bound;
-    if (is_dec && slot_ok && sk && run_dec + o_dec < p.B) {
+    const bool dec_ok =
+        is_dec && slot_ok &&
+        (sk ? run_dec + o_dec < p.B : (int64_t)run_items + o_items + S <= p.dec_bound);
+    if (dec_ok) {
+      atomicMax(&s_wslot, run_slot + o_slot + nslot);
+      if (sk) {
+        atomicMax(&s_wdec, run_dec + o_dec + 1);
+        atomicMax(&s_wst, run_st + o_st + st);
+      } else {
+        atomicMax(&s_witems, run_items + o_items + S);
+      }
+    }
+    if (dec_ok && sk) {
       DecSeq d;
       d.b = b;
       d.n = n;
@@ -896,7 +911,7 @@ __device__ void plan_block(const AttnParams& p) {
       p.dec_seqs[run_dec + o_dec] = d;
       atomicMax(&s_maxst, st);
     }
-    if (is_dec && slot_ok && !sk && (int64_t)run_items + o_items + S <= p.dec_bound) {
+    if (dec_ok && !sk) {
       for (int s = 0; s < S; ++s) {
         DecodeItem itm;
         itm.b = b;
@@ -914,6 +929,7 @@ __device__ void plan_block(const AttnParams& p) {
       }
     }
     if (tiles > 0 && (int64_t)run_pre + o_pre + tiles <= p.pre_bound) {
+      atomicMax(&s_wpre, run_pre + o_pre + tiles);
       for (int k = 0; k < tiles; ++k) {   // the heaviest (latest) tile first
         PrefillItem itm;
         itm.b = b;
@@ -930,19 +946,19 @@ __device__ void plan_block(const AttnParams& p) {
     run_items += t_items;
   }
   __syncthreads();
-  const int ndec = sk ? min(run_dec, p.B) : 0;
+  const int ndec = sk ? s_wdec : 0;
   if (tid == 0) {
-    const int64_t total = (int64_t)p.Hkv * run_st;
+    const int64_t total = (int64_t)p.Hkv * s_wst;
     int64_t W = (total + p.total_warps - 1) / max(1, p.total_warps);
     W = max64(W, kSplitMinKeysDefault / 16);
     if (p.max_splits >= 2) W = max64(W, (s_maxst + p.max_splits - 2) / (p.max_splits - 1));
     p.counts[kCntDecSeqs] = ndec;
-    p.counts[kCntTiles] = (int)min64(run_pre, p.pre_bound) * p.Hkv;
+    p.counts[kCntTiles] = s_wpre * p.Hkv;
     p.counts[kCntStages] = sk ? (int)total : 0;
     p.counts[kCntTileNext] = 0;
     p.counts[kCntW] = (int)W;
-    p.counts[kCntSplitItems] = sk ? 0 : (int)min64(run_items, p.dec_bound);
-    p.counts[kCntSlots] = (int)min64(run_slot, p.slot_bound);
+    p.counts[kCntSplitItems] = sk ? 0 : s_witems;
+    p.counts[kCntSlots] = s_wslot;
     if (s_bad) flag_status(p.status, PKV_DEV_BAD_SEQUENCE);
     if (s_badblk) flag_status(p.status, PKV_DEV_BAD_BLOCK);
   }
