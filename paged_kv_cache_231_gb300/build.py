@@ -50,6 +50,8 @@ def build(force: bool = False, verbose: bool = False, debug: bool = False) -> st
               "-I", CSRC] + ARCH
     if debug:
         common += ["-DPKV_DEBUG=1"]
+    # extra definitions for tuning builds, e.g. "-DPKV_DEC_STAGES=6 -DPKV_CTAS_PER_SM=1"
+    common += os.environ.get("PKV_NVCC_DEFINES", "").split()
     deps = _deps()
     jobs = []
     objs = []

@@ -29,9 +29,22 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 128;  // 4 warps per CTA
-constexpr int kWarps = 4;
-constexpr int kCtasPerSm = 2;
+// Decode ring depth (16-key stages per warp), warps per CTA and CTAs per SM of the
+// persistent kernel; overridable at build time for tuning sweeps.
+#ifndef PKV_DEC_STAGES
+#define PKV_DEC_STAGES 3
+#endif
+#ifndef PKV_WARPS
+#define PKV_WARPS 4
+#endif
+#ifndef PKV_CTAS_PER_SM
+#define PKV_CTAS_PER_SM 2
+#endif
+constexpr int kWarps = PKV_WARPS;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kCtasPerSm = PKV_CTAS_PER_SM;
+constexpr int kDecStages = PKV_DEC_STAGES;
+constexpr int kTileThreads = 128;   // prefill tiles and split items use 4 warps
 constexpr int kPrologueThreads = 256;
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -74,10 +87,10 @@ __device__ __forceinline__ void load_stage(const AttnParams& p, int b, int h, in
                                            uint8_t* sValid, bool& bad) {
   constexpr int CPR = D / 8;
   constexpr int TOTAL = kStageKeys * CPR;
-  static_assert(TOTAL % kThreads == 0, "stage must split evenly over the CTA");
+  static_assert(TOTAL % kTileThreads == 0, "stage must split evenly over 4 warps");
 #pragma unroll
-  for (int it = 0; it < TOTAL / kThreads; ++it) {
-    const int i = threadIdx.x + it * kThreads;
+  for (int it = 0; it < TOTAL / kTileThreads; ++it) {
+    const int i = threadIdx.x + it * kTileThreads;
     const int r = i / CPR;
     const int c = i % CPR;
     const int j = k0 + r;
@@ -101,32 +114,39 @@ __device__ __forceinline__ void load_stage(const AttnParams& p, int b, int h, in
   }
 }
 
-// Warp-wide: stage 16 keys [k0, k0 + 16) of (b, h) into this warp's ring slot. Two
-// lanes per key row, each copying half of the K row and half of the V row.
+// Warp-wide block-table lookup for a 16-key stage: lane r < 16 returns the element
+// offset of key k0 + r of (b, h), or -1 when the key is past kend or unmapped.
+__device__ __forceinline__ int64_t stage_row_offset(const AttnParams& p, int b, int h, int k0,
+                                                    int kend, int lane, bool& bad) {
+  if (lane >= 16) return -1;
+  const int j = k0 + lane;
+  if (j >= kend) return -1;
+  const int64_t off = key_row_offset(p, b, h, j);
+  if (off < 0) bad = true;
+  return off;
+}
+
+// Warp-wide copy of a 16-key stage whose row offsets lanes 0..15 hold: each
+// instruction moves whole 256-byte rows (consecutive lanes, consecutive 16-byte
+// chunks), so every 32-byte sector is requested once.
 template <int D>
-__device__ __forceinline__ void warp_load16(const AttnParams& p, int b, int h, int k0,
-                                            int kend, __half* sK, __half* sV,
-                                            uint8_t* sValid, int lane, bool& bad) {
-  constexpr int CPL = D / 16;  // chunks per lane
-  const int r = lane >> 1;
-  const int c0 = (lane & 1) * CPL;
-  const int j = k0 + r;
-  int64_t off = -1;
-  if (j < kend) {
-    off = key_row_offset(p, b, h, j);
-    if (off < 0) bad = true;
-  }
-  const int nb = off >= 0 ? 16 : 0;
-  const __half* gk = off >= 0 ? p.kc + off : p.kc;
-  const __half* gv = off >= 0 ? p.vc + off : p.vc;
+__device__ __forceinline__ void warp_copy16(const AttnParams& p, int64_t my_off, __half* sK,
+                                            __half* sV, uint8_t* sValid, int lane) {
+  constexpr int CPR = D / 8;        // chunks per row
+  constexpr int RPI = 32 / CPR;     // rows per instruction
+  const int c = lane % CPR;
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-    const int cc = c0 + c;
-    const int sidx = Tile<D>::chunk(r, cc) * 8;
-    cp_async_16(sK + sidx, nb ? gk + cc * 8 : gk, nb);
-    cp_async_16(sV + sidx, nb ? gv + cc * 8 : gv, nb);
+  for (int i = 0; i < 16 / RPI; ++i) {
+    const int r = i * RPI + lane / CPR;
+    const long long off = __shfl_sync(0xffffffffu, (long long)my_off, r);
+    const int nb = off >= 0 ? 16 : 0;
+    const __half* gk = off >= 0 ? p.kc + off + c * 8 : p.kc;
+    const __half* gv = off >= 0 ? p.vc + off + c * 8 : p.vc;
+    const int sidx = Tile<D>::chunk(r, c) * 8;
+    cp_async_16(sK + sidx, gk, nb);
+    cp_async_16(sV + sidx, gv, nb);
   }
-  if ((lane & 1) == 0) sValid[r] = off >= 0 ? 1 : 0;
+  if (lane < 16) sValid[lane] = my_off >= 0 ? 1 : 0;
 }
 
 __device__ __forceinline__ uint32_t ld_half2(const __half* ptr) {
@@ -396,14 +416,18 @@ __device__ void decode_phase(const AttnParams& p, unsigned char* wsm, int gw, in
   __half* rV = rK + NS * 16 * D;
   uint8_t* rValid = reinterpret_cast<uint8_t*>(rV + NS * 16 * D);
 
+  // pc: the next stage to issue; la_off: its row offsets, looked up one iteration
+  // ahead so the block-table latency hides behind the current stage
   Cursor pc = locate(p, (int)g0, ndec);
   Cursor cc = pc;
+  int64_t la_off = stage_row_offset(p, pc.d.b, pc.h, pc.s * 16, pc.d.n, lane, bad);
 #pragma unroll
   for (int k = 0; k < NS - 1; ++k) {
     if (k < nst) {
-      warp_load16<D>(p, pc.d.b, pc.h, pc.s * 16, pc.d.n, rK + k * 16 * D, rV + k * 16 * D,
-                     rValid + k * 16, lane, bad);
+      warp_copy16<D>(p, la_off, rK + k * 16 * D, rV + k * 16 * D, rValid + k * 16, lane);
       advance(p, pc, ndec);
+      if (k + 1 < nst)
+        la_off = stage_row_offset(p, pc.d.b, pc.h, pc.s * 16, pc.d.n, lane, bad);
     }
     cp_async_commit();
   }
@@ -422,9 +446,10 @@ __device__ void decode_phase(const AttnParams& p, unsigned char* wsm, int gw, in
     __syncwarp();
     if (k + NS - 1 < nst) {
       const int bf = (k + NS - 1) % NS;
-      warp_load16<D>(p, pc.d.b, pc.h, pc.s * 16, pc.d.n, rK + bf * 16 * D, rV + bf * 16 * D,
-                     rValid + bf * 16, lane, bad);
+      warp_copy16<D>(p, la_off, rK + bf * 16 * D, rV + bf * 16 * D, rValid + bf * 16, lane);
       advance(p, pc, ndec);
+      if (k + NS < nst)
+        la_off = stage_row_offset(p, pc.d.b, pc.h, pc.s * 16, pc.d.n, lane, bad);
     }
     cp_async_commit();
     const int bf = k % NS;
@@ -460,6 +485,11 @@ __device__ void decode_phase(const AttnParams& p, unsigned char* wsm, int gw, in
   }
   cp_async_wait<0>();
   __syncwarp();
+}
+
+// barrier of the 4 warps that work on a prefill tile (named barrier 1, 128 threads)
+__device__ __forceinline__ void tile_sync() {
+  asm volatile("bar.sync 1, 128;\n" ::: "memory");
 }
 
 // ----------------------------------------------------------------------------------
@@ -526,7 +556,7 @@ __device__ void prefill_tile(const AttnParams& p, unsigned char* smem, int item_
   }
   for (int i = 0; i < nst; ++i) {
     cp_async_wait<NSTAGE - 2>();
-    __syncthreads();
+    tile_sync();
     {
       const int nx = i + NSTAGE - 1;
       if (nx < nst) {
@@ -629,6 +659,8 @@ struct TileRing {
       (size_t)NSTAGE * kStageKeys * D * 2 * 2 + NSTAGE * kStageKeys;
 };
 
+static_assert(kWarps >= 4, "prefill tiles need at least 4 warps");
+
 template <int D, int NS, int NSTAGE>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) attention_kernel(AttnParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -645,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attention_kernel(AttnPar
     const int t = s_tile;
     __syncthreads();
     if (t >= ntiles) break;
-    prefill_tile<D, NSTAGE>(p, smem, t / p.Hkv, t % p.Hkv, bad);
+    if (warp < 4) prefill_tile<D, NSTAGE>(p, smem, t / p.Hkv, t % p.Hkv, bad);
   }
   if (bad) flag_status(p.status, PKV_DEV_BAD_BLOCK);
 }
@@ -656,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attention_kernel(AttnPar
 // partials are merged by the combine kernel.
 // ----------------------------------------------------------------------------------
 template <int D, int NSTAGE>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(AttnParams p) {
+__global__ void __launch_bounds__(kTileThreads) decode_split_kernel(AttnParams p) {
   constexpr int SK = kStageKeys;
   constexpr int DN = D / 8;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -770,7 +802,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(AttnParams p) {
     sL[warp * 16 + g + 8] = l_run[1];
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < R * D; e += kThreads) {
+  for (int e = threadIdx.x; e < R * D; e += kTileThreads) {
     const int r = e / D, d = e % D;
     float M = -INFINITY;
 #pragma unroll
@@ -963,8 +995,10 @@ __device__ void plan_block(const AttnParams& p) {
     if (s_badblk) flag_status(p.status, PKV_DEV_BAD_BLOCK);
   }
   for (int i = tid; i < ndec * p.Hkv; i += kPrologueThreads) p.seg_done[i] = 0;
-  // tokens that no valid sequence covers get zero output
-  for (int i = tid; i < p.T; i += kPrologueThreads) {
+  // tokens that no valid sequence covers get zero output; when every sequence is
+  // valid and cu runs from 0 to T, cu is monotone and covers every token
+  const bool all_covered = s_bad == 0 && p.cu[0] == 0 && p.cu[p.B] == p.T;
+  for (int i = tid; !all_covered && i < p.T; i += kPrologueThreads) {
     int lo = 0, hi = p.B - 1, b = -1;
     while (lo <= hi) {
       const int mid = (lo + hi) >> 1;
@@ -1025,7 +1059,7 @@ cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cud
   if (!p.streamk && p.dec_bound > 0) {
     ProfScope ps("decode_split", s);
     decode_split_kernel<D, NSTAGE>
-        <<<(unsigned)(p.dec_bound * p.Hkv), kThreads, split_smem, s>>>(p);
+        <<<(unsigned)(p.dec_bound * p.Hkv), kTileThreads, split_smem, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1040,13 +1074,14 @@ cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cud
 }  // namespace
 
 int attention_ctas_per_sm() { return kCtasPerSm; }
+int attention_warps_per_cta() { return kWarps; }
 
 cudaError_t launch_attention(const AttnParams& p, const ScatterParams& sp, cudaStream_t s) {
   switch (p.D) {
     case 64:
-      return launch_attention_d<64, 6, 4>(p, sp, s);
+      return launch_attention_d<64, 2 * kDecStages, 4>(p, sp, s);
     case 128:
-      return launch_attention_d<128, 3, 3>(p, sp, s);
+      return launch_attention_d<128, kDecStages, 3>(p, sp, s);
     default:
       return cudaErrorInvalidValue;
   }

@@ -161,6 +161,7 @@ cudaError_t launch_paged_scatter(const ScatterParams& p, cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, const ScatterParams& sp, cudaStream_t s);
 int attention_ctas_per_sm();
+int attention_warps_per_cta();
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s);
 

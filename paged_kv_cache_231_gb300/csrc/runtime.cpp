@@ -408,7 +408,7 @@ int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
   ap.split_min_keys = args->split_min_keys > 0 ? args->split_min_keys : kSplitMinKeysDefault;
   ap.dec_rows = L.dec_rows;
   ap.pre_rows = L.pre_rows;
-  ap.total_warps = num_sms_current() * attention_ctas_per_sm() * 4;
+  ap.total_warps = num_sms_current() * attention_ctas_per_sm() * attention_warps_per_cta();
   ap.counts = reinterpret_cast<int32_t*>(ws + L.off_counts);
   ap.dec_seqs = reinterpret_cast<DecSeq*>(ws + L.off_seqs);
   ap.seg_done = reinterpret_cast<int32_t*>(ws + L.off_done);
