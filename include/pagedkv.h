@@ -178,6 +178,25 @@ int pkv_paged_attention_workspace_size(const pkv_paged_attention_args* args,
 int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* Paged attention without a caller-provided workspace. The pages have no counterpart
+ * to this call: it serves callers that may not allocate device memory (for example an
+ * engine plugin whose enqueue step must not allocate, or a framework that has given
+ * all device memory to its own pool). Scratch comes from a __device__ array of
+ * PKV_STATIC_WORKSPACE_BYTES inside this library, which every GPU that loads the
+ * library holds until the process exits; the call itself allocates nothing.
+ *   - Same arguments, results and status codes as pkv_paged_attention; returns
+ *     PKV_ERR_WORKSPACE when pkv_paged_attention_workspace_size exceeds
+ *     PKV_STATIC_WORKSPACE_BYTES.
+ *   - The first call on a device looks up the array's device address (a runtime
+ *     call, once per device, with that device current): make that first call before
+ *     any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero. Calls whose work overlaps on the GPU (other
+ *     streams, other threads) race on it: serialise them. */
+#define PKV_STATIC_WORKSPACE_BYTES (32u << 20)
+int pkv_paged_attention_static_workspace(const pkv_paged_attention_args* args,
+                                         void* stream);
+
 /* The ScatterKV pass alone (same argument block; query is read only in packed mode,
  * output and the attention fields are ignored). Bit-exact copy when rotary_dim == 0. */
 int pkv_paged_scatter_kv(const pkv_paged_attention_args* args, void* stream);

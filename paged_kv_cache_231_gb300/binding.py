@@ -511,3 +511,24 @@ def pkv_profiler_query(kernel: str):
 
 def default_scale(head_size: int) -> float:
     return 1.0 / math.sqrt(head_size)
+
+
+def pkv_paged_attention_static_workspace(query, key, value, key_cache, value_cache,
+                                         cumulative_sequence_length, past_seqlens,
+                                         block_table, slot_mapping=None, *, num_heads: int,
+                                         kv_num_heads: int, scale: float = 0.0,
+                                         output, device_status=None, stream=None, **kw):
+    """Paged attention for callers that may not allocate device memory: scratch comes
+    from the library's fixed device array (PKV_STATIC_WORKSPACE_BYTES per GPU), so this
+    call allocates nothing, not even the output, which the caller passes in. Calls that
+    overlap on the GPU share that array and must be serialised."""
+    lib = load_library()
+    fn = lib.pkv_paged_attention_static_workspace
+    fn.restype = c_i32
+    fn.argtypes = [ctypes.POINTER(PagedAttentionArgs), c_vp]
+    a = make_paged_args(query, key, value, key_cache, value_cache,
+                        cumulative_sequence_length, past_seqlens, block_table, slot_mapping,
+                        output, num_heads=num_heads, kv_num_heads=kv_num_heads, scale=scale,
+                        device_status=device_status, **kw)
+    _check("pkv_paged_attention_static_workspace", fn(ctypes.byref(a), _stream(stream)))
+    return output

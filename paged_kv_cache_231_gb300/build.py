@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
-SOURCES = ["runtime.cpp", "attention.cu", "scatter.cu", "combine.cu", "sparse.cu"]
+SOURCES = ["runtime.cpp", "attention.cu", "scatter.cu", "combine.cu", "sparse.cu",
+           "static_workspace.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
