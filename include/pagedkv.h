@@ -72,6 +72,9 @@ typedef enum pkv_status {
                                     unmapped; an edge whose q_idx, head, batch or
                                     block lies outside the tensors gets the empty
                                     partial */
+#define PKV_DEV_TIMEOUT 32u      /* a bounded wait on the tensor core gave up: the
+                                    affected prefill tile's output is not written and
+                                    the kernel freed its resources and returned */
 
 typedef enum pkv_dtype { PKV_F16 = 1, PKV_BF16 = 2, PKV_F32 = 3, PKV_I32 = 4 } pkv_dtype;
 

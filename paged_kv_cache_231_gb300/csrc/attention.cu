@@ -15,16 +15,21 @@
 //     ticket, no waiting) merges its partials into the fp16 output, so the split count
 //     adapts per sequence and the load is balanced to one stage;
 //   * prefill (many new tokens): tiles of query positions x query heads, taken by the
-//     same persistent CTAs from an atomic counter, so K/V is read once per tile;
-//   * QK^T and PV run on tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate),
-//     the score accumulators are reused in registers as the A operand of PV, and the
-//     online softmax works in base 2 (scores pre-scaled by log2 e).
+//     same persistent CTAs from an atomic counter, so K/V is read once per tile. For
+//     head size 128 a tile is 128 rows on the 5th-generation tensor core: Q, K, V and P
+//     in 128-byte-swizzled shared memory, S and O accumulators in tensor memory,
+//     tcgen05.mma issued by one thread and completed through mbarriers, one softmax
+//     thread per row reading its TMEM lane;
+//   * decode and the head-size-64 tiles run QK^T and PV on mma.sync m16n8k16 (fp16 in,
+//     fp32 accumulate) with the score accumulators reused in registers as the A
+//     operand of PV. Softmax works in base 2 (scores pre-scaled by log2 e).
 #include <limits.h>
 #include <math.h>
 
 #include "device_common.cuh"
 #include "internal.h"
 #include "scatter_dev.cuh"
+#include "tcgen05.cuh"
 
 namespace pkv {
 namespace {
@@ -35,10 +40,10 @@ namespace {
 #define PKV_DEC_STAGES 3
 #endif
 #ifndef PKV_WARPS
-#define PKV_WARPS 4
+#define PKV_WARPS 8
 #endif
 #ifndef PKV_CTAS_PER_SM
-#define PKV_CTAS_PER_SM 2
+#define PKV_CTAS_PER_SM 1
 #endif
 constexpr int kWarps = PKV_WARPS;
 constexpr int kThreads = 32 * kWarps;
@@ -646,6 +651,302 @@ __device__ void prefill_tile(const AttnParams& p, unsigned char* smem, int item_
   }
 }
 
+
+// ----------------------------------------------------------------------------------
+// Prefill tile on tcgen05 (head size 128): 128 rows = (128 / G) positions x G query
+// heads of one sequence and kv head; 128-key stages, two K/V buffers. Per stage:
+//   S = Q K^T   (tcgen05.mma, M=N=128, K-major A and B, fp32 in TMEM columns 0..127)
+//   softmax: thread r < 128 reads row r of S from TMEM, masks, exponentiates against a
+//            running max that is only raised when the new max exceeds it by more than
+//            2^8 (then O and l are rescaled), and writes P (fp16) to shared memory
+//   O += P V    (tcgen05.mma, K-major P, MN-major V, fp32 in TMEM columns 128..255)
+// ----------------------------------------------------------------------------------
+struct TcLayout {  // byte offsets from a 1024-byte-aligned base
+  static constexpr uint32_t kQ = 0;                 // 2 x [128][64] fp16 sub-tiles
+  static constexpr uint32_t kK = 32768;             // 2 stages x 32 KB
+  static constexpr uint32_t kV = kK + 65536;        // 2 stages x 32 KB
+  static constexpr uint32_t kP = kV + 65536;        // 32 KB
+  static constexpr uint32_t kValid = kP + 32768;    // 2 x 128 B key flags
+  static constexpr uint32_t kFull = kValid + 256;   // 2 x int: stage fully visible
+  static constexpr uint32_t kRowOff = kFull + 16;   // 128 x int64 row offsets
+  static constexpr uint32_t kBars = kRowOff + 1024; // mbarriers S, O
+  static constexpr uint32_t kTmem = kBars + 16;     // TMEM base address
+  static constexpr uint32_t kEnd = kTmem + 16;
+};
+constexpr uint32_t kTcWaitTries = 1u << 22;
+constexpr float kTcRescale = 8.f;   // log2 of the largest weight a stale max may give
+
+struct TcState {
+  uint32_t tmem;
+  uint32_t ph_s, ph_o;
+  bool failed;
+};
+
+// Stage keys [j*128, j*128 + 128) of (b, h) into buffer `buf` (all threads).
+__device__ __forceinline__ void tc_load_kv(const AttnParams& p, unsigned char* sm, int b,
+                                           int h, int j, int kend, int buf, bool& bad) {
+  constexpr int D = 128;
+  int64_t* rowoff = reinterpret_cast<int64_t*>(sm + TcLayout::kRowOff);
+  uint8_t* valid = sm + TcLayout::kValid + buf * 128;
+  int* full = reinterpret_cast<int*>(sm + TcLayout::kFull);
+  const int tid = threadIdx.x;
+  bool ok = true;
+  if (tid < 128) {
+    const int key = j * 128 + tid;
+    int64_t off = -1;
+    if (key < kend) {
+      off = key_row_offset(p, b, h, key);
+      if (off < 0) bad = true;
+    }
+    rowoff[tid] = off;
+    valid[tid] = off >= 0 ? 1 : 0;
+    ok = off >= 0;
+  }
+  const int all = __syncthreads_and(ok ? 1 : 0);
+  if (tid == 0) full[buf] = all;
+  unsigned char* Ks = sm + TcLayout::kK + buf * 32768;
+  unsigned char* Vs = sm + TcLayout::kV + buf * 32768;
+  for (int i = tid; i < 128 * 16; i += blockDim.x) {
+    const int r = i >> 4, c = i & 15;
+    const int64_t off = rowoff[r];
+    const int nb = off >= 0 ? 16 : 0;
+    const uint32_t dst = (uint32_t)(c >> 3) * 16384u + tc::sw128(r, c & 7);
+    cp_async_16(Ks + dst, off >= 0 ? p.kc + off + c * 8 : p.kc, nb);
+    cp_async_16(Vs + dst, off >= 0 ? p.vc + off + c * 8 : p.vc, nb);
+  }
+  cp_async_commit();
+}
+
+__device__ void prefill_tile_tc(const AttnParams& p, unsigned char* sm, int item_idx, int h,
+                                TcState& ts, bool& bad) {
+  constexpr int D = 128;
+  const int tid = threadIdx.x;
+  const PrefillItem it = p.pre_items[item_idx];
+  const int b = it.b;
+  const int cu0 = p.cu[b];
+  const int P = p.past[b];
+  const int kend = seq_keys(p, P, it.q0 + it.nq);
+  const int nblk = (kend + 127) / 128;
+  const int PT = 128 / p.G;   // positions per tile
+  unsigned char* Qs = sm + TcLayout::kQ;
+  unsigned char* Ps = sm + TcLayout::kP;
+  uint64_t* bar_s = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
+  uint64_t* bar_o = bar_s + 1;
+  const int* full = reinterpret_cast<const int*>(sm + TcLayout::kFull);
+
+  // Q tile (rows past the tile's positions are zero)
+  for (int i = tid; i < 128 * 16; i += blockDim.x) {
+    const int r = i >> 4, c = i & 15;
+    const int pl = r / p.G;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < PT * p.G && pl < it.nq)
+      v = __ldg(reinterpret_cast<const uint4*>(
+          p.q + (int64_t)(cu0 + it.q0 + pl) * p.q_stride +
+          (int64_t)(h * p.G + r % p.G) * D + c * 8));
+    *reinterpret_cast<uint4*>(Qs + (c >> 3) * 16384 + tc::sw128(r, c & 7)) = v;
+  }
+  tc_load_kv(p, sm, b, h, 0, kend, 0, bad);
+
+  // softmax row of this thread
+  const int r = tid;
+  const int pl = r / p.G;
+  const bool rvalid = tid < 128 && r < PT * p.G && pl < it.nq;
+  const int lim = rvalid ? (int)min64((int64_t)P + it.q0 + pl, INT32_MAX) : -1;
+  const uint32_t lane_taddr = ts.tmem + ((uint32_t)(tid & ~31) << 16);
+  float m_used = -INFINITY, l = 0.f;
+  const uint32_t idesc_qk = tc::idesc_f16(128, 128, false, false);
+  const uint32_t idesc_pv = tc::idesc_f16(128, 128, false, true);
+  const uint32_t q0a = smem_u32(Qs), p0a = smem_u32(Ps);
+
+  for (int j = 0; j < nblk; ++j) {
+    const int buf = j & 1;
+    cp_async_wait<0>();
+    tc::fence_async_shared();
+    tc::fence_before_sync();
+    if (__syncthreads_or(ts.failed ? 1 : 0)) {
+      ts.failed = true;
+      break;
+    }
+    if (tid == 128) {   // warp 4 issues S = Q K^T
+      tc::fence_after_sync();
+      const uint32_t k0a = smem_u32(sm + TcLayout::kK + buf * 32768);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        tc::mma_f16(ts.tmem, tc::smem_desc(q0a + koff, 16, 1024),
+                    tc::smem_desc(k0a + koff, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
+      }
+      tc::commit(bar_s);
+    }
+    // the other buffer and P are free once the previous O += P V has completed
+    if (j > 0) {
+      if (!tc::mbar_wait(bar_o, ts.ph_o, kTcWaitTries)) ts.failed = true;
+      ts.ph_o ^= 1u;
+    }
+    if (j + 1 < nblk) tc_load_kv(p, sm, b, h, j + 1, kend, buf ^ 1, bad);
+    if (!tc::mbar_wait(bar_s, ts.ph_s, kTcWaitTries)) ts.failed = true;
+    ts.ph_s ^= 1u;
+    // every TMEM access below is warp-collective: decide failure for the whole CTA
+    if (__syncthreads_or(ts.failed ? 1 : 0)) {
+      ts.failed = true;
+      break;
+    }
+    tc::fence_after_sync();
+    if (tid < 128) {
+      // two passes over the row in TMEM, 32 columns at a time: max, then weights
+      const int kbase = j * 128;
+      const bool no_mask = full[buf] && kbase + 127 <= lim;
+      const uint8_t* vld = sm + TcLayout::kValid + buf * 128;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        float v[32];
+        tc::tmem_ld32(lane_taddr + ch * 32, v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = ch * 32 + i;
+          if (no_mask || (vld[c] && kbase + c <= lim)) mx = fmaxf(mx, v[i] * p.scale_log2);
+        }
+      }
+      const bool first = m_used == -INFINITY;
+      if ((first && mx != -INFINITY) || (!first && mx > m_used + kTcRescale)) {
+        if (!first) {
+          const float alpha = ex2(m_used - mx);
+          l *= alpha;
+          if (j > 0) {
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              float v[32];
+              tc::tmem_ld32(lane_taddr + 128 + ch * 32, v);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= alpha;
+              tc::tmem_st32(lane_taddr + 128 + ch * 32, v);
+            }
+            tc::tmem_wait_st();
+          }
+        }
+        m_used = mx;
+      }
+      const float base = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        float v[32];
+        tc::tmem_ld32(lane_taddr + ch * 32, v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i0 = q * 8 + 2 * e;
+            const int c0 = ch * 32 + i0;
+            const bool ok0 = no_mask || (vld[c0] && kbase + c0 <= lim);
+            const bool ok1 = no_mask || (vld[c0 + 1] && kbase + c0 + 1 <= lim);
+            const float p0 = ok0 ? ex2(v[i0] * p.scale_log2 - base) : 0.f;
+            const float p1 = ok1 ? ex2(v[i0 + 1] * p.scale_log2 - base) : 0.f;
+            l += p0 + p1;
+            w[e] = pack_half2(p0, p1);
+          }
+          const int c8 = ch * 4 + q;   // 16-byte chunk of the 128-key row
+          *reinterpret_cast<uint4*>(Ps + (c8 >> 3) * 16384 + tc::sw128(r, c8 & 7)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    tc::fence_async_shared();
+    tc::fence_before_sync();
+    if (__syncthreads_or(ts.failed ? 1 : 0)) {
+      ts.failed = true;
+      break;
+    }
+    if (tid == 128) {   // O += P V
+      tc::fence_after_sync();
+      const uint32_t v0a = smem_u32(sm + TcLayout::kV + buf * 32768);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t poff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        tc::mma_f16(ts.tmem + 128, tc::smem_desc(p0a + poff, 16, 1024),
+                    tc::smem_desc(v0a + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv,
+                    (j > 0 || ks > 0) ? 1u : 0u);
+      }
+      tc::commit(bar_o);
+    }
+  }
+  if (!ts.failed) {
+    if (!tc::mbar_wait(bar_o, ts.ph_o, kTcWaitTries)) ts.failed = true;
+    ts.ph_o ^= 1u;
+  }
+  if (__syncthreads_or(ts.failed ? 1 : 0)) ts.failed = true;
+  tc::fence_after_sync();
+  if (tid < 128 && !ts.failed) {   // warp-uniform: the TMEM loads need the whole warp
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    __half* orow =
+        p.out + (int64_t)(cu0 + it.q0 + pl) * p.Hq * D + (int64_t)(h * p.G + r % p.G) * D;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+      float v[32];
+      tc::tmem_ld32(lane_taddr + 128 + ch * 32, v);
+      tc::tmem_wait_ld();
+      if (rvalid) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(orow + ch * 32 + q * 8) =
+              make_uint4(pack_half2(v[q * 8 + 0] * inv, v[q * 8 + 1] * inv),
+                         pack_half2(v[q * 8 + 2] * inv, v[q * 8 + 3] * inv),
+                         pack_half2(v[q * 8 + 4] * inv, v[q * 8 + 5] * inv),
+                         pack_half2(v[q * 8 + 6] * inv, v[q * 8 + 7] * inv));
+      }
+    }
+  }
+  cp_async_wait<0>();
+  tc::fence_before_sync();
+  __syncthreads();
+}
+
+// Phase 2 with tcgen05 tiles: barriers and 256 TMEM columns held for the whole phase.
+__device__ void prefill_phase_tc(const AttnParams& p, unsigned char* sm, int* s_tile,
+                                 bool& bad) {
+  const int ntiles = p.counts[kCntTiles];
+  if (ntiles == 0) return;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TcLayout::kTmem);
+  if (threadIdx.x == 0) {
+    tc::mbar_init(bars, 1);
+    tc::mbar_init(bars + 1, 1);
+    tc::mbar_init_fence();
+  }
+  if (threadIdx.x < 32) {
+    tc::tmem_alloc(tslot, 256);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  TcState ts;
+  ts.tmem = *tslot;
+  ts.ph_s = ts.ph_o = 0;
+  ts.failed = false;
+  while (true) {
+    if (threadIdx.x == 0) *s_tile = atomicAdd(&p.counts[kCntTileNext], 1);
+    __syncthreads();
+    const int t = *s_tile;
+    __syncthreads();
+    if (t >= ntiles || ts.failed) break;
+    prefill_tile_tc(p, sm, t / p.Hkv, t % p.Hkv, ts, bad);
+  }
+  if (ts.failed) {
+    // give any tensor-core work still in flight a bounded chance to finish
+    tc::mbar_wait(bars + 1, ts.ph_o, kTcWaitTries);
+    if (threadIdx.x == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (threadIdx.x < 32) tc::tmem_dealloc(ts.tmem, 256);
+}
+
 // ring sizes (bytes) of the two phases; the dynamic shared memory is their maximum
 template <int D, int NS>
 struct DecodeRing {
@@ -663,13 +964,23 @@ static_assert(kWarps >= 4, "prefill tiles need at least 4 warps");
 
 template <int D, int NS, int NSTAGE>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) attention_kernel(AttnParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ int s_tile;
+  // 1024-byte alignment for the swizzled tensor-core tiles (the launch adds the slack)
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   bool bad = false;
   decode_phase<D, NS>(p, smem + warp * DecodeRing<D, NS>::kWarpBytes,
                       blockIdx.x * kWarps + warp, lane, bad);
   __syncthreads();
+  if constexpr (D == 128) {
+    if (p.tc_prefill) {
+      prefill_phase_tc(p, smem, &s_tile, bad);
+      if (bad) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+      return;
+    }
+  }
   const int ntiles = p.counts[kCntTiles];
   while (true) {
     if (threadIdx.x == 0) s_tile = atomicAdd(&p.counts[kCntTileNext], 1);
@@ -1032,9 +1343,12 @@ __global__ void __launch_bounds__(kPrologueThreads) prologue_kernel(AttnParams p
 
 template <int D, int NS, int NSTAGE>
 cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cudaStream_t s) {
-  constexpr size_t smem = DecodeRing<D, NS>::kBytes > TileRing<D, NSTAGE>::kBytes
-                              ? DecodeRing<D, NS>::kBytes
-                              : TileRing<D, NSTAGE>::kBytes;
+  constexpr size_t ring = DecodeRing<D, NS>::kBytes > TileRing<D, NSTAGE>::kBytes
+                             ? DecodeRing<D, NS>::kBytes
+                             : TileRing<D, NSTAGE>::kBytes;
+  constexpr size_t tc_bytes = D == 128 ? TcLayout::kEnd : 0;
+  constexpr size_t smem = (ring > tc_bytes ? ring : tc_bytes) + 1024;   // + alignment slack
+  static_assert(smem <= 232448, "dynamic shared memory over the per-block limit");
   constexpr size_t split_smem = TileRing<D, NSTAGE>::kBytes;
   static bool configured = false;
   if (!configured) {

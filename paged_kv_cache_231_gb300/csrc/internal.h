@@ -98,6 +98,7 @@ struct AttnParams {
   int dec_rows;            // max new tokens of a sequence handled as decode
   int pre_rows;            // query positions per prefill tile
   int total_warps;         // warps of the persistent kernel
+  int tc_prefill;          // 1: prefill tiles of 128 rows on tcgen05 (head size 128)
   // workspace
   int32_t* counts;         // kCnt* words
   DecSeq* dec_seqs;        // stream-K

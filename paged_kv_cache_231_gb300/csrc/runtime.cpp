@@ -175,7 +175,9 @@ int check_paged(const pkv_paged_attention_args* a, bool attention, PagedLayout* 
     L->fixed_splits = a->fixed_splits;
   }
   L->dec_rows = (int)(16 / G);
-  L->pre_rows = 4 * L->dec_rows;
+  // prefill tiles: 128 rows on the 5th-generation tensor core (head size 128), else
+  // 64 rows of mma.sync tiles
+  L->pre_rows = a->head_size == 128 ? (int)(128 / G) : 4 * L->dec_rows;
   const int64_t T = a->num_tokens, B = a->batch;
   L->dec_bound = L->streamk ? 0 : B * L->max_splits;
   L->pre_bound = ceil_div(T, L->pre_rows) + std::min<int64_t>(B, T / (L->dec_rows + 1));
@@ -409,6 +411,7 @@ int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
   ap.dec_rows = L.dec_rows;
   ap.pre_rows = L.pre_rows;
   ap.total_warps = num_sms_current() * attention_ctas_per_sm() * attention_warps_per_cta();
+  ap.tc_prefill = args->head_size == 128 ? 1 : 0;
   ap.counts = reinterpret_cast<int32_t*>(ws + L.off_counts);
   ap.dec_seqs = reinterpret_cast<DecSeq*>(ws + L.off_seqs);
   ap.seg_done = reinterpret_cast<int32_t*>(ws + L.off_done);
