@@ -50,6 +50,7 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kCtasPerSm = PKV_CTAS_PER_SM;
 constexpr int kDecStages = PKV_DEC_STAGES;
 constexpr int kTileThreads = 128;   // prefill tiles and split items use 4 warps
+constexpr int kTileWarps = kTileThreads / 32;
 constexpr int kPrologueThreads = 256;
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -674,6 +675,8 @@ struct TcLayout {  // byte offsets from a 1024-byte-aligned base
   static constexpr uint32_t kEnd = kTmem + 16;
 };
 constexpr uint32_t kTcWaitTries = 1u << 22;
+// the thread that issues tcgen05.mma: lane 0 of the first warp that does no softmax
+constexpr int kMmaThread = kWarps > 4 ? 128 : 0;
 constexpr float kTcRescale = 8.f;   // log2 of the largest weight a stale max may give
 
 struct TcState {
@@ -767,7 +770,7 @@ __device__ void prefill_tile_tc(const AttnParams& p, unsigned char* sm, int item
       ts.failed = true;
       break;
     }
-    if (tid == 128) {   // warp 4 issues S = Q K^T
+    if (tid == kMmaThread) {   // S = Q K^T
       tc::fence_after_sync();
       const uint32_t k0a = smem_u32(sm + TcLayout::kK + buf * 32768);
 #pragma unroll
@@ -861,7 +864,7 @@ __device__ void prefill_tile_tc(const AttnParams& p, unsigned char* sm, int item
       ts.failed = true;
       break;
     }
-    if (tid == 128) {   // O += P V
+    if (tid == kMmaThread) {   // O += P V
       tc::fence_after_sync();
       const uint32_t v0a = smem_u32(sm + TcLayout::kV + buf * 32768);
 #pragma unroll
@@ -1096,9 +1099,9 @@ __global__ void __launch_bounds__(kTileThreads) decode_split_kernel(AttnParams p
     l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
     l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
   }
-  float* sO = reinterpret_cast<float*>(smem);  // [kWarps][16][D]
-  float* sM = sO + kWarps * 16 * D;            // [kWarps][16]
-  float* sL = sM + kWarps * 16;
+  float* sO = reinterpret_cast<float*>(smem);  // [kTileWarps][16][D]
+  float* sM = sO + kTileWarps * 16 * D;            // [kTileWarps][16]
+  float* sL = sM + kTileWarps * 16;
 #pragma unroll
   for (int d = 0; d < DN; ++d) {
     const int c = d * 8 + 2 * t4;
@@ -1117,11 +1120,11 @@ __global__ void __launch_bounds__(kTileThreads) decode_split_kernel(AttnParams p
     const int r = e / D, d = e % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sM[w * 16 + r]);
+    for (int w = 0; w < kTileWarps; ++w) M = fmaxf(M, sM[w * 16 + r]);
     float num = 0.f, L = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < kTileWarps; ++w) {
         const float wt = ex2(sM[w * 16 + r] - M);
         num += wt * sO[(w * 16 + r) * D + d];
         L += wt * sL[w * 16 + r];
