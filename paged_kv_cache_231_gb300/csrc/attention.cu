@@ -40,10 +40,10 @@ namespace {
 #define PKV_DEC_STAGES 3
 #endif
 #ifndef PKV_WARPS
-#define PKV_WARPS 8
+#define PKV_WARPS 4
 #endif
 #ifndef PKV_CTAS_PER_SM
-#define PKV_CTAS_PER_SM 1
+#define PKV_CTAS_PER_SM 2
 #endif
 constexpr int kWarps = PKV_WARPS;
 constexpr int kThreads = 32 * kWarps;
@@ -675,8 +675,9 @@ struct TcLayout {  // byte offsets from a 1024-byte-aligned base
   static constexpr uint32_t kEnd = kTmem + 16;
 };
 constexpr uint32_t kTcWaitTries = 1u << 22;
-// the thread that issues tcgen05.mma: lane 0 of the first warp that does no softmax
-constexpr int kMmaThread = kWarps > 4 ? 128 : 0;
+constexpr int kTcThreads = 256;   // prefill kernel: 4 softmax warps + MMA/loader warps
+// the thread that issues tcgen05.mma: lane 0 of warp 4, which does no softmax
+constexpr int kMmaThread = 128;
 constexpr float kTcRescale = 8.f;   // log2 of the largest weight a stale max may give
 
 struct TcState {
@@ -950,6 +951,20 @@ __device__ void prefill_phase_tc(const AttnParams& p, unsigned char* sm, int* s_
   if (threadIdx.x < 32) tc::tmem_dealloc(ts.tmem, 256);
 }
 
+// Persistent tensor-core prefill kernel: one CTA of 8 warps per SM, tiles from the
+// planner's counter.
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(AttnParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ int s_tile;
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  bool bad = false;
+  prefill_phase_tc(p, smem, &s_tile, bad);
+  if (bad) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+}
+constexpr size_t kTcSmem = TcLayout::kEnd + 1024;   // + slack for the 1024-byte alignment
+static_assert(kTcSmem <= 232448, "tensor-core prefill shared memory over the limit");
+
 // ring sizes (bytes) of the two phases; the dynamic shared memory is their maximum
 template <int D, int NS>
 struct DecodeRing {
@@ -967,24 +982,18 @@ static_assert(kWarps >= 4, "prefill tiles need at least 4 warps");
 
 template <int D, int NS, int NSTAGE>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) attention_kernel(AttnParams p) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_tile;
-  // 1024-byte alignment for the swizzled tensor-core tiles (the launch adds the slack)
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // the tensor-core prefill kernel behind this one may start as SMs free up; it reads
+  // only what the prologue wrote and writes disjoint output rows
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   bool bad = false;
   decode_phase<D, NS>(p, smem + warp * DecodeRing<D, NS>::kWarpBytes,
                       blockIdx.x * kWarps + warp, lane, bad);
   __syncthreads();
-  if constexpr (D == 128) {
-    if (p.tc_prefill) {
-      prefill_phase_tc(p, smem, &s_tile, bad);
-      if (bad) flag_status(p.status, PKV_DEV_BAD_BLOCK);
-      return;
-    }
-  }
-  const int ntiles = p.counts[kCntTiles];
+  // with tensor-core prefill the tiles belong to prefill_tc_kernel
+  const int ntiles = p.tc_prefill ? 0 : p.counts[kCntTiles];
   while (true) {
     if (threadIdx.x == 0) s_tile = atomicAdd(&p.counts[kCntTileNext], 1);
     __syncthreads();
@@ -1346,11 +1355,9 @@ __global__ void __launch_bounds__(kPrologueThreads) prologue_kernel(AttnParams p
 
 template <int D, int NS, int NSTAGE>
 cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cudaStream_t s) {
-  constexpr size_t ring = DecodeRing<D, NS>::kBytes > TileRing<D, NSTAGE>::kBytes
-                             ? DecodeRing<D, NS>::kBytes
-                             : TileRing<D, NSTAGE>::kBytes;
-  constexpr size_t tc_bytes = D == 128 ? TcLayout::kEnd : 0;
-  constexpr size_t smem = (ring > tc_bytes ? ring : tc_bytes) + 1024;   // + alignment slack
+  constexpr size_t smem = DecodeRing<D, NS>::kBytes > TileRing<D, NSTAGE>::kBytes
+                              ? DecodeRing<D, NS>::kBytes
+                              : TileRing<D, NSTAGE>::kBytes;
   static_assert(smem <= 232448, "dynamic shared memory over the per-block limit");
   constexpr size_t split_smem = TileRing<D, NSTAGE>::kBytes;
   static bool configured = false;
@@ -1362,6 +1369,11 @@ cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cud
     e = cudaFuncSetAttribute(decode_split_kernel<D, NSTAGE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)split_smem);
     if (e != cudaSuccess) return e;
+    if (D == 128) {
+      e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kTcSmem);
+      if (e != cudaSuccess) return e;
+    }
     configured = true;
   }
   const int64_t scatter_threads = (int64_t)sp.T * sp.Hkv * (sp.D / 8);
@@ -1385,7 +1397,21 @@ cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cud
     attention_kernel<D, NS, NSTAGE>
         <<<(unsigned)(p.total_warps / kWarps), kThreads, smem, s>>>(p);
   }
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !p.tc_prefill) return e;
+  // programmatic dependent launch: prefill CTAs take SMs as decode CTAs retire
+  ProfScope ps("prefill_tc", s);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.total_warps / (kWarps * kCtasPerSm)));
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kTcSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, p);
 }
 
 }  // namespace
