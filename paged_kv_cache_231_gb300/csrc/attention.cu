@@ -992,9 +992,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attention_kernel(AttnPar
   decode_phase<D, NS>(p, smem + warp * DecodeRing<D, NS>::kWarpBytes,
                       blockIdx.x * kWarps + warp, lane, bad);
   __syncthreads();
-  // with tensor-core prefill the tiles belong to prefill_tc_kernel
+  // with tensor-core prefill the tiles (and their counter) belong to prefill_tc_kernel
   const int ntiles = p.tc_prefill ? 0 : p.counts[kCntTiles];
-  while (true) {
+  while (ntiles > 0) {
     if (threadIdx.x == 0) s_tile = atomicAdd(&p.counts[kCntTileNext], 1);
     __syncthreads();
     const int t = s_tile;
