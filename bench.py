@@ -289,7 +289,8 @@ def setup_paged(name, args):
         w.metric = "varlen prefill+decode attention TFLOP/s (causal pairs)"
         w.unit, w.work, w.dtype = "TFLOP/s", fl / 1e12, "f16"
         w.tokens = case.num_tokens
-        w.dominant, w.dom_work, w.bound, w.dom_unit = "attention", fl / 1e12, "tensor", "TFLOP/s"
+        # prefill tiles run in the tensor-core kernel (decode tokens in the attention one)
+        w.dominant, w.dom_work, w.bound, w.dom_unit = "prefill_tc", fl / 1e12, "tensor", "TFLOP/s"
         w.traffic_summary, w.traffic_sources = None, ATTN_SOURCES
         w.config = {"workload": "varlen_mixed", "batch": case.batch, "tokens": case.num_tokens,
                     "num_heads": 32, "kv_num_heads": 8, "head_size": 128, "block_size": 32,

@@ -654,312 +654,394 @@ __device__ void prefill_tile(const AttnParams& p, unsigned char* smem, int item_
 
 
 // ----------------------------------------------------------------------------------
-// Prefill tile on tcgen05 (head size 128): 128 rows = (128 / G) positions x G query
-// heads of one sequence and kv head; 128-key stages, two K/V buffers. Per stage:
-//   S = Q K^T   (tcgen05.mma, M=N=128, K-major A and B, fp32 in TMEM columns 0..127)
-//   softmax: thread r < 128 reads row r of S from TMEM, masks, exponentiates against a
-//            running max that is only raised when the new max exceeds it by more than
-//            2^8 (then O and l are rescaled), and writes P (fp16) to shared memory
-//   O += P V    (tcgen05.mma, K-major P, MN-major V, fp32 in TMEM columns 128..255)
+// Tensor-core prefill (head size 128), warp-specialised. A tile is 128 rows =
+// (128 / G) query positions x G query heads of one sequence and kv head, streamed
+// against 128-key blocks:
+//   warps 5-7 (loaders): Q tile and K/V blocks into 128-byte-swizzled shared memory
+//            with cp.async; completion is tracked by mbarriers (cp.async.mbarrier.arrive)
+//   warp 4 (lane 0):     S_j = Q K_j^T into TMEM buffer j % 2, then O += P_{j-1} V_{j-1},
+//            tcgen05.mma + tcgen05.commit
+//   warps 0-3 (softmax): thread r reads row r of S_j from TMEM, keeps a running max that
+//            is raised only when exceeded by more than 2^8 (then O and l are rescaled),
+//            writes P_j (fp16) to shared memory, and finally normalises O.
+// TMEM: S0 columns 0..127, S1 128..255, O 256..383. Every barrier phase is waited in
+// order by each role, so a parity wait never falls two phases behind.
 // ----------------------------------------------------------------------------------
 struct TcLayout {  // byte offsets from a 1024-byte-aligned base
-  static constexpr uint32_t kQ = 0;                 // 2 x [128][64] fp16 sub-tiles
-  static constexpr uint32_t kK = 32768;             // 2 stages x 32 KB
-  static constexpr uint32_t kV = kK + 65536;        // 2 stages x 32 KB
-  static constexpr uint32_t kP = kV + 65536;        // 32 KB
-  static constexpr uint32_t kValid = kP + 32768;    // 2 x 128 B key flags
-  static constexpr uint32_t kFull = kValid + 256;   // 2 x int: stage fully visible
-  static constexpr uint32_t kRowOff = kFull + 16;   // 128 x int64 row offsets
-  static constexpr uint32_t kBars = kRowOff + 1024; // mbarriers S, O
-  static constexpr uint32_t kTmem = kBars + 16;     // TMEM base address
-  static constexpr uint32_t kEnd = kTmem + 16;
+  static constexpr uint32_t kQ = 0;                  // 2 x [128][64] fp16 sub-tiles
+  static constexpr uint32_t kK = 32768;              // 2 stages x 32 KB
+  static constexpr uint32_t kV = kK + 65536;         // 2 stages x 32 KB
+  static constexpr uint32_t kP = kV + 65536;         // 32 KB
+  static constexpr uint32_t kRowOff = kP + 32768;    // 2 stages x 128 int64
+  static constexpr uint32_t kValid = kRowOff + 2048; // 2 stages x 128 flags
+  static constexpr uint32_t kFull = kValid + 256;    // 2 stages x int: block fully valid
+  static constexpr uint32_t kBars = kFull + 16;      // mbarriers (see TcBar)
+  static constexpr uint32_t kTmem = kBars + 128;     // TMEM base address
+  static constexpr uint32_t kTile = kTmem + 4;       // current tile index
+  static constexpr uint32_t kAbort = kTile + 4;      // set when a bounded wait gives up
+  static constexpr uint32_t kEnd = kAbort + 8;
+};
+enum TcBar {  // mbarrier slots
+  kBarQFull = 0,     // count 96: loaders' Q copies landed
+  kBarKvFull0 = 1,   // + stage, count 192: loaders' K/V copies landed and flags written
+  kBarKvEmpty0 = 3,  // + stage, count 1: MMA that read the stage completed
+  kBarSFull0 = 5,    // + buffer, count 1: S_j in TMEM
+  kBarPFull = 7,     // count 128: softmax wrote P_j and is done with S_j
+  kBarODone = 8,     // count 1: O += P_j V_j completed
+  kNumBars = 9
 };
 constexpr uint32_t kTcWaitTries = 1u << 22;
-constexpr int kTcThreads = 256;   // prefill kernel: 4 softmax warps + MMA/loader warps
-// the thread that issues tcgen05.mma: lane 0 of warp 4, which does no softmax
-constexpr int kMmaThread = 128;
-constexpr float kTcRescale = 8.f;   // log2 of the largest weight a stale max may give
+constexpr int kTcThreads = 256;
+constexpr int kMmaThread = 128;    // lane 0 of warp 4
+constexpr int kLoaderBase = 160;   // warps 5-7
+constexpr int kLoaders = 96;
+constexpr float kTcRescale = 8.f;  // log2 of the largest weight a stale max may give
 
-struct TcState {
-  uint32_t tmem;
-  uint32_t ph_s, ph_o;
-  bool failed;
-};
-
-// Stage keys [j*128, j*128 + 128) of (b, h) into buffer `buf` (all threads).
-__device__ __forceinline__ void tc_load_kv(const AttnParams& p, unsigned char* sm, int b,
-                                           int h, int j, int kend, int buf, bool& bad) {
-  constexpr int D = 128;
-  int64_t* rowoff = reinterpret_cast<int64_t*>(sm + TcLayout::kRowOff);
-  uint8_t* valid = sm + TcLayout::kValid + buf * 128;
-  int* full = reinterpret_cast<int*>(sm + TcLayout::kFull);
-  const int tid = threadIdx.x;
-  bool ok = true;
-  if (tid < 128) {
-    const int key = j * 128 + tid;
-    int64_t off = -1;
-    if (key < kend) {
-      off = key_row_offset(p, b, h, key);
-      if (off < 0) bad = true;
-    }
-    rowoff[tid] = off;
-    valid[tid] = off >= 0 ? 1 : 0;
-    ok = off >= 0;
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// arrive when every cp.async this thread issued so far has landed (count not raised)
+__device__ __forceinline__ void mbar_arrive_cp_async(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void loader_sync() {
+  asm volatile("bar.sync 2, 96;\n" ::: "memory");
+}
+// bounded wait that also gives up when another thread of the CTA already did
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const uint32_t addr = smem_u32(bar);
+  for (uint32_t i = 0; i < kTcWaitTries; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((i & 255u) == 255u && *abort) return false;
   }
-  const int all = __syncthreads_and(ok ? 1 : 0);
-  if (tid == 0) full[buf] = all;
-  unsigned char* Ks = sm + TcLayout::kK + buf * 32768;
-  unsigned char* Vs = sm + TcLayout::kV + buf * 32768;
-  for (int i = tid; i < 128 * 16; i += blockDim.x) {
-    const int r = i >> 4, c = i & 15;
-    const int64_t off = rowoff[r];
-    const int nb = off >= 0 ? 16 : 0;
-    const uint32_t dst = (uint32_t)(c >> 3) * 16384u + tc::sw128(r, c & 7);
-    cp_async_16(Ks + dst, off >= 0 ? p.kc + off + c * 8 : p.kc, nb);
-    cp_async_16(Vs + dst, off >= 0 ? p.vc + off + c * 8 : p.vc, nb);
-  }
-  cp_async_commit();
+  *abort = 1;
+  return false;
 }
 
-__device__ void prefill_tile_tc(const AttnParams& p, unsigned char* sm, int item_idx, int h,
-                                TcState& ts, bool& bad) {
-  constexpr int D = 128;
-  const int tid = threadIdx.x;
-  const PrefillItem it = p.pre_items[item_idx];
-  const int b = it.b;
-  const int cu0 = p.cu[b];
-  const int P = p.past[b];
-  const int kend = seq_keys(p, P, it.q0 + it.nq);
-  const int nblk = (kend + 127) / 128;
-  const int PT = 128 / p.G;   // positions per tile
-  unsigned char* Qs = sm + TcLayout::kQ;
-  unsigned char* Ps = sm + TcLayout::kP;
-  uint64_t* bar_s = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
-  uint64_t* bar_o = bar_s + 1;
-  const int* full = reinterpret_cast<const int*>(sm + TcLayout::kFull);
+struct TcTile {
+  int b, h, q0, nq, cu0, P, kend, nblk, PT;
+};
 
-  // Q tile (rows past the tile's positions are zero)
-  for (int i = tid; i < 128 * 16; i += blockDim.x) {
+__device__ __forceinline__ TcTile tc_tile(const AttnParams& p, int t) {
+  const PrefillItem it = p.pre_items[t / p.Hkv];
+  TcTile d;
+  d.b = it.b;
+  d.h = t % p.Hkv;
+  d.q0 = it.q0;
+  d.nq = it.nq;
+  d.cu0 = p.cu[it.b];
+  d.P = p.past[it.b];
+  d.kend = seq_keys(p, d.P, it.q0 + it.nq);
+  d.nblk = (d.kend + 127) / 128;
+  d.PT = 128 / p.G;
+  return d;
+}
+
+// Loader warps: Q tile, then every K/V block of the tile.
+__device__ void tc_loader(const AttnParams& p, unsigned char* sm, const TcTile& t,
+                          uint32_t (&kv_use)[2], bool& bad) {
+  constexpr int D = 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
+  const int lt = threadIdx.x - kLoaderBase;
+  unsigned char* Qs = sm + TcLayout::kQ;
+  for (int i = lt; i < 128 * 16; i += kLoaders) {
     const int r = i >> 4, c = i & 15;
     const int pl = r / p.G;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r < PT * p.G && pl < it.nq)
-      v = __ldg(reinterpret_cast<const uint4*>(
-          p.q + (int64_t)(cu0 + it.q0 + pl) * p.q_stride +
-          (int64_t)(h * p.G + r % p.G) * D + c * 8));
-    *reinterpret_cast<uint4*>(Qs + (c >> 3) * 16384 + tc::sw128(r, c & 7)) = v;
+    const bool ok = r < t.PT * p.G && pl < t.nq;
+    const __half* src = ok ? p.q + (int64_t)(t.cu0 + t.q0 + pl) * p.q_stride +
+                                 (int64_t)(t.h * p.G + r % p.G) * D + c * 8
+                           : p.q;
+    cp_async_16(Qs + (c >> 3) * 16384 + tc::sw128(r, c & 7), src, ok ? 16 : 0);
   }
-  tc_load_kv(p, sm, b, h, 0, kend, 0, bad);
+  mbar_arrive_cp_async(bars + kBarQFull);
+  for (int j = 0; j < t.nblk; ++j) {
+    const int s = j & 1;
+    if (kv_use[s] > 0 && !tc_wait(bars + kBarKvEmpty0 + s, (kv_use[s] - 1) & 1u, abort))
+      return;
+    int64_t* rowoff = reinterpret_cast<int64_t*>(sm + TcLayout::kRowOff) + s * 128;
+    uint8_t* valid = sm + TcLayout::kValid + s * 128;
+    bool all = true;
+    for (int r = lt; r < 128; r += kLoaders) {
+      const int key = j * 128 + r;
+      int64_t off = -1;
+      if (key < t.kend) {
+        off = key_row_offset(p, t.b, t.h, key);
+        if (off < 0) bad = true;
+      }
+      rowoff[r] = off;
+      valid[r] = off >= 0 ? 1 : 0;
+      all = all && off >= 0;
+    }
+    if (!all) reinterpret_cast<int*>(sm + TcLayout::kFull)[s] = 0;
+    loader_sync();
+    unsigned char* Ks = sm + TcLayout::kK + s * 32768;
+    unsigned char* Vs = sm + TcLayout::kV + s * 32768;
+    for (int i = lt; i < 128 * 16; i += kLoaders) {
+      const int r = i >> 4, c = i & 15;
+      const int64_t off = rowoff[r];
+      const uint32_t dst = (uint32_t)(c >> 3) * 16384u + tc::sw128(r, c & 7);
+      cp_async_16(Ks + dst, off >= 0 ? p.kc + off + c * 8 : p.kc, off >= 0 ? 16 : 0);
+      cp_async_16(Vs + dst, off >= 0 ? p.vc + off + c * 8 : p.vc, off >= 0 ? 16 : 0);
+    }
+    mbar_arrive_cp_async(bars + kBarKvFull0 + s);
+    mbar_arrive(bars + kBarKvFull0 + s);
+    ++kv_use[s];
+  }
+}
 
-  // softmax row of this thread
-  const int r = tid;
-  const int pl = r / p.G;
-  const bool rvalid = tid < 128 && r < PT * p.G && pl < it.nq;
-  const int lim = rvalid ? (int)min64((int64_t)P + it.q0 + pl, INT32_MAX) : -1;
-  const uint32_t lane_taddr = ts.tmem + ((uint32_t)(tid & ~31) << 16);
-  float m_used = -INFINITY, l = 0.f;
+// Warp 4, lane 0: the MMA stream of the tile.
+__device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
+                       uint32_t tmem, uint32_t q_use, uint32_t (&kv_use)[2],
+                       uint32_t& blk_use) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const uint32_t idesc_qk = tc::idesc_f16(128, 128, false, false);
   const uint32_t idesc_pv = tc::idesc_f16(128, 128, false, true);
-  const uint32_t q0a = smem_u32(Qs), p0a = smem_u32(Ps);
-
-  for (int j = 0; j < nblk; ++j) {
-    const int buf = j & 1;
-    cp_async_wait<0>();
-    tc::fence_async_shared();
-    tc::fence_before_sync();
-    if (__syncthreads_or(ts.failed ? 1 : 0)) {
-      ts.failed = true;
-      break;
-    }
-    if (tid == kMmaThread) {   // S = Q K^T
-      tc::fence_after_sync();
-      const uint32_t k0a = smem_u32(sm + TcLayout::kK + buf * 32768);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-        tc::mma_f16(ts.tmem, tc::smem_desc(q0a + koff, 16, 1024),
-                    tc::smem_desc(k0a + koff, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
-      }
-      tc::commit(bar_s);
-    }
-    // the other buffer and P are free once the previous O += P V has completed
-    if (j > 0) {
-      if (!tc::mbar_wait(bar_o, ts.ph_o, kTcWaitTries)) ts.failed = true;
-      ts.ph_o ^= 1u;
-    }
-    if (j + 1 < nblk) tc_load_kv(p, sm, b, h, j + 1, kend, buf ^ 1, bad);
-    if (!tc::mbar_wait(bar_s, ts.ph_s, kTcWaitTries)) ts.failed = true;
-    ts.ph_s ^= 1u;
-    // every TMEM access below is warp-collective: decide failure for the whole CTA
-    if (__syncthreads_or(ts.failed ? 1 : 0)) {
-      ts.failed = true;
-      break;
-    }
+  const uint32_t qa = smem_u32(sm + TcLayout::kQ), pa = smem_u32(sm + TcLayout::kP);
+  if (!tc_wait(bars + kBarQFull, q_use & 1u, abort)) return;
+  tc::fence_async_shared();
+  auto issue_pv = [&](int j) -> bool {
+    // P_j written and S_j no longer read by the softmax warps
+    if (!tc_wait(bars + kBarPFull, (blk_use + j) & 1u, abort)) return false;
     tc::fence_after_sync();
-    if (tid < 128) {
-      // two passes over the row in TMEM, 32 columns at a time: max, then weights
-      const int kbase = j * 128;
-      const bool no_mask = full[buf] && kbase + 127 <= lim;
-      const uint8_t* vld = sm + TcLayout::kValid + buf * 128;
-      float mx = -INFINITY;
+    const uint32_t va = smem_u32(sm + TcLayout::kV + (j & 1) * 32768);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        float v[32];
-        tc::tmem_ld32(lane_taddr + ch * 32, v);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = ch * 32 + i;
-          if (no_mask || (vld[c] && kbase + c <= lim)) mx = fmaxf(mx, v[i] * p.scale_log2);
-        }
-      }
-      const bool first = m_used == -INFINITY;
-      if ((first && mx != -INFINITY) || (!first && mx > m_used + kTcRescale)) {
-        if (!first) {
-          const float alpha = ex2(m_used - mx);
-          l *= alpha;
-          if (j > 0) {
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-              float v[32];
-              tc::tmem_ld32(lane_taddr + 128 + ch * 32, v);
-              tc::tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= alpha;
-              tc::tmem_st32(lane_taddr + 128 + ch * 32, v);
-            }
-            tc::tmem_wait_st();
-          }
-        }
-        m_used = mx;
-      }
-      const float base = m_used == -INFINITY ? 0.f : m_used;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        float v[32];
-        tc::tmem_ld32(lane_taddr + ch * 32, v);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i0 = q * 8 + 2 * e;
-            const int c0 = ch * 32 + i0;
-            const bool ok0 = no_mask || (vld[c0] && kbase + c0 <= lim);
-            const bool ok1 = no_mask || (vld[c0 + 1] && kbase + c0 + 1 <= lim);
-            const float p0 = ok0 ? ex2(v[i0] * p.scale_log2 - base) : 0.f;
-            const float p1 = ok1 ? ex2(v[i0 + 1] * p.scale_log2 - base) : 0.f;
-            l += p0 + p1;
-            w[e] = pack_half2(p0, p1);
-          }
-          const int c8 = ch * 4 + q;   // 16-byte chunk of the 128-key row
-          *reinterpret_cast<uint4*>(Ps + (c8 >> 3) * 16384 + tc::sw128(r, c8 & 7)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t poff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+      tc::mma_f16(tmem + 256, tc::smem_desc(pa + poff, 16, 1024),
+                  tc::smem_desc(va + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv,
+                  (j > 0 || ks > 0) ? 1u : 0u);
     }
+    tc::commit(bars + kBarODone);
+    tc::commit(bars + kBarKvEmpty0 + (j & 1));
+    return true;
+  };
+  for (int j = 0; j < t.nblk; ++j) {
+    const int s = j & 1;
+    if (!tc_wait(bars + kBarKvFull0 + s, kv_use[s] & 1u, abort)) return;
+    ++kv_use[s];
     tc::fence_async_shared();
-    tc::fence_before_sync();
-    if (__syncthreads_or(ts.failed ? 1 : 0)) {
-      ts.failed = true;
-      break;
-    }
-    if (tid == kMmaThread) {   // O += P V
-      tc::fence_after_sync();
-      const uint32_t v0a = smem_u32(sm + TcLayout::kV + buf * 32768);
+    tc::fence_after_sync();
+    const uint32_t ka = smem_u32(sm + TcLayout::kK + s * 32768);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t poff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-        tc::mma_f16(ts.tmem + 128, tc::smem_desc(p0a + poff, 16, 1024),
-                    tc::smem_desc(v0a + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv,
-                    (j > 0 || ks > 0) ? 1u : 0u);
-      }
-      tc::commit(bar_o);
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+      tc::mma_f16(tmem + s * 128, tc::smem_desc(qa + koff, 16, 1024),
+                  tc::smem_desc(ka + koff, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
     }
+    tc::commit(bars + kBarSFull0 + s);
+    if (j > 0 && !issue_pv(j - 1)) return;
   }
-  if (!ts.failed) {
-    if (!tc::mbar_wait(bar_o, ts.ph_o, kTcWaitTries)) ts.failed = true;
-    ts.ph_o ^= 1u;
-  }
-  if (__syncthreads_or(ts.failed ? 1 : 0)) ts.failed = true;
-  tc::fence_after_sync();
-  if (tid < 128 && !ts.failed) {   // warp-uniform: the TMEM loads need the whole warp
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    __half* orow =
-        p.out + (int64_t)(cu0 + it.q0 + pl) * p.Hq * D + (int64_t)(h * p.G + r % p.G) * D;
+  issue_pv(t.nblk - 1);
+  blk_use += t.nblk;
+}
+
+// Warps 0-3: softmax and the normalised output of row threadIdx.x.
+__device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile& t,
+                           uint32_t tmem, uint32_t (&kv_use)[2], uint32_t (&s_use)[2],
+                           uint32_t& blk_use) {
+  constexpr int D = 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
+  const int r = threadIdx.x;
+  const int pl = r / p.G;
+  const bool rvalid = r < t.PT * p.G && pl < t.nq;
+  const int lim = rvalid ? (int)min64((int64_t)t.P + t.q0 + pl, INT32_MAX) : -1;
+  const uint32_t lane_taddr = tmem + ((uint32_t)(r & ~31) << 16);
+  unsigned char* Ps = sm + TcLayout::kP;
+  float m_used = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < t.nblk && ok; ++j) {
+    const int s = j & 1;
+    // flags of block j, then S_j
+    ok = tc_wait(bars + kBarKvFull0 + s, kv_use[s] & 1u, abort);
+    ++kv_use[s];
+    ok = ok && tc_wait(bars + kBarSFull0 + s, s_use[s] & 1u, abort);
+    ++s_use[s];
+    ok = __all_sync(0xffffffffu, ok);   // TMEM loads below are warp-collective
+    if (!ok) break;
+    tc::fence_after_sync();
+    const int kbase = j * 128;
+    const bool no_mask =
+        reinterpret_cast<const int*>(sm + TcLayout::kFull)[s] && kbase + 127 <= lim;
+    const uint8_t* vld = sm + TcLayout::kValid + s * 128;
+    const uint32_t sa = lane_taddr + s * 128;
+    float mx = -INFINITY;
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) {
       float v[32];
-      tc::tmem_ld32(lane_taddr + 128 + ch * 32, v);
+      tc::tmem_ld32(sa + ch * 32, v);
       tc::tmem_wait_ld();
-      if (rvalid) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(orow + ch * 32 + q * 8) =
-              make_uint4(pack_half2(v[q * 8 + 0] * inv, v[q * 8 + 1] * inv),
-                         pack_half2(v[q * 8 + 2] * inv, v[q * 8 + 3] * inv),
-                         pack_half2(v[q * 8 + 4] * inv, v[q * 8 + 5] * inv),
-                         pack_half2(v[q * 8 + 6] * inv, v[q * 8 + 7] * inv));
+      for (int i = 0; i < 32; ++i) {
+        const int c = ch * 32 + i;
+        if (no_mask || (vld[c] && kbase + c <= lim)) mx = fmaxf(mx, v[i] * p.scale_log2);
+      }
+    }
+    // O and the P buffer are free once O += P_{j-1} V_{j-1} has completed
+    if (j > 0) {
+      ok = __all_sync(0xffffffffu, tc_wait(bars + kBarODone, (blk_use + j - 1) & 1u, abort));
+      if (!ok) break;
+      tc::fence_after_sync();
+    }
+    const bool first = m_used == -INFINITY;
+    if ((first && mx != -INFINITY) || (!first && mx > m_used + kTcRescale)) {
+      if (!first) {
+        const float alpha = ex2(m_used - mx);
+        l *= alpha;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          float v[32];
+          tc::tmem_ld32(lane_taddr + 256 + ch * 32, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= alpha;
+          tc::tmem_st32(lane_taddr + 256 + ch * 32, v);
+        }
+        tc::tmem_wait_st();
+      }
+      m_used = mx;
+    }
+    const float base = m_used == -INFINITY ? 0.f : m_used;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+      float v[32];
+      tc::tmem_ld32(sa + ch * 32, v);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i0 = q * 8 + 2 * e;
+          const int c0 = ch * 32 + i0;
+          const bool ok0 = no_mask || (vld[c0] && kbase + c0 <= lim);
+          const bool ok1 = no_mask || (vld[c0 + 1] && kbase + c0 + 1 <= lim);
+          const float p0 = ok0 ? ex2(v[i0] * p.scale_log2 - base) : 0.f;
+          const float p1 = ok1 ? ex2(v[i0 + 1] * p.scale_log2 - base) : 0.f;
+          l += p0 + p1;
+          w[e] = pack_half2(p0, p1);
+        }
+        const int c8 = ch * 4 + q;
+        *reinterpret_cast<uint4*>(Ps + (c8 >> 3) * 16384 + tc::sw128(r, c8 & 7)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    tc::fence_async_shared();
+    tc::fence_before_sync();
+    mbar_arrive(bars + kBarPFull);
+  }
+  if (ok) {
+    ok = __all_sync(0xffffffffu,
+                    tc_wait(bars + kBarODone, (blk_use + t.nblk - 1) & 1u, abort));
+    if (ok) {
+      tc::fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __half* orow = p.out + (int64_t)(t.cu0 + t.q0 + pl) * p.Hq * D +
+                     (int64_t)(t.h * p.G + r % p.G) * D;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        float v[32];
+        tc::tmem_ld32(lane_taddr + 256 + ch * 32, v);
+        tc::tmem_wait_ld();
+        if (rvalid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(orow + ch * 32 + q * 8) =
+                make_uint4(pack_half2(v[q * 8 + 0] * inv, v[q * 8 + 1] * inv),
+                           pack_half2(v[q * 8 + 2] * inv, v[q * 8 + 3] * inv),
+                           pack_half2(v[q * 8 + 4] * inv, v[q * 8 + 5] * inv),
+                           pack_half2(v[q * 8 + 6] * inv, v[q * 8 + 7] * inv));
+        }
       }
     }
   }
-  cp_async_wait<0>();
-  tc::fence_before_sync();
-  __syncthreads();
+  blk_use += t.nblk;
 }
 
-// Phase 2 with tcgen05 tiles: barriers and 256 TMEM columns held for the whole phase.
-__device__ void prefill_phase_tc(const AttnParams& p, unsigned char* sm, int* s_tile,
-                                 bool& bad) {
+// Tiles from the planner's counter; barriers and 512 TMEM columns held throughout.
+__device__ void prefill_phase_tc(const AttnParams& p, unsigned char* sm, bool& bad) {
   const int ntiles = p.counts[kCntTiles];
   if (ntiles == 0) return;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TcLayout::kTmem);
-  if (threadIdx.x == 0) {
-    tc::mbar_init(bars, 1);
-    tc::mbar_init(bars + 1, 1);
+  volatile int* tile = reinterpret_cast<volatile int*>(sm + TcLayout::kTile);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    tc::mbar_init(bars + kBarQFull, kLoaders);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(bars + kBarKvFull0 + s, 2 * kLoaders);
+      tc::mbar_init(bars + kBarKvEmpty0 + s, 1);
+      tc::mbar_init(bars + kBarSFull0 + s, 1);
+    }
+    tc::mbar_init(bars + kBarPFull, 128);
+    tc::mbar_init(bars + kBarODone, 1);
     tc::mbar_init_fence();
+    *abort = 0;
   }
-  if (threadIdx.x < 32) {
-    tc::tmem_alloc(tslot, 256);
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, 512);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  TcState ts;
-  ts.tmem = *tslot;
-  ts.ph_s = ts.ph_o = 0;
-  ts.failed = false;
+  const uint32_t tmem = *tslot;
+  // per-role phase counters (each role waits every phase it depends on, in order)
+  uint32_t kv_use[2] = {0u, 0u}, s_use[2] = {0u, 0u}, q_use = 0u, blk_use = 0u;
   while (true) {
-    if (threadIdx.x == 0) *s_tile = atomicAdd(&p.counts[kCntTileNext], 1);
+    if (tid == 0) *tile = atomicAdd(&p.counts[kCntTileNext], 1);
+    if (tid >= kLoaderBase && tid < kLoaderBase + kLoaders && tid - kLoaderBase < 2)
+      reinterpret_cast<int*>(sm + TcLayout::kFull)[tid - kLoaderBase] = 1;
     __syncthreads();
-    const int t = *s_tile;
+    const int ti = *tile;
+    const bool stop = ti >= ntiles || *abort;
     __syncthreads();
-    if (t >= ntiles || ts.failed) break;
-    prefill_tile_tc(p, sm, t / p.Hkv, t % p.Hkv, ts, bad);
+    if (stop) break;
+    const TcTile t = tc_tile(p, ti);
+    if (tid < 128) {
+      tc_softmax(p, sm, t, tmem, kv_use, s_use, blk_use);
+    } else if (tid == kMmaThread) {
+      tc_mma(p, sm, t, tmem, q_use, kv_use, blk_use);
+    } else if (tid >= kLoaderBase) {
+      tc_loader(p, sm, t, kv_use, bad);
+    }
+    ++q_use;
+    // the next tile reuses Q, the flags and the "fully valid" words
+    cp_async_wait<0>();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
   }
-  if (ts.failed) {
-    // give any tensor-core work still in flight a bounded chance to finish
-    tc::mbar_wait(bars + 1, ts.ph_o, kTcWaitTries);
-    if (threadIdx.x == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
-  }
+  if (*abort && tid == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
+  cp_async_wait<0>();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (threadIdx.x < 32) tc::tmem_dealloc(ts.tmem, 256);
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 // Persistent tensor-core prefill kernel: one CTA of 8 warps per SM, tiles from the
 // planner's counter.
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(AttnParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ int s_tile;
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   bool bad = false;
-  prefill_phase_tc(p, smem, &s_tile, bad);
+  prefill_phase_tc(p, smem, bad);
   if (bad) flag_status(p.status, PKV_DEV_BAD_BLOCK);
 }
 constexpr size_t kTcSmem = TcLayout::kEnd + 1024;   // + slack for the 1024-byte alignment
