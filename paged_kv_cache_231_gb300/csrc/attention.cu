@@ -877,68 +877,57 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
     const bool no_mask =
         reinterpret_cast<const int*>(sm + TcLayout::kFull)[s] && kbase + 127 <= lim;
     const uint8_t* vld = sm + TcLayout::kValid + s * 128;
-    const uint32_t sa = lane_taddr + s * 128;
+    // the whole row of S_j in one TMEM round trip
+    float v[128];
+    {
+      float (*v32)[32] = reinterpret_cast<float (*)[32]>(v);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(lane_taddr + s * 128 + ch * 32, v32[ch]);
+      tc::tmem_wait_ld();
+    }
     float mx = -INFINITY;
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-      float v[32];
-      tc::tmem_ld32(sa + ch * 32, v);
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int c = ch * 32 + i;
-        if (no_mask || (vld[c] && kbase + c <= lim)) mx = fmaxf(mx, v[i] * p.scale_log2);
-      }
+    for (int c = 0; c < 128; ++c) {
+      const bool vis = no_mask || (vld[c] && kbase + c <= lim);
+      v[c] = vis ? v[c] * p.scale_log2 : -INFINITY;
+      mx = fmaxf(mx, v[c]);
     }
+    const bool first = m_used == -INFINITY;
+    const bool raise = (first && mx != -INFINITY) || (!first && mx > m_used + kTcRescale);
+    const float alpha = raise && !first ? ex2(m_used - mx) : 1.f;
+    if (raise) m_used = mx;
+    const float base = m_used == -INFINITY ? 0.f : m_used;
+    uint32_t w[64];
+    float lsum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 128; c += 2) {
+      const float p0 = ex2(v[c] - base), p1 = ex2(v[c + 1] - base);
+      lsum += p0 + p1;
+      w[c / 2] = pack_half2(p0, p1);
+    }
+    l = l * alpha + lsum;
     // O and the P buffer are free once O += P_{j-1} V_{j-1} has completed
     if (j > 0) {
       ok = __all_sync(0xffffffffu, tc_wait(bars + kBarODone, (blk_use + j - 1) & 1u, abort));
       if (!ok) break;
       tc::fence_after_sync();
-    }
-    const bool first = m_used == -INFINITY;
-    if ((first && mx != -INFINITY) || (!first && mx > m_used + kTcRescale)) {
-      if (!first) {
-        const float alpha = ex2(m_used - mx);
-        l *= alpha;
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {   // warp-collective TMEM rescale of O
+        float o[128];
+        float (*o32)[32] = reinterpret_cast<float (*)[32]>(o);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float v[32];
-          tc::tmem_ld32(lane_taddr + 256 + ch * 32, v);
-          tc::tmem_wait_ld();
+        for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(lane_taddr + 256 + ch * 32, o32[ch]);
+        tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= alpha;
-          tc::tmem_st32(lane_taddr + 256 + ch * 32, v);
-        }
+        for (int c = 0; c < 128; ++c) o[c] *= alpha;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tc::tmem_st32(lane_taddr + 256 + ch * 32, o32[ch]);
         tc::tmem_wait_st();
       }
-      m_used = mx;
     }
-    const float base = m_used == -INFINITY ? 0.f : m_used;
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-      float v[32];
-      tc::tmem_ld32(sa + ch * 32, v);
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i0 = q * 8 + 2 * e;
-          const int c0 = ch * 32 + i0;
-          const bool ok0 = no_mask || (vld[c0] && kbase + c0 <= lim);
-          const bool ok1 = no_mask || (vld[c0 + 1] && kbase + c0 + 1 <= lim);
-          const float p0 = ok0 ? ex2(v[i0] * p.scale_log2 - base) : 0.f;
-          const float p1 = ok1 ? ex2(v[i0 + 1] * p.scale_log2 - base) : 0.f;
-          l += p0 + p1;
-          w[e] = pack_half2(p0, p1);
-        }
-        const int c8 = ch * 4 + q;
-        *reinterpret_cast<uint4*>(Ps + (c8 >> 3) * 16384 + tc::sw128(r, c8 & 7)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
+    for (int c8 = 0; c8 < 16; ++c8)
+      *reinterpret_cast<uint4*>(Ps + (c8 >> 3) * 16384 + tc::sw128(r, c8 & 7)) =
+          make_uint4(w[c8 * 4], w[c8 * 4 + 1], w[c8 * 4 + 2], w[c8 * 4 + 3]);
     tc::fence_async_shared();
     tc::fence_before_sync();
     mbar_arrive(bars + kBarPFull);
@@ -951,20 +940,19 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __half* orow = p.out + (int64_t)(t.cu0 + t.q0 + pl) * p.Hq * D +
                      (int64_t)(t.h * p.G + r % p.G) * D;
+      float o[128];
+      float (*o32)[32] = reinterpret_cast<float (*)[32]>(o);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        float v[32];
-        tc::tmem_ld32(lane_taddr + 256 + ch * 32, v);
-        tc::tmem_wait_ld();
-        if (rvalid) {
+      for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(lane_taddr + 256 + ch * 32, o32[ch]);
+      tc::tmem_wait_ld();
+      if (rvalid) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(orow + ch * 32 + q * 8) =
-                make_uint4(pack_half2(v[q * 8 + 0] * inv, v[q * 8 + 1] * inv),
-                           pack_half2(v[q * 8 + 2] * inv, v[q * 8 + 3] * inv),
-                           pack_half2(v[q * 8 + 4] * inv, v[q * 8 + 5] * inv),
-                           pack_half2(v[q * 8 + 6] * inv, v[q * 8 + 7] * inv));
-        }
+        for (int q = 0; q < 16; ++q)
+          *reinterpret_cast<uint4*>(orow + q * 8) =
+              make_uint4(pack_half2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
+                         pack_half2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
+                         pack_half2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
+                         pack_half2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
       }
     }
   }
