@@ -673,9 +673,8 @@ struct TcLayout {  // byte offsets from a 1024-byte-aligned base
   static constexpr uint32_t kV = kK + 65536;         // 2 stages x 32 KB
   static constexpr uint32_t kP = kV + 65536;         // 32 KB
   static constexpr uint32_t kRowOff = kP + 32768;    // 2 stages x 128 int64
-  static constexpr uint32_t kValid = kRowOff + 2048; // 2 stages x 128 flags
-  static constexpr uint32_t kFull = kValid + 256;    // 2 stages x int: block fully valid
-  static constexpr uint32_t kBars = kFull + 16;      // mbarriers (see TcBar)
+  static constexpr uint32_t kValid = kRowOff + 2048; // 2 stages x 128-bit mask of mapped keys
+  static constexpr uint32_t kBars = kValid + 32;     // mbarriers (see TcBar)
   static constexpr uint32_t kTmem = kBars + 128;     // TMEM base address
   static constexpr uint32_t kTile = kTmem + 4;       // current tile index
   static constexpr uint32_t kAbort = kTile + 4;      // set when a bounded wait gives up
@@ -771,8 +770,8 @@ __device__ void tc_loader(const AttnParams& p, unsigned char* sm, const TcTile& 
     if (kv_use[s] > 0 && !tc_wait(bars + kBarKvEmpty0 + s, (kv_use[s] - 1) & 1u, abort))
       return;
     int64_t* rowoff = reinterpret_cast<int64_t*>(sm + TcLayout::kRowOff) + s * 128;
-    uint8_t* valid = sm + TcLayout::kValid + s * 128;
-    bool all = true;
+    uint32_t* valid = reinterpret_cast<uint32_t*>(sm + TcLayout::kValid) + s * 4;
+    // every lane of a loader warp runs the same number of rows (32-row words of the mask)
     for (int r = lt; r < 128; r += kLoaders) {
       const int key = j * 128 + r;
       int64_t off = -1;
@@ -781,10 +780,9 @@ __device__ void tc_loader(const AttnParams& p, unsigned char* sm, const TcTile& 
         if (off < 0) bad = true;
       }
       rowoff[r] = off;
-      valid[r] = off >= 0 ? 1 : 0;
-      all = all && off >= 0;
+      const uint32_t word = __ballot_sync(0xffffffffu, off >= 0);
+      if ((r & 31) == 0) valid[r >> 5] = word;
     }
-    if (!all) reinterpret_cast<int*>(sm + TcLayout::kFull)[s] = 0;
     loader_sync();
     unsigned char* Ks = sm + TcLayout::kK + s * 32768;
     unsigned char* Vs = sm + TcLayout::kV + s * 32768;
@@ -874,9 +872,9 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
     if (!ok) break;
     tc::fence_after_sync();
     const int kbase = j * 128;
-    const bool no_mask =
-        reinterpret_cast<const int*>(sm + TcLayout::kFull)[s] && kbase + 127 <= lim;
-    const uint8_t* vld = sm + TcLayout::kValid + s * 128;
+    const uint4 vm = *reinterpret_cast<const uint4*>(sm + TcLayout::kValid + s * 16);
+    const int cut = lim - kbase + 1;  // columns below cut are causally visible to this row
+    const bool full = (vm.x & vm.y & vm.z & vm.w) == 0xffffffffu && cut >= 128;
     // the whole row of S_j in one TMEM round trip
     float v[128];
     {
@@ -885,27 +883,38 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
       for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(lane_taddr + s * 128 + ch * 32, v32[ch]);
       tc::tmem_wait_ld();
     }
-    float mx = -INFINITY;
+    const float sl2 = p.scale_log2;
+    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (__all_sync(0xffffffffu, full)) {
 #pragma unroll
-    for (int c = 0; c < 128; ++c) {
-      const bool vis = no_mask || (vld[c] && kbase + c <= lim);
-      v[c] = vis ? v[c] * p.scale_log2 : -INFINITY;
-      mx = fmaxf(mx, v[c]);
+      for (int c = 0; c < 128; ++c) {
+        v[c] *= sl2;
+        mx4[c & 3] = fmaxf(mx4[c & 3], v[c]);
+      }
+    } else {
+      const uint32_t words[4] = {vm.x, vm.y, vm.z, vm.w};
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const bool vis = c < cut && ((words[c >> 5] >> (c & 31)) & 1u);
+        v[c] = vis ? v[c] * sl2 : -INFINITY;
+        mx4[c & 3] = fmaxf(mx4[c & 3], v[c]);
+      }
     }
+    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
     const bool first = m_used == -INFINITY;
     const bool raise = (first && mx != -INFINITY) || (!first && mx > m_used + kTcRescale);
     const float alpha = raise && !first ? ex2(m_used - mx) : 1.f;
     if (raise) m_used = mx;
     const float base = m_used == -INFINITY ? 0.f : m_used;
     uint32_t w[64];
-    float lsum = 0.f;
+    float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < 128; c += 2) {
       const float p0 = ex2(v[c] - base), p1 = ex2(v[c + 1] - base);
-      lsum += p0 + p1;
+      ls4[(c >> 1) & 3] += p0 + p1;
       w[c / 2] = pack_half2(p0, p1);
     }
-    l = l * alpha + lsum;
+    l = l * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
     // O and the P buffer are free once O += P_{j-1} V_{j-1} has completed
     if (j > 0) {
       ok = __all_sync(0xffffffffu, tc_wait(bars + kBarODone, (blk_use + j - 1) & 1u, abort));
@@ -992,8 +1001,6 @@ __device__ void prefill_phase_tc(const AttnParams& p, unsigned char* sm, bool& b
   uint32_t kv_use[2] = {0u, 0u}, s_use[2] = {0u, 0u}, q_use = 0u, blk_use = 0u;
   while (true) {
     if (tid == 0) *tile = atomicAdd(&p.counts[kCntTileNext], 1);
-    if (tid >= kLoaderBase && tid < kLoaderBase + kLoaders && tid - kLoaderBase < 2)
-      reinterpret_cast<int*>(sm + TcLayout::kFull)[tid - kLoaderBase] = 1;
     __syncthreads();
     const int ti = *tile;
     const bool stop = ti >= ntiles || *abort;
