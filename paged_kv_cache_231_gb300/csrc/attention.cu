@@ -23,6 +23,8 @@
 //   * decode and the head-size-64 tiles run QK^T and PV on mma.sync m16n8k16 (fp16 in,
 //     fp32 accumulate) with the score accumulators reused in registers as the A
 //     operand of PV. Softmax works in base 2 (scores pre-scaled by log2 e).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <limits.h>
 #include <math.h>
 
@@ -657,43 +659,58 @@ __device__ void prefill_tile(const AttnParams& p, unsigned char* smem, int item_
 // Tensor-core prefill (head size 128), warp-specialised. A tile is 128 rows =
 // (128 / G) query positions x G query heads of one sequence and kv head, streamed
 // against 128-key blocks:
-//   warps 5-7 (loaders): Q tile and K/V blocks into 128-byte-swizzled shared memory
-//            with cp.async; completion is tracked by mbarriers (cp.async.mbarrier.arrive)
-//   warp 4 (lane 0):     S_j = Q K_j^T into TMEM buffer j % 2, then O += P_{j-1} V_{j-1},
-//            tcgen05.mma + tcgen05.commit
-//   warps 0-3 (softmax): thread r reads row r of S_j from TMEM, keeps a running max that
-//            is raised only when exceeded by more than 2^8 (then O and l are rescaled),
-//            writes P_j (fp16) to shared memory, and finally normalises O.
-// TMEM: S0 columns 0..127, S1 128..255, O 256..383. Every barrier phase is waited in
-// order by each role, so a parity wait never falls two phases behind.
+//   warp 5 (loader):   the Q tile and the K/V boxes of each block by TMA, straight from
+//            the paged cache into 128-byte-swizzled shared memory. A box is R
+//            consecutive keys of one cache block (R = the largest power of two <= 128
+//            dividing the block size) and is issued by one lane. Value rows of keys
+//            that are unmapped or past the tile's last visible key are zero-filled with
+//            cp.async instead, so that masked columns meet zeros in P V. K and V
+//            stages are released separately: K_{j+2} streams in once S_j is computed,
+//            V_{j+2} once O += P_j V_j is.
+//   warp 4 (lane 0):   tcgen05.mma issuer. S_j = Q K_j^T into TMEM buffer j % 2 and
+//            O += P_j V_j are each issued as soon as their operands are ready.
+//   warps 0-3 (softmax): thread r reads row r of S_j from TMEM, masks it by key
+//            validity (block table entries looked up by the warp itself) and causality,
+//            keeps a running max that is raised only when exceeded by more than 2^8
+//            (then O and l are rescaled), writes P_j (fp16) to shared memory, and
+//            finally normalises O.
+// TMEM: S0 columns 0..127, S1 128..255, O 256..383. Each role waits every phase of the
+// barriers it consumes in order, and no producer can run two phases ahead of a
+// consumer, so parity waits never alias.
 // ----------------------------------------------------------------------------------
+struct TcMaps {     // TMA descriptors (kernel parameters)
+  CUtensorMap q;    // query [tokens][Hq][128], box 64 x G x 128/G
+  CUtensorMap k;    // key cache [blocks * block_size][Hkv][128], box 64 x 1 x R
+  CUtensorMap v;    // value cache, same geometry
+};
 struct TcLayout {  // byte offsets from a 1024-byte-aligned base
-  static constexpr uint32_t kQ = 0;                  // 2 x [128][64] fp16 sub-tiles
-  static constexpr uint32_t kK = 32768;              // 2 stages x 32 KB
-  static constexpr uint32_t kV = kK + 65536;         // 2 stages x 32 KB
-  static constexpr uint32_t kP = kV + 65536;         // 32 KB
-  static constexpr uint32_t kRowOff = kP + 32768;    // 2 stages x 128 int64
-  static constexpr uint32_t kValid = kRowOff + 2048; // 2 stages x 128-bit mask of mapped keys
-  static constexpr uint32_t kBars = kValid + 32;     // mbarriers (see TcBar)
-  static constexpr uint32_t kTmem = kBars + 128;     // TMEM base address
-  static constexpr uint32_t kTile = kTmem + 4;       // current tile index
-  static constexpr uint32_t kAbort = kTile + 4;      // set when a bounded wait gives up
+  static constexpr uint32_t kQ = 0;               // 2 x [128][64] fp16 sub-tiles
+  static constexpr uint32_t kK = 32768;           // 2 stages x 32 KB
+  static constexpr uint32_t kV = kK + 65536;      // 2 stages x 32 KB
+  static constexpr uint32_t kP = kV + 65536;      // 32 KB
+  static constexpr uint32_t kBars = kP + 32768;   // mbarriers (see TcBar)
+  static constexpr uint32_t kTmem = kBars + 128;  // TMEM base address
+  static constexpr uint32_t kTile = kTmem + 4;    // current tile index
+  static constexpr uint32_t kAbort = kTile + 4;   // set when a bounded wait gives up
   static constexpr uint32_t kEnd = kAbort + 8;
 };
 enum TcBar {  // mbarrier slots
-  kBarQFull = 0,     // count 96: loaders' Q copies landed
-  kBarKvFull0 = 1,   // + stage, count 192: loaders' K/V copies landed and flags written
-  kBarKvEmpty0 = 3,  // + stage, count 1: MMA that read the stage completed
-  kBarSFull0 = 5,    // + buffer, count 1: S_j in TMEM
-  kBarPFull = 7,     // count 128: softmax wrote P_j and is done with S_j
-  kBarODone = 8,     // count 1: O += P_j V_j completed
-  kNumBars = 9
+  kBarQFull = 0,     // count 1 + tx: Q boxes landed
+  kBarKFull0 = 1,    // + stage, count 1 + tx: K boxes landed
+  kBarVFull0 = 3,    // + stage, count 32 + tx: V boxes and zero-filled rows landed
+  kBarKEmpty0 = 5,   // + stage, count 1: the S = Q K^T that read the stage completed
+  kBarVEmpty0 = 7,   // + stage, count 1: the O += P V that read the stage completed
+  kBarSFull0 = 9,    // + buffer, count 1: S_j in TMEM
+  kBarPFull = 11,    // count 128: softmax wrote P_j and is done with S_j
+  kBarODone = 12,    // count 1: O += P_j V_j completed
+  kBarDrain = 13,    // count 1: MMAs in flight when a wait gave up
+  kNumBars = 14
 };
+static_assert(kNumBars * 8 <= 128, "mbarrier slots");
 constexpr uint32_t kTcWaitTries = 1u << 22;
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 192;
 constexpr int kMmaThread = 128;    // lane 0 of warp 4
-constexpr int kLoaderBase = 160;   // warps 5-7
-constexpr int kLoaders = 96;
+constexpr int kLoaderWarp = 5;
 constexpr float kTcRescale = 8.f;  // log2 of the largest weight a stale max may give
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -703,9 +720,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ void mbar_arrive_cp_async(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar))
                : "memory");
-}
-__device__ __forceinline__ void loader_sync() {
-  asm volatile("bar.sync 2, 96;\n" ::: "memory");
 }
 // bounded wait that also gives up when another thread of the CTA already did
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -747,113 +761,160 @@ __device__ __forceinline__ TcTile tc_tile(const AttnParams& p, int t) {
   return d;
 }
 
-// Loader warps: Q tile, then every K/V block of the tile.
-__device__ void tc_loader(const AttnParams& p, unsigned char* sm, const TcTile& t,
-                          uint32_t (&kv_use)[2], bool& bad) {
+// Loader warp: Q tile, then the K and V boxes of every block of the tile.
+__device__ void tc_loader(const AttnParams& p, const TcMaps& maps, unsigned char* sm,
+                          const TcTile& t, uint32_t (&k_use)[2], uint32_t (&v_use)[2],
+                          bool& bad) {
   constexpr int D = 128;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
-  const int lt = threadIdx.x - kLoaderBase;
-  unsigned char* Qs = sm + TcLayout::kQ;
-  for (int i = lt; i < 128 * 16; i += kLoaders) {
-    const int r = i >> 4, c = i & 15;
-    const int pl = r / p.G;
-    const bool ok = r < t.PT * p.G && pl < t.nq;
-    const __half* src = ok ? p.q + (int64_t)(t.cu0 + t.q0 + pl) * p.q_stride +
-                                 (int64_t)(t.h * p.G + r % p.G) * D + c * 8
-                           : p.q;
-    cp_async_16(Qs + (c >> 3) * 16384 + tc::sw128(r, c & 7), src, ok ? 16 : 0);
+  const int lane = threadIdx.x & 31;
+  const int R = p.tc_rows, nbox = 128 / R;
+  if (lane == 0) {
+    // rows past the tile's positions hold other tokens (or zeros past the last token)
+    // and are never written out
+    unsigned char* Qs = sm + TcLayout::kQ;
+    tc::mbar_arrive_expect_tx(bars + kBarQFull, (uint32_t)(t.PT * p.G) * 256u);
+    tc::tma_load_3d(Qs, &maps.q, 0, t.h * p.G, t.cu0 + t.q0, bars + kBarQFull);
+    tc::tma_load_3d(Qs + 16384, &maps.q, 64, t.h * p.G, t.cu0 + t.q0, bars + kBarQFull);
   }
-  mbar_arrive_cp_async(bars + kBarQFull);
   for (int j = 0; j < t.nblk; ++j) {
     const int s = j & 1;
-    if (kv_use[s] > 0 && !tc_wait(bars + kBarKvEmpty0 + s, (kv_use[s] - 1) & 1u, abort))
-      return;
-    int64_t* rowoff = reinterpret_cast<int64_t*>(sm + TcLayout::kRowOff) + s * 128;
-    uint32_t* valid = reinterpret_cast<uint32_t*>(sm + TcLayout::kValid) + s * 4;
-    // every lane of a loader warp runs the same number of rows (32-row words of the mask)
-    for (int r = lt; r < 128; r += kLoaders) {
-      const int key = j * 128 + r;
-      int64_t off = -1;
-      if (key < t.kend) {
-        off = key_row_offset(p, t.b, t.h, key);
-        if (off < 0) bad = true;
+    const int kbase = j * 128;
+    // box `lane`: keys [key0, key0 + R) of one cache block
+    const int key0 = kbase + lane * R;
+    bool mapped = false;
+    int row = 0;
+    if (lane < nbox && key0 < t.kend) {
+      const int col = p.bs_shift >= 0 ? key0 >> p.bs_shift : key0 / p.BS;
+      const int blk = __ldg(&p.block_table[(int64_t)t.b * p.MB + col]);
+      if (blk >= 0 && (int64_t)blk < p.NB) {
+        mapped = true;
+        row = blk * p.BS + (key0 - col * p.BS);
+      } else {
+        bad = true;
       }
-      rowoff[r] = off;
-      const uint32_t word = __ballot_sync(0xffffffffu, off >= 0);
-      if ((r & 31) == 0) valid[r >> 5] = word;
     }
-    loader_sync();
+    const bool whole = mapped && key0 + R <= t.kend;
+    // K: every mapped box; keys past the visible range are masked by the softmax
+    bool ok = k_use[s] == 0 || tc_wait(bars + kBarKEmpty0 + s, (k_use[s] - 1) & 1u, abort);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    ++k_use[s];
+    const uint32_t kbits = __ballot_sync(0xffffffffu, mapped);
+    if (lane == 0)
+      tc::mbar_arrive_expect_tx(bars + kBarKFull0 + s, (uint32_t)__popc(kbits) * R * 256u);
+    __syncwarp();
     unsigned char* Ks = sm + TcLayout::kK + s * 32768;
-    unsigned char* Vs = sm + TcLayout::kV + s * 32768;
-    for (int i = lt; i < 128 * 16; i += kLoaders) {
-      const int r = i >> 4, c = i & 15;
-      const int64_t off = rowoff[r];
-      const uint32_t dst = (uint32_t)(c >> 3) * 16384u + tc::sw128(r, c & 7);
-      cp_async_16(Ks + dst, off >= 0 ? p.kc + off + c * 8 : p.kc, off >= 0 ? 16 : 0);
-      cp_async_16(Vs + dst, off >= 0 ? p.vc + off + c * 8 : p.vc, off >= 0 ? 16 : 0);
+    if (mapped) {
+      tc::tma_load_3d(Ks + lane * R * 128, &maps.k, 0, t.h, row, bars + kBarKFull0 + s);
+      tc::tma_load_3d(Ks + 16384 + lane * R * 128, &maps.k, 64, t.h, row,
+                      bars + kBarKFull0 + s);
     }
-    mbar_arrive_cp_async(bars + kBarKvFull0 + s);
-    mbar_arrive(bars + kBarKvFull0 + s);
-    ++kv_use[s];
+    // V: whole boxes by TMA, the rest through zero-filling cp.async
+    ok = v_use[s] == 0 || tc_wait(bars + kBarVEmpty0 + s, (v_use[s] - 1) & 1u, abort);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    ++v_use[s];
+    const uint32_t vbits = __ballot_sync(0xffffffffu, whole);
+    if (lane == 0)
+      tc::mbar_expect_tx(bars + kBarVFull0 + s, (uint32_t)__popc(vbits) * R * 256u);
+    __syncwarp();
+    unsigned char* Vs = sm + TcLayout::kV + s * 32768;
+    if (whole) {
+      tc::tma_load_3d(Vs + lane * R * 128, &maps.v, 0, t.h, row, bars + kBarVFull0 + s);
+      tc::tma_load_3d(Vs + 16384 + lane * R * 128, &maps.v, 64, t.h, row,
+                      bars + kBarVFull0 + s);
+    }
+    uint32_t rest = __ballot_sync(0xffffffffu, lane < nbox && !whole);
+    while (rest) {
+      const int i = __ffs(rest) - 1;
+      rest &= rest - 1;
+      const int rowi = __shfl_sync(0xffffffffu, row, i);
+      const int mi = __shfl_sync(0xffffffffu, mapped ? 1 : 0, i);
+      const int k0 = kbase + i * R;
+      for (int idx = lane; idx < R * 16; idx += 32) {
+        const int rr = idx >> 4, c = idx & 15;
+        const bool live = mi && k0 + rr < t.kend;
+        const __half* src =
+            live ? p.vc + (((int64_t)(rowi + rr) * p.Hkv + t.h) * D + c * 8) : p.vc;
+        cp_async_16(Vs + (c >> 3) * 16384 + tc::sw128(i * R + rr, c & 7), src, live ? 16 : 0);
+      }
+    }
+    mbar_arrive_cp_async(bars + kBarVFull0 + s);
   }
 }
 
-// Warp 4, lane 0: the MMA stream of the tile.
+// Warp 4, lane 0: the MMA stream of the tile. S_jq = Q K_jq^T may be issued once K_jq
+// landed and S buffer jq % 2 is free (P_{jq-2} V_{jq-2} issued, i.e. the softmax is done
+// with S_{jq-2}); O += P_jp V_jp once P_jp is written and V_jp landed.
 __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
-                       uint32_t tmem, uint32_t q_use, uint32_t (&kv_use)[2],
-                       uint32_t& blk_use) {
+                       uint32_t tmem, uint32_t q_use, uint32_t (&k_use)[2],
+                       uint32_t (&v_use)[2], uint32_t& blk_use) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const uint32_t idesc_qk = tc::idesc_f16(128, 128, false, false);
   const uint32_t idesc_pv = tc::idesc_f16(128, 128, false, true);
   const uint32_t qa = smem_u32(sm + TcLayout::kQ), pa = smem_u32(sm + TcLayout::kP);
   if (!tc_wait(bars + kBarQFull, q_use & 1u, abort)) return;
-  tc::fence_async_shared();
-  auto issue_pv = [&](int j) -> bool {
-    // P_j written and S_j no longer read by the softmax warps
-    if (!tc_wait(bars + kBarPFull, (blk_use + j) & 1u, abort)) return false;
-    tc::fence_after_sync();
-    const uint32_t va = smem_u32(sm + TcLayout::kV + (j & 1) * 32768);
+  int jq = 0, jp = 0;
+  uint32_t idle = 0;
+  while (jp < t.nblk) {
+    bool progress = false;
+    if (jq < t.nblk && jq <= jp + 1) {
+      const int s = jq & 1;
+      if (tc::mbar_test(bars + kBarKFull0 + s, k_use[s] & 1u)) {
+        ++k_use[s];
+        tc::fence_after_sync();
+        const uint32_t ka = smem_u32(sm + TcLayout::kK + s * 32768);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t poff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-      tc::mma_f16(tmem + 256, tc::smem_desc(pa + poff, 16, 1024),
-                  tc::smem_desc(va + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv,
-                  (j > 0 || ks > 0) ? 1u : 0u);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+          tc::mma_f16(tmem + s * 128, tc::smem_desc(qa + koff, 16, 1024),
+                      tc::smem_desc(ka + koff, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
+        }
+        tc::commit(bars + kBarSFull0 + s);
+        tc::commit(bars + kBarKEmpty0 + s);
+        ++jq;
+        progress = true;
+      }
     }
-    tc::commit(bars + kBarODone);
-    tc::commit(bars + kBarKvEmpty0 + (j & 1));
-    return true;
-  };
-  for (int j = 0; j < t.nblk; ++j) {
-    const int s = j & 1;
-    if (!tc_wait(bars + kBarKvFull0 + s, kv_use[s] & 1u, abort)) return;
-    ++kv_use[s];
-    tc::fence_async_shared();
-    tc::fence_after_sync();
-    const uint32_t ka = smem_u32(sm + TcLayout::kK + s * 32768);
+    if (jp < jq) {
+      const int s = jp & 1;
+      if (tc::mbar_test(bars + kBarPFull, (blk_use + jp) & 1u) &&
+          tc::mbar_test(bars + kBarVFull0 + s, v_use[s] & 1u)) {
+        ++v_use[s];
+        tc::fence_async_shared();   // zero-filled value rows were written by cp.async
+        tc::fence_after_sync();
+        const uint32_t va = smem_u32(sm + TcLayout::kV + s * 32768);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-      tc::mma_f16(tmem + s * 128, tc::smem_desc(qa + koff, 16, 1024),
-                  tc::smem_desc(ka + koff, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t poff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+          tc::mma_f16(tmem + 256, tc::smem_desc(pa + poff, 16, 1024),
+                      tc::smem_desc(va + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv,
+                      (jp > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc::commit(bars + kBarODone);
+        tc::commit(bars + kBarVEmpty0 + s);
+        ++jp;
+        progress = true;
+      }
     }
-    tc::commit(bars + kBarSFull0 + s);
-    if (j > 0 && !issue_pv(j - 1)) return;
+    if (progress) {
+      idle = 0;
+    } else if (++idle >= kTcWaitTries || ((idle & 255u) == 0 && *abort)) {
+      *abort = 1;
+      return;
+    }
   }
-  issue_pv(t.nblk - 1);
   blk_use += t.nblk;
 }
 
 // Warps 0-3: softmax and the normalised output of row threadIdx.x.
 __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile& t,
-                           uint32_t tmem, uint32_t (&kv_use)[2], uint32_t (&s_use)[2],
-                           uint32_t& blk_use) {
+                           uint32_t tmem, uint32_t (&s_use)[2], uint32_t& blk_use) {
   constexpr int D = 128;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
-  const int r = threadIdx.x;
+  const int r = threadIdx.x, lane = r & 31;
   const int pl = r / p.G;
   const bool rvalid = r < t.PT * p.G && pl < t.nq;
   const int lim = rvalid ? (int)min64((int64_t)t.P + t.q0 + pl, INT32_MAX) : -1;
@@ -863,18 +924,27 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
   bool ok = true;
   for (int j = 0; j < t.nblk && ok; ++j) {
     const int s = j & 1;
-    // flags of block j, then S_j
-    ok = tc_wait(bars + kBarKvFull0 + s, kv_use[s] & 1u, abort);
-    ++kv_use[s];
-    ok = ok && tc_wait(bars + kBarSFull0 + s, s_use[s] & 1u, abort);
+    const int kbase = j * 128;
+    // key validity of block j: lane covers keys [kbase + 4 lane, + 4), which lie in one
+    // cache block because the block size is a multiple of 8; key c of the block is bit
+    // c / 4 of words[c % 4]
+    const int key0 = kbase + 4 * lane;
+    bool page = false;
+    if (key0 < t.kend) {
+      const int col = p.bs_shift >= 0 ? key0 >> p.bs_shift : key0 / p.BS;
+      const int blk = __ldg(&p.block_table[(int64_t)t.b * p.MB + col]);
+      page = blk >= 0 && (int64_t)blk < p.NB;
+    }
+    uint32_t words[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) words[i] = __ballot_sync(0xffffffffu, page && key0 + i < t.kend);
+    ok = tc_wait(bars + kBarSFull0 + s, s_use[s] & 1u, abort);
     ++s_use[s];
     ok = __all_sync(0xffffffffu, ok);   // TMEM loads below are warp-collective
     if (!ok) break;
     tc::fence_after_sync();
-    const int kbase = j * 128;
-    const uint4 vm = *reinterpret_cast<const uint4*>(sm + TcLayout::kValid + s * 16);
     const int cut = lim - kbase + 1;  // columns below cut are causally visible to this row
-    const bool full = (vm.x & vm.y & vm.z & vm.w) == 0xffffffffu && cut >= 128;
+    const bool full = (words[0] & words[1] & words[2] & words[3]) == 0xffffffffu && cut >= 128;
     // the whole row of S_j in one TMEM round trip
     float v[128];
     {
@@ -892,10 +962,9 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
         mx4[c & 3] = fmaxf(mx4[c & 3], v[c]);
       }
     } else {
-      const uint32_t words[4] = {vm.x, vm.y, vm.z, vm.w};
 #pragma unroll
       for (int c = 0; c < 128; ++c) {
-        const bool vis = c < cut && ((words[c >> 5] >> (c & 31)) & 1u);
+        const bool vis = c < cut && ((words[c & 3] >> (c >> 2)) & 1u);
         v[c] = vis ? v[c] * sl2 : -INFINITY;
         mx4[c & 3] = fmaxf(mx4[c & 3], v[c]);
       }
@@ -969,25 +1038,34 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
 }
 
 // Tiles from the planner's counter; barriers and 512 TMEM columns held throughout.
-__device__ void prefill_phase_tc(const AttnParams& p, unsigned char* sm, bool& bad) {
+__device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsigned char* sm,
+                                 bool& bad) {
   const int ntiles = p.counts[kCntTiles];
   if (ntiles == 0) return;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TcLayout::kTmem);
   volatile int* tile = reinterpret_cast<volatile int*>(sm + TcLayout::kTile);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    tc::mbar_init(bars + kBarQFull, kLoaders);
+    tc::mbar_init(bars + kBarQFull, 1);
     for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(bars + kBarKvFull0 + s, 2 * kLoaders);
-      tc::mbar_init(bars + kBarKvEmpty0 + s, 1);
+      tc::mbar_init(bars + kBarKFull0 + s, 1);
+      tc::mbar_init(bars + kBarVFull0 + s, 32);
+      tc::mbar_init(bars + kBarKEmpty0 + s, 1);
+      tc::mbar_init(bars + kBarVEmpty0 + s, 1);
       tc::mbar_init(bars + kBarSFull0 + s, 1);
     }
     tc::mbar_init(bars + kBarPFull, 128);
     tc::mbar_init(bars + kBarODone, 1);
+    tc::mbar_init(bars + kBarDrain, 1);
     tc::mbar_init_fence();
     *abort = 0;
+  }
+  if (warp == kLoaderWarp && lane == 0) {
+    tc::tma_prefetch_desc(&maps.q);
+    tc::tma_prefetch_desc(&maps.k);
+    tc::tma_prefetch_desc(&maps.v);
   }
   if (warp == 0) {
     tc::tmem_alloc(tslot, 512);
@@ -998,7 +1076,9 @@ __device__ void prefill_phase_tc(const AttnParams& p, unsigned char* sm, bool& b
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
   // per-role phase counters (each role waits every phase it depends on, in order)
-  uint32_t kv_use[2] = {0u, 0u}, s_use[2] = {0u, 0u}, q_use = 0u, blk_use = 0u;
+  uint32_t k_use[2] = {0u, 0u}, v_use[2] = {0u, 0u}, s_use[2] = {0u, 0u};
+  uint32_t q_use = 0u, blk_use = 0u;
+  bool mma_aborted = false;
   while (true) {
     if (tid == 0) *tile = atomicAdd(&p.counts[kCntTileNext], 1);
     __syncthreads();
@@ -1008,20 +1088,36 @@ __device__ void prefill_phase_tc(const AttnParams& p, unsigned char* sm, bool& b
     if (stop) break;
     const TcTile t = tc_tile(p, ti);
     if (tid < 128) {
-      tc_softmax(p, sm, t, tmem, kv_use, s_use, blk_use);
+      tc_softmax(p, sm, t, tmem, s_use, blk_use);
     } else if (tid == kMmaThread) {
-      tc_mma(p, sm, t, tmem, q_use, kv_use, blk_use);
-    } else if (tid >= kLoaderBase) {
-      tc_loader(p, sm, t, kv_use, bad);
+      tc_mma(p, sm, t, tmem, q_use, k_use, v_use, blk_use);
+      mma_aborted = *abort != 0;
+    } else if (warp == kLoaderWarp) {
+      tc_loader(p, maps, sm, t, k_use, v_use, bad);
     }
     ++q_use;
-    // the next tile reuses Q, the flags and the "fully valid" words
+    // the next tile rewrites Q: every MMA of this tile has completed (the softmax waited
+    // for the last O += P V, and MMAs complete in issue order)
     cp_async_wait<0>();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
   }
-  if (*abort && tid == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
+  if (*abort) {
+    // a wait gave up: let the copies and MMAs this CTA issued land before it exits
+    if (tid == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
+    if (tid == kMmaThread && mma_aborted) {
+      tc::commit(bars + kBarDrain);
+      tc::mbar_wait(bars + kBarDrain, 0, kTcWaitTries);
+    }
+    if (warp == kLoaderWarp && lane == 0) {
+      if (q_use > 0) tc::mbar_wait(bars + kBarQFull, (q_use - 1) & 1u, kTcWaitTries);
+      for (int s = 0; s < 2; ++s) {
+        if (k_use[s] > 0) tc::mbar_wait(bars + kBarKFull0 + s, (k_use[s] - 1) & 1u, kTcWaitTries);
+        if (v_use[s] > 0) tc::mbar_wait(bars + kBarVFull0 + s, (v_use[s] - 1) & 1u, kTcWaitTries);
+      }
+    }
+  }
   cp_async_wait<0>();
   tc::fence_before_sync();
   __syncthreads();
@@ -1029,14 +1125,15 @@ __device__ void prefill_phase_tc(const AttnParams& p, unsigned char* sm, bool& b
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
-// Persistent tensor-core prefill kernel: one CTA of 8 warps per SM, tiles from the
+// Persistent tensor-core prefill kernel: one CTA of 6 warps per SM, tiles from the
 // planner's counter.
-__global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(AttnParams p) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(AttnParams p, const __grid_constant__ TcMaps maps) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   bool bad = false;
-  prefill_phase_tc(p, smem, bad);
+  prefill_phase_tc(p, maps, smem, bad);
   if (bad) flag_status(p.status, PKV_DEV_BAD_BLOCK);
 }
 constexpr size_t kTcSmem = TcLayout::kEnd + 1024;   // + slack for the 1024-byte alignment
@@ -1430,6 +1527,48 @@ __global__ void __launch_bounds__(kPrologueThreads) prologue_kernel(AttnParams p
   paged_scatter_thread(sp, (int64_t)(blockIdx.x - 1) * kPrologueThreads + threadIdx.x);
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// fp16 tensor of dims (d0, d1, d2), innermost first, byte strides s1 and s2 of dims 1 and
+// 2, boxes of b0 x b1 x b2 elements in the 128-byte swizzle; reads past the end give 0
+bool encode_f16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t unit[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// Descriptors of the tensor-core prefill: query tile boxes of 64 columns x G heads x
+// 128/G positions, and cache boxes of 64 columns x 1 kv head x tc_rows keys.
+bool make_tc_maps(const AttnParams& p, TcMaps* m) {
+  const uint64_t row_bytes = 128 * 2;
+  return encode_f16_3d(&m->q, p.q, 128, (uint64_t)p.Hq, (uint64_t)p.T, row_bytes,
+                       (uint64_t)p.q_stride * 2, 64, (uint32_t)p.G, (uint32_t)(128 / p.G)) &&
+         encode_f16_3d(&m->k, p.kc, 128, (uint64_t)p.Hkv, (uint64_t)p.NB * p.BS, row_bytes,
+                       (uint64_t)p.Hkv * row_bytes, 64, 1, (uint32_t)p.tc_rows) &&
+         encode_f16_3d(&m->v, p.vc, 128, (uint64_t)p.Hkv, (uint64_t)p.NB * p.BS, row_bytes,
+                       (uint64_t)p.Hkv * row_bytes, 64, 1, (uint32_t)p.tc_rows);
+}
+
 template <int D, int NS, int NSTAGE>
 cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cudaStream_t s) {
   constexpr size_t smem = DecodeRing<D, NS>::kBytes > TileRing<D, NSTAGE>::kBytes
@@ -1476,6 +1615,8 @@ cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cud
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || !p.tc_prefill) return e;
+  TcMaps maps;
+  if (!make_tc_maps(p, &maps)) return cudaErrorInvalidValue;
   // programmatic dependent launch: prefill CTAs take SMs as decode CTAs retire
   ProfScope ps("prefill_tc", s);
   cudaLaunchConfig_t cfg = {};
@@ -1488,7 +1629,7 @@ cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cud
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, p);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, p, maps);
 }
 
 }  // namespace

@@ -99,6 +99,7 @@ struct AttnParams {
   int pre_rows;            // query positions per prefill tile
   int total_warps;         // warps of the persistent kernel
   int tc_prefill;          // 1: prefill tiles of 128 rows on tcgen05 (head size 128)
+  int tc_rows;             // keys per TMA box of the tcgen05 prefill (power of two, >= 8)
   // workspace
   int32_t* counts;         // kCnt* words
   DecSeq* dec_seqs;        // stream-K

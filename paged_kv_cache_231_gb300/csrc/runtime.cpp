@@ -87,6 +87,7 @@ struct PagedLayout {
   int max_splits = 1;
   int fixed_splits = 1;
   int streamk = 0;
+  int tc_rows = 0;   // > 0: prefill tiles on the tensor core, TMA boxes of tc_rows keys
   int64_t dec_bound = 0, pre_bound = 0, slot_bound = 0;
   size_t off_counts = 0, off_seqs = 0, off_done = 0, off_dec = 0, off_pre = 0,
          off_slot_tok = 0, off_slot_spl = 0, off_po = 0, off_pm = 0, off_pl = 0, total = 0;
@@ -175,9 +176,16 @@ int check_paged(const pkv_paged_attention_args* a, bool attention, PagedLayout* 
     L->fixed_splits = a->fixed_splits;
   }
   L->dec_rows = (int)(16 / G);
-  // prefill tiles: 128 rows on the 5th-generation tensor core (head size 128), else
-  // 64 rows of mma.sync tiles
-  L->pre_rows = a->head_size == 128 ? (int)(128 / G) : 4 * L->dec_rows;
+  // prefill tiles: 128 rows on the 5th-generation tensor core (head size 128, cache
+  // blocks of a multiple of 8 keys, loaded as TMA boxes of up to 128 keys), else 64 rows
+  // of mma.sync tiles
+  if (a->head_size == 128 && a->block_size % 8 == 0 &&
+      a->num_blocks * a->block_size <= INT32_MAX) {
+    int r = 8;
+    while (r < 128 && a->block_size % (2 * r) == 0) r *= 2;
+    L->tc_rows = r;
+  }
+  L->pre_rows = L->tc_rows > 0 ? (int)(128 / G) : 4 * L->dec_rows;
   const int64_t T = a->num_tokens, B = a->batch;
   L->dec_bound = L->streamk ? 0 : B * L->max_splits;
   L->pre_bound = ceil_div(T, L->pre_rows) + std::min<int64_t>(B, T / (L->dec_rows + 1));
@@ -411,7 +419,8 @@ int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
   ap.dec_rows = L.dec_rows;
   ap.pre_rows = L.pre_rows;
   ap.total_warps = num_sms_current() * attention_ctas_per_sm() * attention_warps_per_cta();
-  ap.tc_prefill = args->head_size == 128 ? 1 : 0;
+  ap.tc_prefill = L.tc_rows > 0 ? 1 : 0;
+  ap.tc_rows = L.tc_rows;
   ap.counts = reinterpret_cast<int32_t*>(ws + L.off_counts);
   ap.dec_seqs = reinterpret_cast<DecSeq*>(ws + L.off_seqs);
   ap.seg_done = reinterpret_cast<int32_t*>(ws + L.off_done);

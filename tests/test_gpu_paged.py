@@ -37,6 +37,10 @@ CASES = [
     (36, 6, 2, 64, 16, [10, 90, 3], [5, 6, 21], False, False),
     (37, 8, 2, 128, 5, [12, 0, 77], [1, 30, 4], False, True),
     (38, 4, 1, 64, 64, [1000, 2, 0], [1, 200, 129], True, False),
+    # tensor-core prefill: 16-key boxes over 48-key blocks, 126-row tiles (G = 3)
+    (39, 6, 2, 128, 48, [0, 200, 33], [150, 7, 300], False, True),
+    # tensor-core prefill: 128-key boxes inside 256-key blocks
+    (30, 8, 1, 128, 256, [0, 700], [260, 129], True, False),
 ]
 
 
