@@ -659,14 +659,15 @@ __device__ void prefill_tile(const AttnParams& p, unsigned char* smem, int item_
 // Tensor-core prefill (head size 128), warp-specialised. A tile is 128 rows =
 // (128 / G) query positions x G query heads of one sequence and kv head, streamed
 // against 128-key blocks:
-//   warp 5 (loader):   the Q tile and the K/V boxes of each block by TMA, straight from
-//            the paged cache into 128-byte-swizzled shared memory. A box is R
-//            consecutive keys of one cache block (R = the largest power of two <= 128
-//            dividing the block size) and is issued by one lane. Value rows of keys
-//            that are unmapped or past the tile's last visible key are zero-filled with
-//            cp.async instead, so that masked columns meet zeros in P V. K and V
-//            stages are released separately: K_{j+2} streams in once S_j is computed,
-//            V_{j+2} once O += P_j V_j is.
+//   warps 5 and 6 (loaders): the Q tile and the K boxes (warp 5) and the V boxes
+//            (warp 6) of each block by TMA, straight from the paged cache into
+//            128-byte-swizzled shared memory. A box is R consecutive keys of one cache
+//            block (R = the largest power of two <= 128 dividing the block size) and is
+//            issued by one lane. Value rows of keys that are unmapped or past the tile's
+//            last visible key are zero-filled with cp.async instead, so that masked
+//            columns meet zeros in P V. K (3 stages) and V (2 stages) are released
+//            separately: K_{j+3} streams in once S_j is computed, V_{j+2} once
+//            O += P_j V_j is.
 //   warp 4 (lane 0):   tcgen05.mma issuer. S_j = Q K_j^T into TMEM buffer j % 2 and
 //            O += P_j V_j are each issued as soon as their operands are ready.
 //   warps 0-3 (softmax): thread r reads row r of S_j from TMEM, masks it by key
@@ -685,8 +686,8 @@ struct TcMaps {     // TMA descriptors (kernel parameters)
 };
 struct TcLayout {  // byte offsets from a 1024-byte-aligned base
   static constexpr uint32_t kQ = 0;               // 2 x [128][64] fp16 sub-tiles
-  static constexpr uint32_t kK = 32768;           // 2 stages x 32 KB
-  static constexpr uint32_t kV = kK + 65536;      // 2 stages x 32 KB
+  static constexpr uint32_t kK = 32768;           // kKStages x 32 KB
+  static constexpr uint32_t kV = kK + 98304;      // 2 stages x 32 KB
   static constexpr uint32_t kP = kV + 65536;      // 32 KB
   static constexpr uint32_t kBars = kP + 32768;   // mbarriers (see TcBar)
   static constexpr uint32_t kTmem = kBars + 128;  // TMEM base address
@@ -696,21 +697,23 @@ struct TcLayout {  // byte offsets from a 1024-byte-aligned base
 };
 enum TcBar {  // mbarrier slots
   kBarQFull = 0,     // count 1 + tx: Q boxes landed
-  kBarKFull0 = 1,    // + stage, count 1 + tx: K boxes landed
-  kBarVFull0 = 3,    // + stage, count 32 + tx: V boxes and zero-filled rows landed
-  kBarKEmpty0 = 5,   // + stage, count 1: the S = Q K^T that read the stage completed
-  kBarVEmpty0 = 7,   // + stage, count 1: the O += P V that read the stage completed
-  kBarSFull0 = 9,    // + buffer, count 1: S_j in TMEM
-  kBarPFull = 11,    // count 128: softmax wrote P_j and is done with S_j
-  kBarODone = 12,    // count 1: O += P_j V_j completed
-  kBarDrain = 13,    // count 1: MMAs in flight when a wait gave up
-  kNumBars = 14
+  kBarKFull0 = 1,    // + stage (3), count 1 + tx: K boxes landed
+  kBarVFull0 = 4,    // + stage (2), count 32 + tx: V boxes and zero-filled rows landed
+  kBarKEmpty0 = 6,   // + stage (3), count 1: the S = Q K^T that read the stage completed
+  kBarVEmpty0 = 9,   // + stage (2), count 1: the O += P V that read the stage completed
+  kBarSFull0 = 11,   // + buffer, count 1: S_j in TMEM
+  kBarPFull = 13,    // count 128: softmax wrote P_j and is done with S_j
+  kBarODone = 14,    // count 1: O += P_j V_j completed
+  kBarDrain = 15,    // count 1: MMAs in flight when a wait gave up
+  kNumBars = 16
 };
 static_assert(kNumBars * 8 <= 128, "mbarrier slots");
+constexpr int kKStages = 3;        // K ring depth (V has 2 stages)
 constexpr uint32_t kTcWaitTries = 1u << 22;
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;
 constexpr int kMmaThread = 128;    // lane 0 of warp 4
-constexpr int kLoaderWarp = 5;
+constexpr int kKLoaderWarp = 5;
+constexpr int kVLoaderWarp = 6;
 constexpr float kTcRescale = 8.f;  // log2 of the largest weight a stale max may give
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -761,15 +764,40 @@ __device__ __forceinline__ TcTile tc_tile(const AttnParams& p, int t) {
   return d;
 }
 
-// Loader warp: Q tile, then the K and V boxes of every block of the tile.
-__device__ void tc_loader(const AttnParams& p, const TcMaps& maps, unsigned char* sm,
-                          const TcTile& t, uint32_t (&k_use)[2], uint32_t (&v_use)[2],
-                          bool& bad) {
-  constexpr int D = 128;
+// Box `lane` of key block j: keys [key0, key0 + R) of one cache block, with its first
+// row in the cache when the block-table entry is valid.
+struct TcBox {
+  int key0, row;
+  bool mapped;
+};
+__device__ __forceinline__ TcBox tc_box(const AttnParams& p, const TcTile& t, int j, int lane,
+                                        bool& unmapped) {
+  const int R = p.tc_rows;
+  TcBox x;
+  x.key0 = j * 128 + lane * R;
+  x.row = 0;
+  x.mapped = false;
+  if (lane < 128 / R && x.key0 < t.kend) {
+    const int col = p.bs_shift >= 0 ? x.key0 >> p.bs_shift : x.key0 / p.BS;
+    const int blk = __ldg(&p.block_table[(int64_t)t.b * p.MB + col]);
+    if (blk >= 0 && (int64_t)blk < p.NB) {
+      x.mapped = true;
+      x.row = blk * p.BS + (x.key0 - col * p.BS);
+    } else {
+      unmapped = true;
+    }
+  }
+  return x;
+}
+
+// Key loader warp: Q tile, then the K boxes of every block (keys past the visible range
+// and unmapped boxes are left as they are: the softmax masks them).
+__device__ void tc_load_k(const AttnParams& p, const TcMaps& maps, unsigned char* sm,
+                          const TcTile& t, uint32_t (&k_use)[kKStages], bool& bad) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const int lane = threadIdx.x & 31;
-  const int R = p.tc_rows, nbox = 128 / R;
+  const int R = p.tc_rows;
   if (lane == 0) {
     // rows past the tile's positions hold other tokens (or zeros past the last token)
     // and are never written out
@@ -778,59 +806,58 @@ __device__ void tc_loader(const AttnParams& p, const TcMaps& maps, unsigned char
     tc::tma_load_3d(Qs, &maps.q, 0, t.h * p.G, t.cu0 + t.q0, bars + kBarQFull);
     tc::tma_load_3d(Qs + 16384, &maps.q, 64, t.h * p.G, t.cu0 + t.q0, bars + kBarQFull);
   }
-  for (int j = 0; j < t.nblk; ++j) {
-    const int s = j & 1;
-    const int kbase = j * 128;
-    // box `lane`: keys [key0, key0 + R) of one cache block
-    const int key0 = kbase + lane * R;
-    bool mapped = false;
-    int row = 0;
-    if (lane < nbox && key0 < t.kend) {
-      const int col = p.bs_shift >= 0 ? key0 >> p.bs_shift : key0 / p.BS;
-      const int blk = __ldg(&p.block_table[(int64_t)t.b * p.MB + col]);
-      if (blk >= 0 && (int64_t)blk < p.NB) {
-        mapped = true;
-        row = blk * p.BS + (key0 - col * p.BS);
-      } else {
-        bad = true;
-      }
-    }
-    const bool whole = mapped && key0 + R <= t.kend;
-    // K: every mapped box; keys past the visible range are masked by the softmax
-    bool ok = k_use[s] == 0 || tc_wait(bars + kBarKEmpty0 + s, (k_use[s] - 1) & 1u, abort);
+  for (int j = 0, s = 0; j < t.nblk; ++j, s = s + 1 == kKStages ? 0 : s + 1) {
+    const TcBox x = tc_box(p, t, j, lane, bad);
+    const bool ok = k_use[s] == 0 || tc_wait(bars + kBarKEmpty0 + s, (k_use[s] - 1) & 1u, abort);
     if (!__all_sync(0xffffffffu, ok)) return;
     ++k_use[s];
-    const uint32_t kbits = __ballot_sync(0xffffffffu, mapped);
+    const uint32_t bits = __ballot_sync(0xffffffffu, x.mapped);
     if (lane == 0)
-      tc::mbar_arrive_expect_tx(bars + kBarKFull0 + s, (uint32_t)__popc(kbits) * R * 256u);
+      tc::mbar_arrive_expect_tx(bars + kBarKFull0 + s, (uint32_t)__popc(bits) * R * 256u);
     __syncwarp();
     unsigned char* Ks = sm + TcLayout::kK + s * 32768;
-    if (mapped) {
-      tc::tma_load_3d(Ks + lane * R * 128, &maps.k, 0, t.h, row, bars + kBarKFull0 + s);
-      tc::tma_load_3d(Ks + 16384 + lane * R * 128, &maps.k, 64, t.h, row,
+    if (x.mapped) {
+      tc::tma_load_3d(Ks + lane * R * 128, &maps.k, 0, t.h, x.row, bars + kBarKFull0 + s);
+      tc::tma_load_3d(Ks + 16384 + lane * R * 128, &maps.k, 64, t.h, x.row,
                       bars + kBarKFull0 + s);
     }
-    // V: whole boxes by TMA, the rest through zero-filling cp.async
-    ok = v_use[s] == 0 || tc_wait(bars + kBarVEmpty0 + s, (v_use[s] - 1) & 1u, abort);
+  }
+}
+
+// Value loader warp: whole boxes by TMA, the rest of the rows through zero-filling cp.async
+// (rows of unmapped or not-yet-visible keys must be zeros for P V).
+__device__ void tc_load_v(const AttnParams& p, const TcMaps& maps, unsigned char* sm,
+                          const TcTile& t, uint32_t (&v_use)[2]) {
+  constexpr int D = 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
+  const int lane = threadIdx.x & 31;
+  const int R = p.tc_rows;
+  bool unmapped = false;   // reported by the key loader
+  for (int j = 0; j < t.nblk; ++j) {
+    const int s = j & 1;
+    const TcBox x = tc_box(p, t, j, lane, unmapped);
+    const bool whole = x.mapped && x.key0 + R <= t.kend;
+    const bool ok = v_use[s] == 0 || tc_wait(bars + kBarVEmpty0 + s, (v_use[s] - 1) & 1u, abort);
     if (!__all_sync(0xffffffffu, ok)) return;
     ++v_use[s];
-    const uint32_t vbits = __ballot_sync(0xffffffffu, whole);
+    const uint32_t bits = __ballot_sync(0xffffffffu, whole);
     if (lane == 0)
-      tc::mbar_expect_tx(bars + kBarVFull0 + s, (uint32_t)__popc(vbits) * R * 256u);
+      tc::mbar_expect_tx(bars + kBarVFull0 + s, (uint32_t)__popc(bits) * R * 256u);
     __syncwarp();
     unsigned char* Vs = sm + TcLayout::kV + s * 32768;
     if (whole) {
-      tc::tma_load_3d(Vs + lane * R * 128, &maps.v, 0, t.h, row, bars + kBarVFull0 + s);
-      tc::tma_load_3d(Vs + 16384 + lane * R * 128, &maps.v, 64, t.h, row,
+      tc::tma_load_3d(Vs + lane * R * 128, &maps.v, 0, t.h, x.row, bars + kBarVFull0 + s);
+      tc::tma_load_3d(Vs + 16384 + lane * R * 128, &maps.v, 64, t.h, x.row,
                       bars + kBarVFull0 + s);
     }
-    uint32_t rest = __ballot_sync(0xffffffffu, lane < nbox && !whole);
+    uint32_t rest = __ballot_sync(0xffffffffu, lane < 128 / R && !whole);
     while (rest) {
       const int i = __ffs(rest) - 1;
       rest &= rest - 1;
-      const int rowi = __shfl_sync(0xffffffffu, row, i);
-      const int mi = __shfl_sync(0xffffffffu, mapped ? 1 : 0, i);
-      const int k0 = kbase + i * R;
+      const int rowi = __shfl_sync(0xffffffffu, x.row, i);
+      const int mi = __shfl_sync(0xffffffffu, x.mapped ? 1 : 0, i);
+      const int k0 = j * 128 + i * R;
       for (int idx = lane; idx < R * 16; idx += 32) {
         const int rr = idx >> 4, c = idx & 15;
         const bool live = mi && k0 + rr < t.kend;
@@ -847,7 +874,7 @@ __device__ void tc_loader(const AttnParams& p, const TcMaps& maps, unsigned char
 // landed and S buffer jq % 2 is free (P_{jq-2} V_{jq-2} issued, i.e. the softmax is done
 // with S_{jq-2}); O += P_jp V_jp once P_jp is written and V_jp landed.
 __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
-                       uint32_t tmem, uint32_t q_use, uint32_t (&k_use)[2],
+                       uint32_t tmem, uint32_t q_use, uint32_t (&k_use)[kKStages],
                        uint32_t (&v_use)[2], uint32_t& blk_use) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
@@ -855,16 +882,16 @@ __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
   const uint32_t idesc_pv = tc::idesc_f16(128, 128, false, true);
   const uint32_t qa = smem_u32(sm + TcLayout::kQ), pa = smem_u32(sm + TcLayout::kP);
   if (!tc_wait(bars + kBarQFull, q_use & 1u, abort)) return;
-  int jq = 0, jp = 0;
+  int jq = 0, jp = 0, kq = 0;   // kq = jq % kKStages
   uint32_t idle = 0;
   while (jp < t.nblk) {
     bool progress = false;
     if (jq < t.nblk && jq <= jp + 1) {
       const int s = jq & 1;
-      if (tc::mbar_test(bars + kBarKFull0 + s, k_use[s] & 1u)) {
-        ++k_use[s];
+      if (tc::mbar_test(bars + kBarKFull0 + kq, k_use[kq] & 1u)) {
+        ++k_use[kq];
         tc::fence_after_sync();
-        const uint32_t ka = smem_u32(sm + TcLayout::kK + s * 32768);
+        const uint32_t ka = smem_u32(sm + TcLayout::kK + kq * 32768);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
@@ -872,8 +899,9 @@ __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
                       tc::smem_desc(ka + koff, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
         }
         tc::commit(bars + kBarSFull0 + s);
-        tc::commit(bars + kBarKEmpty0 + s);
+        tc::commit(bars + kBarKEmpty0 + kq);
         ++jq;
+        kq = kq + 1 == kKStages ? 0 : kq + 1;
         progress = true;
       }
     }
@@ -1049,10 +1077,12 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     tc::mbar_init(bars + kBarQFull, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       tc::mbar_init(bars + kBarKFull0 + s, 1);
-      tc::mbar_init(bars + kBarVFull0 + s, 32);
       tc::mbar_init(bars + kBarKEmpty0 + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(bars + kBarVFull0 + s, 32);
       tc::mbar_init(bars + kBarVEmpty0 + s, 1);
       tc::mbar_init(bars + kBarSFull0 + s, 1);
     }
@@ -1062,11 +1092,11 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
     tc::mbar_init_fence();
     *abort = 0;
   }
-  if (warp == kLoaderWarp && lane == 0) {
+  if (warp == kKLoaderWarp && lane == 0) {
     tc::tma_prefetch_desc(&maps.q);
     tc::tma_prefetch_desc(&maps.k);
-    tc::tma_prefetch_desc(&maps.v);
   }
+  if (warp == kVLoaderWarp && lane == 0) tc::tma_prefetch_desc(&maps.v);
   if (warp == 0) {
     tc::tmem_alloc(tslot, 512);
     tc::tmem_relinquish();
@@ -1076,7 +1106,7 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
   // per-role phase counters (each role waits every phase it depends on, in order)
-  uint32_t k_use[2] = {0u, 0u}, v_use[2] = {0u, 0u}, s_use[2] = {0u, 0u};
+  uint32_t k_use[kKStages] = {}, v_use[2] = {0u, 0u}, s_use[2] = {0u, 0u};
   uint32_t q_use = 0u, blk_use = 0u;
   bool mma_aborted = false;
   while (true) {
@@ -1092,8 +1122,10 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
     } else if (tid == kMmaThread) {
       tc_mma(p, sm, t, tmem, q_use, k_use, v_use, blk_use);
       mma_aborted = *abort != 0;
-    } else if (warp == kLoaderWarp) {
-      tc_loader(p, maps, sm, t, k_use, v_use, bad);
+    } else if (warp == kKLoaderWarp) {
+      tc_load_k(p, maps, sm, t, k_use, bad);
+    } else if (warp == kVLoaderWarp) {
+      tc_load_v(p, maps, sm, t, v_use);
     }
     ++q_use;
     // the next tile rewrites Q: every MMA of this tile has completed (the softmax waited
@@ -1110,12 +1142,14 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
       tc::commit(bars + kBarDrain);
       tc::mbar_wait(bars + kBarDrain, 0, kTcWaitTries);
     }
-    if (warp == kLoaderWarp && lane == 0) {
+    if (warp == kKLoaderWarp && lane == 0) {
       if (q_use > 0) tc::mbar_wait(bars + kBarQFull, (q_use - 1) & 1u, kTcWaitTries);
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < kKStages; ++s)
         if (k_use[s] > 0) tc::mbar_wait(bars + kBarKFull0 + s, (k_use[s] - 1) & 1u, kTcWaitTries);
+    }
+    if (warp == kVLoaderWarp && lane == 0) {
+      for (int s = 0; s < 2; ++s)
         if (v_use[s] > 0) tc::mbar_wait(bars + kBarVFull0 + s, (v_use[s] - 1) & 1u, kTcWaitTries);
-      }
     }
   }
   cp_async_wait<0>();
@@ -1125,7 +1159,7 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
-// Persistent tensor-core prefill kernel: one CTA of 6 warps per SM, tiles from the
+// Persistent tensor-core prefill kernel: one CTA of 7 warps per SM, tiles from the
 // planner's counter.
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(AttnParams p, const __grid_constant__ TcMaps maps) {
