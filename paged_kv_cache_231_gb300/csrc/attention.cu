@@ -688,9 +688,9 @@ struct TcLayout {  // byte offsets from a 1024-byte-aligned base
   static constexpr uint32_t kQ = 0;               // 2 x [128][64] fp16 sub-tiles
   static constexpr uint32_t kK = 32768;           // kKStages x 32 KB
   static constexpr uint32_t kV = kK + 98304;      // 2 stages x 32 KB
-  static constexpr uint32_t kP = kV + 65536;      // 32 KB
-  static constexpr uint32_t kBars = kP + 32768;   // mbarriers (see TcBar)
-  static constexpr uint32_t kTmem = kBars + 128;  // TMEM base address
+  static constexpr uint32_t kOnes = kV + 65536;   // [16][64] fp16 ones (row-sum operand)
+  static constexpr uint32_t kBars = kOnes + 2048; // mbarriers (see TcBar)
+  static constexpr uint32_t kTmem = kBars + 256;  // TMEM base address
   static constexpr uint32_t kTile = kTmem + 4;    // current tile index
   static constexpr uint32_t kAbort = kTile + 4;   // set when a bounded wait gives up
   static constexpr uint32_t kEnd = kAbort + 8;
@@ -702,12 +702,16 @@ enum TcBar {  // mbarrier slots
   kBarKEmpty0 = 6,   // + stage (3), count 1: the S = Q K^T that read the stage completed
   kBarVEmpty0 = 9,   // + stage (2), count 1: the O += P V that read the stage completed
   kBarSFull0 = 11,   // + buffer, count 1: S_j in TMEM
-  kBarPFull = 13,    // count 128: softmax wrote P_j and is done with S_j
-  kBarODone = 14,    // count 1: O += P_j V_j completed
+  kBarPFull = 13,    // count 128: softmax wrote P_j to TMEM
+  kBarODone = 14,    // count 1: O += P_j V_j (and l += P_j 1) completed
   kBarDrain = 15,    // count 1: MMAs in flight when a wait gave up
-  kNumBars = 16
+  kBarSEmpty0 = 16,  // + buffer, count 128: softmax has read S_j out of the buffer
+  kNumBars = 18
 };
-static_assert(kNumBars * 8 <= 128, "mbarrier slots");
+static_assert(kNumBars * 8 <= 256, "mbarrier slots");
+// TMEM columns: S_j in buffer j % 2, the O accumulator, the row sums l (first of 16
+// columns), and P_j as fp16 pairs (two keys per 32-bit column)
+constexpr uint32_t kTmS = 0, kTmO = 256, kTmL = 384, kTmP = 448;
 constexpr int kKStages = 3;        // K ring depth (V has 2 stages)
 constexpr uint32_t kTcWaitTries = 1u << 22;
 constexpr int kTcThreads = 224;
@@ -870,32 +874,52 @@ __device__ void tc_load_v(const AttnParams& p, const TcMaps& maps, unsigned char
   }
 }
 
+// O += P V with the A operand (P) read from TMEM
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Warp 4, lane 0: the MMA stream of the tile. S_jq = Q K_jq^T may be issued once K_jq
-// landed and S buffer jq % 2 is free (P_{jq-2} V_{jq-2} issued, i.e. the softmax is done
-// with S_{jq-2}); O += P_jp V_jp once P_jp is written and V_jp landed.
+// landed and the softmax has read S_{jq-2} out of buffer jq % 2 (SEmpty phases are counted
+// per block, across tiles, because the last two of a tile are never waited for); O += P_jp V_jp (and
+// l += P_jp 1, the row sums, on an all-ones operand) once P_jp is in TMEM and V_jp landed.
 __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
                        uint32_t tmem, uint32_t q_use, uint32_t (&k_use)[kKStages],
-                       uint32_t (&v_use)[2], uint32_t& blk_use) {
+                       uint32_t (&v_use)[2], uint32_t (&s_base)[2], uint32_t& blk_use) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const uint32_t idesc_qk = tc::idesc_f16(128, 128, false, false);
   const uint32_t idesc_pv = tc::idesc_f16(128, 128, false, true);
-  const uint32_t qa = smem_u32(sm + TcLayout::kQ), pa = smem_u32(sm + TcLayout::kP);
+  const uint32_t idesc_l = tc::idesc_f16(128, 16, false, false);
+  const uint32_t qa = smem_u32(sm + TcLayout::kQ);
+  // every row and K step of the all-ones operand reads ones: one descriptor serves all
+  const uint64_t ones = tc::smem_desc(smem_u32(sm + TcLayout::kOnes), 16, 1024);
   if (!tc_wait(bars + kBarQFull, q_use & 1u, abort)) return;
   int jq = 0, jp = 0, kq = 0;   // kq = jq % kKStages
   uint32_t idle = 0;
   while (jp < t.nblk) {
     bool progress = false;
-    if (jq < t.nblk && jq <= jp + 1) {
+    if (jq < t.nblk) {
+      // buffer s was last filled with S_{jq-2}: phase s_base[s] + (jq - 2) / 2 of SEmpty_s
       const int s = jq & 1;
-      if (tc::mbar_test(bars + kBarKFull0 + kq, k_use[kq] & 1u)) {
+      if ((jq < 2 ||
+           tc::mbar_test(bars + kBarSEmpty0 + s, (s_base[s] + (uint32_t)((jq - 2) >> 1)) & 1u)) &&
+          tc::mbar_test(bars + kBarKFull0 + kq, k_use[kq] & 1u)) {
         ++k_use[kq];
         tc::fence_after_sync();
         const uint32_t ka = smem_u32(sm + TcLayout::kK + kq * 32768);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-          tc::mma_f16(tmem + s * 128, tc::smem_desc(qa + koff, 16, 1024),
+          tc::mma_f16(tmem + kTmS + s * 128, tc::smem_desc(qa + koff, 16, 1024),
                       tc::smem_desc(ka + koff, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
         }
         tc::commit(bars + kBarSFull0 + s);
@@ -915,10 +939,10 @@ __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
         const uint32_t va = smem_u32(sm + TcLayout::kV + s * 32768);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t poff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-          tc::mma_f16(tmem + 256, tc::smem_desc(pa + poff, 16, 1024),
-                      tc::smem_desc(va + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv,
-                      (jp > 0 || ks > 0) ? 1u : 0u);
+          const uint32_t acc = (jp > 0 || ks > 0) ? 1u : 0u;
+          mma_f16_tmem_a(tmem + kTmO, tmem + kTmP + (uint32_t)ks * 8u,
+                         tc::smem_desc(va + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv, acc);
+          mma_f16_tmem_a(tmem + kTmL, tmem + kTmP + (uint32_t)ks * 8u, ones, idesc_l, acc);
         }
         tc::commit(bars + kBarODone);
         tc::commit(bars + kBarVEmpty0 + s);
@@ -933,10 +957,26 @@ __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
       return;
     }
   }
+  // SEmpty phases of this tile: one per block read from each buffer
+  s_base[0] += (uint32_t)((t.nblk + 1) >> 1);
+  s_base[1] += (uint32_t)(t.nblk >> 1);
   blk_use += t.nblk;
 }
 
-// Warps 0-3: softmax and the normalised output of row threadIdx.x.
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float fmin3f(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Warps 0-3: softmax of row threadIdx.x and its normalised output. The row max is taken
+// over the raw scores (the minimum when the scale is negative), so that each weight is
+// one fused multiply-add and an exp2: p = 2^(s * scale * log2 e - m).
 __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile& t,
                            uint32_t tmem, uint32_t (&s_use)[2], uint32_t& blk_use) {
   constexpr int D = 128;
@@ -947,9 +987,19 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
   const bool rvalid = r < t.PT * p.G && pl < t.nq;
   const int lim = rvalid ? (int)min64((int64_t)t.P + t.q0 + pl, INT32_MAX) : -1;
   const uint32_t lane_taddr = tmem + ((uint32_t)(r & ~31) << 16);
-  unsigned char* Ps = sm + TcLayout::kP;
-  float m_used = -INFINITY, l = 0.f;
+  const float sl2 = p.scale_log2;
+  const bool pos_scale = sl2 >= 0.f;
+  const float hide = pos_scale ? -INFINITY : INFINITY;   // masked raw score
+  float m_used = -INFINITY;
   bool ok = true;
+  // block-table entry of the cache block holding keys [kbase + 4 lane, + 4) of block j
+  auto lookup = [&](int j) -> int {
+    const int key0 = j * 128 + 4 * lane;
+    if (key0 >= t.kend) return -1;
+    const int col = p.bs_shift >= 0 ? key0 >> p.bs_shift : key0 / p.BS;
+    return __ldg(&p.block_table[(int64_t)t.b * p.MB + col]);
+  };
+  int blk_next = lookup(0);
   for (int j = 0; j < t.nblk && ok; ++j) {
     const int s = j & 1;
     const int kbase = j * 128;
@@ -957,12 +1007,8 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
     // cache block because the block size is a multiple of 8; key c of the block is bit
     // c / 4 of words[c % 4]
     const int key0 = kbase + 4 * lane;
-    bool page = false;
-    if (key0 < t.kend) {
-      const int col = p.bs_shift >= 0 ? key0 >> p.bs_shift : key0 / p.BS;
-      const int blk = __ldg(&p.block_table[(int64_t)t.b * p.MB + col]);
-      page = blk >= 0 && (int64_t)blk < p.NB;
-    }
+    const bool page = blk_next >= 0 && (int64_t)blk_next < p.NB;
+    if (j + 1 < t.nblk) blk_next = lookup(j + 1);
     uint32_t words[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) words[i] = __ballot_sync(0xffffffffu, page && key0 + i < t.kend);
@@ -973,68 +1019,80 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
     tc::fence_after_sync();
     const int cut = lim - kbase + 1;  // columns below cut are causally visible to this row
     const bool full = (words[0] & words[1] & words[2] & words[3]) == 0xffffffffu && cut >= 128;
-    // the whole row of S_j in one TMEM round trip
+    // the whole row of S_j in one TMEM round trip; the buffer is then free for S_{j+2}
     float v[128];
     {
       float (*v32)[32] = reinterpret_cast<float (*)[32]>(v);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(lane_taddr + s * 128 + ch * 32, v32[ch]);
+      for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(lane_taddr + kTmS + s * 128 + ch * 32, v32[ch]);
       tc::tmem_wait_ld();
     }
-    const float sl2 = p.scale_log2;
-    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    if (__all_sync(0xffffffffu, full)) {
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        v[c] *= sl2;
-        mx4[c & 3] = fmaxf(mx4[c & 3], v[c]);
-      }
-    } else {
+    tc::fence_before_sync();
+    mbar_arrive(bars + kBarSEmpty0 + s);
+    if (!__all_sync(0xffffffffu, full)) {
 #pragma unroll
       for (int c = 0; c < 128; ++c) {
         const bool vis = c < cut && ((words[c & 3] >> (c >> 2)) & 1u);
-        v[c] = vis ? v[c] * sl2 : -INFINITY;
-        mx4[c & 3] = fmaxf(mx4[c & 3], v[c]);
+        v[c] = vis ? v[c] : hide;
       }
     }
-    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+    float e4[4];
+    if (pos_scale) {
+      e4[0] = fmaxf(v[0], v[1]); e4[1] = fmaxf(v[2], v[3]);
+      e4[2] = fmaxf(v[4], v[5]); e4[3] = fmaxf(v[6], v[7]);
+#pragma unroll
+      for (int c = 8; c < 128; c += 8) {
+        e4[0] = fmax3f(e4[0], v[c], v[c + 1]); e4[1] = fmax3f(e4[1], v[c + 2], v[c + 3]);
+        e4[2] = fmax3f(e4[2], v[c + 4], v[c + 5]); e4[3] = fmax3f(e4[3], v[c + 6], v[c + 7]);
+      }
+      e4[0] = fmax3f(e4[0], e4[1], fmaxf(e4[2], e4[3]));
+    } else {
+      e4[0] = fminf(v[0], v[1]); e4[1] = fminf(v[2], v[3]);
+      e4[2] = fminf(v[4], v[5]); e4[3] = fminf(v[6], v[7]);
+#pragma unroll
+      for (int c = 8; c < 128; c += 8) {
+        e4[0] = fmin3f(e4[0], v[c], v[c + 1]); e4[1] = fmin3f(e4[1], v[c + 2], v[c + 3]);
+        e4[2] = fmin3f(e4[2], v[c + 4], v[c + 5]); e4[3] = fmin3f(e4[3], v[c + 6], v[c + 7]);
+      }
+      e4[0] = fmin3f(e4[0], e4[1], fminf(e4[2], e4[3]));
+    }
+    const float mx = e4[0] * sl2;   // -inf when nothing in the block is visible
     const bool first = m_used == -INFINITY;
     const bool raise = (first && mx != -INFINITY) || (!first && mx > m_used + kTcRescale);
     const float alpha = raise && !first ? ex2(m_used - mx) : 1.f;
     if (raise) m_used = mx;
-    const float base = m_used == -INFINITY ? 0.f : m_used;
-    uint32_t w[64];
-    float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+    const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+    float pw[64];   // P_j row as fp16 pairs (bit patterns)
 #pragma unroll
     for (int c = 0; c < 128; c += 2) {
-      const float p0 = ex2(v[c] - base), p1 = ex2(v[c + 1] - base);
-      ls4[(c >> 1) & 3] += p0 + p1;
-      w[c / 2] = pack_half2(p0, p1);
+      const float p0 = ex2(fmaf(v[c], sl2, nbase)), p1 = ex2(fmaf(v[c + 1], sl2, nbase));
+      pw[c / 2] = __uint_as_float(pack_half2(p0, p1));
     }
-    l = l * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
-    // O and the P buffer are free once O += P_{j-1} V_{j-1} has completed
+    // O, l and the P columns are free once O += P_{j-1} V_{j-1} has completed
     if (j > 0) {
       ok = __all_sync(0xffffffffu, tc_wait(bars + kBarODone, (blk_use + j - 1) & 1u, abort));
       if (!ok) break;
       tc::fence_after_sync();
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {   // warp-collective TMEM rescale of O
-        float o[128];
-        float (*o32)[32] = reinterpret_cast<float (*)[32]>(o);
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {   // warp-collective TMEM rescale of O, l
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(lane_taddr + 256 + ch * 32, o32[ch]);
-        tc::tmem_wait_ld();
+        for (int ch = 0; ch < 4; ++ch) {
+          float o[32];
+          tc::tmem_ld32(lane_taddr + kTmO + ch * 32, o);
+          tc::tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 128; ++c) o[c] *= alpha;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) tc::tmem_st32(lane_taddr + 256 + ch * 32, o32[ch]);
-        tc::tmem_wait_st();
+          for (int c = 0; c < 32; ++c) o[c] *= alpha;
+          tc::tmem_st32(lane_taddr + kTmO + ch * 32, o);
+        }
+        float lv = tc::tmem_ld1(lane_taddr + kTmL);
+        tc::tmem_st1(lane_taddr + kTmL, lv * alpha);
       }
     }
-#pragma unroll
-    for (int c8 = 0; c8 < 16; ++c8)
-      *reinterpret_cast<uint4*>(Ps + (c8 >> 3) * 16384 + tc::sw128(r, c8 & 7)) =
-          make_uint4(w[c8 * 4], w[c8 * 4 + 1], w[c8 * 4 + 2], w[c8 * 4 + 3]);
-    tc::fence_async_shared();
+    {
+      float (*p32)[32] = reinterpret_cast<float (*)[32]>(pw);
+      tc::tmem_st32(lane_taddr + kTmP, p32[0]);
+      tc::tmem_st32(lane_taddr + kTmP + 32, p32[1]);
+    }
+    tc::tmem_wait_st();
     tc::fence_before_sync();
     mbar_arrive(bars + kBarPFull);
   }
@@ -1043,22 +1101,24 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
                     tc_wait(bars + kBarODone, (blk_use + t.nblk - 1) & 1u, abort));
     if (ok) {
       tc::fence_after_sync();
+      const float l = tc::tmem_ld1(lane_taddr + kTmL);
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __half* orow = p.out + (int64_t)(t.cu0 + t.q0 + pl) * p.Hq * D +
                      (int64_t)(t.h * p.G + r % p.G) * D;
-      float o[128];
-      float (*o32)[32] = reinterpret_cast<float (*)[32]>(o);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(lane_taddr + 256 + ch * 32, o32[ch]);
-      tc::tmem_wait_ld();
-      if (rvalid) {
+      for (int ch = 0; ch < 4; ++ch) {
+        float o[32];
+        tc::tmem_ld32(lane_taddr + kTmO + ch * 32, o);
+        tc::tmem_wait_ld();
+        if (rvalid) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          *reinterpret_cast<uint4*>(orow + q * 8) =
-              make_uint4(pack_half2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
-                         pack_half2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
-                         pack_half2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
-                         pack_half2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(orow + ch * 32 + q * 8) =
+                make_uint4(pack_half2(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
+                           pack_half2(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
+                           pack_half2(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
+                           pack_half2(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
+        }
       }
     }
   }
@@ -1085,6 +1145,7 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
       tc::mbar_init(bars + kBarVFull0 + s, 32);
       tc::mbar_init(bars + kBarVEmpty0 + s, 1);
       tc::mbar_init(bars + kBarSFull0 + s, 1);
+      tc::mbar_init(bars + kBarSEmpty0 + s, 128);
     }
     tc::mbar_init(bars + kBarPFull, 128);
     tc::mbar_init(bars + kBarODone, 1);
@@ -1097,6 +1158,10 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
     tc::tma_prefetch_desc(&maps.k);
   }
   if (warp == kVLoaderWarp && lane == 0) tc::tma_prefetch_desc(&maps.v);
+  for (int i = tid; i < 2048 / 16; i += kTcThreads)   // fp16 ones
+    reinterpret_cast<uint4*>(sm + TcLayout::kOnes)[i] =
+        make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+  tc::fence_async_shared();
   if (warp == 0) {
     tc::tmem_alloc(tslot, 512);
     tc::tmem_relinquish();
@@ -1107,6 +1172,7 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
   const uint32_t tmem = *tslot;
   // per-role phase counters (each role waits every phase it depends on, in order)
   uint32_t k_use[kKStages] = {}, v_use[2] = {0u, 0u}, s_use[2] = {0u, 0u};
+  uint32_t s_base[2] = {0u, 0u};
   uint32_t q_use = 0u, blk_use = 0u;
   bool mma_aborted = false;
   while (true) {
@@ -1120,7 +1186,7 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
     if (tid < 128) {
       tc_softmax(p, sm, t, tmem, s_use, blk_use);
     } else if (tid == kMmaThread) {
-      tc_mma(p, sm, t, tmem, q_use, k_use, v_use, blk_use);
+      tc_mma(p, sm, t, tmem, q_use, k_use, v_use, s_base, blk_use);
       mma_aborted = *abort != 0;
     } else if (warp == kKLoaderWarp) {
       tc_load_k(p, maps, sm, t, k_use, bad);
