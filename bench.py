@@ -291,7 +291,7 @@ def setup_paged(name, args):
         w.tokens = case.num_tokens
         # prefill tiles run in the tensor-core kernel (decode tokens in the attention one)
         w.dominant, w.dom_work, w.bound, w.dom_unit = "prefill_tc", fl / 1e12, "tensor", "TFLOP/s"
-        w.traffic_summary, w.traffic_sources = None, ATTN_SOURCES
+        w.traffic_summary, w.traffic_sources = "prefill_tc_varlen_mixed.md", ATTN_SOURCES
         w.config = {"workload": "varlen_mixed", "batch": case.batch, "tokens": case.num_tokens,
                     "num_heads": 32, "kv_num_heads": 8, "head_size": 128, "block_size": 32,
                     "flops_per_step": fl,
