@@ -103,8 +103,9 @@ typedef struct pkv_paged_attention_args {
   void* value_cache;
   /* cumulative_sequence_length int32 [batch + 1]: tokens of sequence b are rows
             [cu[b], cu[b+1]) of query. past_seqlens int32 [batch]: tokens already in
-            the cache. block_table int32 [batch, max_blocks]: physical block of each
-            16.. block_size-token column; -1 (or any id outside the pool) = unmapped. */
+            the cache. block_table int32 [batch, max_blocks]: entry c is the physical
+            block holding keys [c*block_size, (c+1)*block_size) of the sequence; -1 (or
+            any id outside the pool) = unmapped. */
   const int32_t* cumulative_sequence_length;
   const int32_t* past_seqlens;
   const int32_t* block_table;

@@ -14,12 +14,15 @@
 
 #include "internal.h"
 
+constexpr size_t kStaticBytes = PKV_STATIC_WORKSPACE_BYTES;
+
+// Keeps the previous call's contents; nothing needs clearing, because the planner of every
+// call rewrites the counters and piece tickets it later reads.
+static __device__ __align__(256) unsigned char g_static_workspace[kStaticBytes];
+
 namespace {
 
-constexpr size_t kStaticBytes = PKV_STATIC_WORKSPACE_BYTES;
 constexpr int kMaxDevices = 64;
-
-__device__ __align__(256) unsigned char g_static_workspace[kStaticBytes];
 
 std::mutex g_mutex;
 void* g_device_address[kMaxDevices] = {};
