@@ -5,7 +5,8 @@
 // One warp per output row; each lane owns head_dim / 32 consecutive elements, so a
 // partial row is read as one coalesced 512-byte (D = 128) transaction. Pass 1 finds
 // the max m over non-empty partials (l > 0); pass 2 accumulates w = exp(m - M) with
-// w*l into L and w*o into the row; out = row / L, lse = M + ln L.
+// w*l into L and w*o into the row, 32 partials at a time so that the o rows of a chunk
+// are all in flight together; out = row / L, lse = M + ln L.
 #include <math.h>
 
 #include "device_common.cuh"
@@ -54,29 +55,46 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(CombinePara
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  float L = 0.f;
+  float Lpart = 0.f;
   if (M != -INFINITY) {
-#pragma unroll 4
-    for (int64_t e = g0; e < g1; ++e) {
-      const int64_t pr = e * lanes + c;
-      const float lv = p.l[pr];
-      if (lv > 0.f) {
-        const float w = ex2((p.m[pr] - M) * kLog2e);
-        L += w * lv;
+    // 32 partials at a time: lane k computes the weight of partial base + k, then every
+    // o row of the chunk is loaded without waiting on another load (an empty partial's
+    // load is pointed at a non-empty row of the chunk and weighted 0, so its o is never
+    // used)
+    for (int64_t base = g0; base < g1; base += 32) {
+      const int64_t e = base + lane;
+      float w = 0.f;
+      if (e < g1) {
+        const int64_t pr = e * lanes + c;
+        const float lv = p.l[pr];
+        if (lv > 0.f) {
+          w = ex2((p.m[pr] - M) * kLog2e);
+          Lpart += w * lv;
+        }
+      }
+      const uint32_t live = __ballot_sync(0xffffffffu, w > 0.f);
+      if (!live) continue;
+      const int64_t fallback = (base + (__ffs(live) - 1)) * lanes + c;
+      const int n = g1 - base < 32 ? (int)(g1 - base) : 32;
+#pragma unroll 8
+      for (int k = 0; k < n; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, k);
+        const int64_t pr = wk > 0.f ? (base + k) * lanes + c : fallback;
         const float* orow = p.o + pr * D + lane * V;
         if constexpr (V == 4) {
-          const float4 x = *reinterpret_cast<const float4*>(orow);
-          acc[0] += w * x.x;
-          acc[1] += w * x.y;
-          acc[2] += w * x.z;
-          acc[3] += w * x.w;
+          const float4 x = __ldg(reinterpret_cast<const float4*>(orow));
+          acc[0] += wk * x.x;
+          acc[1] += wk * x.y;
+          acc[2] += wk * x.z;
+          acc[3] += wk * x.w;
         } else {
 #pragma unroll
-          for (int v = 0; v < V; ++v) acc[v] += w * orow[v];
+          for (int v = 0; v < V; ++v) acc[v] += wk * __ldg(orow + v);
         }
       }
     }
   }
+  const float L = warp_sum(Lpart);
   const float inv = L > 0.f ? 1.f / L : 0.f;
   if (OUT_F16) {
     __half* dst = reinterpret_cast<__half*>(p.out) + out_row * D + lane * V;
