@@ -5,13 +5,15 @@
 //
 // The page runs one 64-lane workgroup per partial and re-reads the block's K and V
 // rows for every lane and edge. Here the edges are first grouped by (batch, kv head,
-// block) with a device counting sort; one CTA stages a block's K and V in shared
-// memory once and computes the partials of every edge that names it, 64 query rows
-// (edges x lanes) at a time, with register-tiled fp32 FMA for both QK^T and PV.
+// block) with a device counting sort; the block's K and V are staged in shared memory
+// once for the partials of every edge that names it. Head sizes 64 / 128 with blocks of
+// at most 64 keys run both products on the tensor core in 3xTF32 (sparse_tc_kernel);
+// other shapes take 64 query rows (edges x lanes) at a time with register-tiled fp32 FMA.
 #include <math.h>
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace pkv {
 namespace {
@@ -292,6 +294,396 @@ __global__ void __launch_bounds__(kSpThreads, 2) sparse_partials_kernel(SparsePa
   if (bad) flag_status(p.status, PKV_DEV_BAD_EDGE);
 }
 
+// ---- tensor-core partials: 3xTF32 on tcgen05 ----------------------------------------
+// For head size 64/128 and blocks of at most 64 keys. A persistent CTA per SM takes
+// (batch, block, kv head) groups from a counter. The group's raw fp32 K and V rows are
+// staged with cp.async while the previous group computes, then split into tf32 pairs
+// x = hi + lo (hi = x rounded to tf32, lo = x - hi) in 128-byte-swizzled K-major tiles:
+// K [64 keys][D] and V^T [D][64 keys]. For each tile of 128 query rows (edges x query
+// heads) Q (hi, lo) goes to TMEM and S = Q K^T is accumulated from three tf32 products
+// (hi*hi + hi*lo + lo*hi, relative error about 2^-22, i.e. fp32 level); one thread per row
+// forms the partial's max, weights and sum, writes the weights (hi, lo) back to TMEM,
+// and O = P V is accumulated the same way. TMEM: S 0..63, O 64.., Q hi 256.., Q lo 384..,
+// P hi 256..319, P lo 320..383 (P replaces Q once S is complete).
+namespace tcs {
+constexpr int kThreads = 256;
+constexpr int kNK = 64;                 // keys per block tile
+constexpr uint32_t kTries = 1u << 24;   // bound of each MMA-completion wait
+
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4)                      // D format: f32
+         | (2u << 7) | (2u << 10)       // A, B format: tf32
+         | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// x rounded to the nearest tf32 (low 13 mantissa bits cleared)
+__device__ __forceinline__ float tf32_hi(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+}
+
+template <int D>
+struct Layout {   // byte offsets from a 1024-byte-aligned base
+  static constexpr int RS = D + 4;                          // raw row stride (floats)
+  static constexpr uint32_t kKhi = 0;                       // [64][D]: D/32 x [64][128 B]
+  static constexpr uint32_t kKlo = kKhi + D * 256;
+  static constexpr uint32_t kVhi = kKlo + D * 256;          // [D][64]: 2 x [D][128 B]
+  static constexpr uint32_t kVlo = kVhi + D * 256;
+  static constexpr uint32_t kRawK = kVlo + D * 256;         // [64][RS] fp32
+  static constexpr uint32_t kRawV = kRawK + kNK * RS * 4;
+  static constexpr uint32_t kValid = kRawV + kNK * RS * 4;  // [64] key state, current group
+  static constexpr uint32_t kRValid = kValid + 64;          // [64] key state, staged group
+  static constexpr uint32_t kBL = kRValid + 64;             // [128] int: keys of each row
+  static constexpr uint32_t kPI = kBL + 512;                // [128] int: partial of each row
+  static constexpr uint32_t kBar = kPI + 512;               // MMA completion, drain
+  static constexpr uint32_t kTmem = kBar + 16;
+  static constexpr uint32_t kNext = kTmem + 8;              // int64, 8-byte aligned
+  static constexpr uint32_t kEnd = kNext + 8;
+};
+
+// cp.async of group g's K and V rows into the raw buffers; key states into rValid
+// (0 unmapped or past the block, 1 mapped, 2 invalid table reference)
+template <int D>
+__device__ __forceinline__ void stage_raw(const SparseParams& p, unsigned char* sm, int64_t g) {
+  using L = Layout<D>;
+  float* rawK = reinterpret_cast<float*>(sm + L::kRawK);
+  float* rawV = reinterpret_cast<float*>(sm + L::kRawV);
+  uint8_t* rValid = sm + L::kRValid;
+  const int h = (int)(g % p.hkv);
+  const int64_t bb = g / p.hkv;
+  const int blk = (int)(bb % p.nblk);
+  const int batch = (int)(bb / p.nblk);
+  static_assert(kNK * (D / 4) % kThreads == 0, "staging splits evenly over the CTA");
+#pragma unroll
+  for (int it = 0; it < kNK * (D / 4) / kThreads; ++it) {
+    const int i = threadIdx.x + it * kThreads;
+    const int t = i / (D / 4), c = i % (D / 4);
+    int64_t page = -1;
+    uint8_t state = 0;
+    if (t < p.block_size) {
+      const int64_t slot = (int64_t)blk * p.ppb + t / p.page_size;
+      if (slot < p.max_pages) {
+        page = p.bt[(int64_t)batch * p.max_pages + slot];
+        if (page >= p.num_pages) {
+          page = -1;
+          state = 2;
+        }
+      } else {
+        state = 2;
+      }
+    }
+    if (page >= 0) state = 1;
+    const float* gk = p.kp;
+    const float* gv = p.vp;
+    int nb = 0;
+    if (page >= 0) {
+      const int64_t row = ((page * p.hkv + h) * p.page_size + t % p.page_size) * D + c * 4;
+      gk += row;
+      gv += row;
+      nb = 16;
+    }
+    cp_async_16(rawK + t * L::RS + c * 4, gk, nb);
+    cp_async_16(rawV + t * L::RS + c * 4, gv, nb);
+    if (c == 0) rValid[t] = state;
+  }
+  cp_async_commit();
+}
+
+// next group (in counter order) that has edges, or ngroups
+__device__ __forceinline__ int64_t next_group(const SparseParams& p) {
+  int* counter = p.group_count + p.ngroups;
+  while (true) {
+    const int64_t g = atomicAdd(counter, 1);
+    if (g >= p.ngroups) return p.ngroups;
+    if (p.group_off[g + 1] > p.group_off[g]) return g;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) {
+  using L = Layout<D>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const float* rawK = reinterpret_cast<const float*>(sm + L::kRawK);
+  const float* rawV = reinterpret_cast<const float*>(sm + L::kRawV);
+  uint8_t* sValid = sm + L::kValid;
+  const uint8_t* rValid = sm + L::kRValid;
+  int* sBL = reinterpret_cast<int*>(sm + L::kBL);
+  int* sPI = reinterpret_cast<int*>(sm + L::kPI);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::kTmem);
+  volatile int64_t* snext = reinterpret_cast<volatile int64_t*>(sm + L::kNext);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int r = quarter * 32 + lane;   // TMEM lane / tile row of this thread
+  if (tid == 0) {
+    tc::mbar_init(bar, 1);
+    tc::mbar_init(bar + 1, 1);
+    tc::mbar_init_fence();
+    *snext = next_group(p);
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t lane_tm = tmem + ((uint32_t)(quarter * 32) << 16);
+  int64_t g = *snext;
+  if (g < p.ngroups) stage_raw<D>(p, sm, g);
+  uint32_t phase = 0;
+  bool ok = true, bad = false;
+  // edge of this thread's row in a tile starting at edge c0 of a group ending at e1:
+  // (edge, query index, block_len), fetched one tile ahead of its use
+  const int epc = 128 / p.qhead;
+  const int my_er = r / p.qhead, my_qh = r - my_er * p.qhead;
+  auto row_edge = [&](int c0, int e1, int& e, int& qi, int& bl) {
+    e = -1;
+    qi = 0;
+    bl = 0;
+    if (my_er < epc && c0 + my_er < e1) {
+      e = p.perm[c0 + my_er];
+      qi = p.meta[(int64_t)e * 5];
+      bl = min(p.meta[(int64_t)e * 5 + 4], p.block_size);
+    }
+  };
+  int nx_e, nx_q, nx_bl;
+  if (g < p.ngroups) row_edge(p.group_off[g], p.group_off[g + 1], nx_e, nx_q, nx_bl);
+  const uint32_t idesc_s = idesc_tf32(128, kNK), idesc_o = idesc_tf32(128, D);
+  while (g < p.ngroups && ok) {
+    cp_async_wait<0>();
+    __syncthreads();
+    // raw -> tf32 (hi, lo) tiles; K row-wise, V transposed (lane = key, conflict-free)
+    for (int i = tid; i < kNK * (D / 4); i += kThreads) {
+      const int t = i / (D / 4), c = i % (D / 4);
+      const float4 v = *reinterpret_cast<const float4*>(rawK + t * L::RS + c * 4);
+      const float4 hi = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+      const float4 lo = make_float4(v.x - hi.x, v.y - hi.y, v.z - hi.z, v.w - hi.w);
+      const uint32_t off = (uint32_t)(c >> 3) * (kNK * 128) + tc::sw128(t, c & 7);
+      *reinterpret_cast<float4*>(sm + L::kKhi + off) = hi;
+      *reinterpret_cast<float4*>(sm + L::kKlo + off) = lo;
+    }
+    {
+      const int t = lane + 32 * (warp & 1);
+      for (int c = warp >> 1; c < D / 4; c += kThreads / 64) {
+        const float4 v = *reinterpret_cast<const float4*>(rawV + t * L::RS + c * 4);
+        const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int d = c * 4 + k;
+          const uint32_t off = (uint32_t)(t >> 5) * (D * 128) + (uint32_t)d * 128u +
+                               ((uint32_t)(((t & 31) >> 2) ^ (d & 7)) << 4) + (uint32_t)(t & 3) * 4u;
+          const float hi = tf32_hi(x[k]);
+          *reinterpret_cast<float*>(sm + L::kVhi + off) = hi;
+          *reinterpret_cast<float*>(sm + L::kVlo + off) = x[k] - hi;
+        }
+      }
+    }
+    if (tid < kNK) sValid[tid] = rValid[tid];
+    tc::fence_async_shared();
+    if (tid == 0) *snext = next_group(p);
+    __syncthreads();
+    // the raw buffers are free: stage the next group behind this one's compute
+    const int64_t gn = *snext;
+    if (gn < p.ngroups) stage_raw<D>(p, sm, gn);
+    // key masks of this group: bit t of vmask = mapped, of imask = invalid reference
+    uint64_t vmask = 0, imask = 0;
+#pragma unroll 8
+    for (int t = 0; t < kNK; ++t) {
+      const uint8_t st = sValid[t];
+      vmask |= (uint64_t)(st == 1) << t;
+      imask |= (uint64_t)(st == 2) << t;
+    }
+    const int e0 = p.group_off[g], e1 = p.group_off[g + 1];
+    const int h = (int)(g % p.hkv);
+    for (int c0 = e0; c0 < e1 && ok; c0 += epc) {
+      // Q rows of this tile (hi, lo) into TMEM; warps 0-3 / 4-7 take the column halves
+      {
+        const int e = nx_e;
+        const bool live = e >= 0;
+        const float* qrow =
+            live ? p.q + ((int64_t)nx_q * p.hq + h * p.qhead + my_qh) * D + half * (D / 2)
+                 : nullptr;
+        if (half == 0) {
+          sBL[r] = live ? nx_bl : 0;
+          sPI[r] = live ? e * p.qhead + my_qh : -1;
+        }
+        // the next tile's rows: later in this group, else the first tile of the next one
+        if (c0 + epc < e1) row_edge(c0 + epc, e1, nx_e, nx_q, nx_bl);
+        else if (gn < p.ngroups) row_edge(p.group_off[gn], p.group_off[gn + 1], nx_e, nx_q, nx_bl);
+#pragma unroll
+        for (int ch = 0; ch < D / 64; ++ch) {
+          float vh[32], vl[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 v = live ? __ldg(reinterpret_cast<const float4*>(qrow + ch * 32 + k * 4))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              vh[k * 4 + j] = tf32_hi(x[j]);
+              vl[k * 4 + j] = x[j] - vh[k * 4 + j];
+            }
+          }
+          tc::tmem_st32(lane_tm + 256 + half * (D / 2) + ch * 32, vh);
+          tc::tmem_st32(lane_tm + 384 + half * (D / 2) + ch * 32, vl);
+        }
+        tc::tmem_wait_st();
+      }
+      tc::fence_before_sync();
+      __syncthreads();
+      if (tid == 0) {   // S = Qhi Khi + Qhi Klo + Qlo Khi
+        tc::fence_after_sync();
+        int n = 0;
+#pragma unroll
+        for (int pass = 0; pass < 3; ++pass) {
+          const uint32_t a = tmem + (pass == 2 ? 384u : 256u);
+          const uint32_t b = smem_u32(sm + (pass == 1 ? L::kKlo : L::kKhi));
+#pragma unroll
+          for (int ks = 0; ks < D / 8; ++ks, ++n)
+            mma_tf32(tmem, a + ks * 8,
+                     tc::smem_desc(b + (ks >> 2) * (kNK * 128) + (ks & 3) * 32, 16, 1024),
+                     idesc_s, n > 0 ? 1u : 0u);
+        }
+        tc::commit(bar);
+      }
+      ok = __syncthreads_and(tc::mbar_wait(bar, phase & 1u, kTries));
+      ++phase;
+      if (!ok) break;
+      tc::fence_after_sync();
+      float mrow = kNegLarge, lrow = 0.f;
+      if (half == 0) {   // softmax of row r over the block's keys
+        float s[64];
+        float (*s32)[32] = reinterpret_cast<float (*)[32]>(s);
+        tc::tmem_ld32(lane_tm, s32[0]);
+        tc::tmem_ld32(lane_tm + 32, s32[1]);
+        tc::tmem_wait_ld();
+        const int bl = sBL[r];
+        const uint64_t used = bl >= 64 ? ~0ull : ((1ull << bl) - 1ull);
+        if (imask & used) bad = true;
+#pragma unroll
+        for (int t = 0; t < 64; ++t) {
+          const float sv = t < bl ? (((vmask >> t) & 1ull) ? s[t] * p.scale : kNegLarge)
+                                  : -INFINITY;
+          s[t] = sv;
+          mrow = fmaxf(mrow, sv);
+        }
+#pragma unroll
+        for (int t = 0; t < 64; ++t) {
+          const float w = s[t] > 0.5f * kNegLarge ? ex2((s[t] - mrow) * kLog2e) : 0.f;
+          lrow += w;
+          s[t] = w;
+        }
+        float ph[32], pl[32];
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            ph[k] = tf32_hi(s[ch * 32 + k]);
+            pl[k] = s[ch * 32 + k] - ph[k];
+          }
+          tc::tmem_st32(lane_tm + 256 + ch * 32, ph);
+          tc::tmem_st32(lane_tm + 320 + ch * 32, pl);
+        }
+        tc::tmem_wait_st();
+      }
+      tc::fence_before_sync();
+      __syncthreads();
+      if (tid == 0) {   // O = Phi Vhi + Phi Vlo + Plo Vhi
+        tc::fence_after_sync();
+        int n = 0;
+#pragma unroll
+        for (int pass = 0; pass < 3; ++pass) {
+          const uint32_t a = tmem + (pass == 2 ? 320u : 256u);
+          const uint32_t b = smem_u32(sm + (pass == 1 ? L::kVlo : L::kVhi));
+#pragma unroll
+          for (int ks = 0; ks < kNK / 8; ++ks, ++n)
+            mma_tf32(tmem + 64, a + ks * 8,
+                     tc::smem_desc(b + (ks >> 2) * (D * 128) + (ks & 3) * 32, 16, 1024),
+                     idesc_o, n > 0 ? 1u : 0u);
+        }
+        tc::commit(bar);
+      }
+      ok = __syncthreads_and(tc::mbar_wait(bar, phase & 1u, kTries));
+      ++phase;
+      if (!ok) break;
+      tc::fence_after_sync();
+      {   // write the partials of this tile
+        const int pi = sPI[r];
+#pragma unroll
+        for (int ch = 0; ch < D / 64; ++ch) {
+          float o[32];
+          tc::tmem_ld32(lane_tm + 64 + half * (D / 2) + ch * 32, o);
+          tc::tmem_wait_ld();
+          if (pi >= 0) {
+            float* dst = p.o + (int64_t)pi * D + half * (D / 2) + ch * 32;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<float4*>(dst + k * 4) =
+                  make_float4(o[k * 4], o[k * 4 + 1], o[k * 4 + 2], o[k * 4 + 3]);
+          }
+        }
+        if (half == 0 && pi >= 0) {
+          p.m[pi] = mrow;
+          p.l[pi] = lrow;
+        }
+      }
+      tc::fence_before_sync();
+      __syncthreads();   // TMEM Q / P and the row tables are rewritten by the next tile
+      tc::fence_after_sync();
+    }
+    g = gn;
+  }
+  if (!ok) {
+    // an MMA did not complete in time: let what this CTA issued finish before leaving
+    if (tid == 0) {
+      flag_status(p.status, PKV_DEV_TIMEOUT);
+      tc::commit(bar + 1);
+      tc::mbar_wait(bar + 1, 0, kTries);
+    }
+  }
+  cp_async_wait<0>();
+  if (bad) flag_status(p.status, PKV_DEV_BAD_EDGE);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+template <int D>
+cudaError_t launch_tc(const SparseParams& p, cudaStream_t s) {
+  constexpr size_t smem = Layout<D>::kEnd + 1024;
+  static_assert(smem <= 232448, "shared memory over the per-block limit");
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(sparse_tc_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = p.ngroups < sms ? p.ngroups : sms;
+  ProfScope ps("sparse_partials", s);
+  sparse_tc_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+}  // namespace tcs
+
 template <int D, int KB>
 cudaError_t launch_partials(const SparseParams& p, cudaStream_t s) {
   constexpr int KS = D + 4, PS = KB + 4;
@@ -332,6 +724,10 @@ cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.ngroups == 0) return cudaSuccess;
+  if (p.block_size <= tcs::kNK && p.qhead <= 128) {   // 3xTF32 on the tensor core
+    if (p.D == 64) return tcs::launch_tc<64>(p, s);
+    if (p.D == 128) return tcs::launch_tc<128>(p, s);
+  }
   const int kb = p.block_size <= 64 ? 64 : 128;
   if (p.D == 64) return kb == 64 ? launch_partials<64, 64>(p, s) : launch_partials<64, 128>(p, s);
   if (p.D == 128)

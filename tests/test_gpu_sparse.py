@@ -44,8 +44,10 @@ def compare_partials(go, gm, gl, ro, rm, rl, rows):
     assert_f32_close(gl[live], rl[live], "l partial", scalars=True)
 
 
+# blocks of 64 and 32 keys run on the tensor core (3xTF32), 128-key blocks on fp32 FMA;
+# qhead 3 leaves two rows of each 128-row tile unused
 @pytest.mark.parametrize("head_dim,pages_per_block,qhead", [(128, 4, 4), (64, 2, 2),
-                                                            (128, 8, 1)])
+                                                            (128, 8, 1), (128, 4, 3)])
 def test_small_full_parity(head_dim, pages_per_block, qhead):
     c = wl.block_sparse(51, n_seqs=3, kv_len=1024, queries_per_seq=24, hq=4 * qhead,
                         hkv=4, head_dim=head_dim, pages_per_block=pages_per_block,
@@ -59,6 +61,18 @@ def test_small_full_parity(head_dim, pages_per_block, qhead):
     fin = np.isfinite(rlse)
     np.testing.assert_array_equal(np.isfinite(glse), fin)
     assert_f32_close(glse[fin], rlse[fin], "lse", scalars=True)
+
+
+def test_groups_spanning_several_row_tiles():
+    # 8 blocks per sequence and 96 queries naming 6 of them: about 72 edges x 4 query
+    # heads = 288 rows per (sequence, block, kv head) group, i.e. three 128-row tiles
+    c = wl.block_sparse(53, n_seqs=2, kv_len=512, queries_per_seq=96, hq=16, hkv=4,
+                        head_dim=128, pages_per_block=4, blocks_per_query=6,
+                        unmapped_frac=0.05)
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    ro, rm, rl, rst = oracle_partials(c)
+    assert gst == rst
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]))
 
 
 def test_bad_edges_and_pages_are_flagged():
