@@ -194,9 +194,11 @@ def timed_loop(fn, steps, world):
 ATTN_SOURCES = ["paged_kv_cache_231_gb300/csrc/attention.cu",
                 "paged_kv_cache_231_gb300/csrc/device_common.cuh",
                 "paged_kv_cache_231_gb300/csrc/scatter_dev.cuh",
+                "paged_kv_cache_231_gb300/csrc/tcgen05.cuh",
                 "paged_kv_cache_231_gb300/csrc/internal.h"]
 SPARSE_SOURCES = ["paged_kv_cache_231_gb300/csrc/sparse.cu",
                   "paged_kv_cache_231_gb300/csrc/device_common.cuh",
+                  "paged_kv_cache_231_gb300/csrc/tcgen05.cuh",
                   "paged_kv_cache_231_gb300/csrc/internal.h"]
 
 
@@ -338,11 +340,15 @@ def setup_sparse(args):
     w.check = lambda: 0
     w.metric = "block-sparse partials+combine fp32 TFLOP/s"
     w.unit, w.work, w.dtype, w.tokens = "TFLOP/s", flops / 1e12, "f32", c.q.shape[0]
-    w.dominant, w.dom_work, w.bound, w.dom_unit = "sparse_partials", flops / 1e12, "alu", "TFLOP/s"
-    w.traffic_summary, w.traffic_sources = None, SPARSE_SOURCES
+    # the partials run in 3xTF32 on the tensor core (about 0.24 ms of tf32 work at this
+    # size), so their roofline is HBM: K/V pool read once, Q once, partials written once
+    compulsory = (c.k_pages.nbytes + c.v_pages.nbytes + c.q.nbytes + P * (c.head_dim + 2) * 4)
+    w.dominant, w.dom_work, w.bound, w.dom_unit = "sparse_partials", compulsory / 1e9, "hbm", "GB/s"
+    w.traffic_summary, w.traffic_sources = "sparse_partials_block_sparse.md", SPARSE_SOURCES
     w.config = {"workload": "block_sparse", "queries": int(c.q.shape[0]), "edges": c.num_edges,
                 "partials": P, "hq": c.hq, "hkv": c.hkv, "head_dim": c.head_dim,
                 "block": c.block_size, "flops_per_step": flops,
+                "partials_compulsory_bytes": compulsory,
                 "l2": "no flush: K/V pages %.2f GB > L2" % ((kp.numel() + vp.numel()) * 4 / 1e9)}
     return w
 

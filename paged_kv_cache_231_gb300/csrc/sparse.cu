@@ -326,6 +326,33 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint32_t a_tmem, uint6
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// L2 residency: K/V pages and the partials stream through once (evict first); Q rows are
+// re-read by every edge that names their query (evict last).
+__device__ __forceinline__ uint64_t l2_policy_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void cp_async_16_hint(void* smem, const void* gmem, int src_bytes,
+                                                 uint64_t pol) {
+  asm volatile(
+      "cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(smem_u32(smem)),
+      "l"(gmem), "r"(src_bytes), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ float4 ldg_hint(const float* gmem, uint64_t pol) {
+  float4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(gmem), "l"(pol));
+  return v;
+}
+
 // x rounded to the nearest tf32 (low 13 mantissa bits cleared)
 __device__ __forceinline__ float tf32_hi(float x) {
   return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
@@ -362,6 +389,7 @@ __device__ __forceinline__ void stage_raw(const SparseParams& p, unsigned char* 
   const int64_t bb = g / p.hkv;
   const int blk = (int)(bb % p.nblk);
   const int batch = (int)(bb / p.nblk);
+  const uint64_t pol = l2_policy_first();
   static_assert(kNK * (D / 4) % kThreads == 0, "staging splits evenly over the CTA");
 #pragma unroll
   for (int it = 0; it < kNK * (D / 4) / kThreads; ++it) {
@@ -391,8 +419,8 @@ __device__ __forceinline__ void stage_raw(const SparseParams& p, unsigned char* 
       gv += row;
       nb = 16;
     }
-    cp_async_16(rawK + t * L::RS + c * 4, gk, nb);
-    cp_async_16(rawV + t * L::RS + c * 4, gv, nb);
+    cp_async_16_hint(rawK + t * L::RS + c * 4, gk, nb, pol);
+    cp_async_16_hint(rawV + t * L::RS + c * 4, gv, nb, pol);
     if (c == 0) rValid[t] = state;
   }
   cp_async_commit();
@@ -445,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
   if (g < p.ngroups) stage_raw<D>(p, sm, g);
   uint32_t phase = 0;
   bool ok = true, bad = false;
+  const uint64_t keep = l2_policy_last();
   // edge of this thread's row in a tile starting at edge c0 of a group ending at e1:
   // (edge, query index, block_len), fetched one tile ahead of its use
   const int epc = 128 / p.qhead;
@@ -520,16 +549,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
           sBL[r] = live ? nx_bl : 0;
           sPI[r] = live ? e * p.qhead + my_qh : -1;
         }
-        // the next tile's rows: later in this group, else the first tile of the next one
-        if (c0 + epc < e1) row_edge(c0 + epc, e1, nx_e, nx_q, nx_bl);
-        else if (gn < p.ngroups) row_edge(p.group_off[gn], p.group_off[gn + 1], nx_e, nx_q, nx_bl);
+
 #pragma unroll
         for (int ch = 0; ch < D / 64; ++ch) {
           float vh[32], vl[32];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const float4 v = live ? __ldg(reinterpret_cast<const float4*>(qrow + ch * 32 + k * 4))
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 v =
+                live ? ldg_hint(qrow + ch * 32 + k * 4, keep) : make_float4(0.f, 0.f, 0.f, 0.f);
             const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -559,6 +586,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
         }
         tc::commit(bar);
       }
+      // the next tile's rows (later in this group, else the first tile of the next one),
+      // fetched while S is computed: the dependent loads stall here, not on the next tile
+      if (c0 + epc < e1) row_edge(c0 + epc, e1, nx_e, nx_q, nx_bl);
+      else if (gn < p.ngroups) row_edge(p.group_off[gn], p.group_off[gn + 1], nx_e, nx_q, nx_bl);
       ok = __syncthreads_and(tc::mbar_wait(bar, phase & 1u, kTries));
       ++phase;
       if (!ok) break;
@@ -631,13 +662,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
             float* dst = p.o + (int64_t)pi * D + half * (D / 2) + ch * 32;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              *reinterpret_cast<float4*>(dst + k * 4) =
-                  make_float4(o[k * 4], o[k * 4 + 1], o[k * 4 + 2], o[k * 4 + 3]);
+              __stcs(reinterpret_cast<float4*>(dst + k * 4),
+                     make_float4(o[k * 4], o[k * 4 + 1], o[k * 4 + 2], o[k * 4 + 3]));
           }
         }
         if (half == 0 && pi >= 0) {
-          p.m[pi] = mrow;
-          p.l[pi] = lrow;
+          __stcs(p.m + pi, mrow);
+          __stcs(p.l + pi, lrow);
         }
       }
       tc::fence_before_sync();
