@@ -887,7 +887,8 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
-// Warp 4, lane 0: the MMA stream of the tile. S_jq = Q K_jq^T may be issued once K_jq
+// Warp 4, lane 0: the MMA stream of the tile (O += P V checked first: it is on the
+// softmax's critical path, S = Q K^T runs ahead). S_jq = Q K_jq^T may be issued once K_jq
 // landed and the softmax has read S_{jq-2} out of buffer jq % 2 (SEmpty phases are counted
 // per block, across tiles, because the last two of a tile are never waited for); O += P_jp V_jp (and
 // l += P_jp 1, the row sums, on an all-ones operand) once P_jp is in TMEM and V_jp landed.
@@ -907,6 +908,27 @@ __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
   uint32_t idle = 0;
   while (jp < t.nblk) {
     bool progress = false;
+    if (jp < jq) {
+      const int s = jp & 1;
+      if (tc::mbar_test(bars + kBarPFull, (blk_use + jp) & 1u) &&
+          tc::mbar_test(bars + kBarVFull0 + s, v_use[s] & 1u)) {
+        ++v_use[s];
+        tc::fence_async_shared();   // zero-filled value rows were written by cp.async
+        tc::fence_after_sync();
+        const uint32_t va = smem_u32(sm + TcLayout::kV + s * 32768);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t acc = (jp > 0 || ks > 0) ? 1u : 0u;
+          mma_f16_tmem_a(tmem + kTmO, tmem + kTmP + (uint32_t)ks * 8u,
+                         tc::smem_desc(va + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv, acc);
+          mma_f16_tmem_a(tmem + kTmL, tmem + kTmP + (uint32_t)ks * 8u, ones, idesc_l, acc);
+        }
+        tc::commit(bars + kBarODone);
+        tc::commit(bars + kBarVEmpty0 + s);
+        ++jp;
+        progress = true;
+      }
+    }
     if (jq < t.nblk) {
       // buffer s was last filled with S_{jq-2}: phase s_base[s] + (jq - 2) / 2 of SEmpty_s
       const int s = jq & 1;
@@ -926,27 +948,6 @@ __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
         tc::commit(bars + kBarKEmpty0 + kq);
         ++jq;
         kq = kq + 1 == kKStages ? 0 : kq + 1;
-        progress = true;
-      }
-    }
-    if (jp < jq) {
-      const int s = jp & 1;
-      if (tc::mbar_test(bars + kBarPFull, (blk_use + jp) & 1u) &&
-          tc::mbar_test(bars + kBarVFull0 + s, v_use[s] & 1u)) {
-        ++v_use[s];
-        tc::fence_async_shared();   // zero-filled value rows were written by cp.async
-        tc::fence_after_sync();
-        const uint32_t va = smem_u32(sm + TcLayout::kV + s * 32768);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t acc = (jp > 0 || ks > 0) ? 1u : 0u;
-          mma_f16_tmem_a(tmem + kTmO, tmem + kTmP + (uint32_t)ks * 8u,
-                         tc::smem_desc(va + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv, acc);
-          mma_f16_tmem_a(tmem + kTmL, tmem + kTmP + (uint32_t)ks * 8u, ones, idesc_l, acc);
-        }
-        tc::commit(bars + kBarODone);
-        tc::commit(bars + kBarVEmpty0 + s);
-        ++jp;
         progress = true;
       }
     }
