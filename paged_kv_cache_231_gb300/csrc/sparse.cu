@@ -360,18 +360,19 @@ __device__ __forceinline__ float tf32_hi(float x) {
 
 template <int D>
 struct Layout {   // byte offsets from a 1024-byte-aligned base
-  static constexpr int RS = D + 4;                          // raw row stride (floats)
+  static constexpr int RS = D;      // raw row stride (floats); chunk c of row t stored at
+                                    // chunk c ^ (t & 7), so column reads across rows spread
+                                    // over all banks
   static constexpr uint32_t kKhi = 0;                       // [64][D]: D/32 x [64][128 B]
   static constexpr uint32_t kKlo = kKhi + D * 256;
   static constexpr uint32_t kVhi = kKlo + D * 256;          // [D][64]: 2 x [D][128 B]
   static constexpr uint32_t kVlo = kVhi + D * 256;
   static constexpr uint32_t kRawK = kVlo + D * 256;         // [64][RS] fp32
   static constexpr uint32_t kRawV = kRawK + kNK * RS * 4;
-  static constexpr uint32_t kValid = kRawV + kNK * RS * 4;  // [64] key state, current group
+  static constexpr uint32_t kXfer = kRawV + kNK * RS * 4;   // 8 warps x [32][32] fp32 transpose
+  static constexpr uint32_t kValid = kXfer + 8 * 4096;      // [64] key state, current group
   static constexpr uint32_t kRValid = kValid + 64;          // [64] key state, staged group
-  static constexpr uint32_t kBL = kRValid + 64;             // [128] int: keys of each row
-  static constexpr uint32_t kPI = kBL + 512;                // [128] int: partial of each row
-  static constexpr uint32_t kBar = kPI + 512;               // MMA completion, drain
+  static constexpr uint32_t kBar = kRValid + 64;            // MMA completion, drain
   static constexpr uint32_t kTmem = kBar + 16;
   static constexpr uint32_t kNext = kTmem + 8;              // int64, 8-byte aligned
   static constexpr uint32_t kEnd = kNext + 8;
@@ -419,8 +420,9 @@ __device__ __forceinline__ void stage_raw(const SparseParams& p, unsigned char* 
       gv += row;
       nb = 16;
     }
-    cp_async_16_hint(rawK + t * L::RS + c * 4, gk, nb, pol);
-    cp_async_16_hint(rawV + t * L::RS + c * 4, gv, nb, pol);
+    const int cs = c ^ (t & 7);
+    cp_async_16_hint(rawK + t * L::RS + cs * 4, gk, nb, pol);
+    cp_async_16_hint(rawV + t * L::RS + cs * 4, gv, nb, pol);
     if (c == 0) rValid[t] = state;
   }
   cp_async_commit();
@@ -446,8 +448,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
   const float* rawV = reinterpret_cast<const float*>(sm + L::kRawV);
   uint8_t* sValid = sm + L::kValid;
   const uint8_t* rValid = sm + L::kRValid;
-  int* sBL = reinterpret_cast<int*>(sm + L::kBL);
-  int* sPI = reinterpret_cast<int*>(sm + L::kPI);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::kTmem);
   volatile int64_t* snext = reinterpret_cast<volatile int64_t*>(sm + L::kNext);
@@ -490,6 +490,44 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
   };
   int nx_e, nx_q, nx_bl;
   if (g < p.ngroups) row_edge(p.group_off[g], p.group_off[g + 1], nx_e, nx_q, nx_bl);
+  // Row r of the warp's [32][32] fp32 transpose buffer holds its 16-byte chunk q at chunk
+  // q ^ (r & 7): a lane's own row and a warp-wide 4-row x 128-byte slab both map to
+  // distinct banks. Global rows are read and written whole (128 bytes per 8 lanes)
+  // instead of one row per lane.
+  float* xf = reinterpret_cast<float*>(sm + L::kXfer) + warp * 1024;
+  // columns [col0, col0 + ncols) of the Q rows of this warp's 32 TMEM lanes (hi, lo) into
+  // TMEM; zeros for padding rows
+  auto load_q = [&](int h, int e, int qi, int col0, int ncols) {
+    const float* myrow = e >= 0 ? p.q + ((int64_t)qi * p.hq + h * p.qhead + my_qh) * D : nullptr;
+    const int q4 = lane & 7;
+    for (int ch = 0; ch < ncols / 32; ++ch) {
+      const int cbase = col0 + ch * 32;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {   // 4 rows x 32 floats per instruction
+        const int rr = i * 4 + (lane >> 3);
+        const float* src = reinterpret_cast<const float*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(myrow), rr));
+        const float4 v = src ? ldg_hint(src + cbase + q4 * 4, keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(xf + rr * 32 + ((q4 ^ (rr & 7)) << 2)) = v;
+      }
+      __syncwarp();
+      float vh[32], vl[32];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(xf + lane * 32 + ((q ^ (lane & 7)) << 2));
+        const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          vh[q * 4 + j] = tf32_hi(x[j]);
+          vl[q * 4 + j] = x[j] - vh[q * 4 + j];
+        }
+      }
+      __syncwarp();
+      tc::tmem_st32(lane_tm + 256 + cbase, vh);
+      tc::tmem_st32(lane_tm + 384 + cbase, vl);
+    }
+    tc::tmem_wait_st();
+  };
   const uint32_t idesc_s = idesc_tf32(128, kNK), idesc_o = idesc_tf32(128, D);
   while (g < p.ngroups && ok) {
     cp_async_wait<0>();
@@ -497,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
     // raw -> tf32 (hi, lo) tiles; K row-wise, V transposed (lane = key, conflict-free)
     for (int i = tid; i < kNK * (D / 4); i += kThreads) {
       const int t = i / (D / 4), c = i % (D / 4);
-      const float4 v = *reinterpret_cast<const float4*>(rawK + t * L::RS + c * 4);
+      const float4 v = *reinterpret_cast<const float4*>(rawK + t * L::RS + (c ^ (t & 7)) * 4);
       const float4 hi = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
       const float4 lo = make_float4(v.x - hi.x, v.y - hi.y, v.z - hi.z, v.w - hi.w);
       const uint32_t off = (uint32_t)(c >> 3) * (kNK * 128) + tc::sw128(t, c & 7);
@@ -507,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
     {
       const int t = lane + 32 * (warp & 1);
       for (int c = warp >> 1; c < D / 4; c += kThreads / 64) {
-        const float4 v = *reinterpret_cast<const float4*>(rawV + t * L::RS + c * 4);
+        const float4 v = *reinterpret_cast<const float4*>(rawV + t * L::RS + (c ^ (t & 7)) * 4);
         const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -538,37 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
     const int e0 = p.group_off[g], e1 = p.group_off[g + 1];
     const int h = (int)(g % p.hkv);
     for (int c0 = e0; c0 < e1 && ok; c0 += epc) {
-      // Q rows of this tile (hi, lo) into TMEM; warps 0-3 / 4-7 take the column halves
-      {
-        const int e = nx_e;
-        const bool live = e >= 0;
-        const float* qrow =
-            live ? p.q + ((int64_t)nx_q * p.hq + h * p.qhead + my_qh) * D + half * (D / 2)
-                 : nullptr;
-        if (half == 0) {
-          sBL[r] = live ? nx_bl : 0;
-          sPI[r] = live ? e * p.qhead + my_qh : -1;
-        }
-
-#pragma unroll
-        for (int ch = 0; ch < D / 64; ++ch) {
-          float vh[32], vl[32];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float4 v =
-                live ? ldg_hint(qrow + ch * 32 + k * 4, keep) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              vh[k * 4 + j] = tf32_hi(x[j]);
-              vl[k * 4 + j] = x[j] - vh[k * 4 + j];
-            }
-          }
-          tc::tmem_st32(lane_tm + 256 + half * (D / 2) + ch * 32, vh);
-          tc::tmem_st32(lane_tm + 384 + half * (D / 2) + ch * 32, vl);
-        }
-        tc::tmem_wait_st();
-      }
+      // this tile's rows (fetched one tile ahead); Q of a group's first tile is loaded here
+      // by all warps (column halves), later tiles' Q during the previous tile's epilogue
+      const int cur_bl = nx_e >= 0 ? nx_bl : 0;
+      const int cur_pi = nx_e >= 0 ? nx_e * p.qhead + my_qh : -1;
+      if (c0 == e0) load_q(h, nx_e, nx_q, half * (D / 2), D / 2);
       tc::fence_before_sync();
       __syncthreads();
       if (tid == 0) {   // S = Qhi Khi + Qhi Klo + Qlo Khi
@@ -601,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
         tc::tmem_ld32(lane_tm, s32[0]);
         tc::tmem_ld32(lane_tm + 32, s32[1]);
         tc::tmem_wait_ld();
-        const int bl = sBL[r];
+        const int bl = cur_bl;
         const uint64_t used = bl >= 64 ? ~0ull : ((1ull << bl) - 1ull);
         if (imask & used) bad = true;
 #pragma unroll
@@ -651,28 +663,36 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
       ++phase;
       if (!ok) break;
       tc::fence_after_sync();
-      {   // write the partials of this tile
-        const int pi = sPI[r];
-#pragma unroll
-        for (int ch = 0; ch < D / 64; ++ch) {
+      if (half == 0) {   // write the partials of this tile (full rows, 128 bytes per 8 lanes)
+        const int q4 = lane & 7;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
           float o[32];
-          tc::tmem_ld32(lane_tm + 64 + half * (D / 2) + ch * 32, o);
+          tc::tmem_ld32(lane_tm + 64 + ch * 32, o);
           tc::tmem_wait_ld();
-          if (pi >= 0) {
-            float* dst = p.o + (int64_t)pi * D + half * (D / 2) + ch * 32;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              __stcs(reinterpret_cast<float4*>(dst + k * 4),
-                     make_float4(o[k * 4], o[k * 4 + 1], o[k * 4 + 2], o[k * 4 + 3]));
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(xf + lane * 32 + ((q ^ (lane & 7)) << 2)) =
+                make_float4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = i * 4 + (lane >> 3);
+            const int pi = __shfl_sync(0xffffffffu, cur_pi, rr);
+            const float4 v = *reinterpret_cast<const float4*>(xf + rr * 32 + ((q4 ^ (rr & 7)) << 2));
+            if (pi >= 0) __stcs(reinterpret_cast<float4*>(p.o + (int64_t)pi * D + ch * 32 + q4 * 4), v);
           }
+          __syncwarp();
         }
-        if (half == 0 && pi >= 0) {
-          __stcs(p.m + pi, mrow);
-          __stcs(p.l + pi, lrow);
+        if (cur_pi >= 0) {
+          __stcs(p.m + cur_pi, mrow);
+          __stcs(p.l + cur_pi, lrow);
         }
+      } else if (c0 + epc < e1) {   // meanwhile the next tile's Q replaces P
+        load_q(h, nx_e, nx_q, 0, D);
       }
       tc::fence_before_sync();
-      __syncthreads();   // TMEM Q / P and the row tables are rewritten by the next tile
+      __syncthreads();   // the next tile's S = Q K^T follows
       tc::fence_after_sync();
     }
     g = gn;
