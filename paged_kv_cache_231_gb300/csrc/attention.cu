@@ -1677,8 +1677,9 @@ cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cud
                               : TileRing<D, NSTAGE>::kBytes;
   static_assert(smem <= 232448, "dynamic shared memory over the per-block limit");
   constexpr size_t split_smem = TileRing<D, NSTAGE>::kBytes;
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<uint64_t> configured{0};
+  int dev = -1;
+  if (needs_configure(configured, &dev)) {
     cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, NS, NSTAGE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -1691,7 +1692,7 @@ cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cud
                                (int)kTcSmem);
       if (e != cudaSuccess) return e;
     }
-    configured = true;
+    mark_configured(configured, dev);
   }
   const int64_t scatter_threads = (int64_t)sp.T * sp.Hkv * (sp.D / 8);
   {

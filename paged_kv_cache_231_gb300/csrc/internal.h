@@ -1,6 +1,7 @@
 // Internal host/device declarations shared by the library's translation units.
 #pragma once
 
+#include <atomic>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -157,6 +158,17 @@ struct SparseParams {
   int32_t* group_cursor;   // [ngroups]
   int32_t* perm;           // [E]
 };
+
+// Kernel attributes (the dynamic shared memory limit) belong to a device's context: each
+// launcher sets them once per device. Returns true when the current device still needs
+// them; mark_configured records that they were set.
+inline bool needs_configure(const std::atomic<uint64_t>& done, int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) *dev = -1;
+  return *dev < 0 || *dev >= 64 || !(done.load() & (1ull << *dev));
+}
+inline void mark_configured(std::atomic<uint64_t>& done, int dev) {
+  if (dev >= 0 && dev < 64) done.fetch_or(1ull << dev);
+}
 
 // launchers (return cudaSuccess or the launch error)
 cudaError_t launch_paged_scatter(const ScatterParams& p, cudaStream_t s);

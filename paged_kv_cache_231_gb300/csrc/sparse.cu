@@ -717,14 +717,15 @@ template <int D>
 cudaError_t launch_tc(const SparseParams& p, cudaStream_t s) {
   constexpr size_t smem = Layout<D>::kEnd + 1024;
   static_assert(smem <= 232448, "shared memory over the per-block limit");
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<uint64_t> configured{0};
+  int dev = -1;
+  if (needs_configure(configured, &dev)) {
     cudaError_t e = cudaFuncSetAttribute(sparse_tc_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    mark_configured(configured, dev);
   }
-  int dev = 0, sms = 0;
+  int sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
@@ -740,13 +741,14 @@ cudaError_t launch_partials(const SparseParams& p, cudaStream_t s) {
   constexpr int KS = D + 4, PS = KB + 4;
   const size_t smem = sizeof(float) * ((size_t)KB * KS + (size_t)KB * D + kSpRows * KS +
                                        (KB <= D ? 0 : (size_t)kSpRows * PS));
-  static bool configured = false;
-  if (!configured) {
+  static std::atomic<uint64_t> configured{0};
+  int dev = -1;
+  if (needs_configure(configured, &dev)) {
     cudaError_t e = cudaFuncSetAttribute(sparse_partials_kernel<D, KB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    mark_configured(configured, dev);
   }
   ProfScope ps("sparse_partials", s);
   sparse_partials_kernel<D, KB><<<(unsigned)p.ngroups, kSpThreads, smem, s>>>(p);
