@@ -9,6 +9,8 @@
 // once for the partials of every edge that names it. Head sizes 64 / 128 with blocks of
 // at most 64 keys run both products on the tensor core in 3xTF32 (sparse_tc_kernel);
 // other shapes take 64 query rows (edges x lanes) at a time with register-tiled fp32 FMA.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 
 #include "device_common.cuh"
@@ -326,24 +328,12 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint32_t a_tmem, uint6
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// L2 residency: K/V pages and the partials stream through once (evict first); Q rows are
+// L2 residency: the partials stream through once (evict first on store); Q rows are
 // re-read by every edge that names their query (evict last).
-__device__ __forceinline__ uint64_t l2_policy_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
-  return pol;
-}
 __device__ __forceinline__ uint64_t l2_policy_last() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
   return pol;
-}
-__device__ __forceinline__ void cp_async_16_hint(void* smem, const void* gmem, int src_bytes,
-                                                 uint64_t pol) {
-  asm volatile(
-      "cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(smem_u32(smem)),
-      "l"(gmem), "r"(src_bytes), "l"(pol)
-      : "memory");
 }
 __device__ __forceinline__ float4 ldg_hint(const float* gmem, uint64_t pol) {
   float4 v;
@@ -360,72 +350,76 @@ __device__ __forceinline__ float tf32_hi(float x) {
 
 template <int D>
 struct Layout {   // byte offsets from a 1024-byte-aligned base
-  static constexpr int RS = D;      // raw row stride (floats); chunk c of row t stored at
-                                    // chunk c ^ (t & 7), so column reads across rows spread
-                                    // over all banks
   static constexpr uint32_t kKhi = 0;                       // [64][D]: D/32 x [64][128 B]
   static constexpr uint32_t kKlo = kKhi + D * 256;
   static constexpr uint32_t kVhi = kKlo + D * 256;          // [D][64]: 2 x [D][128 B]
   static constexpr uint32_t kVlo = kVhi + D * 256;
-  static constexpr uint32_t kRawK = kVlo + D * 256;         // [64][RS] fp32
-  static constexpr uint32_t kRawV = kRawK + kNK * RS * 4;
-  static constexpr uint32_t kXfer = kRawV + kNK * RS * 4;   // 8 warps x [32][32] fp32 transpose
+  static constexpr uint32_t kRawK = kVlo + D * 256;         // raw K, V as loaded by TMA:
+  static constexpr uint32_t kRawV = kRawK + D * 256;        //   D/32 x [64 keys][128 B], swizzled
+  static constexpr uint32_t kXfer = kRawV + D * 256;        // 8 warps x [32][32] fp32 transpose
   static constexpr uint32_t kValid = kXfer + 8 * 4096;      // [64] key state, current group
   static constexpr uint32_t kRValid = kValid + 64;          // [64] key state, staged group
-  static constexpr uint32_t kBar = kRValid + 64;            // MMA completion, drain
-  static constexpr uint32_t kTmem = kBar + 16;
+  static constexpr uint32_t kBar = kRValid + 64;            // MMA completion, drain, raw K/V
+  static constexpr uint32_t kTmem = kBar + 24;
   static constexpr uint32_t kNext = kTmem + 8;              // int64, 8-byte aligned
   static constexpr uint32_t kEnd = kNext + 8;
 };
 
-// cp.async of group g's K and V rows into the raw buffers; key states into rValid
-// (0 unmapped or past the block, 1 mapped, 2 invalid table reference)
+struct SpMaps {     // TMA descriptors of the K and V pages (kernel parameters)
+  CUtensorMap k;    // [pages * hkv * page_size rows][D] fp32, box 32 x page_size
+  CUtensorMap v;
+};
+
+// One warp: group g's K and V pages by TMA (one box per page and 32-column slice, landing
+// in the 128-byte-swizzled layout of the raw tiles) onto rbar; key states into rValid
+// (0 unmapped or past the block, 1 mapped, 2 invalid table reference). Unmapped pages get
+// no copy: the conversion writes zeros for their keys.
 template <int D>
-__device__ __forceinline__ void stage_raw(const SparseParams& p, unsigned char* sm, int64_t g) {
+__device__ void stage_raw(const SparseParams& p, const SpMaps& maps, unsigned char* sm,
+                          int64_t g, uint64_t* rbar) {
   using L = Layout<D>;
-  float* rawK = reinterpret_cast<float*>(sm + L::kRawK);
-  float* rawV = reinterpret_cast<float*>(sm + L::kRawV);
+  const int lane = threadIdx.x & 31;
   uint8_t* rValid = sm + L::kRValid;
   const int h = (int)(g % p.hkv);
   const int64_t bb = g / p.hkv;
   const int blk = (int)(bb % p.nblk);
   const int batch = (int)(bb / p.nblk);
-  const uint64_t pol = l2_policy_first();
-  static_assert(kNK * (D / 4) % kThreads == 0, "staging splits evenly over the CTA");
 #pragma unroll
-  for (int it = 0; it < kNK * (D / 4) / kThreads; ++it) {
-    const int i = threadIdx.x + it * kThreads;
-    const int t = i / (D / 4), c = i % (D / 4);
-    int64_t page = -1;
+  for (int k = 0; k < 2; ++k) {
+    const int t = lane + 32 * k;
     uint8_t state = 0;
     if (t < p.block_size) {
       const int64_t slot = (int64_t)blk * p.ppb + t / p.page_size;
       if (slot < p.max_pages) {
-        page = p.bt[(int64_t)batch * p.max_pages + slot];
-        if (page >= p.num_pages) {
-          page = -1;
-          state = 2;
-        }
+        const int64_t page = p.bt[(int64_t)batch * p.max_pages + slot];
+        state = page >= p.num_pages ? 2 : page >= 0 ? 1 : 0;
       } else {
         state = 2;
       }
     }
-    if (page >= 0) state = 1;
-    const float* gk = p.kp;
-    const float* gv = p.vp;
-    int nb = 0;
-    if (page >= 0) {
-      const int64_t row = ((page * p.hkv + h) * p.page_size + t % p.page_size) * D + c * 4;
-      gk += row;
-      gv += row;
-      nb = 16;
-    }
-    const int cs = c ^ (t & 7);
-    cp_async_16_hint(rawK + t * L::RS + cs * 4, gk, nb, pol);
-    cp_async_16_hint(rawV + t * L::RS + cs * 4, gv, nb, pol);
-    if (c == 0) rValid[t] = state;
+    rValid[t] = state;
   }
-  cp_async_commit();
+  int row0 = -1;   // first row of page `lane` of the block in the page tensors
+  if (lane < p.ppb) {
+    const int64_t slot = (int64_t)blk * p.ppb + lane;
+    if (slot < p.max_pages) {
+      const int64_t page = p.bt[(int64_t)batch * p.max_pages + slot];
+      if (page >= 0 && page < p.num_pages) row0 = (int)((page * p.hkv + h) * p.page_size);
+    }
+  }
+  const uint32_t bits = __ballot_sync(0xffffffffu, row0 >= 0);
+  __syncwarp();   // the key states are published by lane 0's arrive
+  if (lane == 0)
+    tc::mbar_arrive_expect_tx(rbar, (uint32_t)__popc(bits) * (uint32_t)p.page_size * D * 4u * 2u);
+  __syncwarp();
+  if (row0 >= 0) {
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+      const uint32_t off = (uint32_t)q * (kNK * 128) + (uint32_t)(lane * p.page_size) * 128u;
+      tc::tma_load_2d(sm + L::kRawK + off, &maps.k, q * 32, row0, rbar);
+      tc::tma_load_2d(sm + L::kRawV + off, &maps.v, q * 32, row0, rbar);
+    }
+  }
 }
 
 // next group (in counter order) that has edges, or ngroups
@@ -439,13 +433,12 @@ __device__ __forceinline__ int64_t next_group(const SparseParams& p) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_tc_kernel(SparseParams p, const __grid_constant__ SpMaps maps) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const float* rawK = reinterpret_cast<const float*>(sm + L::kRawK);
-  const float* rawV = reinterpret_cast<const float*>(sm + L::kRawV);
   uint8_t* sValid = sm + L::kValid;
   const uint8_t* rValid = sm + L::kRValid;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
@@ -457,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
   if (tid == 0) {
     tc::mbar_init(bar, 1);
     tc::mbar_init(bar + 1, 1);
+    tc::mbar_init(bar + 2, 1);   // raw K / V landed (count 1 + tx)
     tc::mbar_init_fence();
     *snext = next_group(p);
   }
@@ -470,7 +464,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
   const uint32_t tmem = *tslot;
   const uint32_t lane_tm = tmem + ((uint32_t)(quarter * 32) << 16);
   int64_t g = *snext;
-  if (g < p.ngroups) stage_raw<D>(p, sm, g);
+  uint64_t* rbar = bar + 2;
+  constexpr int kStageWarp = 7;
+  if (warp == kStageWarp && g < p.ngroups) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&maps.k);
+      tc::tma_prefetch_desc(&maps.v);
+    }
+    stage_raw<D>(p, maps, sm, g, rbar);
+  }
+  uint32_t raw_issued = g < p.ngroups ? 1u : 0u, raw_used = 0;
   uint32_t phase = 0;
   bool ok = true, bad = false;
   const uint64_t keep = l2_policy_last();
@@ -530,22 +533,29 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
   };
   const uint32_t idesc_s = idesc_tf32(128, kNK), idesc_o = idesc_tf32(128, D);
   while (g < p.ngroups && ok) {
-    cp_async_wait<0>();
-    __syncthreads();
-    // raw -> tf32 (hi, lo) tiles; K row-wise, V transposed (lane = key, conflict-free)
+    ok = __syncthreads_and(tc::mbar_wait(rbar, raw_used & 1u, kTries));
+    ++raw_used;
+    if (!ok) break;
+    const uint8_t* rValid = sm + L::kRValid;
+    // raw -> tf32 (hi, lo) tiles: K in place (the raw layout is the K-major tile layout),
+    // V transposed (lane = key, conflict-free); keys not mapped become zeros
     for (int i = tid; i < kNK * (D / 4); i += kThreads) {
       const int t = i / (D / 4), c = i % (D / 4);
-      const float4 v = *reinterpret_cast<const float4*>(rawK + t * L::RS + (c ^ (t & 7)) * 4);
+      const uint32_t off = (uint32_t)(c >> 3) * (kNK * 128) + tc::sw128(t, c & 7);
+      float4 v = *reinterpret_cast<const float4*>(sm + L::kRawK + off);
+      if (rValid[t] != 1) v = make_float4(0.f, 0.f, 0.f, 0.f);
       const float4 hi = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
       const float4 lo = make_float4(v.x - hi.x, v.y - hi.y, v.z - hi.z, v.w - hi.w);
-      const uint32_t off = (uint32_t)(c >> 3) * (kNK * 128) + tc::sw128(t, c & 7);
       *reinterpret_cast<float4*>(sm + L::kKhi + off) = hi;
       *reinterpret_cast<float4*>(sm + L::kKlo + off) = lo;
     }
     {
       const int t = lane + 32 * (warp & 1);
+      const bool live = rValid[t] == 1;
       for (int c = warp >> 1; c < D / 4; c += kThreads / 64) {
-        const float4 v = *reinterpret_cast<const float4*>(rawV + t * L::RS + (c ^ (t & 7)) * 4);
+        float4 v = *reinterpret_cast<const float4*>(sm + L::kRawV + (uint32_t)(c >> 3) * (kNK * 128) +
+                                                    tc::sw128(t, c & 7));
+        if (!live) v = make_float4(0.f, 0.f, 0.f, 0.f);
         const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -564,7 +574,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
     __syncthreads();
     // the raw buffers are free: stage the next group behind this one's compute
     const int64_t gn = *snext;
-    if (gn < p.ngroups) stage_raw<D>(p, sm, gn);
+    if (gn < p.ngroups) {
+      if (warp == kStageWarp) stage_raw<D>(p, maps, sm, gn, rbar);
+      ++raw_issued;
+    }
     // key masks of this group: bit t of vmask = mapped, of imask = invalid reference
     uint64_t vmask = 0, imask = 0;
 #pragma unroll 8
@@ -698,19 +711,55 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_tc_kernel(SparseParams p) 
     g = gn;
   }
   if (!ok) {
-    // an MMA did not complete in time: let what this CTA issued finish before leaving
+    // a wait gave up: let what this CTA issued finish before leaving
     if (tid == 0) {
       flag_status(p.status, PKV_DEV_TIMEOUT);
       tc::commit(bar + 1);
       tc::mbar_wait(bar + 1, 0, kTries);
+      if (raw_issued > raw_used) tc::mbar_wait(rbar, raw_used & 1u, kTries);
     }
   }
-  cp_async_wait<0>();
   if (bad) flag_status(p.status, PKV_DEV_BAD_EDGE);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// [pages * hkv * page_size rows][D] fp32 pages, boxes of 32 columns x page_size rows in the
+// 128-byte swizzle
+bool encode_pages(CUtensorMap* m, const void* base, const SparseParams& p) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)p.D, (cuuint64_t)(p.num_pages * p.hkv * p.page_size)};
+  const cuuint64_t strides[1] = {(cuuint64_t)p.D * 4};
+  const cuuint32_t box[2] = {32, (cuuint32_t)p.page_size};
+  const cuuint32_t unit[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+            unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Shapes the tensor-core kernel takes: head size 64/128, blocks of at most 64 keys made of
+// whole pages of a multiple of 8 rows (each page's box starts on a 1024-byte boundary)
+bool eligible(const SparseParams& p) {
+  return (p.D == 64 || p.D == 128) && p.block_size <= kNK && p.qhead <= 128 &&
+         p.page_size % 8 == 0 && (int64_t)p.ppb * p.page_size <= kNK &&
+         p.num_pages * p.hkv * p.page_size <= INT32_MAX;
 }
 
 template <int D>
@@ -729,9 +778,12 @@ cudaError_t launch_tc(const SparseParams& p, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  SpMaps maps;
+  if (!encode_pages(&maps.k, p.kp, p) || !encode_pages(&maps.v, p.vp, p))
+    return cudaErrorInvalidValue;
   const int64_t grid = p.ngroups < sms ? p.ngroups : sms;
   ProfScope ps("sparse_partials", s);
-  sparse_tc_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(p);
+  sparse_tc_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(p, maps);
   return cudaGetLastError();
 }
 }  // namespace tcs
@@ -777,7 +829,7 @@ cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.ngroups == 0) return cudaSuccess;
-  if (p.block_size <= tcs::kNK && p.qhead <= 128) {   // 3xTF32 on the tensor core
+  if (tcs::eligible(p)) {   // 3xTF32 on the tensor core
     if (p.D == 64) return tcs::launch_tc<64>(p, s);
     if (p.D == 128) return tcs::launch_tc<128>(p, s);
   }
