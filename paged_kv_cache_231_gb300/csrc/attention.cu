@@ -665,8 +665,8 @@ __device__ void prefill_tile(const AttnParams& p, unsigned char* smem, int item_
 //            block (R = the largest power of two <= 128 dividing the block size) and is
 //            issued by one lane. Value rows of keys that are unmapped or past the tile's
 //            last visible key are zero-filled with cp.async instead, so that masked
-//            columns meet zeros in P V. K (3 stages) and V (2 stages) are released
-//            separately: K_{j+3} streams in once S_j is computed, V_{j+2} once
+//            columns meet zeros in P V. K (2 stages) and V (3 stages) are released
+//            separately: K_{j+2} streams in once S_j is computed, V_{j+3} once
 //            O += P_j V_j is.
 //   warp 4 (lane 0):   tcgen05.mma issuer. S_j = Q K_j^T into TMEM buffer j % 2 and
 //            O += P_j V_j are each issued as soon as their operands are ready.
@@ -687,8 +687,8 @@ struct TcMaps {     // TMA descriptors (kernel parameters)
 struct TcLayout {  // byte offsets from a 1024-byte-aligned base
   static constexpr uint32_t kQ = 0;               // 2 x [128][64] fp16 sub-tiles
   static constexpr uint32_t kK = 32768;           // kKStages x 32 KB
-  static constexpr uint32_t kV = kK + 98304;      // 2 stages x 32 KB
-  static constexpr uint32_t kOnes = kV + 65536;   // [16][64] fp16 ones (row-sum operand)
+  static constexpr uint32_t kV = kK + 65536;      // kVStages x 32 KB
+  static constexpr uint32_t kOnes = kV + 98304;   // [16][64] fp16 ones (row-sum operand)
   static constexpr uint32_t kBars = kOnes + 2048; // mbarriers (see TcBar)
   static constexpr uint32_t kTmem = kBars + 256;  // TMEM base address
   static constexpr uint32_t kTile = kTmem + 4;    // current tile index
@@ -697,10 +697,10 @@ struct TcLayout {  // byte offsets from a 1024-byte-aligned base
 };
 enum TcBar {  // mbarrier slots
   kBarQFull = 0,     // count 1 + tx: Q boxes landed
-  kBarKFull0 = 1,    // + stage (3), count 1 + tx: K boxes landed
-  kBarVFull0 = 4,    // + stage (2), count 32 + tx: V boxes and zero-filled rows landed
-  kBarKEmpty0 = 6,   // + stage (3), count 1: the S = Q K^T that read the stage completed
-  kBarVEmpty0 = 9,   // + stage (2), count 1: the O += P V that read the stage completed
+  kBarKFull0 = 1,    // + stage (2), count 1 + tx: K boxes landed
+  kBarVFull0 = 3,    // + stage (3), count 32 + tx: V boxes and zero-filled rows landed
+  kBarKEmpty0 = 6,   // + stage (2), count 1: the S = Q K^T that read the stage completed
+  kBarVEmpty0 = 8,   // + stage (3), count 1: the O += P V that read the stage completed
   kBarSFull0 = 11,   // + buffer, count 1: S_j in TMEM
   kBarPFull = 13,    // count 128: softmax wrote P_j to TMEM
   kBarODone = 14,    // count 1: O += P_j V_j (and l += P_j 1) completed
@@ -712,7 +712,8 @@ static_assert(kNumBars * 8 <= 256, "mbarrier slots");
 // TMEM columns: S_j in buffer j % 2, the O accumulator, the row sums l (first of 16
 // columns), and P_j as fp16 pairs (two keys per 32-bit column)
 constexpr uint32_t kTmS = 0, kTmO = 256, kTmL = 384, kTmP = 448;
-constexpr int kKStages = 3;        // K ring depth (V has 2 stages)
+constexpr int kKStages = 2;        // K ring depth
+constexpr int kVStages = 3;        // V ring depth: V_j streams in once O += P_{j-3} V_{j-3} is done
 constexpr uint32_t kTcWaitTries = 1u << 22;
 constexpr int kTcThreads = 224;
 constexpr int kMmaThread = 128;    // lane 0 of warp 4
@@ -831,15 +832,14 @@ __device__ void tc_load_k(const AttnParams& p, const TcMaps& maps, unsigned char
 // Value loader warp: whole boxes by TMA, the rest of the rows through zero-filling cp.async
 // (rows of unmapped or not-yet-visible keys must be zeros for P V).
 __device__ void tc_load_v(const AttnParams& p, const TcMaps& maps, unsigned char* sm,
-                          const TcTile& t, uint32_t (&v_use)[2]) {
+                          const TcTile& t, uint32_t (&v_use)[kVStages]) {
   constexpr int D = 128;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const int lane = threadIdx.x & 31;
   const int R = p.tc_rows;
   bool unmapped = false;   // reported by the key loader
-  for (int j = 0; j < t.nblk; ++j) {
-    const int s = j & 1;
+  for (int j = 0, s = 0; j < t.nblk; ++j, s = s + 1 == kVStages ? 0 : s + 1) {
     const TcBox x = tc_box(p, t, j, lane, unmapped);
     const bool whole = x.mapped && x.key0 + R <= t.kend;
     const bool ok = v_use[s] == 0 || tc_wait(bars + kBarVEmpty0 + s, (v_use[s] - 1) & 1u, abort);
@@ -894,7 +894,7 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
 // l += P_jp 1, the row sums, on an all-ones operand) once P_jp is in TMEM and V_jp landed.
 __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
                        uint32_t tmem, uint32_t q_use, uint32_t (&k_use)[kKStages],
-                       uint32_t (&v_use)[2], uint32_t (&s_base)[2], uint32_t& blk_use) {
+                       uint32_t (&v_use)[kVStages], uint32_t (&s_base)[2], uint32_t& blk_use) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const uint32_t idesc_qk = tc::idesc_f16(128, 128, false, false);
@@ -904,12 +904,12 @@ __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
   // every row and K step of the all-ones operand reads ones: one descriptor serves all
   const uint64_t ones = tc::smem_desc(smem_u32(sm + TcLayout::kOnes), 16, 1024);
   if (!tc_wait(bars + kBarQFull, q_use & 1u, abort)) return;
-  int jq = 0, jp = 0, kq = 0;   // kq = jq % kKStages
+  int jq = 0, jp = 0, kq = 0, vq = 0;   // kq = jq % kKStages, vq = jp % kVStages
   uint32_t idle = 0;
   while (jp < t.nblk) {
     bool progress = false;
     if (jp < jq) {
-      const int s = jp & 1;
+      const int s = vq;
       if (tc::mbar_test(bars + kBarPFull, (blk_use + jp) & 1u) &&
           tc::mbar_test(bars + kBarVFull0 + s, v_use[s] & 1u)) {
         ++v_use[s];
@@ -926,6 +926,7 @@ __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
         tc::commit(bars + kBarODone);
         tc::commit(bars + kBarVEmpty0 + s);
         ++jp;
+        vq = vq + 1 == kVStages ? 0 : vq + 1;
         progress = true;
       }
     }
@@ -1142,9 +1143,11 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
       tc::mbar_init(bars + kBarKFull0 + s, 1);
       tc::mbar_init(bars + kBarKEmpty0 + s, 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kVStages; ++s) {
       tc::mbar_init(bars + kBarVFull0 + s, 32);
       tc::mbar_init(bars + kBarVEmpty0 + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bars + kBarSFull0 + s, 1);
       tc::mbar_init(bars + kBarSEmpty0 + s, 128);
     }
@@ -1172,7 +1175,7 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
   // per-role phase counters (each role waits every phase it depends on, in order)
-  uint32_t k_use[kKStages] = {}, v_use[2] = {0u, 0u}, s_use[2] = {0u, 0u};
+  uint32_t k_use[kKStages] = {}, v_use[kVStages] = {}, s_use[2] = {0u, 0u};
   uint32_t s_base[2] = {0u, 0u};
   uint32_t q_use = 0u, blk_use = 0u;
   bool mma_aborted = false;
@@ -1215,7 +1218,7 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
         if (k_use[s] > 0) tc::mbar_wait(bars + kBarKFull0 + s, (k_use[s] - 1) & 1u, kTcWaitTries);
     }
     if (warp == kVLoaderWarp && lane == 0) {
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < kVStages; ++s)
         if (v_use[s] > 0) tc::mbar_wait(bars + kBarVFull0 + s, (v_use[s] - 1) & 1u, kTcWaitTries);
     }
   }
