@@ -702,10 +702,10 @@ enum TcBar {  // mbarrier slots
   kBarKEmpty0 = 6,   // + stage (2), count 1: the S = Q K^T that read the stage completed
   kBarVEmpty0 = 8,   // + stage (3), count 1: the O += P V that read the stage completed
   kBarSFull0 = 11,   // + buffer, count 1: S_j in TMEM
-  kBarPFull = 13,    // count 128: softmax wrote P_j to TMEM
+  kBarPFull = 13,    // count 4 (one per softmax warp): softmax wrote P_j to TMEM
   kBarODone = 14,    // count 1: O += P_j V_j (and l += P_j 1) completed
   kBarDrain = 15,    // count 1: MMAs in flight when a wait gave up
-  kBarSEmpty0 = 16,  // + buffer, count 128: softmax has read S_j out of the buffer
+  kBarSEmpty0 = 16,  // + buffer, count 4: softmax has read S_j out of the buffer
   kNumBars = 18
 };
 static_assert(kNumBars * 8 <= 256, "mbarrier slots");
@@ -1030,7 +1030,8 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
       tc::tmem_wait_ld();
     }
     tc::fence_before_sync();
-    mbar_arrive(bars + kBarSEmpty0 + s);
+    __syncwarp();   // one arrival per warp: 128 arrivals on one word would serialise
+    if (lane == 0) mbar_arrive(bars + kBarSEmpty0 + s);
     if (!__all_sync(0xffffffffu, full)) {
 #pragma unroll
       for (int c = 0; c < 128; ++c) {
@@ -1096,7 +1097,8 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
     }
     tc::tmem_wait_st();
     tc::fence_before_sync();
-    mbar_arrive(bars + kBarPFull);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + kBarPFull);
   }
   if (ok) {
     ok = __all_sync(0xffffffffu,
@@ -1149,9 +1151,9 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(bars + kBarSFull0 + s, 1);
-      tc::mbar_init(bars + kBarSEmpty0 + s, 128);
+      tc::mbar_init(bars + kBarSEmpty0 + s, 4);
     }
-    tc::mbar_init(bars + kBarPFull, 128);
+    tc::mbar_init(bars + kBarPFull, 4);
     tc::mbar_init(bars + kBarODone, 1);
     tc::mbar_init(bars + kBarDrain, 1);
     tc::mbar_init_fence();
