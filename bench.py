@@ -361,11 +361,18 @@ def setup_append(args):
     ts, kt = to_dev(c.total_sequence_length), to_dev(c.key_total_sequence_lengths)
     cos, sin = to_dev(c.cos_cache), to_dev(c.sin_cache)
 
-    def step():
-        B.pkv_kv_append_rotary(src, None, ts, kt, pk, pv, num_heads=c.num_heads,
-                               kv_num_heads=c.kv_num_heads, batch=c.batch, seq_len=c.seq_len,
-                               packed=True, cos_cache=cos, sin_cache=sin,
-                               rotary_dim=c.rotary_dim, interleaved=False)
+    import ctypes
+    lib = B.load_library()
+    a = B.make_append_args(src, None, ts, kt, pk, pv, num_heads=c.num_heads,
+                           kv_num_heads=c.kv_num_heads, batch=c.batch, seq_len=c.seq_len,
+                           packed=True, cos_cache=cos, sin_cache=sin,
+                           rotary_dim=c.rotary_dim, interleaved=False)
+    aref = ctypes.byref(a)
+
+    def step():   # the C entry point with a prebuilt argument block, as for attention
+        st = lib.pkv_kv_append_rotary(aref, torch.cuda.current_stream().cuda_stream)
+        if st != 0:
+            raise B.PagedKVError("pkv_kv_append_rotary", st)
 
     rows = c.batch * c.seq_len * c.kv_num_heads
     byts = rows * c.head_size * 2 * 4 + c.seq_len * c.rotary_dim * 2

@@ -371,16 +371,12 @@ def pkv_paged_scatter_kv(query, key, value, key_cache, value_cache,
 
 
 # ----------------------------------------------------------------------------- append
-def pkv_kv_append_rotary(source, value, total_sequence_length, key_total_sequence_lengths,
-                         present_key, present_value, *, num_heads: int, kv_num_heads: int,
-                         batch: int, seq_len: int, packed: bool, cos_cache=None,
-                         sin_cache=None, rotary_dim: int = 0, interleaved: bool = False,
-                         device_status=None, stream=None):
-    torch = _torch()
-    for t, n in ((source, "source"), (value, "value"), (present_key, "present_key"),
-                 (present_value, "present_value"), (cos_cache, "cos_cache"),
-                 (sin_cache, "sin_cache")):
-        _require(t, torch.float16, n)
+def make_append_args(source, value, total_sequence_length, key_total_sequence_lengths,
+                     present_key, present_value, *, num_heads: int, kv_num_heads: int,
+                     batch: int, seq_len: int, packed: bool, cos_cache=None, sin_cache=None,
+                     rotary_dim: int = 0, interleaved: bool = False,
+                     device_status=None) -> KVAppendArgs:
+    """Fill the C argument block of pkv_kv_append_rotary from tensors."""
     a = KVAppendArgs()
     a.source, a.value = _ptr(source), _ptr(value)
     a.total_sequence_length = _ptr(total_sequence_length)
@@ -397,6 +393,25 @@ def pkv_kv_append_rotary(source, value, total_sequence_length, key_total_sequenc
     a.packed = 1 if packed else 0
     a.interleaved = 1 if interleaved else 0
     a.dtype = _dtype_code(source)
+    return a
+
+
+def pkv_kv_append_rotary(source, value, total_sequence_length, key_total_sequence_lengths,
+                         present_key, present_value, *, num_heads: int, kv_num_heads: int,
+                         batch: int, seq_len: int, packed: bool, cos_cache=None,
+                         sin_cache=None, rotary_dim: int = 0, interleaved: bool = False,
+                         device_status=None, stream=None):
+    torch = _torch()
+    for t, n in ((source, "source"), (value, "value"), (present_key, "present_key"),
+                 (present_value, "present_value"), (cos_cache, "cos_cache"),
+                 (sin_cache, "sin_cache")):
+        _require(t, torch.float16, n)
+    a = make_append_args(source, value, total_sequence_length, key_total_sequence_lengths,
+                         present_key, present_value, num_heads=num_heads,
+                         kv_num_heads=kv_num_heads, batch=batch, seq_len=seq_len,
+                         packed=packed, cos_cache=cos_cache, sin_cache=sin_cache,
+                         rotary_dim=rotary_dim, interleaved=interleaved,
+                         device_status=device_status)
     _check("pkv_kv_append_rotary",
            load_library().pkv_kv_append_rotary(ctypes.byref(a), _stream(stream)))
 

@@ -1630,7 +1630,11 @@ __global__ void __launch_bounds__(kPrologueThreads) prologue_kernel(AttnParams p
     plan_block(p);
     return;
   }
-  paged_scatter_thread(sp, (int64_t)(blockIdx.x - 1) * kPrologueThreads + threadIdx.x);
+  const int64_t gid = (int64_t)(blockIdx.x - 1) * kPrologueThreads + threadIdx.x;
+  if (sp.row_path)
+    paged_scatter_row(sp, gid >> 4, threadIdx.x & 31);
+  else
+    paged_scatter_thread(sp, gid);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
@@ -1699,7 +1703,7 @@ cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cud
     }
     mark_configured(configured, dev);
   }
-  const int64_t scatter_threads = (int64_t)sp.T * sp.Hkv * (sp.D / 8);
+  const int64_t scatter_threads = pkv::scatter_threads(sp);
   {
     ProfScope ps("prologue", s);
     prologue_kernel<<<(unsigned)(1 + (scatter_threads + kPrologueThreads - 1) /

@@ -32,6 +32,7 @@ struct ScatterParams {
   int T, B, Hkv, D, BS, MB;
   int64_t NB;
   int rotary_dim, rotary_positions, interleaved;
+  int row_path;            // 1: half a warp per (token, kv head) row pair (scatter_dev.cuh)
 };
 
 // ---- BNSH append (SparseAttention append) -----------------------------------------
@@ -49,7 +50,19 @@ struct AppendParams {
   int B, S, Hkv, D;
   int64_t MCS;
   int rotary_dim, rotary_positions, interleaved;
+  int row_path;            // 1: half a warp per (token, kv head) row pair
 };
+
+// Whether a row pair can move as half a warp: head rows of at most 16 chunks and, with a
+// rotation, pairs that stay inside 8-element chunks (NeoX halves of a multiple of 8
+// elements, interleaved rotary_dim a multiple of 8) and 16-byte aligned cos/sin rows.
+inline bool row_path_ok(int D, int R, int interleaved, const void* cos_t, const void* sin_t) {
+  if (D > 128 || D % 8 != 0) return false;
+  if (R == 0) return true;
+  const bool pairs = interleaved ? R % 8 == 0 : (R / 2) % 8 == 0;
+  return pairs && (reinterpret_cast<uintptr_t>(cos_t) & 15u) == 0 &&
+         (reinterpret_cast<uintptr_t>(sin_t) & 15u) == 0;
+}
 
 // ---- attention (AttendSplitK / Attend) ----------------------------------------------
 struct DecodeItem {   // split mode: one split of one short (decoding) sequence
@@ -168,6 +181,12 @@ inline bool needs_configure(const std::atomic<uint64_t>& done, int* dev) {
 }
 inline void mark_configured(std::atomic<uint64_t>& done, int dev) {
   if (dev >= 0 && dev < 64) done.fetch_or(1ull << dev);
+}
+
+// threads of the ScatterKV pass: 16 per row pair on the row path, else one per chunk
+inline int64_t scatter_threads(const ScatterParams& p) {
+  const int64_t rows = (int64_t)p.T * p.Hkv;
+  return p.row_path ? rows * 16 : rows * (p.D / 8);
 }
 
 // launchers (return cudaSuccess or the launch error)

@@ -251,6 +251,7 @@ void fill_scatter(const pkv_paged_attention_args* a, int mode, ScatterParams& sp
   sp.rotary_dim = (int)a->rotary_dim;
   sp.rotary_positions = (int)std::min<int64_t>(a->rotary_positions, INT32_MAX);
   sp.interleaved = a->rotary_interleaved ? 1 : 0;
+  sp.row_path = row_path_ok(sp.D, sp.rotary_dim, sp.interleaved, sp.cos, sp.sin) ? 1 : 0;
 }
 
 int launch_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH; }
@@ -567,6 +568,7 @@ int pkv_kv_append_rotary(const pkv_kv_append_args* a, void* stream) {
   p.rotary_dim = (int)a->rotary_dim;
   p.rotary_positions = (int)std::min<int64_t>(a->rotary_positions, INT32_MAX);
   p.interleaved = a->interleaved ? 1 : 0;
+  p.row_path = row_path_ok(p.D, p.rotary_dim, p.interleaved, p.cos, p.sin) ? 1 : 0;
   return launch_status(launch_append(p, static_cast<cudaStream_t>(stream)));
 }
 

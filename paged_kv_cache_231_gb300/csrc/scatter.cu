@@ -10,8 +10,10 @@
 //   max_cache_seq, head] cache at position history(b) + t, rotating K with the
 //   sparse_rotary rule.
 //
-// One thread moves one 16-byte chunk (8 halves) of a K row and the matching V chunk;
-// consecutive threads take consecutive chunks of a row, so loads and stores coalesce.
+// Row path (head size <= 128, chunk-aligned rotation pairs): half a warp moves a (token,
+// kv head) row pair, rotation partners exchanged between lanes. Otherwise one thread moves
+// one 16-byte chunk (8 halves) of a K row and the matching V chunk; consecutive threads
+// take consecutive chunks of a row, so loads and stores coalesce.
 // The page's one-invocation-per-component dispatch and its 2-D dispatch folding
 // (a WebGPU grid limit) are not needed: CUDA's grid is 1-D up to 2^31 - 1 blocks.
 #include "device_common.cuh"
@@ -25,6 +27,39 @@ constexpr int kScatterThreads = 256;
 
 __global__ void __launch_bounds__(kScatterThreads) paged_scatter_kernel(ScatterParams p) {
   paged_scatter_thread(p, (int64_t)blockIdx.x * kScatterThreads + threadIdx.x);
+}
+
+__global__ void __launch_bounds__(kScatterThreads) paged_scatter_rows_kernel(ScatterParams p) {
+  const int64_t row = ((int64_t)blockIdx.x * kScatterThreads + threadIdx.x) >> 4;
+  paged_scatter_row(p, row, threadIdx.x & 31);
+}
+
+// Row path of the append: half-warp `row` of the (batch, kv head, new token) grid.
+__global__ void __launch_bounds__(kScatterThreads) append_rows_kernel(AppendParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = ((int64_t)blockIdx.x * kScatterThreads + threadIdx.x) >> 4;
+  if (row >= (int64_t)p.B * p.Hkv * p.S) return;
+  const int t = (int)(row % p.S);
+  const int64_t r = row / p.S;
+  const int h = (int)(r % p.Hkv);
+  const int b = (int)(r / p.Hkv);
+  // history length: prompt mode when the scalar total equals the new-token count
+  const uint32_t total0 = (uint32_t)p.total_seq[0];
+  const uint32_t S = (uint32_t)p.S;
+  uint32_t past = 0;
+  if (total0 != S) {
+    const uint32_t tb = (uint32_t)p.key_totals[b];
+    past = tb >= S ? tb - S : 0u;
+  }
+  const int64_t pos = (int64_t)past + t;
+  if (pos >= p.MCS || (p.rotary_dim > 0 && pos >= p.rotary_positions)) {
+    if ((lane & 15) == 0) flag_status(p.status, PKV_DEV_BAD_POSITION);
+    return;
+  }
+  const int64_t src = ((int64_t)b * p.S + t) * p.src_stride + (int64_t)h * p.D;
+  const int64_t dst = (((int64_t)b * p.Hkv + h) * p.MCS + pos) * p.D;
+  move_row_pair(p.k_src + src, p.v_src + src, p.pk + dst, p.pv + dst, p.D, pos, p.cos, p.sin,
+                p.rotary_dim, p.interleaved, lane);
 }
 
 __global__ void __launch_bounds__(kScatterThreads) append_kernel(AppendParams p) {
@@ -70,20 +105,27 @@ __global__ void __launch_bounds__(kScatterThreads) append_kernel(AppendParams p)
 }  // namespace
 
 cudaError_t launch_paged_scatter(const ScatterParams& p, cudaStream_t s) {
-  const int64_t total = (int64_t)p.T * p.Hkv * (p.D / 8);
+  const int64_t total = scatter_threads(p);
   if (total == 0) return cudaSuccess;
   ProfScope ps("scatter", s);
-  paged_scatter_kernel<<<(unsigned)((total + kScatterThreads - 1) / kScatterThreads),
-                         kScatterThreads, 0, s>>>(p);
+  const unsigned grid = (unsigned)((total + kScatterThreads - 1) / kScatterThreads);
+  if (p.row_path)
+    paged_scatter_rows_kernel<<<grid, kScatterThreads, 0, s>>>(p);
+  else
+    paged_scatter_kernel<<<grid, kScatterThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
-  const int64_t total = (int64_t)p.B * p.Hkv * p.S * (p.D / 8);
+  const int64_t rows = (int64_t)p.B * p.Hkv * p.S;
+  const int64_t total = p.row_path ? rows * 16 : rows * (p.D / 8);
   if (total == 0) return cudaSuccess;
   ProfScope ps("append", s);
-  append_kernel<<<(unsigned)((total + kScatterThreads - 1) / kScatterThreads),
-                  kScatterThreads, 0, s>>>(p);
+  const unsigned grid = (unsigned)((total + kScatterThreads - 1) / kScatterThreads);
+  if (p.row_path)
+    append_rows_kernel<<<grid, kScatterThreads, 0, s>>>(p);
+  else
+    append_kernel<<<grid, kScatterThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -50,6 +50,74 @@ __device__ __forceinline__ void rotate_chunk(__half (&x)[8], const __half* row, 
   for (int e = 0; e < 8; ++e) x[e] = __float2half_rn(out[e]);
 }
 
+// Half a warp moves one (token, kv head) row pair: lane c (of 16) the K chunk c (rotated
+// at position pos when R > 0) and the V chunk c. A NeoX partner chunk comes from the lane
+// of the half-warp that holds it and an interleaved partner from the same chunk; the
+// cos/sin values of a chunk's slots are one vector load each. Needs row_path_ok(D, R, ...);
+// every lane of the half-warp calls it (the two halves may take different rows).
+__device__ __forceinline__ void move_row_pair(const __half* krow, const __half* vrow,
+                                              __half* kdst, __half* vdst, int D, int64_t pos,
+                                              const __half* cos_t, const __half* sin_t, int R,
+                                              int interleaved, int lane) {
+  const int c = lane & 15;
+  const bool live = c < D / 8;
+  const unsigned hmask = 0xFFFFu << (lane & 16);
+  uint4 x = make_uint4(0u, 0u, 0u, 0u), v = make_uint4(0u, 0u, 0u, 0u);
+  if (live) {
+    x = *reinterpret_cast<const uint4*>(krow + c * 8);
+    v = *reinterpret_cast<const uint4*>(vrow + c * 8);
+  }
+  if (R > 0) {
+    const int half = R / 2;
+    const int hc = half / 8;   // NeoX: chunks per half
+    const int pc = interleaved ? c : (c < hc ? c + hc : c - hc);
+    const int src = (lane & 16) | (pc & 15);
+    uint4 px;
+    px.x = __shfl_sync(hmask, x.x, src);
+    px.y = __shfl_sync(hmask, x.y, src);
+    px.z = __shfl_sync(hmask, x.z, src);
+    px.w = __shfl_sync(hmask, x.w, src);
+    if (live && c * 8 < R) {
+      __half own[8], par[8], cs[8], sn[8];
+      *reinterpret_cast<uint4*>(own) = x;
+      *reinterpret_cast<uint4*>(par) = px;
+      bool first[8];
+      if (interleaved) {   // pairs (2i, 2i+1), slot i
+        const uint2 c2 = *reinterpret_cast<const uint2*>(cos_t + pos * half + c * 4);
+        const uint2 s2 = *reinterpret_cast<const uint2*>(sin_t + pos * half + c * 4);
+        __half c4[4], s4[4];
+        *reinterpret_cast<uint2*>(c4) = c2;
+        *reinterpret_cast<uint2*>(s4) = s2;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          first[e] = (e & 1) == 0;
+          par[e] = own[e ^ 1];
+          cs[e] = c4[e >> 1];
+          sn[e] = s4[e >> 1];
+        }
+      } else {              // pairs (d, d + half), slot d mod half
+        const bool f = c < hc;
+        const int slot0 = f ? c * 8 : c * 8 - half;
+        *reinterpret_cast<uint4*>(cs) = *reinterpret_cast<const uint4*>(cos_t + pos * half + slot0);
+        *reinterpret_cast<uint4*>(sn) = *reinterpret_cast<const uint4*>(sin_t + pos * half + slot0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) first[e] = f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float o = __half2float(own[e]), pv = __half2float(par[e]);
+        const float cf = __half2float(cs[e]), sf = __half2float(sn[e]);
+        own[e] = __float2half_rn(first[e] ? o * cf - pv * sf : o * cf + pv * sf);
+      }
+      x = *reinterpret_cast<uint4*>(own);
+    }
+  }
+  if (live) {
+    *reinterpret_cast<uint4*>(kdst + c * 8) = x;
+    *reinterpret_cast<uint4*>(vdst + c * 8) = v;
+  }
+}
+
 // One thread of the ScatterKV pass: 16-byte chunk `gid` of the (token, kv head, chunk)
 // grid moves K (rotated when asked) and V into the paged cache.
 __device__ __forceinline__ void paged_scatter_thread(const ScatterParams& p, int64_t gid) {
@@ -122,6 +190,63 @@ __device__ __forceinline__ void paged_scatter_thread(const ScatterParams& p, int
   }
   *reinterpret_cast<uint4*>(p.kc + dst) = kv;
   *reinterpret_cast<uint4*>(p.vc + dst) = vv;
+}
+
+// Half a warp of the ScatterKV pass on the row path: (token, kv head) row pair `row`.
+__device__ __forceinline__ void paged_scatter_row(const ScatterParams& p, int64_t row,
+                                                  int lane) {
+  if (row >= (int64_t)p.T * p.Hkv) return;
+  const int h = (int)(row % p.Hkv);
+  const int i = (int)(row / p.Hkv);
+  int lo = 0, hi = p.B - 1, b = -1;   // sequence of token i: the last b with cu[b] <= i
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if (p.cu[mid] <= i) {
+      b = mid;
+      lo = mid + 1;
+    } else {
+      hi = mid - 1;
+    }
+  }
+  if (b < 0) return;
+  const int s0 = p.cu[b], s1 = p.cu[b + 1], P = p.past[b];
+  if (!(s0 >= 0 && s1 >= s0 && s1 <= p.T && P >= 0)) {
+    if ((lane & 15) == 0 && h == 0) flag_status(p.status, PKV_DEV_BAD_SEQUENCE);
+    return;
+  }
+  if (i >= s1) return;
+  const int64_t pos = (int64_t)P + (i - s0);
+  int64_t blk, off;
+  if (p.slot_mapping) {
+    const int slot = p.slot_mapping[i];
+    if (slot < 0) return;
+    blk = slot / p.BS;
+    off = slot % p.BS;
+    if (blk >= p.NB) {
+      if ((lane & 15) == 0) flag_status(p.status, PKV_DEV_BAD_SLOT);
+      return;
+    }
+  } else {
+    const int64_t col = pos / p.BS;
+    if (col >= p.MB) {
+      if ((lane & 15) == 0) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+      return;
+    }
+    blk = p.block_table[(int64_t)b * p.MB + col];
+    off = pos % p.BS;
+    if (blk < 0 || blk >= p.NB) {
+      if ((lane & 15) == 0) flag_status(p.status, PKV_DEV_BAD_BLOCK);
+      return;
+    }
+  }
+  if (p.rotary_dim > 0 && pos >= p.rotary_positions) {
+    if ((lane & 15) == 0) flag_status(p.status, PKV_DEV_BAD_POSITION);
+    return;
+  }
+  const int64_t dst = ((blk * p.BS + off) * p.Hkv + h) * p.D;
+  move_row_pair(p.k_src + (int64_t)i * p.src_stride + (int64_t)h * p.D,
+                p.v_src + (int64_t)i * p.src_stride + (int64_t)h * p.D, p.kc + dst, p.vc + dst,
+                p.D, pos, p.cos, p.sin, p.rotary_dim, p.interleaved, lane);
 }
 
 }  // namespace pkv

@@ -66,7 +66,9 @@ def test_pages_split_policy():
     check(c, split_policy=B.PKV_SPLIT_PAGES)
 
 
-@pytest.mark.parametrize("rotary_dim,inter", [(128, False), (64, True), (32, False)])
+# rotary_dim 12 keeps rotation pairs across 8-element chunks: the per-chunk fallback path
+@pytest.mark.parametrize("rotary_dim,inter", [(128, False), (64, True), (32, False),
+                                              (12, False), (12, True)])
 def test_rotary_on_append(rotary_dim, inter):
     c = wl.paged_case(42, num_heads=8, kv_num_heads=2, head_size=128, block_size=16,
                       past=[5, 300, 0], new_tokens=[1, 40, 3], rotary_dim=rotary_dim,
