@@ -186,6 +186,36 @@ def kv_append_rotary(source, value, *, packed: bool, num_heads: int, kv_num_head
     return key_out, value_out, written, status
 
 
+def append_query_rotary(source, query, *, packed: bool, num_heads: int, kv_num_heads: int,
+                        head_size: int, batch: int, seq_len: int, total_sequence_length,
+                        key_total_sequence_lengths, cos_cache, sin_cache, rotary_dim: int,
+                        interleaved: bool):
+    """The query heads of the new tokens rotated at the same absolute position as their
+    keys, with the same ``sparse_rotary`` rule and cos/sin tables.
+
+    The append page rotates the key only; rotating the query at the token's position
+    is the other half of rotary attention and uses nothing the page does not already
+    define (history length from ``sparse_schedule``, pair geometry and rotation from
+    ``sparse_rotary``). Query rows come from the packed row's leading num_heads
+    heads, or from ``query`` [batch*seq_len, num_heads*head_size] in separate mode.
+    A position without a cos/sin row (or rotary_dim == 0) leaves the row unrotated.
+    Returns fp64 [batch*seq_len, num_heads*head_size], unrounded."""
+    Hq, D = num_heads, head_size
+    src = np.asarray(source if packed else query)
+    out = _f64(src[:, :Hq * D]).copy()
+    total0 = int(np.asarray(total_sequence_length).reshape(-1)[0])
+    for b in range(batch):
+        past = past_sequence_length(total0, int(key_total_sequence_lengths[b]), seq_len)
+        for t in range(seq_len):
+            pos = past + t
+            row = b * seq_len + t
+            if rotary_dim <= 0 or pos >= cos_cache.shape[0]:
+                continue
+            out[row] = rotate_rows(src[row, :Hq * D].reshape(Hq, D), [pos] * Hq, cos_cache,
+                                   sin_cache, rotary_dim, interleaved).reshape(Hq * D)
+    return out
+
+
 # ======================================================================================
 # PagedAttention (manifest.json)
 # ======================================================================================
@@ -430,13 +460,17 @@ def paged_attention(query, key, value, key_cache, value_cache, cu_seqlens,
                     past_seqlens, block_table, slot_mapping=None, *, num_heads: int,
                     kv_num_heads: int, scale: float = 0.0, cos_cache=None,
                     sin_cache=None, rotary_dim: int = 0,
-                    rotary_interleaved: bool = False, tokens: Optional[Sequence] = None):
+                    rotary_interleaved: bool = False, tokens: Optional[Sequence] = None,
+                    rotary_query: bool = False):
     """The PagedAttention operator: ScatterKV, then causal GQA attention of every new
     token over its sequence's keys read back through the block table.
 
     Query head hq uses kv head hq // (num_heads // kv_num_heads). Token i of
     sequence b at absolute position pos sees keys 0..pos. ``tokens`` restricts the
     attention to a subset of token indices (the scatter always runs in full).
+    With ``rotary_query`` (and rotary_dim > 0) every query head of token i is first
+    rotated at pos with the key's rotation rule and tables (unrounded); a position
+    without a cos/sin row leaves the query unrotated.
 
     Returns (out [T, Hq*D] fp64 with rows outside ``tokens`` left zero,
     key_cache, value_cache, status).
@@ -452,6 +486,12 @@ def paged_attention(query, key, value, key_cache, value_cache, cu_seqlens,
     T = q_all.shape[0]
     out = np.zeros((T, Hq, D), dtype=np.float64)
     smap, _ = sequence_map(cu_seqlens, past_seqlens, T)
+    if rotary_query and rotary_dim > 0:
+        q_all = _f64(q_all).copy()
+        for i in range(T):
+            if smap[i] is not None and smap[i][2] < cos_cache.shape[0]:
+                q_all[i] = rotate_rows(q_all[i], [smap[i][2]] * Hq, cos_cache, sin_cache,
+                                       rotary_dim, rotary_interleaved)
     wanted = range(T) if tokens is None else tokens
     by_seq = {}
     for i in wanted:
