@@ -11,8 +11,9 @@ Prints ONE JSON line. ``value`` is KV+Q+O bytes per step / device time per step 
 the step's inputs and D2H of its output inside the timed region). ``--impl reference``
 times the CPU oracle on a bounded sample of the same workload instead.
 
-Other workloads (``--workload varlen_mixed|block_sparse|append_prompt``) print the same
-structure with their own metric; they are not the headline line.
+Other workloads (``--workload llama8b_decode_rope|varlen_mixed|block_sparse|
+append_prompt``) print the same structure with their own metric; they are not the
+headline line.
 """
 import argparse
 import hashlib
@@ -46,8 +47,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b_decode",
-                    choices=["llama8b_decode", "varlen_mixed", "block_sparse",
-                             "append_prompt"])
+                    choices=["llama8b_decode", "llama8b_decode_rope", "varlen_mixed",
+                             "block_sparse", "append_prompt"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps")
@@ -228,7 +229,12 @@ def setup_paged(name, args):
     from paged_kv_cache_231_gb300 import binding as B
     from paged_kv_cache_231_gb300 import workloads as wl
     lib = B.load_library()
-    case = wl.llama8b_decode() if name == "llama8b_decode" else wl.varlen_mixed()
+    rope = name == "llama8b_decode_rope"
+    case = wl.llama8b_decode(rotary=rope) if name.startswith("llama8b_decode") \
+        else wl.varlen_mixed()
+    # RoPE variant: new keys and every query head rotated at the token's position
+    rot = dict(cos_cache=to_dev(case.cos_cache), sin_cache=to_dev(case.sin_cache),
+               rotary_dim=case.rotary_dim, rotary_query=True) if rope else {}
     q, k, v = to_dev(case.query), to_dev(case.key), to_dev(case.value)
     kc, vc = to_dev(case.key_cache), to_dev(case.value_cache)
     cu, past, bt = to_dev(case.cu_seqlens), to_dev(case.past_seqlens), to_dev(case.block_table)
@@ -238,7 +244,7 @@ def setup_paged(name, args):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     a = B.make_paged_args(q, k, v, kc, vc, cu, past, bt, sm, out,
                           num_heads=case.num_heads, kv_num_heads=case.kv_num_heads,
-                          scale=case.scale, device_status=status)
+                          scale=case.scale, device_status=status, **rot)
     nws = B.pkv_paged_attention_workspace_size(a)
     ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
     import ctypes
@@ -265,22 +271,26 @@ def setup_paged(name, args):
                 d.copy_(h, non_blocking=True)
         B.pkv_paged_attention(q, k, v, kc, vc, cu, past, bt, sm, num_heads=case.num_heads,
                               kv_num_heads=case.kv_num_heads, scale=case.scale, output=out,
-                              workspace=ws)
+                              workspace=ws, **rot)
         h_out.copy_(out, non_blocking=True)
 
     w = Workload()
     w.case, w.step, w.e2e_step, w.h2d, w.d2h = case, step, e2e_step, h2d, d2h
     w.status = status
     w.check = lambda: int(status.item())
-    if name == "llama8b_decode":
+    if name.startswith("llama8b_decode"):
         kvb, qb, ob = decode_bytes(case)
         w.metric, w.unit, w.work, w.dtype = METRIC, "GB/s", (kvb + qb + ob) / 1e9, "f16"
+        if rope:
+            w.metric = METRIC + ", RoPE on new keys and queries"
         w.tokens = case.num_tokens
         # the persistent attention kernel reads K/V and Q and writes O (fused combine)
         w.dominant, w.dom_work, w.bound = "attention", (kvb + qb + ob) / 1e9, "hbm"
         w.dom_unit = "GB/s"
         w.traffic_summary, w.traffic_sources = "attention_llama8b_decode.md", ATTN_SOURCES
-        w.config = {"workload": "llama8b_decode", "batch": case.batch, "tokens": case.num_tokens,
+        if rope:   # the summary's counters were taken on the unrotated workload
+            w.traffic_summary = None
+        w.config = {"workload": name, "batch": case.batch, "tokens": case.num_tokens,
                     "num_heads": 32, "kv_num_heads": 8, "head_size": 128, "block_size": 16,
                     "context": "U[512,8192]", "mean_context": float(case.context_lengths().mean()),
                     "kv_bytes_per_step": kvb, "bytes_per_step": kvb + qb + ob,
@@ -399,10 +409,12 @@ def oracle_sample(name, seconds):
     from oracle import pagedkv_oracle as orc
     from paged_kv_cache_231_gb300 import workloads as wl
     if name not in _CASES:   # inputs are drawn once, outside the timed sample
-        _CASES[name] = {"llama8b_decode": wl.llama8b_decode, "varlen_mixed": wl.varlen_mixed,
+        _CASES[name] = {"llama8b_decode": wl.llama8b_decode,
+                        "llama8b_decode_rope": lambda: wl.llama8b_decode(rotary=True),
+                        "varlen_mixed": wl.varlen_mixed,
                         "block_sparse": wl.block_sparse,
                         "append_prompt": lambda: wl.append_rotary(2, mode="prompt")}[name]()
-    if name in ("llama8b_decode", "varlen_mixed"):
+    if name in ("llama8b_decode", "llama8b_decode_rope", "varlen_mixed"):
         case = _CASES[name]
         D, Hkv, Hq = case.head_size, case.kv_num_heads, case.num_heads
         done_work, done_tok, spent, seqs = 0.0, 0, 0.0, 0
@@ -412,11 +424,13 @@ def oracle_sample(name, seconds):
             orc.paged_attention(sub.query, sub.key, sub.value, sub.key_cache, sub.value_cache,
                                 sub.cu_seqlens, sub.past_seqlens, sub.block_table,
                                 sub.slot_mapping, num_heads=Hq, kv_num_heads=Hkv,
-                                scale=sub.scale)
+                                scale=sub.scale, cos_cache=sub.cos_cache,
+                                sin_cache=sub.sin_cache, rotary_dim=sub.rotary_dim,
+                                rotary_query=sub.rotary_dim > 0)
             spent += time.perf_counter() - t0
             seqs += 1
             done_tok += sub.num_tokens
-            if name == "llama8b_decode":
+            if name != "varlen_mixed":
                 kvb, qb, ob = decode_bytes(sub)
                 done_work += (kvb + qb + ob) / 1e9
             else:
@@ -473,7 +487,9 @@ def _subcase(case, b):
         key_cache=case.key_cache[used], value_cache=case.value_cache[used],
         cu_seqlens=np.array([0, hi - lo], dtype=np.int32),
         past_seqlens=case.past_seqlens[b:b + 1], block_table=bt,
-        slot_mapping=None, scale=case.scale)
+        slot_mapping=None, scale=case.scale, cos_cache=case.cos_cache,
+        sin_cache=case.sin_cache, rotary_dim=case.rotary_dim,
+        rotary_interleaved=case.rotary_interleaved)
 
 
 def cpu_cores():
@@ -487,9 +503,10 @@ def cpu_cores():
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    unit = {"llama8b_decode": "GB/s", "varlen_mixed": "TFLOP/s", "block_sparse": "TFLOP/s",
-            "append_prompt": "GB/s"}[args.workload]
+    unit = {"llama8b_decode": "GB/s", "llama8b_decode_rope": "GB/s", "varlen_mixed": "TFLOP/s",
+            "block_sparse": "TFLOP/s", "append_prompt": "GB/s"}[args.workload]
     metric = {"llama8b_decode": METRIC,
+              "llama8b_decode_rope": METRIC + ", RoPE on new keys and queries",
               "varlen_mixed": "varlen prefill+decode attention TFLOP/s (causal pairs)",
               "block_sparse": "block-sparse partials+combine fp32 TFLOP/s",
               "append_prompt": "KV append+RoPE GB/s (prompt)"}[args.workload]
@@ -534,6 +551,7 @@ def main():
     barrier(world)
     B.load_library()
     setup = {"llama8b_decode": lambda: setup_paged("llama8b_decode", args),
+             "llama8b_decode_rope": lambda: setup_paged("llama8b_decode_rope", args),
              "varlen_mixed": lambda: setup_paged("varlen_mixed", args),
              "block_sparse": lambda: setup_sparse(args),
              "append_prompt": lambda: setup_append(args)}[args.workload]

@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 2
 
 typedef enum pkv_status {
   PKV_OK = 0,
@@ -143,6 +143,15 @@ typedef struct pkv_paged_attention_args {
   int32_t fixed_splits;      /* for PKV_SPLIT_FIXED */
   int32_t max_splits;        /* 0 = 16 (manifest MAX_SPLITS) */
   int32_t split_min_keys;    /* 0 = 128 (manifest SPLIT_MIN_KEYS) */
+  /* 1 (with rotary_dim > 0): every query head of a new token is rotated at the token's
+            absolute position with the key's rule and cos/sin tables before the
+            attention (the append page rotates keys only; this is the query half of
+            rotary attention). The rotated query is rounded to fp16 into the workspace
+            (num_tokens*num_heads*head_size*2 more bytes); the query input is not
+            written. A token whose position has no cos/sin row keeps its query
+            unrotated (its key is skipped with PKV_DEV_BAD_POSITION). 0: keys only. */
+  int32_t rotary_query;
+  int32_t reserved;
 } pkv_paged_attention_args;
 
 typedef struct pkv_paged_plan {
@@ -267,6 +276,15 @@ typedef struct pkv_kv_append_args {
   int32_t interleaved;
   int32_t dtype;                             /* PKV_F16 */
   int32_t reserved;
+  /* optional query rotation (query_out NULL: none). The num_heads query heads of each
+     new row, read from the packed row's leading heads or, in separate mode, from
+     `query` [batch*seq_len, num_heads*head_size], are rotated at the row's position
+     with K's rule and tables and written to query_out fp16 [batch*seq_len,
+     num_heads*head_size]; with rotary_dim == 0, or at a position without a cos/sin
+     row, the row is copied unrotated. The page rotates keys only; the query half
+     uses nothing it does not define. Independent of max_cache_seq. */
+  const void* query;
+  void* query_out;
 } pkv_kv_append_args;
 
 /* For each (batch b, kv head h, new token t): position = history(b) + t with the
@@ -275,7 +293,8 @@ typedef struct pkv_kv_append_args {
  * partner*sin, fp32 math, fp16 round-to-nearest-even), V copied; written to row
  * `position` of (b, h). Rows no new token lands on are untouched. position >=
  * max_cache_seq (or >= rotary_positions when rotating) skips the row and sets
- * PKV_DEV_BAD_POSITION. */
+ * PKV_DEV_BAD_POSITION. With query_out, the query heads are rotated the same way.
+ * query_out must not overlap the source or the caches. */
 int pkv_kv_append_rotary(const pkv_kv_append_args* args, void* stream);
 
 /* ---------------------------------------------------------------------------------

@@ -48,7 +48,8 @@ class PagedAttentionArgs(ctypes.Structure):
                 ("rotary_dim", c_i64), ("rotary_positions", c_i64),
                 ("rotary_interleaved", c_i32), ("is_causal", c_i32), ("dtype", c_i32),
                 ("scale", c_f32), ("split_policy", c_i32), ("fixed_splits", c_i32),
-                ("max_splits", c_i32), ("split_min_keys", c_i32)]
+                ("max_splits", c_i32), ("split_min_keys", c_i32), ("rotary_query", c_i32),
+                ("reserved", c_i32)]
 
 
 class PagedPlan(ctypes.Structure):
@@ -81,7 +82,7 @@ class KVAppendArgs(ctypes.Structure):
                 ("num_heads", c_i64), ("kv_num_heads", c_i64), ("head_size", c_i64),
                 ("max_cache_seq", c_i64), ("rotary_dim", c_i64), ("rotary_positions", c_i64),
                 ("packed", c_i32), ("interleaved", c_i32), ("dtype", c_i32),
-                ("reserved", c_i32)]
+                ("reserved", c_i32), ("query", c_vp), ("query_out", c_vp)]
 
 
 class SparseArgs(ctypes.Structure):
@@ -148,7 +149,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = c_i32
         fn.argtypes = args
-    if lib.pkv_abi_version() != 1:
+    if lib.pkv_abi_version() != 2:
         raise RuntimeError("libpagedkv ABI version mismatch")
     for name, cls in STRUCTS.items():
         n = lib.pkv_sizeof_struct(name.encode())
@@ -251,7 +252,8 @@ def make_paged_args(query, key, value, key_cache, value_cache, cumulative_sequen
                     is_causal: int = 1, device_status=None, cos_cache=None, sin_cache=None,
                     rotary_dim: int = 0, rotary_interleaved: bool = False,
                     split_policy: int = PKV_SPLIT_AUTO, fixed_splits: int = 0,
-                    max_splits: int = 0, split_min_keys: int = 0) -> PagedAttentionArgs:
+                    max_splits: int = 0, split_min_keys: int = 0,
+                    rotary_query: bool = False) -> PagedAttentionArgs:
     """Fill the C argument block from tensors (no validation beyond rank checks; the
     library validates). Works for host-only planning too (pointers may be host)."""
     a = PagedAttentionArgs()
@@ -279,6 +281,7 @@ def make_paged_args(query, key, value, key_cache, value_cache, cumulative_sequen
     a.scale = float(scale)
     a.split_policy, a.fixed_splits = int(split_policy), int(fixed_splits)
     a.max_splits, a.split_min_keys = int(max_splits), int(split_min_keys)
+    a.rotary_query = 1 if rotary_query else 0
     return a
 
 
@@ -319,7 +322,8 @@ def pkv_paged_attention(query, key, value, key_cache, value_cache,
                         device_status=None, cos_cache=None, sin_cache=None,
                         rotary_dim: int = 0, rotary_interleaved: bool = False,
                         split_policy: int = PKV_SPLIT_AUTO, fixed_splits: int = 0,
-                        max_splits: int = 0, split_min_keys: int = 0, stream=None):
+                        max_splits: int = 0, split_min_keys: int = 0,
+                        rotary_query: bool = False, stream=None):
     """PagedAttention: scatter new K/V into the caches (in place), then causal GQA
     attention. Returns the fp16 output [num_tokens, num_heads*head_size]."""
     torch = _torch()
@@ -339,7 +343,7 @@ def pkv_paged_attention(query, key, value, key_cache, value_cache,
                         cos_cache=cos_cache, sin_cache=sin_cache, rotary_dim=rotary_dim,
                         rotary_interleaved=rotary_interleaved, split_policy=split_policy,
                         fixed_splits=fixed_splits, max_splits=max_splits,
-                        split_min_keys=split_min_keys)
+                        split_min_keys=split_min_keys, rotary_query=rotary_query)
     need = pkv_paged_attention_workspace_size(a)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=query.device)
@@ -375,7 +379,7 @@ def make_append_args(source, value, total_sequence_length, key_total_sequence_le
                      present_key, present_value, *, num_heads: int, kv_num_heads: int,
                      batch: int, seq_len: int, packed: bool, cos_cache=None, sin_cache=None,
                      rotary_dim: int = 0, interleaved: bool = False,
-                     device_status=None) -> KVAppendArgs:
+                     device_status=None, query=None, query_out=None) -> KVAppendArgs:
     """Fill the C argument block of pkv_kv_append_rotary from tensors."""
     a = KVAppendArgs()
     a.source, a.value = _ptr(source), _ptr(value)
@@ -393,6 +397,7 @@ def make_append_args(source, value, total_sequence_length, key_total_sequence_le
     a.packed = 1 if packed else 0
     a.interleaved = 1 if interleaved else 0
     a.dtype = _dtype_code(source)
+    a.query, a.query_out = _ptr(query), _ptr(query_out)
     return a
 
 
@@ -400,18 +405,21 @@ def pkv_kv_append_rotary(source, value, total_sequence_length, key_total_sequenc
                          present_key, present_value, *, num_heads: int, kv_num_heads: int,
                          batch: int, seq_len: int, packed: bool, cos_cache=None,
                          sin_cache=None, rotary_dim: int = 0, interleaved: bool = False,
-                         device_status=None, stream=None):
+                         device_status=None, query=None, query_out=None, stream=None):
+    """KV append (+ RoPE of K); with ``query_out`` the query heads are rotated at the
+    same positions into it ([batch*seq_len, num_heads*head_size] fp16; ``query`` gives
+    the query rows in separate mode)."""
     torch = _torch()
     for t, n in ((source, "source"), (value, "value"), (present_key, "present_key"),
                  (present_value, "present_value"), (cos_cache, "cos_cache"),
-                 (sin_cache, "sin_cache")):
+                 (sin_cache, "sin_cache"), (query, "query"), (query_out, "query_out")):
         _require(t, torch.float16, n)
     a = make_append_args(source, value, total_sequence_length, key_total_sequence_lengths,
                          present_key, present_value, num_heads=num_heads,
                          kv_num_heads=kv_num_heads, batch=batch, seq_len=seq_len,
                          packed=packed, cos_cache=cos_cache, sin_cache=sin_cache,
                          rotary_dim=rotary_dim, interleaved=interleaved,
-                         device_status=device_status)
+                         device_status=device_status, query=query, query_out=query_out)
     _check("pkv_kv_append_rotary",
            load_library().pkv_kv_append_rotary(ctypes.byref(a), _stream(stream)))
 

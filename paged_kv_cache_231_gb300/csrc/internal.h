@@ -33,6 +33,12 @@ struct ScatterParams {
   int64_t NB;
   int rotary_dim, rotary_positions, interleaved;
   int row_path;            // 1: half a warp per (token, kv head) row pair (scatter_dev.cuh)
+  // query rotation (q_dst NULL: none): head hq of token i read at q_src + i*q_stride +
+  // hq*D, written rotated at q_dst + (i*Hq + hq)*D
+  const __half* q_src;
+  __half* q_dst;
+  int64_t q_stride;
+  int Hq;
 };
 
 // ---- BNSH append (SparseAttention append) -----------------------------------------
@@ -51,6 +57,12 @@ struct AppendParams {
   int64_t MCS;
   int rotary_dim, rotary_positions, interleaved;
   int row_path;            // 1: half a warp per (token, kv head) row pair
+  // query rotation (q_dst NULL: none): head hq of source row r read at q_src +
+  // r*q_stride + hq*D, written at q_dst + (r*Hq + hq)*D
+  const __half* q_src;
+  __half* q_dst;
+  int64_t q_stride;
+  int Hq;
 };
 
 // Whether a row pair can move as half a warp: head rows of at most 16 chunks and, with a

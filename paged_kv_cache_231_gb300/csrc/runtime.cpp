@@ -90,7 +90,9 @@ struct PagedLayout {
   int tc_rows = 0;   // > 0: prefill tiles on the tensor core, TMA boxes of tc_rows keys
   int64_t dec_bound = 0, pre_bound = 0, slot_bound = 0;
   size_t off_counts = 0, off_seqs = 0, off_done = 0, off_dec = 0, off_pre = 0,
-         off_slot_tok = 0, off_slot_spl = 0, off_po = 0, off_pm = 0, off_pl = 0, total = 0;
+         off_slot_tok = 0, off_slot_spl = 0, off_po = 0, off_pm = 0, off_pl = 0,
+         off_qrot = 0, total = 0;
+  bool rotate_query = false;
   int pages_splits = 1;
 };
 
@@ -216,6 +218,9 @@ int check_paged(const pkv_paged_attention_args* a, bool attention, PagedLayout* 
   off += align_up(4 * (size_t)prow);
   L->off_pl = off;
   off += align_up(4 * (size_t)prow);
+  L->rotate_query = a->rotary_query != 0 && a->rotary_dim > 0;
+  L->off_qrot = off;
+  off += align_up(L->rotate_query ? 2 * (size_t)T * a->num_heads * a->head_size : 0);
   L->total = off;
   return PKV_OK;
 }
@@ -432,6 +437,14 @@ int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
   ap.part_o = reinterpret_cast<float*>(ws + L.off_po);
   ap.part_m = reinterpret_cast<float*>(ws + L.off_pm);
   ap.part_l = reinterpret_cast<float*>(ws + L.off_pl);
+  if (L.rotate_query) {   // the prologue writes the rotated query; the attention reads it
+    sp.q_src = static_cast<const __half*>(args->query);
+    sp.q_stride = args->query_hidden;
+    sp.q_dst = reinterpret_cast<__half*>(ws + L.off_qrot);
+    sp.Hq = (int)args->num_heads;
+    ap.q = sp.q_dst;
+    ap.q_stride = args->num_heads * args->head_size;
+  }
   ap.dec_bound = L.dec_bound;
   ap.pre_bound = L.pre_bound;
   ap.slot_bound = L.slot_bound;
@@ -538,6 +551,9 @@ int pkv_kv_append_rotary(const pkv_kv_append_args* a, void* stream) {
   if (!aligned16(a->source) || (!a->packed && !aligned16(a->value)) ||
       !aligned16(a->present_key) || !aligned16(a->present_value))
     return PKV_ERR_ALIGN;
+  if (a->query_out && !a->packed && !a->query) return PKV_ERR_NULL;
+  if (a->query_out && (!aligned16(a->query_out) || (!a->packed && !aligned16(a->query))))
+    return PKV_ERR_ALIGN;
   if (a->batch * a->seq_len > INT32_MAX / 2 || a->batch > INT32_MAX / 2)
     return PKV_ERR_UNSUPPORTED;
   if (a->batch == 0 || a->seq_len == 0) return PKV_OK;
@@ -569,6 +585,12 @@ int pkv_kv_append_rotary(const pkv_kv_append_args* a, void* stream) {
   p.rotary_positions = (int)std::min<int64_t>(a->rotary_positions, INT32_MAX);
   p.interleaved = a->interleaved ? 1 : 0;
   p.row_path = row_path_ok(p.D, p.rotary_dim, p.interleaved, p.cos, p.sin) ? 1 : 0;
+  if (a->query_out) {
+    p.q_src = a->packed ? src : static_cast<const __half*>(a->query);
+    p.q_stride = a->packed ? p.src_stride : a->num_heads * D;
+    p.q_dst = static_cast<__half*>(a->query_out);
+    p.Hq = (int)a->num_heads;
+  }
   return launch_status(launch_append(p, static_cast<cudaStream_t>(stream)));
 }
 

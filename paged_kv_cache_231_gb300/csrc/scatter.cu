@@ -8,7 +8,8 @@
 // append_kernel: the KV-append main of "com.microsoft.SparseAttention
 //   sparse-kv-append.wgsl.jinja" - writes new rows into a [batch, kv_heads,
 //   max_cache_seq, head] cache at position history(b) + t, rotating K with the
-//   sparse_rotary rule.
+//   sparse_rotary rule; optionally the query heads are rotated at the same position
+//   into a separate output (the page rotates keys only).
 //
 // Row path (head size <= 128, chunk-aligned rotation pairs): half a warp moves a (token,
 // kv head) row pair, rotation partners exchanged between lanes. Otherwise one thread moves
@@ -52,6 +53,13 @@ __global__ void __launch_bounds__(kScatterThreads) append_rows_kernel(AppendPara
     past = tb >= S ? tb - S : 0u;
   }
   const int64_t pos = (int64_t)past + t;
+  if (p.q_dst) {   // the G query heads of kv head h (copied unrotated past the table)
+    const int G = p.Hq / p.Hkv;
+    const int64_t qr = (int64_t)b * p.S + t;
+    rotate_query_rows(p.q_src + qr * p.q_stride + (int64_t)h * G * p.D,
+                      p.q_dst + (qr * p.Hq + (int64_t)h * G) * p.D, G, p.D, pos, p.cos, p.sin,
+                      pos < p.rotary_positions ? p.rotary_dim : 0, p.interleaved, lane);
+  }
   if (pos >= p.MCS || (p.rotary_dim > 0 && pos >= p.rotary_positions)) {
     if ((lane & 15) == 0) flag_status(p.status, PKV_DEV_BAD_POSITION);
     return;
@@ -83,6 +91,20 @@ __global__ void __launch_bounds__(kScatterThreads) append_kernel(AppendParams p)
     past = tb >= S ? tb - S : 0u;
   }
   const int64_t pos = (int64_t)past + t;
+  if (p.q_dst) {   // the G query heads of kv head h, chunk c (copied unrotated past the table)
+    const int G = p.Hq / p.Hkv;
+    const int64_t qr = (int64_t)b * p.S + t;
+    const bool rot = p.rotary_dim > 0 && c * 8 < p.rotary_dim && pos < p.rotary_positions;
+    for (int g = 0; g < G; ++g) {
+      const int hq = h * G + g;
+      const __half* qrow = p.q_src + qr * p.q_stride + (int64_t)hq * p.D;
+      __half x[8];
+      *reinterpret_cast<uint4*>(x) = *reinterpret_cast<const uint4*>(qrow + c * 8);
+      if (rot) rotate_chunk(x, qrow, c * 8, pos, p.cos, p.sin, p.rotary_dim, p.interleaved);
+      *reinterpret_cast<uint4*>(p.q_dst + (qr * p.Hq + hq) * p.D + c * 8) =
+          *reinterpret_cast<uint4*>(x);
+    }
+  }
   if (pos >= p.MCS || (p.rotary_dim > 0 && pos >= p.rotary_positions)) {
     if (c == 0) flag_status(p.status, PKV_DEV_BAD_POSITION);
     return;

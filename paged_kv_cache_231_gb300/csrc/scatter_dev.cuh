@@ -5,7 +5,9 @@
 // rows go to the paged cache [num_blocks, block_size, kv_heads, head] at the row
 // slot_mapping names, or at the block-table row of the token's absolute position
 // past + t. Optionally the key is first rotated at that position with the rotation
-// rule of "com.microsoft.SparseAttention sparse-kv-append.wgsl.jinja" (sparse_rotary).
+// rule of "com.microsoft.SparseAttention sparse-kv-append.wgsl.jinja" (sparse_rotary),
+// and the token's query heads are rotated at the same position into a separate buffer
+// (the page rotates keys only; the query uses the same rule and tables).
 #pragma once
 
 #include "device_common.cuh"
@@ -50,71 +52,105 @@ __device__ __forceinline__ void rotate_chunk(__half (&x)[8], const __half* row, 
   for (int e = 0; e < 8; ++e) x[e] = __float2half_rn(out[e]);
 }
 
-// Half a warp moves one (token, kv head) row pair: lane c (of 16) the K chunk c (rotated
-// at position pos when R > 0) and the V chunk c. A NeoX partner chunk comes from the lane
-// of the half-warp that holds it and an interleaved partner from the same chunk; the
+// Half a warp rotates one head row at position pos: lane c (of 16) holds chunk c (eight
+// elements) in `x` and gets it back rotated when R > 0. A NeoX partner chunk comes from the
+// lane of the half-warp that holds it and an interleaved partner from the same chunk; the
 // cos/sin values of a chunk's slots are one vector load each. Needs row_path_ok(D, R, ...);
 // every lane of the half-warp calls it (the two halves may take different rows).
+__device__ __forceinline__ uint4 rope_chunk_half(uint4 x, bool live, int64_t pos,
+                                                 const __half* cos_t, const __half* sin_t,
+                                                 int R, int interleaved, int lane) {
+  if (R <= 0) return x;
+  const int c = lane & 15;
+  const unsigned hmask = 0xFFFFu << (lane & 16);
+  const int half = R / 2;
+  const int hc = half / 8;   // NeoX: chunks per half
+  const int pc = interleaved ? c : (c < hc ? c + hc : c - hc);
+  const int src = (lane & 16) | (pc & 15);
+  uint4 px;
+  px.x = __shfl_sync(hmask, x.x, src);
+  px.y = __shfl_sync(hmask, x.y, src);
+  px.z = __shfl_sync(hmask, x.z, src);
+  px.w = __shfl_sync(hmask, x.w, src);
+  if (!live || c * 8 >= R) return x;
+  __half own[8], par[8], cs[8], sn[8];
+  *reinterpret_cast<uint4*>(own) = x;
+  *reinterpret_cast<uint4*>(par) = px;
+  bool first[8];
+  if (interleaved) {   // pairs (2i, 2i+1), slot i
+    const uint2 c2 = *reinterpret_cast<const uint2*>(cos_t + pos * half + c * 4);
+    const uint2 s2 = *reinterpret_cast<const uint2*>(sin_t + pos * half + c * 4);
+    __half c4[4], s4[4];
+    *reinterpret_cast<uint2*>(c4) = c2;
+    *reinterpret_cast<uint2*>(s4) = s2;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      first[e] = (e & 1) == 0;
+      par[e] = own[e ^ 1];
+      cs[e] = c4[e >> 1];
+      sn[e] = s4[e >> 1];
+    }
+  } else {              // pairs (d, d + half), slot d mod half
+    const bool f = c < hc;
+    const int slot0 = f ? c * 8 : c * 8 - half;
+    *reinterpret_cast<uint4*>(cs) = *reinterpret_cast<const uint4*>(cos_t + pos * half + slot0);
+    *reinterpret_cast<uint4*>(sn) = *reinterpret_cast<const uint4*>(sin_t + pos * half + slot0);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) first[e] = f;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float o = __half2float(own[e]), pv = __half2float(par[e]);
+    const float cf = __half2float(cs[e]), sf = __half2float(sn[e]);
+    own[e] = __float2half_rn(first[e] ? o * cf - pv * sf : o * cf + pv * sf);
+  }
+  return *reinterpret_cast<uint4*>(own);
+}
+
+// Half a warp moves one (token, kv head) row pair: lane c (of 16) the K chunk c (rotated
+// at position pos when R > 0) and the V chunk c.
 __device__ __forceinline__ void move_row_pair(const __half* krow, const __half* vrow,
                                               __half* kdst, __half* vdst, int D, int64_t pos,
                                               const __half* cos_t, const __half* sin_t, int R,
                                               int interleaved, int lane) {
   const int c = lane & 15;
   const bool live = c < D / 8;
-  const unsigned hmask = 0xFFFFu << (lane & 16);
   uint4 x = make_uint4(0u, 0u, 0u, 0u), v = make_uint4(0u, 0u, 0u, 0u);
   if (live) {
     x = *reinterpret_cast<const uint4*>(krow + c * 8);
     v = *reinterpret_cast<const uint4*>(vrow + c * 8);
   }
-  if (R > 0) {
-    const int half = R / 2;
-    const int hc = half / 8;   // NeoX: chunks per half
-    const int pc = interleaved ? c : (c < hc ? c + hc : c - hc);
-    const int src = (lane & 16) | (pc & 15);
-    uint4 px;
-    px.x = __shfl_sync(hmask, x.x, src);
-    px.y = __shfl_sync(hmask, x.y, src);
-    px.z = __shfl_sync(hmask, x.z, src);
-    px.w = __shfl_sync(hmask, x.w, src);
-    if (live && c * 8 < R) {
-      __half own[8], par[8], cs[8], sn[8];
-      *reinterpret_cast<uint4*>(own) = x;
-      *reinterpret_cast<uint4*>(par) = px;
-      bool first[8];
-      if (interleaved) {   // pairs (2i, 2i+1), slot i
-        const uint2 c2 = *reinterpret_cast<const uint2*>(cos_t + pos * half + c * 4);
-        const uint2 s2 = *reinterpret_cast<const uint2*>(sin_t + pos * half + c * 4);
-        __half c4[4], s4[4];
-        *reinterpret_cast<uint2*>(c4) = c2;
-        *reinterpret_cast<uint2*>(s4) = s2;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          first[e] = (e & 1) == 0;
-          par[e] = own[e ^ 1];
-          cs[e] = c4[e >> 1];
-          sn[e] = s4[e >> 1];
-        }
-      } else {              // pairs (d, d + half), slot d mod half
-        const bool f = c < hc;
-        const int slot0 = f ? c * 8 : c * 8 - half;
-        *reinterpret_cast<uint4*>(cs) = *reinterpret_cast<const uint4*>(cos_t + pos * half + slot0);
-        *reinterpret_cast<uint4*>(sn) = *reinterpret_cast<const uint4*>(sin_t + pos * half + slot0);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) first[e] = f;
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float o = __half2float(own[e]), pv = __half2float(par[e]);
-        const float cf = __half2float(cs[e]), sf = __half2float(sn[e]);
-        own[e] = __float2half_rn(first[e] ? o * cf - pv * sf : o * cf + pv * sf);
-      }
-      x = *reinterpret_cast<uint4*>(own);
-    }
-  }
+  x = rope_chunk_half(x, live, pos, cos_t, sin_t, R, interleaved, lane);
   if (live) {
     *reinterpret_cast<uint4*>(kdst + c * 8) = x;
     *reinterpret_cast<uint4*>(vdst + c * 8) = v;
+  }
+}
+
+// Half a warp rotates the G query heads of one (token, kv head) at position pos (R = 0:
+// plain copy). Head g's row is at qsrc + g*D and goes to qdst + g*D; four heads' chunks
+// are loaded before any is stored.
+__device__ __forceinline__ void rotate_query_rows(const __half* qsrc, __half* qdst, int G,
+                                                  int D, int64_t pos, const __half* cos_t,
+                                                  const __half* sin_t, int R, int interleaved,
+                                                  int lane) {
+  const int c = lane & 15;
+  const bool live = c < D / 8;
+  for (int g0 = 0; g0 < G; g0 += 4) {
+    uint4 x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (live && g0 + j < G)
+        x[j] = *reinterpret_cast<const uint4*>(qsrc + (int64_t)(g0 + j) * D + c * 8);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (g0 + j < G) {   // uniform over the half-warp
+        x[j] = rope_chunk_half(x[j], live, pos, cos_t, sin_t, R, interleaved, lane);
+        if (live) *reinterpret_cast<uint4*>(qdst + (int64_t)(g0 + j) * D + c * 8) = x[j];
+      }
+    }
   }
 }
 
@@ -149,6 +185,19 @@ __device__ __forceinline__ void paged_scatter_thread(const ScatterParams& p, int
   }
   if (i >= s1) return;  // token past the last sequence: not part of the batch
   const int64_t pos = (int64_t)P + (i - s0);
+  if (p.q_dst) {   // the G query heads of kv head h, chunk c (copied unrotated past the table)
+    const int G = p.Hq / p.Hkv;
+    const bool rot = p.rotary_dim > 0 && c * 8 < p.rotary_dim && pos < p.rotary_positions;
+    for (int g = 0; g < G; ++g) {
+      const int hq = h * G + g;
+      const __half* qrow = p.q_src + (int64_t)i * p.q_stride + (int64_t)hq * p.D;
+      __half x[8];
+      *reinterpret_cast<uint4*>(x) = *reinterpret_cast<const uint4*>(qrow + c * 8);
+      if (rot) rotate_chunk(x, qrow, c * 8, pos, p.cos, p.sin, p.rotary_dim, p.interleaved);
+      *reinterpret_cast<uint4*>(p.q_dst + ((int64_t)i * p.Hq + hq) * p.D + c * 8) =
+          *reinterpret_cast<uint4*>(x);
+    }
+  }
 
   int64_t blk, off;
   if (p.slot_mapping) {
@@ -216,6 +265,13 @@ __device__ __forceinline__ void paged_scatter_row(const ScatterParams& p, int64_
   }
   if (i >= s1) return;
   const int64_t pos = (int64_t)P + (i - s0);
+  if (p.q_dst) {   // the G query heads of kv head h (copied unrotated past the table)
+    const int G = p.Hq / p.Hkv;
+    rotate_query_rows(p.q_src + (int64_t)i * p.q_stride + (int64_t)h * G * p.D,
+                      p.q_dst + ((int64_t)i * p.Hq + (int64_t)h * G) * p.D, G, p.D, pos,
+                      p.cos, p.sin, pos < p.rotary_positions ? p.rotary_dim : 0,
+                      p.interleaved, lane);
+  }
   int64_t blk, off;
   if (p.slot_mapping) {
     const int slot = p.slot_mapping[i];

@@ -76,13 +76,14 @@ def run_paged_gpu(case, **kw) -> PagedRun:
     return PagedRun(host(out), host(kc), host(vc), int(status.item()))
 
 
-def run_paged_oracle(case, tokens=None) -> PagedRun:
+def run_paged_oracle(case, tokens=None, rotary_query=False) -> PagedRun:
     out, kc, vc, st = orc.paged_attention(
         case.query, case.key, case.value, case.key_cache, case.value_cache,
         case.cu_seqlens, case.past_seqlens, case.block_table, case.slot_mapping,
         num_heads=case.num_heads, kv_num_heads=case.kv_num_heads, scale=case.scale,
         cos_cache=case.cos_cache, sin_cache=case.sin_cache, rotary_dim=case.rotary_dim,
-        rotary_interleaved=case.rotary_interleaved, tokens=tokens)
+        rotary_interleaved=case.rotary_interleaved, tokens=tokens,
+        rotary_query=rotary_query)
     return PagedRun(out, kc, vc, st)
 
 

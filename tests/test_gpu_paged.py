@@ -13,9 +13,9 @@ from .gpu_util import (DEV, assert_f16_close, compare_caches, dev, host, run_pag
 pytestmark = pytest.mark.gpu
 
 
-def check(case, tokens=None, **kw):
-    g = run_paged_gpu(case, **kw)
-    r = run_paged_oracle(case, tokens)
+def check(case, tokens=None, rotary_query=False, **kw):
+    g = run_paged_gpu(case, rotary_query=rotary_query, **kw)
+    r = run_paged_oracle(case, tokens, rotary_query=rotary_query)
     rows = slice(None) if tokens is None else np.asarray(tokens)
     err = assert_f16_close(g.out[rows], r.out[rows], "attention output")
     compare_caches(g, r, case.rotary_dim > 0, "caches")
@@ -74,6 +74,28 @@ def test_rotary_on_append(rotary_dim, inter):
                       past=[5, 300, 0], new_tokens=[1, 40, 3], rotary_dim=rotary_dim,
                       rotary_interleaved=inter)
     check(c)
+
+
+# query heads rotated with the keys: decode (stream-K), tensor-core prefill (head 128,
+# blocks of 16) and mma.sync prefill (head 64) read the rotated query from the workspace
+@pytest.mark.parametrize("D,rotary_dim,inter,packed", [(128, 128, False, False),
+                                                       (128, 64, True, True),
+                                                       (128, 12, False, False),
+                                                       (64, 64, False, True),
+                                                       (64, 12, True, False)])
+def test_rotary_query(D, rotary_dim, inter, packed):
+    c = wl.paged_case(44, num_heads=8, kv_num_heads=2, head_size=D, block_size=16,
+                      past=[5, 300, 0, 1000], new_tokens=[1, 40, 130, 1], packed=packed,
+                      rotary_dim=rotary_dim, rotary_interleaved=inter)
+    check(c, rotary_query=True)
+
+
+def test_rotary_query_position_past_table():
+    c = wl.paged_case(45, num_heads=4, kv_num_heads=1, head_size=128, block_size=16,
+                      past=[5, 60], new_tokens=[3, 1], rotary_dim=128)
+    c.cos_cache = c.cos_cache[:7]     # token 2 of sequence 0 and sequence 1: past the table
+    c.sin_cache = c.sin_cache[:7]
+    check(c, rotary_query=True)
 
 
 def test_llama8b_decode_full_size():
