@@ -12,8 +12,8 @@ the step's inputs and D2H of its output inside the timed region). ``--impl refer
 times the CPU oracle on a bounded sample of the same workload instead.
 
 Other workloads (``--workload llama8b_decode_rope|varlen_mixed|block_sparse|
-append_prompt``) print the same structure with their own metric; they are not the
-headline line.
+block_sparse_f16|append_prompt``) print the same structure with their own metric; they
+are not the headline line.
 """
 import argparse
 import hashlib
@@ -48,7 +48,7 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b_decode",
                     choices=["llama8b_decode", "llama8b_decode_rope", "varlen_mixed",
-                             "block_sparse", "append_prompt"])
+                             "block_sparse", "block_sparse_f16", "append_prompt"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps")
@@ -201,6 +201,10 @@ SPARSE_SOURCES = ["paged_kv_cache_231_gb300/csrc/sparse.cu",
                   "paged_kv_cache_231_gb300/csrc/device_common.cuh",
                   "paged_kv_cache_231_gb300/csrc/tcgen05.cuh",
                   "paged_kv_cache_231_gb300/csrc/internal.h"]
+SPARSE16_SOURCES = ["paged_kv_cache_231_gb300/csrc/sparse16.cu",
+                    "paged_kv_cache_231_gb300/csrc/device_common.cuh",
+                    "paged_kv_cache_231_gb300/csrc/tcgen05.cuh",
+                    "paged_kv_cache_231_gb300/csrc/internal.h"]
 
 
 def decode_bytes(case):
@@ -312,12 +316,12 @@ def setup_paged(name, args):
     return w
 
 
-def setup_sparse(args):
+def setup_sparse(args, f16=False):
     from paged_kv_cache_231_gb300 import binding as B
     from paged_kv_cache_231_gb300 import workloads as wl
     import ctypes
     lib = B.load_library()
-    c = wl.block_sparse()
+    c = wl.block_sparse(dtype=np.float16 if f16 else np.float32)
     q, kp, vp = to_dev(c.q), to_dev(c.k_pages), to_dev(c.v_pages)
     em, bt, so = to_dev(c.edge_meta), to_dev(c.block_tables), to_dev(c.seg_offsets)
     P = c.num_edges * c.qhead
@@ -348,18 +352,24 @@ def setup_sparse(args):
     w = Workload()
     w.case, w.step, w.e2e_step, w.h2d, w.d2h = c, step, None, 0, 0
     w.check = lambda: 0
-    w.metric = "block-sparse partials+combine fp32 TFLOP/s"
-    w.unit, w.work, w.dtype, w.tokens = "TFLOP/s", flops / 1e12, "f32", c.q.shape[0]
-    # the partials run in 3xTF32 on the tensor core (about 0.24 ms of tf32 work at this
-    # size), so their roofline is HBM: K/V pool read once, Q once, partials written once
+    w.metric = "block-sparse partials+combine %s TFLOP/s" % ("fp16" if f16 else "fp32")
+    w.unit, w.work, w.dtype, w.tokens = "TFLOP/s", flops / 1e12, "f16" if f16 else "f32", \
+        c.q.shape[0]
+    # the partials run on the tensor core (3xTF32 for fp32 inputs: about 0.24 ms of tf32
+    # work at this size; kind::f16 for fp16), so their roofline is HBM: K/V pool read once,
+    # Q once, partials (fp32) written once
     compulsory = (c.k_pages.nbytes + c.v_pages.nbytes + c.q.nbytes + P * (c.head_dim + 2) * 4)
     w.dominant, w.dom_work, w.bound, w.dom_unit = "sparse_partials", compulsory / 1e9, "hbm", "GB/s"
     w.traffic_summary, w.traffic_sources = "sparse_partials_block_sparse.md", SPARSE_SOURCES
-    w.config = {"workload": "block_sparse", "queries": int(c.q.shape[0]), "edges": c.num_edges,
+    if f16:
+        w.traffic_summary, w.traffic_sources = "sparse_tc16_block_sparse_f16.md", SPARSE16_SOURCES
+    w.config = {"workload": "block_sparse_f16" if f16 else "block_sparse",
+                "queries": int(c.q.shape[0]), "edges": c.num_edges,
                 "partials": P, "hq": c.hq, "hkv": c.hkv, "head_dim": c.head_dim,
                 "block": c.block_size, "flops_per_step": flops,
                 "partials_compulsory_bytes": compulsory,
-                "l2": "no flush: K/V pages %.2f GB > L2" % ((kp.numel() + vp.numel()) * 4 / 1e9)}
+                "l2": "no flush: K/V pages %.2f GB > L2"
+                      % ((kp.numel() + vp.numel()) * kp.element_size() / 1e9)}
     return w
 
 
@@ -413,6 +423,7 @@ def oracle_sample(name, seconds):
                         "llama8b_decode_rope": lambda: wl.llama8b_decode(rotary=True),
                         "varlen_mixed": wl.varlen_mixed,
                         "block_sparse": wl.block_sparse,
+                        "block_sparse_f16": lambda: wl.block_sparse(dtype=np.float16),
                         "append_prompt": lambda: wl.append_rotary(2, mode="prompt")}[name]()
     if name in ("llama8b_decode", "llama8b_decode_rope", "varlen_mixed"):
         case = _CASES[name]
@@ -439,7 +450,7 @@ def oracle_sample(name, seconds):
                 break
         return done_work / spent, done_tok / spent, \
             f"{seqs} of {case.batch} sequences, whole (scatter + attention), {spent:.1f} s"
-    if name == "block_sparse":
+    if name in ("block_sparse", "block_sparse_f16"):
         c = _CASES[name]
         rng = np.random.default_rng(0)
         order = rng.permutation(c.num_edges)
@@ -504,11 +515,13 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     unit = {"llama8b_decode": "GB/s", "llama8b_decode_rope": "GB/s", "varlen_mixed": "TFLOP/s",
-            "block_sparse": "TFLOP/s", "append_prompt": "GB/s"}[args.workload]
+            "block_sparse": "TFLOP/s", "block_sparse_f16": "TFLOP/s",
+            "append_prompt": "GB/s"}[args.workload]
     metric = {"llama8b_decode": METRIC,
               "llama8b_decode_rope": METRIC + ", RoPE on new keys and queries",
               "varlen_mixed": "varlen prefill+decode attention TFLOP/s (causal pairs)",
               "block_sparse": "block-sparse partials+combine fp32 TFLOP/s",
+              "block_sparse_f16": "block-sparse partials+combine fp16 TFLOP/s",
               "append_prompt": "KV append+RoPE GB/s (prompt)"}[args.workload]
     # each step is a bounded sample (at least one whole sequence / edge batch); the
     # whole run is kept to about two minutes of CPU work
@@ -554,6 +567,7 @@ def main():
              "llama8b_decode_rope": lambda: setup_paged("llama8b_decode_rope", args),
              "varlen_mixed": lambda: setup_paged("varlen_mixed", args),
              "block_sparse": lambda: setup_sparse(args),
+             "block_sparse_f16": lambda: setup_sparse(args, f16=True),
              "append_prompt": lambda: setup_append(args)}[args.workload]
     w = setup()
     hbm, bf16, bf16_sus, peak_kind = measured_peaks()

@@ -301,9 +301,9 @@ int pkv_kv_append_rotary(const pkv_kv_append_args* args, void* stream);
  * Block-sparse partials (sparse_attention_forward.wgsl)
  * ------------------------------------------------------------------------------- */
 typedef struct pkv_sparse_args {
-  const float* q;              /* [num_queries, hq, head_dim] */
-  const float* k_pages;        /* [num_pages, hkv, page_size, head_dim] */
-  const float* v_pages;
+  const void* q;               /* [num_queries, hq, head_dim], element type `dtype` */
+  const void* k_pages;         /* [num_pages, hkv, page_size, head_dim], `dtype` */
+  const void* v_pages;
   const int32_t* edge_meta;    /* [num_edges, 5]: q_idx, h (kv head), blk, batch, block_len */
   const int32_t* block_tables; /* [num_seqs, max_pages]: page id or -1 (unmapped) */
   float* o_partial;            /* [num_edges*qhead, head_dim] */
@@ -323,7 +323,9 @@ typedef struct pkv_sparse_args {
   int64_t page_size;
   int64_t pages_per_block;
   float softmax_scale;
-  int32_t reserved;
+  /* element type of q, k_pages, v_pages: PKV_F32 (0 is taken as PKV_F32) or PKV_F16.
+     The partials are fp32 either way. */
+  int32_t dtype;
 } pkv_sparse_args;
 
 /* Host only: workspace bytes for the edge grouping of pkv_sparse_attention_partials. */
@@ -338,7 +340,12 @@ int pkv_sparse_attention_partials_workspace_size(const pkv_sparse_args* args,
  * block_len <= 0 -> (o = 0, m = -1e30, l = 0). No causal mask. fp32 throughout.
  * The GPU form groups edges by (batch, kv head, block) so each K/V block is read
  * once for all edges that name it. Supported: head_dim in {64, 128}, block_size
- * <= 128, qhead <= 64. */
+ * <= 128, qhead <= 64.
+ * dtype PKV_F16 (the page computes in fp32; this is the half-precision variant): scores
+ * are fp16 products summed in fp32, the weights are rounded once to fp16 for the
+ * weighted sum of value rows and l sums those rounded weights; everything else as above.
+ * Supported for fp16: head_dim in {64, 128}, block_size <= 64, page_size a multiple of
+ * 8 with pages_per_block * page_size <= 64; else PKV_ERR_UNSUPPORTED. */
 int pkv_sparse_attention_partials(const pkv_sparse_args* args, void* workspace,
                                   size_t workspace_bytes, void* stream);
 

@@ -92,7 +92,7 @@ class SparseArgs(ctypes.Structure):
                 ("num_edges", c_i64), ("num_seqs", c_i64), ("max_pages", c_i64),
                 ("num_pages", c_i64), ("qhead", c_i64), ("hq", c_i64), ("hkv", c_i64),
                 ("head_dim", c_i64), ("block_size", c_i64), ("page_size", c_i64),
-                ("pages_per_block", c_i64), ("softmax_scale", c_f32), ("reserved", c_i32)]
+                ("pages_per_block", c_i64), ("softmax_scale", c_f32), ("dtype", c_i32)]
 
 
 class CombineArgs(ctypes.Structure):
@@ -441,6 +441,7 @@ def make_sparse_args(q, k_pages, v_pages, edge_meta, block_tables, o, m, l, *, q
     a.block_size, a.page_size = int(block_size), int(page_size)
     a.pages_per_block = int(pages_per_block)
     a.softmax_scale = float(softmax_scale)
+    a.dtype = _dtype_code(q)
     return a
 
 
@@ -457,10 +458,12 @@ def pkv_sparse_attention_partials(q, k_pages, v_pages, edge_meta, block_tables, 
                                   pages_per_block: int, softmax_scale: float,
                                   o=None, m=None, l=None, workspace=None,
                                   device_status=None, stream=None):
-    """Block-sparse (o, m, l) partials, partial index edge*qhead + lane."""
+    """Block-sparse (o, m, l) partials, partial index edge*qhead + lane. q and the pages
+    are all fp32 or all fp16; the partials are fp32."""
     torch = _torch()
+    dt = torch.float16 if q.dtype == torch.float16 else torch.float32
     for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
-        _require(t, torch.float32, n)
+        _require(t, dt, n)
     _require(edge_meta, torch.int32, "edge_meta")
     _require(block_tables, torch.int32, "block_tables")
     P = int(edge_meta.shape[0]) * qhead

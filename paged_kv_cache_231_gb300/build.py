@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 SOURCES = ["runtime.cpp", "attention.cu", "scatter.cu", "combine.cu", "sparse.cu",
-           "static_workspace.cu"]
+           "sparse16.cu", "static_workspace.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -175,6 +175,11 @@ struct SparseParams {
   int64_t Tq, E, nseq, max_pages, num_pages;
   int qhead, hq, hkv, D, block_size, page_size, ppb;
   float scale;
+  // fp16 inputs (f16 = 1): the same tensors as q / kp / vp, as halves
+  int f16;
+  const __half* q16;
+  const __half* kp16;
+  const __half* vp16;
   // grouping workspace
   int64_t nblk;            // blocks per sequence row of the table
   int64_t ngroups;         // nseq * nblk * hkv
@@ -182,6 +187,7 @@ struct SparseParams {
   int32_t* group_off;      // [ngroups + 1]
   int32_t* group_cursor;   // [ngroups]
   int32_t* perm;           // [E]
+  int4* edge_rec;          // [E] (edge, q_idx, block_len clipped to block_size, 0), grouped order
 };
 
 // Kernel attributes (the dynamic shared memory limit) belong to a device's context: each
@@ -209,6 +215,8 @@ int attention_ctas_per_sm();
 int attention_warps_per_cta();
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s);
+bool sparse_f16_eligible(const SparseParams& p);                        // sparse16.cu
+cudaError_t launch_sparse_tc16(const SparseParams& p, cudaStream_t s);  // sparse16.cu
 
 // profiler hooks (runtime.cpp)
 void prof_begin(const char* name, cudaStream_t s);

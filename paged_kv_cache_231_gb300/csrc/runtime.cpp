@@ -605,6 +605,11 @@ int check_sparse(const pkv_sparse_args* a, int64_t* nblk, int64_t* ngroups, size
     return PKV_ERR_SHAPE;
   if (a->head_dim != 64 && a->head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (a->block_size > 128 || a->qhead > 64) return PKV_ERR_UNSUPPORTED;
+  if (a->dtype != 0 && a->dtype != PKV_F32 && a->dtype != PKV_F16) return PKV_ERR_DTYPE;
+  if (a->dtype == PKV_F16 &&
+      (a->block_size > 64 || a->page_size % 8 != 0 || a->page_size * a->pages_per_block > 64 ||
+       a->num_pages * a->hkv * a->page_size > INT32_MAX))
+    return PKV_ERR_UNSUPPORTED;
   if (a->num_edges > INT32_MAX / 64) return PKV_ERR_UNSUPPORTED;
   const int64_t nb = (a->max_pages + a->pages_per_block - 1) / a->pages_per_block;
   const int64_t ng = a->num_seqs * nb * a->hkv;
@@ -612,7 +617,7 @@ int check_sparse(const pkv_sparse_args* a, int64_t* nblk, int64_t* ngroups, size
   *nblk = nb;
   *ngroups = ng;
   *bytes = 2 * align_up(4 * (size_t)(ng + 1)) + align_up(4 * (size_t)ng) +
-           align_up(4 * (size_t)a->num_edges);
+           align_up(4 * (size_t)a->num_edges) + align_up(16 * (size_t)a->num_edges);
   return PKV_OK;
 }
 }  // namespace
@@ -641,9 +646,16 @@ int pkv_sparse_attention_partials(const pkv_sparse_args* a, void* workspace,
     return PKV_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   SparseParams p{};
-  p.q = a->q;
-  p.kp = a->k_pages;
-  p.vp = a->v_pages;
+  p.f16 = a->dtype == PKV_F16 ? 1 : 0;
+  if (p.f16) {
+    p.q16 = static_cast<const __half*>(a->q);
+    p.kp16 = static_cast<const __half*>(a->k_pages);
+    p.vp16 = static_cast<const __half*>(a->v_pages);
+  } else {
+    p.q = static_cast<const float*>(a->q);
+    p.kp = static_cast<const float*>(a->k_pages);
+    p.vp = static_cast<const float*>(a->v_pages);
+  }
   p.meta = a->edge_meta;
   p.bt = a->block_tables;
   p.o = a->o_partial;
@@ -673,6 +685,8 @@ int pkv_sparse_attention_partials(const pkv_sparse_args* a, void* workspace,
   p.group_cursor = reinterpret_cast<int32_t*>(ws + off);
   off += align_up(4 * (size_t)ng);
   p.perm = reinterpret_cast<int32_t*>(ws + off);
+  off += align_up(4 * (size_t)a->num_edges);
+  p.edge_rec = reinterpret_cast<int4*>(ws + off);
   return launch_status(launch_sparse(p, static_cast<cudaStream_t>(stream)));
 }
 

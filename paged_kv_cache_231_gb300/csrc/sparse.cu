@@ -96,7 +96,10 @@ __global__ void sparse_fill_kernel(SparseParams p) {
   const int64_t key = edge_group(p, e, false);
   if (key < 0) return;
   const int at = atomicAdd(&p.group_cursor[key], 1);
-  p.perm[p.group_off[key] + at] = (int32_t)e;
+  const int pos = p.group_off[key] + at;
+  p.perm[pos] = (int32_t)e;
+  const int32_t* m = p.meta + e * 5;
+  p.edge_rec[pos] = make_int4((int)e, m[0], min(m[4], p.block_size), 0);
 }
 
 // One CTA per (batch, block, kv head) group. Thread (tr, tk) owns rows tr + 16 i and
@@ -829,6 +832,7 @@ cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.ngroups == 0) return cudaSuccess;
+  if (p.f16) return launch_sparse_tc16(p, s);   // fp16 on the tensor core
   if (tcs::eligible(p)) {   // 3xTF32 on the tensor core
     if (p.D == 64) return tcs::launch_tc<64>(p, s);
     if (p.D == 128) return tcs::launch_tc<128>(p, s);

@@ -363,7 +363,8 @@ def block_sparse(seed: int = 5, *, n_seqs: int = 8, kv_len: int = 16384,
                  queries_per_seq: int = 512, hq: int = 32, hkv: int = 8,
                  head_dim: int = 128, page_size: int = 16, pages_per_block: int = 4,
                  blocks_per_query: int = 16, clip_max: int = 63,
-                 unmapped_frac: float = 0.02, n_empty_edges: int = 0) -> SparseCase:
+                 unmapped_frac: float = 0.02, n_empty_edges: int = 0,
+                 dtype=np.float32) -> SparseCase:
     """Block-sparse workload. Each sequence holds kv_len tokens in pages of
     page_size; its used length is U{kv_len - clip_max .. kv_len} so the last block
     is clipped. Query i of sequence b sits at position used_b - queries_per_seq + i
@@ -372,7 +373,7 @@ def block_sparse(seed: int = 5, *, n_seqs: int = 8, kv_len: int = 16384,
     last used block, sorted by (query, head, block). block_len is the used length
     clipped to the block. A fraction of block-table entries is set to -1, and
     n_empty_edges edges get block_len 0 (or a negative value) to exercise the
-    empty-edge rule."""
+    empty-edge rule. dtype float16 draws q and the pages as fp16 instead of fp32."""
     rng = rng_for(seed)
     qhead = hq // hkv
     BSZ = page_size * pages_per_block
@@ -385,9 +386,10 @@ def block_sparse(seed: int = 5, *, n_seqs: int = 8, kv_len: int = 16384,
     block_tables[unmapped] = -1
     used = kv_len - rng.integers(0, clip_max + 1, size=n_seqs)
     Tq = n_seqs * queries_per_seq
-    q = normal_f32(rng, (Tq, hq, head_dim))
-    k_pages = normal_f32(rng, (num_pages, hkv, page_size, head_dim))
-    v_pages = normal_f32(rng, (num_pages, hkv, page_size, head_dim))
+    draw = normal_f16 if np.dtype(dtype) == np.float16 else normal_f32
+    q = draw(rng, (Tq, hq, head_dim))
+    k_pages = draw(rng, (num_pages, hkv, page_size, head_dim))
+    v_pages = draw(rng, (num_pages, hkv, page_size, head_dim))
     last_blk = (used - 1) // BSZ
     edges = []
     for b in range(n_seqs):

@@ -38,10 +38,11 @@ def assert_f16_close(got, ref, what=""):
     return float(err.max()) if err.size else 0.0
 
 
-def assert_f32_close(got, ref, what="", scalars=False):
+def assert_f32_close(got, ref, what="", scalars=False, rtol=None):
     """Rows are the last axis (a 1-D array is one row) unless ``scalars`` is set, in
-    which case every element is its own row: then the floor is 1e-4 * max(|ref|, 1),
-    the scale of a softmax statistic such as m."""
+    which case every element is its own row: then the floor is rtol * max(|ref|, 1),
+    the scale of a softmax statistic such as m. rtol defaults to 1e-4 (fp32 inputs)."""
+    rtol = F32_RTOL if rtol is None else rtol
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     if scalars:
@@ -49,7 +50,7 @@ def assert_f32_close(got, ref, what="", scalars=False):
     else:
         row_scale = np.max(np.abs(ref), axis=-1, keepdims=True)
     err = np.abs(got - ref)
-    tol = F32_RTOL * (np.abs(ref) + row_scale) + 1e-30
+    tol = rtol * (np.abs(ref) + row_scale) + 1e-30
     bad = ~(err <= tol)
     if bad.any():
         idx = np.argwhere(bad)[:5]

@@ -34,14 +34,20 @@ def oracle_partials(c, edges=None):
         pages_per_block=c.pages_per_block, softmax_scale=c.softmax_scale, edges=edges)
 
 
-def compare_partials(go, gm, gl, ro, rm, rl, rows):
+# fp16 inputs: scores are exact fp16 products summed in fp32 (m to fp32 level), but the
+# weights are rounded once to fp16 (relative 2^-12) before O = P V and in l
+F16_PARTIAL_RTOL = 5e-3
+
+
+def compare_partials(go, gm, gl, ro, rm, rl, rows, f16=False):
     np.testing.assert_array_equal(gl[rows] == 0, rl[rows] == 0)
     empty = rl[rows] == 0
     assert (gm[rows][empty] == -1e30).all() and (go[rows][empty] == 0).all()
     live = rows[~empty]
-    assert_f32_close(go[live], ro[live], "o partial")
+    rt = F16_PARTIAL_RTOL if f16 else None
+    assert_f32_close(go[live], ro[live], "o partial", rtol=rt)
     assert_f32_close(gm[live], rm[live], "m partial", scalars=True)
-    assert_f32_close(gl[live], rl[live], "l partial", scalars=True)
+    assert_f32_close(gl[live], rl[live], "l partial", scalars=True, rtol=rt)
 
 
 # blocks of 64 and 32 keys run on the tensor core (3xTF32), 128-key blocks on fp32 FMA;
@@ -110,6 +116,70 @@ def test_block_sparse_full_size_sampled():
             pr = [e * c.qhead + qh for e in range(e0, e1)]
             ref, rlse = orc.combine_rows(ro[pr], rm[pr], rl[pr])
             assert_f32_close(gout[s * c.qhead + qh], ref, "combined row")
+
+
+# fp16 q and pages: tensor-core kind::f16 kernel (blocks of 64 / 32 keys, qhead 3 and 1)
+@pytest.mark.parametrize("head_dim,pages_per_block,qhead", [(128, 4, 4), (64, 2, 2),
+                                                            (128, 2, 3), (64, 4, 1)])
+def test_f16_small_full_parity(head_dim, pages_per_block, qhead):
+    c = wl.block_sparse(54, n_seqs=3, kv_len=1024, queries_per_seq=24, hq=4 * qhead,
+                        hkv=4, head_dim=head_dim, pages_per_block=pages_per_block,
+                        blocks_per_query=5, n_empty_edges=6, unmapped_frac=0.05,
+                        dtype=np.float16)
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    ro, rm, rl, rst = oracle_partials(c)
+    assert gst == rst
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]), f16=True)
+    rout, rlse = orc.combine_partials(ro, rm, rl, c.seg_offsets, c.qhead)
+    assert_f32_close(gout, rout, "combined output", rtol=F16_PARTIAL_RTOL)
+    fin = np.isfinite(rlse)
+    np.testing.assert_array_equal(np.isfinite(glse), fin)
+    assert_f32_close(glse[fin], rlse[fin], "lse", scalars=True, rtol=F16_PARTIAL_RTOL)
+
+
+def test_f16_groups_spanning_several_row_tiles_and_flags():
+    c = wl.block_sparse(55, n_seqs=2, kv_len=512, queries_per_seq=96, hq=16, hkv=4,
+                        head_dim=128, pages_per_block=4, blocks_per_query=6,
+                        unmapped_frac=0.05, dtype=np.float16)
+    c.edge_meta[0, 4] = 1000          # block_len past the block: clipped, flagged
+    c.block_tables[1, 5] = c.num_pages + 2   # page id past the pool: flagged
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    ro, rm, rl, rst = oracle_partials(c)
+    assert gst == rst == orc.ST_BAD_EDGE
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]), f16=True)
+
+
+def test_f16_block_sparse_full_size_sampled():
+    """The block-sparse workload with fp16 q and pages, full size, in the benchmark's
+    launch configuration; 1500 sampled edges and 40 whole segments against the oracle."""
+    c = wl.block_sparse(5, n_empty_edges=16, dtype=np.float16)
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    rng = np.random.default_rng(8)
+    segs = rng.choice(c.seg_offsets.shape[0] - 1, size=40, replace=False)
+    edges = set(rng.choice(c.num_edges, size=1500, replace=False).tolist())
+    for s in segs:
+        edges |= set(range(int(c.seg_offsets[s]), int(c.seg_offsets[s + 1])))
+    edges |= set(np.nonzero(c.edge_meta[:, 4] <= 0)[0].tolist())
+    edges = sorted(edges)
+    ro, rm, rl, rst = oracle_partials(c, edges)
+    rows = (np.asarray(edges)[:, None] * c.qhead + np.arange(c.qhead)[None, :]).reshape(-1)
+    compare_partials(go, gm, gl, ro, rm, rl, rows, f16=True)
+    for s in segs:
+        e0, e1 = int(c.seg_offsets[s]), int(c.seg_offsets[s + 1])
+        for qh in range(c.qhead):
+            pr = [e * c.qhead + qh for e in range(e0, e1)]
+            ref, _ = orc.combine_rows(ro[pr], rm[pr], rl[pr])
+            assert_f32_close(gout[s * c.qhead + qh], ref, "combined row",
+                             rtol=F16_PARTIAL_RTOL)
+
+
+def test_f16_rejects_blocks_past_64_keys():
+    c = wl.block_sparse(56, n_seqs=1, kv_len=512, queries_per_seq=4, hq=4, hkv=1,
+                        head_dim=128, pages_per_block=8, blocks_per_query=2,
+                        dtype=np.float16)
+    with pytest.raises(B.PagedKVError) as ei:
+        run_gpu(c)
+    assert ei.value.name == "PKV_ERR_UNSUPPORTED"
 
 
 def _random_partials(rng, n, D, empty_frac=0.2):
