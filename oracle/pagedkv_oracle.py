@@ -534,7 +534,7 @@ def attention_partial(q, K, V, visible, scale: float):
 # ======================================================================================
 def sparse_partial(q_buf, k_pages, v_pages, meta, block_tables, qh: int, *, qhead: int,
                    hq: int, head_dim: int, block_size: int, page_size: int,
-                   pages_per_block: int, softmax_scale: float):
+                   pages_per_block: int, softmax_scale: float, query_positions=None):
     """(o, m, l, status) of one partial = (edge, query-head lane qh) (``sparse_forward``).
 
     edge meta = [q_idx, h, blk, batch, block_len]; block_len <= 0 gives the empty
@@ -549,6 +549,13 @@ def sparse_partial(q_buf, k_pages, v_pages, meta, block_tables, qh: int, *, qhea
     the pool counts as unmapped; each sets a status bit. An edge with block_len > 0
     whose q_idx, head, batch or block lies outside the tensors gets the empty
     partial and a status bit.
+
+    Right-aligned causal (the page leaves it unimplemented): with ``query_positions``
+    (the absolute position of each query in its sequence; right-aligned queries of a
+    sequence sit at used_len - n_queries + i), key t of the block (absolute position
+    blk * block_size + t) takes part only when that position is at most the query's.
+    Keys that take no part are not looked up (and flag nothing); a partial with no
+    key taking part is the empty partial.
     """
     q_idx, h, blk, batch, block_len = (int(x) for x in meta)
     status = 0
@@ -562,13 +569,21 @@ def sparse_partial(q_buf, k_pages, v_pages, meta, block_tables, qh: int, *, qhea
             and 0 <= batch < block_tables.shape[0] and blk >= 0
             and blk * pages_per_block < block_tables.shape[1]):
         return np.zeros(D), NEG_LARGE, 0.0, status | ST_BAD_EDGE
+    keys = range(block_len)
+    if query_positions is not None:
+        pos = int(query_positions[q_idx])
+        keys = [t for t in keys if blk * block_size + t <= pos]
+        if not keys:
+            return np.zeros(D), NEG_LARGE, 0.0, status
     q = _f64(q_buf[q_idx, h * qhead + qh])
     num_pages = k_pages.shape[0]
     max_pages = block_tables.shape[1]
     scores = np.full(block_len, NEG_LARGE)
     rows_k = np.zeros((block_len, D))
     rows_v = np.zeros((block_len, D))
-    for t in range(block_len):
+    taking_part = np.zeros(block_len, dtype=bool)
+    for t in keys:
+        taking_part[t] = True
         page_slot = blk * pages_per_block + t // page_size
         page_id = int(block_tables[batch, page_slot]) if page_slot < max_pages else -1
         if page_slot >= max_pages or page_id >= num_pages:
@@ -578,6 +593,8 @@ def sparse_partial(q_buf, k_pages, v_pages, meta, block_tables, qh: int, *, qhea
             rows_k[t] = k_pages[page_id, h, t % page_size]
             rows_v[t] = v_pages[page_id, h, t % page_size]
             scores[t] = float(rows_k[t] @ q) * softmax_scale
+    scores = scores[taking_part]
+    rows_v = rows_v[taking_part]
     m = max(NEG_LARGE, float(scores.max()))
     p = np.where(scores > HALF_NEG_LARGE, np.exp(scores - m), 0.0)
     l = float(p.sum())
@@ -588,10 +605,11 @@ def sparse_partial(q_buf, k_pages, v_pages, meta, block_tables, qh: int, *, qhea
 def sparse_attention_partials(case_q, k_pages, v_pages, edge_meta, block_tables, *,
                               qhead: int, hq: int, head_dim: int, block_size: int,
                               page_size: int, pages_per_block: int, softmax_scale: float,
-                              edges: Optional[Sequence[int]] = None):
+                              edges: Optional[Sequence[int]] = None, query_positions=None):
     """All partials (or those of the listed edges): partial index = edge * qhead + qh;
     o [P, D], m [P], l [P] fp64 plus the OR of status bits. Partials of unlisted
-    edges are left as NaN."""
+    edges are left as NaN. ``query_positions``: right-aligned causal mask (see
+    sparse_partial)."""
     E = edge_meta.shape[0]
     P = E * qhead
     o = np.full((P, head_dim), np.nan)
@@ -603,7 +621,8 @@ def sparse_attention_partials(case_q, k_pages, v_pages, edge_meta, block_tables,
             oo, mm, ll, st = sparse_partial(
                 case_q, k_pages, v_pages, edge_meta[e], block_tables, qh, qhead=qhead,
                 hq=hq, head_dim=head_dim, block_size=block_size, page_size=page_size,
-                pages_per_block=pages_per_block, softmax_scale=softmax_scale)
+                pages_per_block=pages_per_block, softmax_scale=softmax_scale,
+                query_positions=query_positions)
             i = e * qhead + qh
             o[i], m[i], l[i] = oo, mm, ll
             status |= st

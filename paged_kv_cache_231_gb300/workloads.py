@@ -346,6 +346,13 @@ class SparseCase:
     used_kv_lens: np.ndarray  # [B] int64 (how block_len was derived)
     seg_offsets: np.ndarray   # [Tq*hkv + 1] int32: edges of (q_idx, h) are contiguous
 
+    def query_positions(self) -> np.ndarray:
+        """Right-aligned absolute position of each query in its sequence: with n queries
+        per sequence, query i of sequence b sits at used_b - n + i."""
+        B = int(self.used_kv_lens.shape[0])
+        n = int(self.q.shape[0]) // B
+        return (np.repeat(self.used_kv_lens, n) - n + np.tile(np.arange(n), B)).astype(np.int32)
+
     @property
     def num_edges(self) -> int:
         return int(self.edge_meta.shape[0])

@@ -193,3 +193,59 @@ def test_out_of_range_edge_fields_give_flagged_sentinel():
     # an empty edge is never flagged, whatever its other fields hold
     o, m, l, st = sp(q, kp, vp, [9, 9, 9, 9, 0], bt)
     assert st == 0 and l == 0.0
+
+
+# ---- right-aligned causal mask (the sparse page leaves it unimplemented) -------------
+def test_causal_partials_then_combine_equals_dense_causal_attention():
+    # Edges covering every block of the sequence: with the right-aligned causal mask the
+    # combined result is softmax attention of the query at position p over keys 0..p,
+    # computed here directly.
+    c = wl.block_sparse(23, n_seqs=2, kv_len=256, queries_per_seq=70, hq=4, hkv=2,
+                        head_dim=8, blocks_per_query=4, unmapped_frac=0.0, clip_max=40)
+    pos = c.query_positions()
+    assert pos.min() < 256 - 64   # some queries sit before the last block
+    o, m, l, st = orc.sparse_attention_partials(
+        c.q, c.k_pages, c.v_pages, c.edge_meta, c.block_tables, qhead=2, hq=4,
+        head_dim=8, block_size=64, page_size=16, pages_per_block=4,
+        softmax_scale=c.softmax_scale, query_positions=pos)
+    assert st == 0
+    out, lse = orc.combine_partials(o, m, l, c.seg_offsets, 2)
+    for q_idx in range(0, c.q.shape[0], 7):
+        b = q_idx // 70
+        n = int(pos[q_idx]) + 1
+        pages = c.block_tables[b, np.arange(n) // 16]
+        for h in range(2):
+            K = c.k_pages[pages, h, np.arange(n) % 16].astype(np.float64)
+            V = c.v_pages[pages, h, np.arange(n) % 16].astype(np.float64)
+            for qh in range(2):
+                s = c.softmax_scale * (K @ c.q[q_idx, h * 2 + qh].astype(np.float64))
+                w = np.exp(s - s.max())
+                row = (q_idx * 2 + h) * 2 + qh
+                np.testing.assert_allclose(out[row], (w / w.sum()) @ V, rtol=1e-11,
+                                           atol=1e-13)
+                assert lse[row] == pytest.approx(s.max() + np.log(w.sum()), rel=1e-12)
+
+
+def test_causal_mask_keeps_the_keys_up_to_the_query():
+    q, kp, vp, bt = tiny_pages()
+    bt = np.array([[1, 0]])
+    kp[0, 0, 0] = [3, 0]                      # key t = 2 (block 0, page slot 1)
+    meta = [0, 0, 0, 0, 4]
+    full = sp(q, kp, vp, meta, bt)
+    # query at position 1: keys 0 and 1 only = the unmasked partial of block_len 2
+    o, m, l, st = sp(q, kp, vp, meta, bt, query_positions=[1])
+    o2, m2, l2, _ = sp(q, kp, vp, [0, 0, 0, 0, 2], bt)
+    np.testing.assert_allclose(o, o2, rtol=1e-15)
+    assert (m, l) == (m2, l2) and st == 0
+    assert m == 1.0 and m != full[1]          # key 2 (score 3) is masked out
+    # query at position 3 or later sees the whole block
+    np.testing.assert_allclose(sp(q, kp, vp, meta, bt, query_positions=[9])[0], full[0])
+
+
+def test_causal_block_after_the_query_is_the_empty_partial_and_unread():
+    q, kp, vp, bt = tiny_pages()
+    bt = np.array([[1, -1, 99, 99]])          # block 1 names a page past the pool
+    o, m, l, st = sp(q, kp, vp, [0, 0, 1, 0, 4], bt, query_positions=[3])
+    assert (o == 0).all() and m == orc.NEG_LARGE and l == 0 and st == 0
+    # without the mask the bad page is read and flagged
+    assert sp(q, kp, vp, [0, 0, 1, 0, 4], bt)[3] == orc.ST_BAD_EDGE
