@@ -12,8 +12,8 @@ the step's inputs and D2H of its output inside the timed region). ``--impl refer
 times the CPU oracle on a bounded sample of the same workload instead.
 
 Other workloads (``--workload llama8b_decode_rope|varlen_mixed|block_sparse|
-block_sparse_f16|append_prompt``) print the same structure with their own metric; they
-are not the headline line.
+block_sparse_f16|block_sparse_causal|append_prompt``) print the same structure with their
+own metric; they are not the headline line.
 """
 import argparse
 import hashlib
@@ -48,7 +48,8 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b_decode",
                     choices=["llama8b_decode", "llama8b_decode_rope", "varlen_mixed",
-                             "block_sparse", "block_sparse_f16", "append_prompt"])
+                             "block_sparse", "block_sparse_f16", "block_sparse_causal",
+                             "append_prompt"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps")
@@ -316,7 +317,7 @@ def setup_paged(name, args):
     return w
 
 
-def setup_sparse(args, f16=False):
+def setup_sparse(args, f16=False, causal=False):
     from paged_kv_cache_231_gb300 import binding as B
     from paged_kv_cache_231_gb300 import workloads as wl
     import ctypes
@@ -324,6 +325,8 @@ def setup_sparse(args, f16=False):
     c = wl.block_sparse(dtype=np.float16 if f16 else np.float32)
     q, kp, vp = to_dev(c.q), to_dev(c.k_pages), to_dev(c.v_pages)
     em, bt, so = to_dev(c.edge_meta), to_dev(c.block_tables), to_dev(c.seg_offsets)
+    # right-aligned causal: keys after the query's position take no part
+    qpos = c.query_positions() if causal else None
     P = c.num_edges * c.qhead
     o = torch.empty((P, c.head_dim), dtype=torch.float32, device="cuda")
     m = torch.empty(P, dtype=torch.float32, device="cuda")
@@ -332,7 +335,7 @@ def setup_sparse(args, f16=False):
     out = torch.empty((nseg * c.qhead, c.head_dim), dtype=torch.float32, device="cuda")
     a = B.make_sparse_args(q, kp, vp, em, bt, o, m, l, qhead=c.qhead, block_size=c.block_size,
                            page_size=c.page_size, pages_per_block=c.pages_per_block,
-                           softmax_scale=c.softmax_scale)
+                           softmax_scale=c.softmax_scale, query_positions=to_dev(qpos))
     nws = B.pkv_sparse_attention_partials_workspace_size(a)
     ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
     ca = B.CombineArgs()
@@ -348,11 +351,15 @@ def setup_sparse(args, f16=False):
             raise B.PagedKVError("sparse step", st)
 
     bl = np.clip(c.edge_meta[:, 4], 0, c.block_size).astype(np.int64)
+    if causal:   # keys at or before the query's position
+        lim = qpos[c.edge_meta[:, 0]].astype(np.int64) - c.edge_meta[:, 2].astype(np.int64) * c.block_size + 1
+        bl = np.clip(np.minimum(bl, lim), 0, None)
     flops = 4.0 * c.head_dim * c.qhead * float(bl.sum())
     w = Workload()
     w.case, w.step, w.e2e_step, w.h2d, w.d2h = c, step, None, 0, 0
     w.check = lambda: 0
-    w.metric = "block-sparse partials+combine %s TFLOP/s" % ("fp16" if f16 else "fp32")
+    w.metric = "block-sparse partials+combine %s TFLOP/s%s" % (
+        "fp16" if f16 else "fp32", ", right-aligned causal" if causal else "")
     w.unit, w.work, w.dtype, w.tokens = "TFLOP/s", flops / 1e12, "f16" if f16 else "f32", \
         c.q.shape[0]
     # the partials run on the tensor core (3xTF32 for fp32 inputs: about 0.24 ms of tf32
@@ -363,7 +370,10 @@ def setup_sparse(args, f16=False):
     w.traffic_summary, w.traffic_sources = "sparse_partials_block_sparse.md", SPARSE_SOURCES
     if f16:
         w.traffic_summary, w.traffic_sources = "sparse_tc16_block_sparse_f16.md", SPARSE16_SOURCES
-    w.config = {"workload": "block_sparse_f16" if f16 else "block_sparse",
+    if causal:   # the committed counters are for the unmasked workload
+        w.traffic_summary = None
+    w.config = {"workload": "block_sparse_causal" if causal else
+                ("block_sparse_f16" if f16 else "block_sparse"),
                 "queries": int(c.q.shape[0]), "edges": c.num_edges,
                 "partials": P, "hq": c.hq, "hkv": c.hkv, "head_dim": c.head_dim,
                 "block": c.block_size, "flops_per_step": flops,
@@ -424,6 +434,7 @@ def oracle_sample(name, seconds):
                         "varlen_mixed": wl.varlen_mixed,
                         "block_sparse": wl.block_sparse,
                         "block_sparse_f16": lambda: wl.block_sparse(dtype=np.float16),
+                        "block_sparse_causal": wl.block_sparse,
                         "append_prompt": lambda: wl.append_rotary(2, mode="prompt")}[name]()
     if name in ("llama8b_decode", "llama8b_decode_rope", "varlen_mixed"):
         case = _CASES[name]
@@ -450,8 +461,14 @@ def oracle_sample(name, seconds):
                 break
         return done_work / spent, done_tok / spent, \
             f"{seqs} of {case.batch} sequences, whole (scatter + attention), {spent:.1f} s"
-    if name in ("block_sparse", "block_sparse_f16"):
+    if name in ("block_sparse", "block_sparse_f16", "block_sparse_causal"):
         c = _CASES[name]
+        qpos = c.query_positions() if name == "block_sparse_causal" else None
+        keys = np.clip(c.edge_meta[:, 4], 0, c.block_size).astype(np.int64)
+        if qpos is not None:
+            lim = (qpos[c.edge_meta[:, 0]].astype(np.int64)
+                   - c.edge_meta[:, 2].astype(np.int64) * c.block_size + 1)
+            keys = np.clip(np.minimum(keys, lim), 0, None)
         rng = np.random.default_rng(0)
         order = rng.permutation(c.num_edges)
         spent, n, fl = 0.0, 0, 0.0
@@ -461,9 +478,10 @@ def oracle_sample(name, seconds):
             orc.sparse_attention_partials(
                 c.q, c.k_pages, c.v_pages, c.edge_meta, c.block_tables, qhead=c.qhead,
                 hq=c.hq, head_dim=c.head_dim, block_size=c.block_size, page_size=c.page_size,
-                pages_per_block=c.pages_per_block, softmax_scale=c.softmax_scale, edges=edges)
+                pages_per_block=c.pages_per_block, softmax_scale=c.softmax_scale, edges=edges,
+                query_positions=qpos)
             n += len(edges)
-            fl += 4.0 * c.head_dim * c.qhead * float(np.clip(c.edge_meta[edges, 4], 0, 64).sum())
+            fl += 4.0 * c.head_dim * c.qhead * float(keys[edges].sum())
             spent = time.perf_counter() - t0
             if spent >= seconds:
                 break
@@ -516,12 +534,15 @@ def run_reference(args, world, rank):
         return
     unit = {"llama8b_decode": "GB/s", "llama8b_decode_rope": "GB/s", "varlen_mixed": "TFLOP/s",
             "block_sparse": "TFLOP/s", "block_sparse_f16": "TFLOP/s",
+            "block_sparse_causal": "TFLOP/s",
             "append_prompt": "GB/s"}[args.workload]
     metric = {"llama8b_decode": METRIC,
               "llama8b_decode_rope": METRIC + ", RoPE on new keys and queries",
               "varlen_mixed": "varlen prefill+decode attention TFLOP/s (causal pairs)",
               "block_sparse": "block-sparse partials+combine fp32 TFLOP/s",
               "block_sparse_f16": "block-sparse partials+combine fp16 TFLOP/s",
+              "block_sparse_causal":
+                  "block-sparse partials+combine fp32 TFLOP/s, right-aligned causal",
               "append_prompt": "KV append+RoPE GB/s (prompt)"}[args.workload]
     # each step is a bounded sample (at least one whole sequence / edge batch); the
     # whole run is kept to about two minutes of CPU work
@@ -568,6 +589,7 @@ def main():
              "varlen_mixed": lambda: setup_paged("varlen_mixed", args),
              "block_sparse": lambda: setup_sparse(args),
              "block_sparse_f16": lambda: setup_sparse(args, f16=True),
+             "block_sparse_causal": lambda: setup_sparse(args, causal=True),
              "append_prompt": lambda: setup_append(args)}[args.workload]
     w = setup()
     hbm, bf16, bf16_sus, peak_kind = measured_peaks()

@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 2
+#define PKV_ABI_VERSION 3
 
 typedef enum pkv_status {
   PKV_OK = 0,
@@ -326,6 +326,11 @@ typedef struct pkv_sparse_args {
   /* element type of q, k_pages, v_pages: PKV_F32 (0 is taken as PKV_F32) or PKV_F16.
      The partials are fp32 either way. */
   int32_t dtype;
+  /* optional [num_queries] int32: absolute position of each query in its sequence
+     (right-aligned causal; the page leaves it unimplemented). Key t of block blk takes
+     part only when blk*block_size + t <= position; right-aligned queries of a sequence
+     with n queries and used length u sit at u - n + i. NULL: no causal mask. */
+  const int32_t* query_positions;
 } pkv_sparse_args;
 
 /* Host only: workspace bytes for the edge grouping of pkv_sparse_attention_partials. */
@@ -345,7 +350,9 @@ int pkv_sparse_attention_partials_workspace_size(const pkv_sparse_args* args,
  * are fp16 products summed in fp32, the weights are rounded once to fp16 for the
  * weighted sum of value rows and l sums those rounded weights; everything else as above.
  * Supported for fp16: head_dim in {64, 128}, block_size <= 64, page_size a multiple of
- * 8 with pages_per_block * page_size <= 64; else PKV_ERR_UNSUPPORTED. */
+ * 8 with pages_per_block * page_size <= 64; else PKV_ERR_UNSUPPORTED.
+ * With query_positions the keys after the query's position take no part (they are not
+ * read and flag nothing); an edge left with no key gets the empty partial. */
 int pkv_sparse_attention_partials(const pkv_sparse_args* args, void* workspace,
                                   size_t workspace_bytes, void* stream);
 

@@ -92,7 +92,8 @@ class SparseArgs(ctypes.Structure):
                 ("num_edges", c_i64), ("num_seqs", c_i64), ("max_pages", c_i64),
                 ("num_pages", c_i64), ("qhead", c_i64), ("hq", c_i64), ("hkv", c_i64),
                 ("head_dim", c_i64), ("block_size", c_i64), ("page_size", c_i64),
-                ("pages_per_block", c_i64), ("softmax_scale", c_f32), ("dtype", c_i32)]
+                ("pages_per_block", c_i64), ("softmax_scale", c_f32), ("dtype", c_i32),
+                ("query_positions", c_vp)]
 
 
 class CombineArgs(ctypes.Structure):
@@ -149,7 +150,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = c_i32
         fn.argtypes = args
-    if lib.pkv_abi_version() != 2:
+    if lib.pkv_abi_version() != 3:
         raise RuntimeError("libpagedkv ABI version mismatch")
     for name, cls in STRUCTS.items():
         n = lib.pkv_sizeof_struct(name.encode())
@@ -427,7 +428,8 @@ def pkv_kv_append_rotary(source, value, total_sequence_length, key_total_sequenc
 # ----------------------------------------------------------------------------- sparse
 def make_sparse_args(q, k_pages, v_pages, edge_meta, block_tables, o, m, l, *, qhead: int,
                      block_size: int, page_size: int, pages_per_block: int,
-                     softmax_scale: float, device_status=None) -> SparseArgs:
+                     softmax_scale: float, device_status=None,
+                     query_positions=None) -> SparseArgs:
     a = SparseArgs()
     a.q, a.k_pages, a.v_pages = _ptr(q), _ptr(k_pages), _ptr(v_pages)
     a.edge_meta, a.block_tables = _ptr(edge_meta), _ptr(block_tables)
@@ -442,6 +444,7 @@ def make_sparse_args(q, k_pages, v_pages, edge_meta, block_tables, o, m, l, *, q
     a.pages_per_block = int(pages_per_block)
     a.softmax_scale = float(softmax_scale)
     a.dtype = _dtype_code(q)
+    a.query_positions = _ptr(query_positions)
     return a
 
 
@@ -457,15 +460,17 @@ def pkv_sparse_attention_partials(q, k_pages, v_pages, edge_meta, block_tables, 
                                   qhead: int, block_size: int, page_size: int,
                                   pages_per_block: int, softmax_scale: float,
                                   o=None, m=None, l=None, workspace=None,
-                                  device_status=None, stream=None):
+                                  device_status=None, query_positions=None, stream=None):
     """Block-sparse (o, m, l) partials, partial index edge*qhead + lane. q and the pages
-    are all fp32 or all fp16; the partials are fp32."""
+    are all fp32 or all fp16; the partials are fp32. ``query_positions`` (int32 per
+    query) applies the right-aligned causal mask."""
     torch = _torch()
     dt = torch.float16 if q.dtype == torch.float16 else torch.float32
     for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
         _require(t, dt, n)
     _require(edge_meta, torch.int32, "edge_meta")
     _require(block_tables, torch.int32, "block_tables")
+    _require(query_positions, torch.int32, "query_positions")
     P = int(edge_meta.shape[0]) * qhead
     D = int(q.shape[2])
     if o is None:
@@ -477,7 +482,7 @@ def pkv_sparse_attention_partials(q, k_pages, v_pages, edge_meta, block_tables, 
     a = make_sparse_args(q, k_pages, v_pages, edge_meta, block_tables, o, m, l, qhead=qhead,
                          block_size=block_size, page_size=page_size,
                          pages_per_block=pages_per_block, softmax_scale=softmax_scale,
-                         device_status=device_status)
+                         device_status=device_status, query_positions=query_positions)
     need = pkv_sparse_attention_partials_workspace_size(a)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)

@@ -175,6 +175,7 @@ struct SparseParams {
   int64_t Tq, E, nseq, max_pages, num_pages;
   int qhead, hq, hkv, D, block_size, page_size, ppb;
   float scale;
+  const int32_t* qpos;     // [Tq] query positions (right-aligned causal) or NULL
   // fp16 inputs (f16 = 1): the same tensors as q / kp / vp, as halves
   int f16;
   const __half* q16;
@@ -216,6 +217,17 @@ int attention_warps_per_cta();
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s);
 bool sparse_f16_eligible(const SparseParams& p);                        // sparse16.cu
+
+// Keys of an edge that take part: block_len clipped to the block and, with query
+// positions, to the keys at or before the query's position (right-aligned causal).
+__device__ __forceinline__ int edge_keys(const SparseParams& p, int q_idx, int blk, int bl) {
+  int n = bl < p.block_size ? bl : p.block_size;
+  if (p.qpos) {
+    const int64_t lim = (int64_t)p.qpos[q_idx] - (int64_t)blk * p.block_size + 1;
+    if (lim < n) n = (int)(lim < 0 ? 0 : lim);
+  }
+  return n;
+}
 cudaError_t launch_sparse_tc16(const SparseParams& p, cudaStream_t s);  // sparse16.cu
 
 // profiler hooks (runtime.cpp)

@@ -675,6 +675,7 @@ int pkv_sparse_attention_partials(const pkv_sparse_args* a, void* workspace,
   p.page_size = (int)a->page_size;
   p.ppb = (int)a->pages_per_block;
   p.scale = a->softmax_scale;
+  p.qpos = a->query_positions;
   p.nblk = nb;
   p.ngroups = ng;
   size_t off = 0;

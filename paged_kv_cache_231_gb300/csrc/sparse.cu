@@ -52,6 +52,10 @@ __device__ __forceinline__ int64_t edge_group(const SparseParams& p, int64_t e, 
     return -1;
   }
   if (write && bl > p.block_size) flag_status(p.status, PKV_DEV_BAD_EDGE);
+  if (edge_keys(p, q_idx, blk, bl) <= 0) {   // every key after the query (causal)
+    if (write) write_sentinel(p, e);
+    return -1;
+  }
   return ((int64_t)batch * p.nblk + blk) * p.hkv + h;
 }
 
@@ -99,7 +103,7 @@ __global__ void sparse_fill_kernel(SparseParams p) {
   const int pos = p.group_off[key] + at;
   p.perm[pos] = (int32_t)e;
   const int32_t* m = p.meta + e * 5;
-  p.edge_rec[pos] = make_int4((int)e, m[0], min(m[4], p.block_size), 0);
+  p.edge_rec[pos] = make_int4((int)e, m[0], edge_keys(p, m[0], m[2], m[4]), 0);
 }
 
 // One CTA per (batch, block, kv head) group. Thread (tr, tk) owns rows tr + 16 i and
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kSpThreads, 2) sparse_partials_kernel(SparsePa
         v = *reinterpret_cast<const float4*>(
             p.q + ((int64_t)q_idx * p.hq + h * p.qhead + qh) * D + c * 4);
         if (c == 0) {
-          sBL[r] = min(p.meta[e * 5 + 4], p.block_size);
+          sBL[r] = edge_keys(p, q_idx, p.meta[e * 5 + 2], p.meta[e * 5 + 4]);
           sPI[r] = (int)(e * p.qhead + qh);
         }
       } else if (c == 0) {
@@ -491,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (my_er < epc && c0 + my_er < e1) {
       e = p.perm[c0 + my_er];
       qi = p.meta[(int64_t)e * 5];
-      bl = min(p.meta[(int64_t)e * 5 + 4], p.block_size);
+      bl = edge_keys(p, qi, p.meta[(int64_t)e * 5 + 2], p.meta[(int64_t)e * 5 + 4]);
     }
   };
   int nx_e, nx_q, nx_bl;

@@ -12,13 +12,13 @@ from .gpu_util import DEV, assert_f16_close, assert_f32_close, dev, host
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu(c):
+def run_gpu(c, qpos=None):
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     o, m, l = B.pkv_sparse_attention_partials(
         dev(c.q), dev(c.k_pages), dev(c.v_pages), dev(c.edge_meta), dev(c.block_tables),
         qhead=c.qhead, block_size=c.block_size, page_size=c.page_size,
         pages_per_block=c.pages_per_block, softmax_scale=c.softmax_scale,
-        device_status=status)
+        device_status=status, query_positions=dev(qpos))
     nseg = c.seg_offsets.shape[0] - 1
     lse = torch.empty(nseg * c.qhead, dtype=torch.float32, device=DEV)
     out, _ = B.pkv_combine_partials(o, m, l, dev(c.seg_offsets), num_segments=nseg,
@@ -27,11 +27,12 @@ def run_gpu(c):
     return host(o), host(m), host(l), host(out), host(lse), int(status.item())
 
 
-def oracle_partials(c, edges=None):
+def oracle_partials(c, edges=None, qpos=None):
     return orc.sparse_attention_partials(
         c.q, c.k_pages, c.v_pages, c.edge_meta, c.block_tables, qhead=c.qhead, hq=c.hq,
         head_dim=c.head_dim, block_size=c.block_size, page_size=c.page_size,
-        pages_per_block=c.pages_per_block, softmax_scale=c.softmax_scale, edges=edges)
+        pages_per_block=c.pages_per_block, softmax_scale=c.softmax_scale, edges=edges,
+        query_positions=qpos)
 
 
 # fp16 inputs: scores are exact fp16 products summed in fp32 (m to fp32 level), but the
@@ -180,6 +181,43 @@ def test_f16_rejects_blocks_past_64_keys():
     with pytest.raises(B.PagedKVError) as ei:
         run_gpu(c)
     assert ei.value.name == "PKV_ERR_UNSUPPORTED"
+
+
+# right-aligned causal mask: 3xTF32 tensor-core (64-key blocks), fp32 FMA (128-key
+# blocks) and fp16 tensor-core paths
+@pytest.mark.parametrize("head_dim,pages_per_block,qhead,dtype",
+                         [(128, 4, 4, np.float32), (64, 8, 2, np.float32),
+                          (128, 4, 3, np.float16), (64, 2, 2, np.float16)])
+def test_causal_small_full_parity(head_dim, pages_per_block, qhead, dtype):
+    c = wl.block_sparse(57, n_seqs=3, kv_len=1024, queries_per_seq=40, hq=4 * qhead,
+                        hkv=4, head_dim=head_dim, pages_per_block=pages_per_block,
+                        blocks_per_query=6, n_empty_edges=6, unmapped_frac=0.05, dtype=dtype)
+    qpos = c.query_positions()
+    bs = c.block_size
+    starts = c.edge_meta[:, 2].astype(np.int64) * bs
+    q_at = qpos[c.edge_meta[:, 0]]
+    # blocks cut by the query position (and, for 32/64-key blocks, blocks wholly after it)
+    assert ((starts <= q_at) & (q_at < starts + bs - 1)).any()
+    assert bs > 64 or (starts > q_at).any()
+    go, gm, gl, gout, glse, gst = run_gpu(c, qpos)
+    ro, rm, rl, rst = oracle_partials(c, qpos=qpos)
+    assert gst == rst
+    f16 = dtype == np.float16
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]), f16=f16)
+    rout, rlse = orc.combine_partials(ro, rm, rl, c.seg_offsets, c.qhead)
+    assert_f32_close(gout, rout, "combined output", rtol=F16_PARTIAL_RTOL if f16 else None)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+def test_causal_block_sparse_full_size_sampled(dtype):
+    c = wl.block_sparse(5, dtype=dtype)
+    qpos = c.query_positions()
+    go, gm, gl, gout, glse, gst = run_gpu(c, qpos)
+    rng = np.random.default_rng(9)
+    edges = sorted(rng.choice(c.num_edges, size=1500, replace=False).tolist())
+    ro, rm, rl, rst = oracle_partials(c, edges, qpos)
+    rows = (np.asarray(edges)[:, None] * c.qhead + np.arange(c.qhead)[None, :]).reshape(-1)
+    compare_partials(go, gm, gl, ro, rm, rl, rows, f16=dtype == np.float16)
 
 
 def _random_partials(rng, n, D, empty_frac=0.2):
