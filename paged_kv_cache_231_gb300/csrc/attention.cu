@@ -1624,6 +1624,9 @@ __device__ void plan_block(const AttnParams& p) {
   }
 }
 
+// kQ: the scatter blocks also rotate the query heads into the workspace (the kernel
+// without kQ carries none of that code)
+template <bool kQ>
 __global__ void __launch_bounds__(kPrologueThreads) prologue_kernel(AttnParams p,
                                                                     ScatterParams sp) {
   if (blockIdx.x == 0) {
@@ -1632,9 +1635,9 @@ __global__ void __launch_bounds__(kPrologueThreads) prologue_kernel(AttnParams p
   }
   const int64_t gid = (int64_t)(blockIdx.x - 1) * kPrologueThreads + threadIdx.x;
   if (sp.row_path)
-    paged_scatter_row(sp, gid >> 4, threadIdx.x & 31);
+    paged_scatter_row<kQ>(sp, gid >> 4, threadIdx.x & 31);
   else
-    paged_scatter_thread(sp, gid);
+    paged_scatter_thread<kQ>(sp, gid);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
@@ -1706,9 +1709,12 @@ cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cud
   const int64_t scatter_threads = pkv::scatter_threads(sp);
   {
     ProfScope ps("prologue", s);
-    prologue_kernel<<<(unsigned)(1 + (scatter_threads + kPrologueThreads - 1) /
-                                         kPrologueThreads),
-                      kPrologueThreads, 0, s>>>(p, sp);
+    const unsigned pgrid =
+        (unsigned)(1 + (scatter_threads + kPrologueThreads - 1) / kPrologueThreads);
+    if (sp.q_dst)
+      prologue_kernel<true><<<pgrid, kPrologueThreads, 0, s>>>(p, sp);
+    else
+      prologue_kernel<false><<<pgrid, kPrologueThreads, 0, s>>>(p, sp);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

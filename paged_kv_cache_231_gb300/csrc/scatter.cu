@@ -27,15 +27,17 @@ namespace {
 constexpr int kScatterThreads = 256;
 
 __global__ void __launch_bounds__(kScatterThreads) paged_scatter_kernel(ScatterParams p) {
-  paged_scatter_thread(p, (int64_t)blockIdx.x * kScatterThreads + threadIdx.x);
+  paged_scatter_thread<false>(p, (int64_t)blockIdx.x * kScatterThreads + threadIdx.x);
 }
 
 __global__ void __launch_bounds__(kScatterThreads) paged_scatter_rows_kernel(ScatterParams p) {
   const int64_t row = ((int64_t)blockIdx.x * kScatterThreads + threadIdx.x) >> 4;
-  paged_scatter_row(p, row, threadIdx.x & 31);
+  paged_scatter_row<false>(p, row, threadIdx.x & 31);
 }
 
-// Row path of the append: half-warp `row` of the (batch, kv head, new token) grid.
+// Row path of the append: half-warp `row` of the (batch, kv head, new token) grid; with kQ
+// also the query heads (the kernels without kQ carry none of that code).
+template <bool kQ>
 __global__ void __launch_bounds__(kScatterThreads) append_rows_kernel(AppendParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t row = ((int64_t)blockIdx.x * kScatterThreads + threadIdx.x) >> 4;
@@ -53,7 +55,7 @@ __global__ void __launch_bounds__(kScatterThreads) append_rows_kernel(AppendPara
     past = tb >= S ? tb - S : 0u;
   }
   const int64_t pos = (int64_t)past + t;
-  if (p.q_dst) {   // the G query heads of kv head h (copied unrotated past the table)
+  if constexpr (kQ) {   // the G query heads of kv head h (copied unrotated past the table)
     const int G = p.Hq / p.Hkv;
     const int64_t qr = (int64_t)b * p.S + t;
     rotate_query_rows(p.q_src + qr * p.q_stride + (int64_t)h * G * p.D,
@@ -70,6 +72,7 @@ __global__ void __launch_bounds__(kScatterThreads) append_rows_kernel(AppendPara
                 p.rotary_dim, p.interleaved, lane);
 }
 
+template <bool kQ>
 __global__ void __launch_bounds__(kScatterThreads) append_kernel(AppendParams p) {
   const int CPR = p.D / 8;
   const int64_t gid = (int64_t)blockIdx.x * kScatterThreads + threadIdx.x;
@@ -91,10 +94,11 @@ __global__ void __launch_bounds__(kScatterThreads) append_kernel(AppendParams p)
     past = tb >= S ? tb - S : 0u;
   }
   const int64_t pos = (int64_t)past + t;
-  if (p.q_dst) {   // the G query heads of kv head h, chunk c (copied unrotated past the table)
+  if constexpr (kQ) {   // the G query heads of kv head h, chunk c (unrotated past the table)
     const int G = p.Hq / p.Hkv;
     const int64_t qr = (int64_t)b * p.S + t;
     const bool rot = p.rotary_dim > 0 && c * 8 < p.rotary_dim && pos < p.rotary_positions;
+#pragma unroll 1
     for (int g = 0; g < G; ++g) {
       const int hq = h * G + g;
       const __half* qrow = p.q_src + qr * p.q_stride + (int64_t)hq * p.D;
@@ -144,10 +148,17 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
   if (total == 0) return cudaSuccess;
   ProfScope ps("append", s);
   const unsigned grid = (unsigned)((total + kScatterThreads - 1) / kScatterThreads);
-  if (p.row_path)
-    append_rows_kernel<<<grid, kScatterThreads, 0, s>>>(p);
-  else
-    append_kernel<<<grid, kScatterThreads, 0, s>>>(p);
+  if (p.row_path) {
+    if (p.q_dst)
+      append_rows_kernel<true><<<grid, kScatterThreads, 0, s>>>(p);
+    else
+      append_rows_kernel<false><<<grid, kScatterThreads, 0, s>>>(p);
+  } else {
+    if (p.q_dst)
+      append_kernel<true><<<grid, kScatterThreads, 0, s>>>(p);
+    else
+      append_kernel<false><<<grid, kScatterThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -129,7 +129,7 @@ __device__ __forceinline__ void move_row_pair(const __half* krow, const __half* 
 
 // Half a warp rotates the G query heads of one (token, kv head) at position pos (R = 0:
 // plain copy). Head g's row is at qsrc + g*D and goes to qdst + g*D; four heads' chunks
-// are loaded before any is stored.
+// are loaded before any is stored. Only the query-rotating kernels carry this code.
 __device__ __forceinline__ void rotate_query_rows(const __half* qsrc, __half* qdst, int G,
                                                   int D, int64_t pos, const __half* cos_t,
                                                   const __half* sin_t, int R, int interleaved,
@@ -154,8 +154,27 @@ __device__ __forceinline__ void rotate_query_rows(const __half* qsrc, __half* qd
   }
 }
 
+// Chunk c of the G query heads of kv head h of token i (copied unrotated past the table).
+__device__ __forceinline__ void rotate_query_chunks(const ScatterParams& p, int i, int h, int c,
+                                                 int64_t pos) {
+  const int G = p.Hq / p.Hkv;
+  const bool rot = p.rotary_dim > 0 && c * 8 < p.rotary_dim && pos < p.rotary_positions;
+#pragma unroll 1
+  for (int g = 0; g < G; ++g) {
+    const int hq = h * G + g;
+    const __half* qrow = p.q_src + (int64_t)i * p.q_stride + (int64_t)hq * p.D;
+    __half x[8];
+    *reinterpret_cast<uint4*>(x) = *reinterpret_cast<const uint4*>(qrow + c * 8);
+    if (rot) rotate_chunk(x, qrow, c * 8, pos, p.cos, p.sin, p.rotary_dim, p.interleaved);
+    *reinterpret_cast<uint4*>(p.q_dst + ((int64_t)i * p.Hq + hq) * p.D + c * 8) =
+        *reinterpret_cast<uint4*>(x);
+  }
+}
+
 // One thread of the ScatterKV pass: 16-byte chunk `gid` of the (token, kv head, chunk)
-// grid moves K (rotated when asked) and V into the paged cache.
+// grid moves K (rotated when asked) and V into the paged cache; with kQ, also the chunk of
+// the token's query heads (the kernels without kQ carry none of that code).
+template <bool kQ>
 __device__ __forceinline__ void paged_scatter_thread(const ScatterParams& p, int64_t gid) {
   const int CPR = p.D / 8;
   const int64_t total = (int64_t)p.T * p.Hkv * CPR;
@@ -185,19 +204,7 @@ __device__ __forceinline__ void paged_scatter_thread(const ScatterParams& p, int
   }
   if (i >= s1) return;  // token past the last sequence: not part of the batch
   const int64_t pos = (int64_t)P + (i - s0);
-  if (p.q_dst) {   // the G query heads of kv head h, chunk c (copied unrotated past the table)
-    const int G = p.Hq / p.Hkv;
-    const bool rot = p.rotary_dim > 0 && c * 8 < p.rotary_dim && pos < p.rotary_positions;
-    for (int g = 0; g < G; ++g) {
-      const int hq = h * G + g;
-      const __half* qrow = p.q_src + (int64_t)i * p.q_stride + (int64_t)hq * p.D;
-      __half x[8];
-      *reinterpret_cast<uint4*>(x) = *reinterpret_cast<const uint4*>(qrow + c * 8);
-      if (rot) rotate_chunk(x, qrow, c * 8, pos, p.cos, p.sin, p.rotary_dim, p.interleaved);
-      *reinterpret_cast<uint4*>(p.q_dst + ((int64_t)i * p.Hq + hq) * p.D + c * 8) =
-          *reinterpret_cast<uint4*>(x);
-    }
-  }
+  if constexpr (kQ) rotate_query_chunks(p, i, h, c, pos);
 
   int64_t blk, off;
   if (p.slot_mapping) {
@@ -241,7 +248,9 @@ __device__ __forceinline__ void paged_scatter_thread(const ScatterParams& p, int
   *reinterpret_cast<uint4*>(p.vc + dst) = vv;
 }
 
-// Half a warp of the ScatterKV pass on the row path: (token, kv head) row pair `row`.
+// Half a warp of the ScatterKV pass on the row path: (token, kv head) row pair `row`;
+// with kQ also the token's query heads of that kv head.
+template <bool kQ>
 __device__ __forceinline__ void paged_scatter_row(const ScatterParams& p, int64_t row,
                                                   int lane) {
   if (row >= (int64_t)p.T * p.Hkv) return;
@@ -265,7 +274,7 @@ __device__ __forceinline__ void paged_scatter_row(const ScatterParams& p, int64_
   }
   if (i >= s1) return;
   const int64_t pos = (int64_t)P + (i - s0);
-  if (p.q_dst) {   // the G query heads of kv head h (copied unrotated past the table)
+  if constexpr (kQ) {   // the G query heads of kv head h (copied unrotated past the table)
     const int G = p.Hq / p.Hkv;
     rotate_query_rows(p.q_src + (int64_t)i * p.q_stride + (int64_t)h * G * p.D,
                       p.q_dst + ((int64_t)i * p.Hq + (int64_t)h * G) * p.D, G, p.D, pos,
