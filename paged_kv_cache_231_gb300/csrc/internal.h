@@ -216,7 +216,6 @@ int attention_ctas_per_sm();
 int attention_warps_per_cta();
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s);
-bool sparse_f16_eligible(const SparseParams& p);                        // sparse16.cu
 
 // Keys of an edge that take part: block_len clipped to the block and, with query
 // positions, to the keys at or before the query's position (right-aligned causal).
@@ -228,7 +227,8 @@ __device__ __forceinline__ int edge_keys(const SparseParams& p, int q_idx, int b
   }
   return n;
 }
-cudaError_t launch_sparse_tc16(const SparseParams& p, cudaStream_t s);  // sparse16.cu
+// fp16 partials (sparse16.cu); the runtime has checked the shapes it takes
+cudaError_t launch_sparse_tc16(const SparseParams& p, cudaStream_t s);
 
 // profiler hooks (runtime.cpp)
 void prof_begin(const char* name, cudaStream_t s);

@@ -722,12 +722,6 @@ cudaError_t launch_d(const SparseParams& p, cudaStream_t s) {
 
 }  // namespace
 
-bool sparse_f16_eligible(const SparseParams& p) {
-  return (p.D == 64 || p.D == 128) && p.block_size <= kNK && p.qhead <= 128 &&
-         p.page_size % 8 == 0 && (int64_t)p.ppb * p.page_size <= kNK &&
-         p.num_pages * p.hkv * p.page_size <= INT32_MAX;
-}
-
 cudaError_t launch_sparse_tc16(const SparseParams& p, cudaStream_t s) {
   if (p.D == 64) return launch_d<64>(p, s);
   if (p.D == 128) return launch_d<128>(p, s);
