@@ -261,22 +261,38 @@ def setup_paged(name, args):
         if st != 0:
             raise B.PagedKVError("pkv_paged_attention", st)
 
-    # end-to-end: the public call with pinned host inputs, H2D + call + D2H per step
-    pin = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
-    h_in = [pin(case.query), pin(case.key), pin(case.value), pin(case.cu_seqlens),
-            pin(case.past_seqlens), pin(case.block_table), pin(case.slot_mapping)]
-    d_in = [q, k, v, cu, past, bt, sm]
+    # end-to-end: the public call with pinned host inputs, H2D + call + D2H per step. The
+    # step's inputs (query, new K/V, lengths, block table, slots) sit in one pinned host
+    # buffer, as a serving loop stages a batch, and move in one copy; the call's device
+    # tensors are views into one device buffer. The caches stay resident on the device.
+    parts = [case.query, case.key, case.value, case.cu_seqlens, case.past_seqlens,
+             case.block_table, case.slot_mapping]
+    offs, nbytes = [], 0
+    for a in parts:
+        offs.append(nbytes)
+        nbytes += 0 if a is None else (a.nbytes + 255) // 256 * 256
+    h_buf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+    def view(buf, a, off):
+        if a is None:
+            return None
+        src = torch.from_numpy(np.ascontiguousarray(a))
+        return buf[off:off + src.numel() * src.element_size()].view(src.dtype).view(src.shape)
+
+    for a, off in zip(parts, offs):
+        if a is not None:
+            view(h_buf, a, off).copy_(torch.from_numpy(np.ascontiguousarray(a)))
+    eq, ek, ev, ecu, epast, ebt, esm = (view(d_buf, a, off) for a, off in zip(parts, offs))
     h_out = torch.empty(out.shape, dtype=torch.float16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in h_in if t is not None)
+    h2d = nbytes
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        for h, d in zip(h_in, d_in):
-            if h is not None:
-                d.copy_(h, non_blocking=True)
-        B.pkv_paged_attention(q, k, v, kc, vc, cu, past, bt, sm, num_heads=case.num_heads,
-                              kv_num_heads=case.kv_num_heads, scale=case.scale, output=out,
-                              workspace=ws, **rot)
+        d_buf.copy_(h_buf, non_blocking=True)
+        B.pkv_paged_attention(eq, ek, ev, kc, vc, ecu, epast, ebt, esm,
+                              num_heads=case.num_heads, kv_num_heads=case.kv_num_heads,
+                              scale=case.scale, output=out, workspace=ws, **rot)
         h_out.copy_(out, non_blocking=True)
 
     w = Workload()
