@@ -9,8 +9,7 @@
 // weights exp(s - m), l = their sum, o = the weighted sum of value rows (unnormalised).
 // The page computes in fp32; this variant takes fp16 q and pages (the partials stay
 // fp32, so the combine is unchanged). Scores are fp16 products summed in fp32; the
-// weights are rounded once to fp16 for O = P V, and l sums the rounded weights, so o / l
-// is a convex combination of value rows with exactly the weights the tensor core used.
+// weights are computed in fp32, summed into l, and rounded once to fp16 for O = P V.
 //
 // GB300 form (edges grouped by (batch, block, kv head) by the grouping kernels of the
 // fp32 path): a persistent CTA per SM, warp-specialised, every hand-off on an mbarrier.
@@ -292,23 +291,26 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
       const int bl = ri.y;
       const uint64_t inblk = bl >= 64 ? ~0ull : ((1ull << bl) - 1ull);
       if (imask & inblk) bad = true;
-      float mrow = kNegLarge;
+      // scores in base-2 units (scale * log2(e) * <q, k>): the weights are 2^(s - max)
+      const float sl2 = p.scale * kLog2e;
+      float m2 = kNegLarge;
 #pragma unroll
       for (int k = 0; k < 64; ++k) {
-        const float sv = k < bl ? (((vmask >> k) & 1ull) ? s[k] * p.scale : kNegLarge) : -INFINITY;
+        const float sv = k < bl ? (((vmask >> k) & 1ull) ? s[k] * sl2 : kNegLarge) : -INFINITY;
         s[k] = sv;
-        mrow = fmaxf(mrow, sv);
+        m2 = fmaxf(m2, sv);
       }
-      float pw[32];   // weights as fp16 pairs; l sums the rounded weights
+      float pw[32];   // weights as fp16 pairs; l sums the fp32 weights
       float lrow = 0.f;
 #pragma unroll
       for (int k = 0; k < 64; k += 2) {
-        const float w0 = s[k] > 0.5f * kNegLarge ? ex2((s[k] - mrow) * kLog2e) : 0.f;
-        const float w1 = s[k + 1] > 0.5f * kNegLarge ? ex2((s[k + 1] - mrow) * kLog2e) : 0.f;
-        const __half2 hw = __floats2half2_rn(w0, w1);
-        lrow += __low2float(hw) + __high2float(hw);
-        pw[k / 2] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&hw));
+        const float w0 = s[k] > 0.5f * kNegLarge ? ex2(s[k] - m2) : 0.f;
+        const float w1 = s[k + 1] > 0.5f * kNegLarge ? ex2(s[k + 1] - m2) : 0.f;
+        lrow += w0 + w1;
+        pw[k / 2] = __uint_as_float(pack_half2(w0, w1));
       }
+      // m in natural-log units (the -1e30 sentinel as is when no key takes part)
+      const float mrow = m2 > 0.5f * kNegLarge ? m2 * 0.6931471805599453f : kNegLarge;
       // P buffer t % 4 is free once O(t-4) = P(t-4) V has completed
       const uint32_t pb = t & 3u;
       if (t >= 4 && !warp_wait(bars + kPEmpty + pb, ((t >> 2) - 1) & 1u, abort)) return;
