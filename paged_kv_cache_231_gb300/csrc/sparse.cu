@@ -636,19 +636,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bl = cur_bl;
         const uint64_t used = bl >= 64 ? ~0ull : ((1ull << bl) - 1ull);
         if (imask & used) bad = true;
+        // scores in base-2 units (scale * log2(e) * <q, k>): the weights are 2^(s - max)
+        const float sl2 = p.scale * kLog2e;
+        float m2 = kNegLarge;
 #pragma unroll
         for (int t = 0; t < 64; ++t) {
-          const float sv = t < bl ? (((vmask >> t) & 1ull) ? s[t] * p.scale : kNegLarge)
+          const float sv = t < bl ? (((vmask >> t) & 1ull) ? s[t] * sl2 : kNegLarge)
                                   : -INFINITY;
           s[t] = sv;
-          mrow = fmaxf(mrow, sv);
+          m2 = fmaxf(m2, sv);
         }
 #pragma unroll
         for (int t = 0; t < 64; ++t) {
-          const float w = s[t] > 0.5f * kNegLarge ? ex2((s[t] - mrow) * kLog2e) : 0.f;
+          const float w = s[t] > 0.5f * kNegLarge ? ex2(s[t] - m2) : 0.f;
           lrow += w;
           s[t] = w;
         }
+        // m in natural-log units (the -1e30 sentinel as is when no key takes part)
+        mrow = m2 > 0.5f * kNegLarge ? m2 * 0.6931471805599453f : kNegLarge;
         float ph[32], pl[32];
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
