@@ -66,32 +66,42 @@ __global__ void sparse_count_kernel(SparseParams p) {
   if (key >= 0) atomicAdd(&p.group_count[key], 1);
 }
 
-// exclusive scan of group_count into group_off (one CTA); clears the fill cursors
+// exclusive scan of group_count into group_off (one CTA); clears the fill cursors. Thread i
+// owns the i-th run of ceil(ngroups / 1024) consecutive groups: the run totals are scanned
+// across the block (warp shuffles), then each thread walks its run.
 __global__ void __launch_bounds__(1024) sparse_scan_kernel(SparseParams p) {
-  __shared__ int s[1024];
-  __shared__ int carry;
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
-  for (int64_t c0 = 0; c0 < p.ngroups; c0 += 1024) {
-    const int64_t g = c0 + threadIdx.x;
-    const int v = g < p.ngroups ? p.group_count[g] : 0;
-    s[threadIdx.x] = v;
-    __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {
-      const int x = threadIdx.x >= off ? s[threadIdx.x - off] : 0;
-      __syncthreads();
-      s[threadIdx.x] += x;
-      __syncthreads();
-    }
-    if (g < p.ngroups) {
-      p.group_off[g] = carry + s[threadIdx.x] - v;
-      p.group_cursor[g] = 0;
-    }
-    __syncthreads();
-    if (threadIdx.x == 1023) carry += s[1023];
-    __syncthreads();
+  __shared__ int warp_tot[32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t per = (p.ngroups + 1023) / 1024;
+  const int64_t g0 = (int64_t)threadIdx.x * per;
+  const int64_t g1 = g0 + per < p.ngroups ? g0 + per : p.ngroups;
+  int run = 0;
+  for (int64_t g = g0; g < g1; ++g) run += p.group_count[g];
+  int x = run;   // inclusive scan of the run totals
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  if (threadIdx.x == 0) p.group_off[p.ngroups] = carry;
+  if (lane == 31) warp_tot[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_tot[lane] = s;
+  }
+  __syncthreads();
+  int off = (w > 0 ? warp_tot[w - 1] : 0) + x - run;
+  for (int64_t g = g0; g < g1; ++g) {
+    p.group_off[g] = off;
+    p.group_cursor[g] = 0;
+    off += p.group_count[g];
+  }
+  if (threadIdx.x == 1023) p.group_off[p.ngroups] = warp_tot[31];
 }
 
 __global__ void sparse_fill_kernel(SparseParams p) {
