@@ -90,6 +90,17 @@ def test_rotary_query(D, rotary_dim, inter, packed):
     check(c, rotary_query=True)
 
 
+def test_rotary_query_with_slot_padding():
+    # a padding slot skips the key write but the token still attends (over the stale row)
+    # with its query rotated; the oracle does the same
+    c = wl.paged_case(46, num_heads=8, kv_num_heads=2, head_size=128, block_size=16,
+                      past=[7, 40], new_tokens=[3, 1], use_slot_mapping=True,
+                      rotary_dim=128, extra_blocks=2)
+    c.slot_mapping = c.slot_mapping.copy()
+    c.slot_mapping[1] = -1
+    check(c, rotary_query=True)
+
+
 def test_rotary_query_position_past_table():
     c = wl.paged_case(45, num_heads=4, kv_num_heads=1, head_size=128, block_size=16,
                       past=[5, 60], new_tokens=[3, 1], rotary_dim=128)

@@ -220,6 +220,30 @@ def test_causal_block_sparse_full_size_sampled(dtype):
     compare_partials(go, gm, gl, ro, rm, rl, rows, f16=dtype == np.float16)
 
 
+@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+def test_no_edges_and_all_empty_edges(dtype):
+    c = wl.block_sparse(58, n_seqs=2, kv_len=512, queries_per_seq=8, hq=8, hkv=2,
+                        head_dim=128, blocks_per_query=3, dtype=dtype)
+    # zero edges: nothing to compute, nothing written, no error
+    c0 = wl.block_sparse(58, n_seqs=2, kv_len=512, queries_per_seq=8, hq=8, hkv=2,
+                         head_dim=128, blocks_per_query=3, dtype=dtype)
+    c0.edge_meta = c0.edge_meta[:0].copy()
+    o, m, l = B.pkv_sparse_attention_partials(
+        dev(c0.q), dev(c0.k_pages), dev(c0.v_pages), dev(c0.edge_meta),
+        dev(c0.block_tables), qhead=c0.qhead, block_size=c0.block_size,
+        page_size=c0.page_size, pages_per_block=c0.pages_per_block,
+        softmax_scale=c0.softmax_scale)
+    torch.cuda.synchronize()
+    assert o.shape[0] == 0 and m.shape[0] == 0 and l.shape[0] == 0
+    # every edge empty (block_len 0 or negative): every partial is the sentinel
+    c.edge_meta = c.edge_meta.copy()
+    c.edge_meta[:, 4] = np.where(np.arange(c.num_edges) % 2 == 0, 0, -5)
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    assert gst == 0
+    assert (go == 0).all() and (gm == -1e30).all() and (gl == 0).all()
+    assert (gout == 0).all() and np.isneginf(glse).all()
+
+
 def _random_partials(rng, n, D, empty_frac=0.2):
     o = rng.standard_normal((n, D)).astype(np.float32) * 3
     m = (rng.standard_normal(n) * 4).astype(np.float32)
