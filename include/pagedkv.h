@@ -342,13 +342,15 @@ int pkv_sparse_attention_partials_workspace_size(const pkv_sparse_args* args,
  * of the sequence's table row, row t % page_size; unmapped page -> score -1e30.
  * s = softmax_scale * <q, k>; m = max s (>= -1e30); weights exp(s - m) for s > -5e29
  * else 0; l = sum of weights; o = weighted sum of value rows (unnormalised).
- * block_len <= 0 -> (o = 0, m = -1e30, l = 0). No causal mask. fp32 throughout.
+ * block_len <= 0 -> (o = 0, m = -1e30, l = 0). No causal mask unless query_positions
+ * is given. fp32 throughout for dtype PKV_F32.
  * The GPU form groups edges by (batch, kv head, block) so each K/V block is read
  * once for all edges that name it. Supported: head_dim in {64, 128}, block_size
  * <= 128, qhead <= 64.
  * dtype PKV_F16 (the page computes in fp32; this is the half-precision variant): scores
- * are fp16 products summed in fp32, the weights are rounded once to fp16 for the
- * weighted sum of value rows and l sums those rounded weights; everything else as above.
+ * are fp16 products summed in fp32, the weights are computed in fp32 and summed into l,
+ * and rounded once to fp16 for the weighted sum of value rows; the partials are fp32;
+ * everything else as above.
  * Supported for fp16: head_dim in {64, 128}, block_size <= 64, page_size a multiple of
  * 8 with pages_per_block * page_size <= 64; else PKV_ERR_UNSUPPORTED.
  * With query_positions the keys after the query's position take no part (they are not
