@@ -92,8 +92,8 @@ struct Layout {   // byte offsets from a 1024-byte-aligned base
   static constexpr uint32_t kXfer = kQ + kQBufs * kQBuf;   // 4 store warps x [32][32] fp32
   static constexpr uint32_t kRowInfo = kXfer + 4 * 4096;   // [8][128] (partial, block_len)
   static constexpr uint32_t kML = kRowInfo + kRows * 128 * 8;      // [8][128] (m, l)
-  static constexpr uint32_t kValid = kML + kRows * 128 * 8;        // [3][64] key states
-  static constexpr uint32_t kRingOff = kValid + kStages * kNK;
+  static constexpr uint32_t kMasks = kML + kRows * 128 * 8;        // [3][2] key masks
+  static constexpr uint32_t kRingOff = kMasks + kStages * 16;
   static constexpr uint32_t kBar = kRingOff + kRing * sizeof(GroupEntry);
   static constexpr uint32_t kAbort = kBar + kNumBars * 8;
   static constexpr uint32_t kTmem = kAbort + 4;
@@ -175,8 +175,9 @@ __device__ __forceinline__ int64_t next_group(const SparseParams& p) {
   }
 }
 
-// One warp: group g's K and V pages into stage `st` by TMA onto sbar; key states into
-// valid[st] (0 unmapped or past the block, 1 mapped, 2 invalid table reference).
+// One warp: group g's K and V pages into stage `st` by TMA onto sbar; the key states into
+// masks[st] = {bit t set: key t mapped, bit t set: key t an invalid table reference}
+// (keys past the block and keys of unmapped pages in neither), two ballots per mask.
 // Unmapped pages get no copy: their rows keep earlier (finite) contents or the zeros the
 // kernel starts with, and their weights are exactly 0.
 template <int D>
@@ -184,15 +185,16 @@ __device__ void stage_group(const SparseParams& p, const Maps& maps, unsigned ch
                             int64_t g, uint32_t st, uint64_t* sbar) {
   using L = Layout<D>;
   const int lane = threadIdx.x & 31;
-  uint8_t* valid = sm + L::kValid + st * kNK;
+  uint64_t* masks = reinterpret_cast<uint64_t*>(sm + L::kMasks) + 2 * st;
   const int h = (int)(g % p.hkv);
   const int64_t bb = g / p.hkv;
   const int blk = (int)(bb % p.nblk);
   const int batch = (int)(bb / p.nblk);
+  uint64_t vmask = 0, imask = 0;
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int t = lane + 32 * k;
-    uint8_t state = 0;
+    int state = 0;
     if (t < p.block_size) {
       const int64_t slot = (int64_t)blk * p.ppb + t / p.page_size;
       if (slot < p.max_pages) {
@@ -202,7 +204,12 @@ __device__ void stage_group(const SparseParams& p, const Maps& maps, unsigned ch
         state = 2;
       }
     }
-    valid[t] = state;
+    vmask |= (uint64_t)__ballot_sync(0xffffffffu, state == 1) << (32 * k);
+    imask |= (uint64_t)__ballot_sync(0xffffffffu, state == 2) << (32 * k);
+  }
+  if (lane == 0) {
+    masks[0] = vmask;
+    masks[1] = imask;
   }
   int row0 = -1;   // first row of page `lane` of the block in the page tensors
   if (lane < p.ppb) {
@@ -266,14 +273,8 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
     const uint32_t st = gi % kStages;
     if (!warp_wait(bars + kKVFull + st, (gi / kStages) & 1u, abort)) return;
     // key masks of the group: bit t of vmask = mapped, of imask = invalid reference
-    const uint8_t* valid = sm + L::kValid + st * kNK;
-    uint64_t vmask = 0, imask = 0;
-#pragma unroll 8
-    for (int k = 0; k < kNK; ++k) {
-      const uint8_t s = valid[k];
-      vmask |= (uint64_t)(s == 1) << k;
-      imask |= (uint64_t)(s == 2) << k;
-    }
+    const uint64_t* masks = reinterpret_cast<const uint64_t*>(sm + L::kMasks) + 2 * st;
+    const uint64_t vmask = masks[0], imask = masks[1];
     for (int c0 = e0; c0 < e1; c0 += epc, ++t) {
       if (!warp_wait(bars + kRowFull + (t % kRows), (t / kRows) & 1u, abort)) return;
       const int2 ri = rowinfo[(t % kRows) * 128 + r];   // (partial index or -1, block_len)
@@ -291,24 +292,35 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
       const int bl = ri.y;
       const uint64_t inblk = bl >= 64 ? ~0ull : ((1ull << bl) - 1ull);
       if (imask & inblk) bad = true;
-      // scores in base-2 units (scale * log2(e) * <q, k>): the weights are 2^(s - max)
+      // keys that take part: mapped and inside the block (the rest score -1e30, and keys
+      // past the block never raise m above that sentinel either)
+      const uint64_t live = vmask & inblk;
+      const uint32_t live_lo = (uint32_t)live, live_hi = (uint32_t)(live >> 32);
+      // scores in base-2 units (scale * log2(e) * <q, k>): the weights are 2^(s - max);
+      // four partial maxima and sums keep the dependency chains short
       const float sl2 = p.scale * kLog2e;
-      float m2 = kNegLarge;
+      float mp[4] = {kNegLarge, kNegLarge, kNegLarge, kNegLarge};
 #pragma unroll
       for (int k = 0; k < 64; ++k) {
-        const float sv = k < bl ? (((vmask >> k) & 1ull) ? s[k] * sl2 : kNegLarge) : -INFINITY;
+        const uint32_t word = k < 32 ? live_lo : live_hi;
+        const float sv = ((word >> (k & 31)) & 1u) ? s[k] * sl2 : kNegLarge;
         s[k] = sv;
-        m2 = fmaxf(m2, sv);
+        mp[k & 3] = fmaxf(mp[k & 3], sv);
       }
+      const float m2 = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
+      // 2^(-1e30 - m) is exactly 0 for every finite m; with no key taking part m is the
+      // sentinel itself, and subtracting 0 instead keeps every weight 0
+      const float msub = m2 > 0.5f * kNegLarge ? m2 : 0.f;
       float pw[32];   // weights as fp16 pairs; l sums the fp32 weights
-      float lrow = 0.f;
+      float lp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 64; k += 2) {
-        const float w0 = s[k] > 0.5f * kNegLarge ? ex2(s[k] - m2) : 0.f;
-        const float w1 = s[k + 1] > 0.5f * kNegLarge ? ex2(s[k + 1] - m2) : 0.f;
-        lrow += w0 + w1;
+        const float w0 = ex2(s[k] - msub);
+        const float w1 = ex2(s[k + 1] - msub);
+        lp[(k >> 1) & 3] += w0 + w1;
         pw[k / 2] = __uint_as_float(pack_half2(w0, w1));
       }
+      const float lrow = (lp[0] + lp[1]) + (lp[2] + lp[3]);
       // m in natural-log units (the -1e30 sentinel as is when no key takes part)
       const float mrow = m2 > 0.5f * kNegLarge ? m2 * 0.6931471805599453f : kNegLarge;
       // P buffer t % 4 is free once O(t-4) = P(t-4) V has completed
