@@ -374,7 +374,7 @@ struct Layout {   // byte offsets from a 1024-byte-aligned base
   static constexpr uint32_t kRawK = kVlo + D * 256;         // raw K, V as loaded by TMA:
   static constexpr uint32_t kRawV = kRawK + D * 256;        //   D/32 x [64 keys][128 B], swizzled
   static constexpr uint32_t kXfer = kRawV + D * 256;        // 8 warps x [32][32] fp32 transpose
-  static constexpr uint32_t kValid = kXfer + 8 * 4096;      // [64] key state, current group
+  static constexpr uint32_t kValid = kXfer + 8 * 4096;      // key masks, current group (16 B)
   static constexpr uint32_t kRValid = kValid + 64;          // [64] key state, staged group
   static constexpr uint32_t kBar = kRValid + 64;            // MMA completion, drain, raw K/V
   static constexpr uint32_t kTmem = kBar + 24;
@@ -456,8 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sValid = sm + L::kValid;
-  const uint8_t* rValid = sm + L::kRValid;
+  uint32_t* sMask = reinterpret_cast<uint32_t*>(sm + L::kValid);   // {mapped, invalid} x 64 bits
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::kTmem);
   volatile int64_t* snext = reinterpret_cast<volatile int64_t*>(sm + L::kNext);
@@ -585,7 +584,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (tid < kNK) sValid[tid] = rValid[tid];
+    if (warp < 2) {   // the key masks of this group, 32 keys per warp
+      const uint8_t st = rValid[tid];
+      const uint32_t vb = __ballot_sync(0xffffffffu, st == 1);
+      const uint32_t ib = __ballot_sync(0xffffffffu, st == 2);
+      if (lane == 0) {
+        sMask[warp] = vb;
+        sMask[2 + warp] = ib;
+      }
+    }
     tc::fence_async_shared();
     if (tid == 0) *snext = next_group(p);
     __syncthreads();
@@ -596,13 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++raw_issued;
     }
     // key masks of this group: bit t of vmask = mapped, of imask = invalid reference
-    uint64_t vmask = 0, imask = 0;
-#pragma unroll 8
-    for (int t = 0; t < kNK; ++t) {
-      const uint8_t st = sValid[t];
-      vmask |= (uint64_t)(st == 1) << t;
-      imask |= (uint64_t)(st == 2) << t;
-    }
+    const uint64_t vmask = reinterpret_cast<const uint64_t*>(sMask)[0];
+    const uint64_t imask = reinterpret_cast<const uint64_t*>(sMask)[1];
     const int e0 = p.group_off[g], e1 = p.group_off[g + 1];
     const int h = (int)(g % p.hkv);
     for (int c0 = e0; c0 < e1 && ok; c0 += epc) {
@@ -646,22 +648,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bl = cur_bl;
         const uint64_t used = bl >= 64 ? ~0ull : ((1ull << bl) - 1ull);
         if (imask & used) bad = true;
-        // scores in base-2 units (scale * log2(e) * <q, k>): the weights are 2^(s - max)
+        // keys that take part: mapped and inside the block (the rest score -1e30, and keys
+        // past the block never raise m above that sentinel either)
+        const uint64_t live = vmask & used;
+        const uint32_t live_lo = (uint32_t)live, live_hi = (uint32_t)(live >> 32);
+        // scores in base-2 units (scale * log2(e) * <q, k>): the weights are 2^(s - max);
+        // four partial maxima and sums keep the dependency chains short
         const float sl2 = p.scale * kLog2e;
-        float m2 = kNegLarge;
+        float mp[4] = {kNegLarge, kNegLarge, kNegLarge, kNegLarge};
 #pragma unroll
         for (int t = 0; t < 64; ++t) {
-          const float sv = t < bl ? (((vmask >> t) & 1ull) ? s[t] * sl2 : kNegLarge)
-                                  : -INFINITY;
+          const uint32_t word = t < 32 ? live_lo : live_hi;
+          const float sv = ((word >> (t & 31)) & 1u) ? s[t] * sl2 : kNegLarge;
           s[t] = sv;
-          m2 = fmaxf(m2, sv);
+          mp[t & 3] = fmaxf(mp[t & 3], sv);
         }
+        const float m2 = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
+        // 2^(-1e30 - m) is exactly 0 for every finite m; with no key taking part m is the
+        // sentinel itself, and subtracting 0 instead keeps every weight 0
+        const float msub = m2 > 0.5f * kNegLarge ? m2 : 0.f;
+        float lp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int t = 0; t < 64; ++t) {
-          const float w = s[t] > 0.5f * kNegLarge ? ex2(s[t] - m2) : 0.f;
-          lrow += w;
+          const float w = ex2(s[t] - msub);
+          lp[t & 3] += w;
           s[t] = w;
         }
+        lrow = (lp[0] + lp[1]) + (lp[2] + lp[3]);
         // m in natural-log units (the -1e30 sentinel as is when no key takes part)
         mrow = m2 > 0.5f * kNegLarge ? m2 * 0.6931471805599453f : kNegLarge;
         float ph[32], pl[32];
