@@ -52,7 +52,7 @@ typedef enum pkv_status {
   PKV_ERR_CAUSAL = 6,      /* is_causal != 1 (the manifest admits only 1) */
   PKV_ERR_WORKSPACE = 7,   /* workspace NULL, too small or not 256-byte aligned */
   PKV_ERR_ALIGN = 8,       /* a tensor pointer is not 16-byte aligned */
-  PKV_ERR_UNSUPPORTED = 9, /* a size outside what this build compiles (see each call) */
+  PKV_ERR_UNSUPPORTED = 9, /* a size outside the compiled kernel variants (see each call) */
   PKV_ERR_LAUNCH = 10      /* a CUDA launch or API call failed */
 } pkv_status;
 

@@ -288,7 +288,7 @@ const char* pkv_status_string(int status) {
     case PKV_ERR_CAUSAL: return "is_causal must be 1";
     case PKV_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
     case PKV_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
-    case PKV_ERR_UNSUPPORTED: return "size outside what this build supports";
+    case PKV_ERR_UNSUPPORTED: return "size outside the compiled kernel variants";
     case PKV_ERR_LAUNCH: return "CUDA launch failed";
     default: return "unknown status";
   }
