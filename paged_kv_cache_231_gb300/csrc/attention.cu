@@ -688,8 +688,7 @@ struct TcLayout {  // byte offsets from a 1024-byte-aligned base
   static constexpr uint32_t kQ = 0;               // 2 x [128][64] fp16 sub-tiles
   static constexpr uint32_t kK = 32768;           // kKStages x 32 KB
   static constexpr uint32_t kV = kK + 65536;      // kVStages x 32 KB
-  static constexpr uint32_t kOnes = kV + 98304;   // [16][64] fp16 ones (row-sum operand)
-  static constexpr uint32_t kBars = kOnes + 2048; // mbarriers (see TcBar)
+  static constexpr uint32_t kBars = kV + 98304;   // mbarriers (see TcBar)
   static constexpr uint32_t kTmem = kBars + 256;  // TMEM base address
   static constexpr uint32_t kTile = kTmem + 4;    // current tile index
   static constexpr uint32_t kAbort = kTile + 4;   // set when a bounded wait gives up
@@ -703,15 +702,15 @@ enum TcBar {  // mbarrier slots
   kBarVEmpty0 = 8,   // + stage (3), count 1: the O += P V that read the stage completed
   kBarSFull0 = 11,   // + buffer, count 1: S_j in TMEM
   kBarPFull = 13,    // count 4 (one per softmax warp): softmax wrote P_j to TMEM
-  kBarODone = 14,    // count 1: O += P_j V_j (and l += P_j 1) completed
+  kBarODone = 14,    // count 1: O += P_j V_j completed
   kBarDrain = 15,    // count 1: MMAs in flight when a wait gave up
   kBarSEmpty0 = 16,  // + buffer, count 4: softmax has read S_j out of the buffer
   kNumBars = 18
 };
 static_assert(kNumBars * 8 <= 256, "mbarrier slots");
-// TMEM columns: S_j in buffer j % 2, the O accumulator, the row sums l (first of 16
-// columns), and P_j as fp16 pairs (two keys per 32-bit column)
-constexpr uint32_t kTmS = 0, kTmO = 256, kTmL = 384, kTmP = 448;
+// TMEM columns: S_j in buffer j % 2, the O accumulator, and P_j as fp16 pairs (two keys
+// per 32-bit column); the row sums l stay in the softmax threads' registers
+constexpr uint32_t kTmS = 0, kTmO = 256, kTmP = 448;
 constexpr int kKStages = 2;        // K ring depth
 constexpr int kVStages = 3;        // V ring depth: V_j streams in once O += P_{j-3} V_{j-3} is done
 constexpr uint32_t kTcWaitTries = 1u << 22;
@@ -890,8 +889,8 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
 // Warp 4, lane 0: the MMA stream of the tile (O += P V checked first: it is on the
 // softmax's critical path, S = Q K^T runs ahead). S_jq = Q K_jq^T may be issued once K_jq
 // landed and the softmax has read S_{jq-2} out of buffer jq % 2 (SEmpty phases are counted
-// per block, across tiles, because the last two of a tile are never waited for); O += P_jp V_jp (and
-// l += P_jp 1, the row sums, on an all-ones operand) once P_jp is in TMEM and V_jp landed.
+// per block, across tiles, because the last two of a tile are never waited for); O += P_jp V_jp
+// once P_jp is in TMEM and V_jp landed.
 __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
                        uint32_t tmem, uint32_t q_use, uint32_t (&k_use)[kKStages],
                        uint32_t (&v_use)[kVStages], uint32_t (&s_base)[2], uint32_t& blk_use) {
@@ -899,10 +898,7 @@ __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const uint32_t idesc_qk = tc::idesc_f16(128, 128, false, false);
   const uint32_t idesc_pv = tc::idesc_f16(128, 128, false, true);
-  const uint32_t idesc_l = tc::idesc_f16(128, 16, false, false);
   const uint32_t qa = smem_u32(sm + TcLayout::kQ);
-  // every row and K step of the all-ones operand reads ones: one descriptor serves all
-  const uint64_t ones = tc::smem_desc(smem_u32(sm + TcLayout::kOnes), 16, 1024);
   if (!tc_wait(bars + kBarQFull, q_use & 1u, abort)) return;
   int jq = 0, jp = 0, kq = 0, vq = 0;   // kq = jq % kKStages, vq = jp % kVStages
   uint32_t idle = 0;
@@ -921,7 +917,6 @@ __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
           const uint32_t acc = (jp > 0 || ks > 0) ? 1u : 0u;
           mma_f16_tmem_a(tmem + kTmO, tmem + kTmP + (uint32_t)ks * 8u,
                          tc::smem_desc(va + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv, acc);
-          mma_f16_tmem_a(tmem + kTmL, tmem + kTmP + (uint32_t)ks * 8u, ones, idesc_l, acc);
         }
         tc::commit(bars + kBarODone);
         tc::commit(bars + kBarVEmpty0 + s);
@@ -993,6 +988,7 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
   const bool pos_scale = sl2 >= 0.f;
   const float hide = pos_scale ? -INFINITY : INFINITY;   // masked raw score
   float m_used = -INFINITY;
+  float l_run = 0.f;   // row sum of the weights, relative to m_used like O
   bool ok = true;
   // block-table entry of the cache block holding keys [kbase + 4 lane, + 4) of block j
   auto lookup = [&](int j) -> int {
@@ -1066,17 +1062,20 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
     if (raise) m_used = mx;
     const float nbase = m_used == -INFINITY ? 0.f : -m_used;
     float pw[64];   // P_j row as fp16 pairs (bit patterns)
+    float lp[4] = {0.f, 0.f, 0.f, 0.f};   // l sums the fp32 weights, four short chains
 #pragma unroll
     for (int c = 0; c < 128; c += 2) {
       const float p0 = ex2(fmaf(v[c], sl2, nbase)), p1 = ex2(fmaf(v[c + 1], sl2, nbase));
+      lp[(c >> 1) & 3] += p0 + p1;
       pw[c / 2] = __uint_as_float(pack_half2(p0, p1));
     }
-    // O, l and the P columns are free once O += P_{j-1} V_{j-1} has completed
+    l_run = l_run * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
+    // O and the P columns are free once O += P_{j-1} V_{j-1} has completed
     if (j > 0) {
       ok = __all_sync(0xffffffffu, tc_wait(bars + kBarODone, (blk_use + j - 1) & 1u, abort));
       if (!ok) break;
       tc::fence_after_sync();
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {   // warp-collective TMEM rescale of O, l
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {   // warp-collective TMEM rescale of O
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           float o[32];
@@ -1086,8 +1085,6 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
           for (int c = 0; c < 32; ++c) o[c] *= alpha;
           tc::tmem_st32(lane_taddr + kTmO + ch * 32, o);
         }
-        float lv = tc::tmem_ld1(lane_taddr + kTmL);
-        tc::tmem_st1(lane_taddr + kTmL, lv * alpha);
       }
     }
     {
@@ -1105,8 +1102,7 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
                     tc_wait(bars + kBarODone, (blk_use + t.nblk - 1) & 1u, abort));
     if (ok) {
       tc::fence_after_sync();
-      const float l = tc::tmem_ld1(lane_taddr + kTmL);
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       __half* orow = p.out + (int64_t)(t.cu0 + t.q0 + pl) * p.Hq * D +
                      (int64_t)(t.h * p.G + r % p.G) * D;
 #pragma unroll
@@ -1164,10 +1160,6 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
     tc::tma_prefetch_desc(&maps.k);
   }
   if (warp == kVLoaderWarp && lane == 0) tc::tma_prefetch_desc(&maps.v);
-  for (int i = tid; i < 2048 / 16; i += kTcThreads)   // fp16 ones
-    reinterpret_cast<uint4*>(sm + TcLayout::kOnes)[i] =
-        make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
-  tc::fence_async_shared();
   if (warp == 0) {
     tc::tmem_alloc(tslot, 512);
     tc::tmem_relinquish();
