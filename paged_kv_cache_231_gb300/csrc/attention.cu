@@ -1062,14 +1062,17 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
     if (raise) m_used = mx;
     const float nbase = m_used == -INFINITY ? 0.f : -m_used;
     float pw[64];   // P_j row as fp16 pairs (bit patterns)
-    float lp[4] = {0.f, 0.f, 0.f, 0.f};   // l sums the fp32 weights, four short chains
+    // l sums the fp32 weights: four pairs of accumulators, each pair one f32x2 add
+    float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < 128; c += 2) {
-      const float p0 = ex2(fmaf(v[c], sl2, nbase)), p1 = ex2(fmaf(v[c + 1], sl2, nbase));
-      lp[(c >> 1) & 3] += p0 + p1;
+      float e0, e1;
+      fma2(e0, e1, v[c], v[c + 1], sl2, nbase);
+      const float p0 = ex2(e0), p1 = ex2(e1);
+      add2(la[(c >> 1) & 3], lb[(c >> 1) & 3], p0, p1);
       pw[c / 2] = __uint_as_float(pack_half2(p0, p1));
     }
-    l_run = l_run * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
+    l_run = l_run * alpha + (((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3])));
     // O and the P columns are free once O += P_{j-1} V_{j-1} has completed
     if (j > 0) {
       ok = __all_sync(0xffffffffu, tc_wait(bars + kBarODone, (blk_use + j - 1) & 1u, abort));

@@ -298,29 +298,38 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
       const uint32_t live_lo = (uint32_t)live, live_hi = (uint32_t)(live >> 32);
       // scores in base-2 units (scale * log2(e) * <q, k>): the weights are 2^(s - max);
       // four partial maxima and sums keep the dependency chains short
+      // (pairs of keys go through one f32x2 instruction; each result is rounded as the
+      // scalar operation)
       const float sl2 = p.scale * kLog2e;
       float mp[4] = {kNegLarge, kNegLarge, kNegLarge, kNegLarge};
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
+      for (int k = 0; k < 64; k += 2) {
         const uint32_t word = k < 32 ? live_lo : live_hi;
-        const float sv = ((word >> (k & 31)) & 1u) ? s[k] * sl2 : kNegLarge;
-        s[k] = sv;
-        mp[k & 3] = fmaxf(mp[k & 3], sv);
+        float x0, x1;
+        fma2(x0, x1, s[k], s[k + 1], sl2, 0.f);
+        const float sv0 = ((word >> (k & 31)) & 1u) ? x0 : kNegLarge;
+        const float sv1 = ((word >> ((k + 1) & 31)) & 1u) ? x1 : kNegLarge;
+        s[k] = sv0;
+        s[k + 1] = sv1;
+        mp[k & 3] = fmaxf(mp[k & 3], sv0);
+        mp[(k + 1) & 3] = fmaxf(mp[(k + 1) & 3], sv1);
       }
       const float m2 = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
       // 2^(-1e30 - m) is exactly 0 for every finite m; with no key taking part m is the
       // sentinel itself, and subtracting 0 instead keeps every weight 0
       const float msub = m2 > 0.5f * kNegLarge ? m2 : 0.f;
       float pw[32];   // weights as fp16 pairs; l sums the fp32 weights
-      float lp[4] = {0.f, 0.f, 0.f, 0.f};
+      float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 64; k += 2) {
-        const float w0 = ex2(s[k] - msub);
-        const float w1 = ex2(s[k + 1] - msub);
-        lp[(k >> 1) & 3] += w0 + w1;
+        float d0, d1;
+        fma2(d0, d1, s[k], s[k + 1], 1.f, -msub);   // s - m, exactly as a subtraction
+        const float w0 = ex2(d0), w1 = ex2(d1);
+        add2(la[(k >> 1) & 3], lb[(k >> 1) & 3], w0, w1);
         pw[k / 2] = __uint_as_float(pack_half2(w0, w1));
       }
-      const float lrow = (lp[0] + lp[1]) + (lp[2] + lp[3]);
+      const float lrow =
+          ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
       // m in natural-log units (the -1e30 sentinel as is when no key takes part)
       const float mrow = m2 > 0.5f * kNegLarge ? m2 * 0.6931471805599453f : kNegLarge;
       // P buffer t % 4 is free once O(t-4) = P(t-4) V has completed
