@@ -60,13 +60,21 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Paired fp32 arithmetic (one f32x2 instruction for two lanes of work, each rounded as
-// the scalar operation): (r0, r1) = (a0, a1) * b + c, and (r0, r1) += (a0, a1).
+// the scalar operation): (r0, r1) = (a0, a1) * b + c, (r0, r1) = (a0, a1) - (b0, b1),
+// (r0, r1) += (a0, a1).
 __device__ __forceinline__ void fma2(float& r0, float& r1, float a0, float a1, float b,
                                      float c) {
   asm("{\n.reg .b64 a, b, c, d;\nmov.b64 a, {%2, %3};\nmov.b64 b, {%4, %4};\n"
       "mov.b64 c, {%5, %5};\nfma.rn.f32x2 d, a, b, c;\nmov.b64 {%0, %1}, d;\n}\n"
       : "=f"(r0), "=f"(r1)
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void sub2(float& r0, float& r1, float a0, float a1, float b0,
+                                     float b1) {
+  asm("{\n.reg .b64 a, b;\nmov.b64 a, {%2, %3};\nmov.b64 b, {%4, %5};\n"
+      "sub.rn.f32x2 a, a, b;\nmov.b64 {%0, %1}, a;\n}\n"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 __device__ __forceinline__ void add2(float& r0, float& r1, float a0, float a1) {
   asm("{\n.reg .b64 a, b;\nmov.b64 a, {%0, %1};\nmov.b64 b, {%2, %3};\n"

@@ -536,10 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4 v = *reinterpret_cast<const float4*>(xf + lane * 32 + ((q ^ (lane & 7)) << 2));
         const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          vh[q * 4 + j] = tf32_hi(x[j]);
-          vl[q * 4 + j] = x[j] - vh[q * 4 + j];
-        }
+        for (int j = 0; j < 4; ++j) vh[q * 4 + j] = tf32_hi(x[j]);
+        sub2(vl[q * 4], vl[q * 4 + 1], x[0], x[1], vh[q * 4], vh[q * 4 + 1]);
+        sub2(vl[q * 4 + 2], vl[q * 4 + 3], x[2], x[3], vh[q * 4 + 2], vh[q * 4 + 3]);
       }
       __syncwarp();
       tc::tmem_st32(lane_tm + 256 + cbase, vh);
@@ -561,7 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float4 v = *reinterpret_cast<const float4*>(sm + L::kRawK + off);
       if (rValid[t] != 1) v = make_float4(0.f, 0.f, 0.f, 0.f);
       const float4 hi = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
-      const float4 lo = make_float4(v.x - hi.x, v.y - hi.y, v.z - hi.z, v.w - hi.w);
+      float4 lo;
+      sub2(lo.x, lo.y, v.x, v.y, hi.x, hi.y);
+      sub2(lo.z, lo.w, v.z, v.w, hi.z, hi.w);
       *reinterpret_cast<float4*>(sm + L::kKhi + off) = hi;
       *reinterpret_cast<float4*>(sm + L::kKlo + off) = lo;
     }
@@ -654,36 +655,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t live_lo = (uint32_t)live, live_hi = (uint32_t)(live >> 32);
         // scores in base-2 units (scale * log2(e) * <q, k>): the weights are 2^(s - max);
         // four partial maxima and sums keep the dependency chains short
+        // (pairs of keys go through one f32x2 instruction, each rounded as the scalar one)
         const float sl2 = p.scale * kLog2e;
         float mp[4] = {kNegLarge, kNegLarge, kNegLarge, kNegLarge};
 #pragma unroll
-        for (int t = 0; t < 64; ++t) {
+        for (int t = 0; t < 64; t += 2) {
           const uint32_t word = t < 32 ? live_lo : live_hi;
-          const float sv = ((word >> (t & 31)) & 1u) ? s[t] * sl2 : kNegLarge;
-          s[t] = sv;
-          mp[t & 3] = fmaxf(mp[t & 3], sv);
+          float x0, x1;
+          fma2(x0, x1, s[t], s[t + 1], sl2, 0.f);
+          s[t] = ((word >> (t & 31)) & 1u) ? x0 : kNegLarge;
+          s[t + 1] = ((word >> ((t + 1) & 31)) & 1u) ? x1 : kNegLarge;
+          mp[t & 3] = fmaxf(mp[t & 3], s[t]);
+          mp[(t + 1) & 3] = fmaxf(mp[(t + 1) & 3], s[t + 1]);
         }
         const float m2 = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
         // 2^(-1e30 - m) is exactly 0 for every finite m; with no key taking part m is the
         // sentinel itself, and subtracting 0 instead keeps every weight 0
         const float msub = m2 > 0.5f * kNegLarge ? m2 : 0.f;
-        float lp[4] = {0.f, 0.f, 0.f, 0.f};
+        float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int t = 0; t < 64; ++t) {
-          const float w = ex2(s[t] - msub);
-          lp[t & 3] += w;
-          s[t] = w;
+        for (int t = 0; t < 64; t += 2) {
+          float d0, d1;
+          fma2(d0, d1, s[t], s[t + 1], 1.f, -msub);   // s - m, exactly as a subtraction
+          s[t] = ex2(d0);
+          s[t + 1] = ex2(d1);
+          add2(la[(t >> 1) & 3], lb[(t >> 1) & 3], s[t], s[t + 1]);
         }
-        lrow = (lp[0] + lp[1]) + (lp[2] + lp[3]);
+        lrow = ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
         // m in natural-log units (the -1e30 sentinel as is when no key takes part)
         mrow = m2 > 0.5f * kNegLarge ? m2 * 0.6931471805599453f : kNegLarge;
         float ph[32], pl[32];
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
+          for (int k = 0; k < 32; k += 2) {
             ph[k] = tf32_hi(s[ch * 32 + k]);
-            pl[k] = s[ch * 32 + k] - ph[k];
+            ph[k + 1] = tf32_hi(s[ch * 32 + k + 1]);
+            sub2(pl[k], pl[k + 1], s[ch * 32 + k], s[ch * 32 + k + 1], ph[k], ph[k + 1]);
           }
           tc::tmem_st32(lane_tm + 256 + ch * 32, ph);
           tc::tmem_st32(lane_tm + 320 + ch * 32, pl);
