@@ -16,10 +16,10 @@
 //     adapts per sequence and the load is balanced to one stage;
 //   * prefill (many new tokens): tiles of query positions x query heads, taken by the
 //     same persistent CTAs from an atomic counter, so K/V is read once per tile. For
-//     head size 128 a tile is 128 rows on the 5th-generation tensor core: Q, K, V and P
-//     in 128-byte-swizzled shared memory, S and O accumulators in tensor memory,
+//     head size 128 a tile is 128 rows on the 5th-generation tensor core: Q, K and V in
+//     128-byte-swizzled shared memory, the S and O accumulators and P in tensor memory,
 //     tcgen05.mma issued by one thread and completed through mbarriers, one softmax
-//     thread per row reading its TMEM lane;
+//     thread per row reading its TMEM lane and keeping the row sum in a register;
 //   * decode and the head-size-64 tiles run QK^T and PV on mma.sync m16n8k16 (fp16 in,
 //     fp32 accumulate) with the score accumulators reused in registers as the A
 //     operand of PV. Softmax works in base 2 (scores pre-scaled by log2 e).
