@@ -20,7 +20,9 @@ namespace pkv {
 // ---------------------------------------------------------------- profiler / counters
 namespace {
 std::atomic<int64_t> g_launches{0};
-bool g_prof = false;
+// read by every launch on any thread; the event records themselves are single-threaded
+// (the profiler is documented as not thread-safe)
+std::atomic<bool> g_prof{false};
 struct Rec {
   cudaEvent_t a, b;
 };
@@ -41,14 +43,14 @@ cudaEvent_t pooled_event() {
 }  // namespace
 
 void prof_begin(const char* name, cudaStream_t s) {
-  if (!g_prof) return;
+  if (!g_prof.load(std::memory_order_relaxed)) return;
   cudaEvent_t e = pooled_event();
   cudaEventRecord(e, s);
   g_open.emplace_back(name, e);
 }
 
 void prof_end(const char* name, cudaStream_t s) {
-  if (!g_prof || g_open.empty()) return;
+  if (!g_prof.load(std::memory_order_relaxed) || g_open.empty()) return;
   cudaEvent_t e = pooled_event();
   cudaEventRecord(e, s);
   auto top = g_open.back();
@@ -67,16 +69,22 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// SM count of the current device, cached per device (safe to call from several host
+// threads: each slot is written with the same value by whichever thread gets there first)
 int num_sms_current() {
+  constexpr int kFallback = 152;   // a GB300; used only if the runtime cannot be queried
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  static std::map<int, int> cache;
-  auto it = cache.find(dev);
-  if (it != cache.end()) return it->second;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kFallback;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    n = 148;
-  cache[dev] = n;
+    return kFallback;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -309,7 +317,7 @@ size_t pkv_sizeof_struct(const char* name) {
 
 int64_t pkv_launch_count(void) { return g_launches.load(); }
 
-void pkv_profiler_enable(int on) { g_prof = on != 0; }
+void pkv_profiler_enable(int on) { g_prof.store(on != 0, std::memory_order_relaxed); }
 
 void pkv_profiler_reset(void) {
   for (auto& kv : g_recs)
