@@ -124,6 +124,10 @@ int check_paged(const pkv_paged_attention_args* a, bool attention, PagedLayout* 
   if (a->head_size <= 0 || a->block_size <= 0 || a->num_blocks <= 0 || a->batch < 1 ||
       a->max_blocks < 1 || a->num_tokens < 0)
     return PKV_ERR_SHAPE;
+  // every size below is formed from these as int64 products: bound the factors first
+  if (a->num_heads > INT32_MAX || a->head_size > INT32_MAX || a->block_size > INT32_MAX ||
+      a->max_blocks > INT32_MAX || a->num_blocks > INT32_MAX)
+    return PKV_ERR_UNSUPPORTED;
   if (a->num_tokens == 0) {   // nothing is read or written; empty tensors may be NULL
     if (L) {
       L->mode = 0;
@@ -547,6 +551,10 @@ int pkv_kv_append_rotary(const pkv_kv_append_args* a, void* stream) {
     return PKV_ERR_HEADS;
   if (a->batch < 0 || a->seq_len < 0 || a->head_size <= 0 || a->max_cache_seq <= 0)
     return PKV_ERR_SHAPE;
+  // offsets below are int64 products of these: bound the factors first
+  if (a->num_heads > INT32_MAX || a->head_size > INT32_MAX || a->max_cache_seq > INT32_MAX ||
+      a->batch > INT32_MAX / 2 || a->seq_len > INT32_MAX / 2)
+    return PKV_ERR_UNSUPPORTED;
   if (a->rotary_dim < 0 || a->rotary_dim % 2 != 0 || a->rotary_dim > a->head_size)
     return PKV_ERR_SHAPE;
   if (!a->source || !a->present_key || !a->present_value || !a->total_sequence_length ||
@@ -606,6 +614,11 @@ int pkv_kv_append_rotary(const pkv_kv_append_args* a, void* stream) {
 namespace {
 int check_sparse(const pkv_sparse_args* a, int64_t* nblk, int64_t* ngroups, size_t* bytes) {
   if (!a) return PKV_ERR_NULL;
+  // the sizes below are int64 products of these: bound the factors first
+  if (a->hkv > INT32_MAX || a->qhead > INT32_MAX || a->page_size > INT32_MAX ||
+      a->pages_per_block > INT32_MAX || a->max_pages > INT32_MAX || a->num_pages > INT32_MAX ||
+      a->num_seqs > INT32_MAX)
+    return PKV_ERR_UNSUPPORTED;
   if (a->hkv <= 0 || a->qhead <= 0 || a->hq != a->hkv * a->qhead) return PKV_ERR_HEADS;
   if (a->num_edges < 0 || a->num_queries < 0 || a->num_seqs < 0 || a->max_pages <= 0 ||
       a->num_pages < 0 || a->page_size <= 0 || a->pages_per_block <= 0 ||
@@ -616,12 +629,12 @@ int check_sparse(const pkv_sparse_args* a, int64_t* nblk, int64_t* ngroups, size
   if (a->dtype != 0 && a->dtype != PKV_F32 && a->dtype != PKV_F16) return PKV_ERR_DTYPE;
   if (a->dtype == PKV_F16 &&
       (a->block_size > 64 || a->page_size % 8 != 0 || a->page_size * a->pages_per_block > 64 ||
-       a->num_pages * a->hkv * a->page_size > INT32_MAX))
+       a->num_pages > INT32_MAX / (a->hkv * a->page_size)))
     return PKV_ERR_UNSUPPORTED;
   if (a->num_edges > INT32_MAX / 64) return PKV_ERR_UNSUPPORTED;
   const int64_t nb = (a->max_pages + a->pages_per_block - 1) / a->pages_per_block;
+  if (a->num_seqs > (INT32_MAX / 2) / (nb * a->hkv)) return PKV_ERR_UNSUPPORTED;
   const int64_t ng = a->num_seqs * nb * a->hkv;
-  if (ng > INT32_MAX / 2) return PKV_ERR_UNSUPPORTED;
   *nblk = nb;
   *ngroups = ng;
   *bytes = 2 * align_up(4 * (size_t)(ng + 1)) + align_up(4 * (size_t)ng) +

@@ -271,3 +271,29 @@ def test_sparse_and_combine_argument_checks(lib):
 def test_binding_raises_without_library(tmp_path):
     with pytest.raises(RuntimeError):
         B.load_library(str(tmp_path / "missing.so"))
+
+
+def test_huge_sizes_are_refused_before_any_product_overflows(lib):
+    # Sizes whose int64 products would overflow are refused up front (no launch, no GPU).
+    big = 1 << 40
+    a = B.make_paged_args(*_host_case()[:9], output=torch.zeros((2, 4 * 64), dtype=torch.float16),
+                          num_heads=4, kv_num_heads=2)
+    for field in ("max_blocks", "block_size", "num_blocks", "num_heads"):
+        b = B.PagedAttentionArgs.from_buffer_copy(a)
+        setattr(b, field, big)
+        if field == "num_heads":
+            b.kv_num_heads = big // 2   # keep the head ratio valid
+        plan = B.PagedPlan()
+        st = lib.pkv_paged_attention_plan(ctypes.byref(b), ctypes.byref(plan))
+        assert B.STATUS_NAMES[st] == "PKV_ERR_UNSUPPORTED", field
+    s = B.SparseArgs(num_queries=4, num_edges=4, num_seqs=1, max_pages=8, num_pages=8,
+                     qhead=4, hq=32, hkv=8, head_dim=128, block_size=64, page_size=16,
+                     pages_per_block=4, softmax_scale=0.1, dtype=0)
+    n = ctypes.c_size_t(0)
+    assert lib.pkv_sparse_attention_partials_workspace_size(ctypes.byref(s), ctypes.byref(n)) == 0
+    for field, value in (("num_seqs", big), ("max_pages", big), ("num_pages", big),
+                         ("num_seqs", (1 << 31) - 1)):
+        t = B.SparseArgs.from_buffer_copy(s)
+        setattr(t, field, value)
+        st = lib.pkv_sparse_attention_partials_workspace_size(ctypes.byref(t), ctypes.byref(n))
+        assert B.STATUS_NAMES[st] == "PKV_ERR_UNSUPPORTED", (field, value)
