@@ -12,8 +12,8 @@ the step's inputs and D2H of its output inside the timed region). ``--impl refer
 times the CPU oracle on a bounded sample of the same workload instead.
 
 Other workloads (``--workload llama8b_decode_rope|varlen_mixed|block_sparse|
-block_sparse_f16|block_sparse_causal|append_prompt``) print the same structure with their
-own metric; they are not the headline line.
+block_sparse_f16|block_sparse_causal|append_prompt|tiny_decode``) print the same structure
+with their own metric; they are not the headline line.
 """
 import argparse
 import hashlib
@@ -37,6 +37,21 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention KV GB/s and % of HBM peak; tokens/s at Llama-8B shape"
 L2_BYTES = 129 * 1024 * 1024
+WORKLOADS = ["llama8b_decode", "llama8b_decode_rope", "varlen_mixed", "block_sparse",
+             "block_sparse_f16", "block_sparse_causal", "append_prompt", "tiny_decode"]
+# metric, unit and direction of every workload (shared by both arms of the benchmark)
+METRICS = {
+    "llama8b_decode": (METRIC, "GB/s", True),
+    "llama8b_decode_rope": (METRIC + ", RoPE on new keys and queries", "GB/s", True),
+    "varlen_mixed": ("varlen prefill+decode attention TFLOP/s (causal pairs)", "TFLOP/s", True),
+    "block_sparse": ("block-sparse partials+combine fp32 TFLOP/s", "TFLOP/s", True),
+    "block_sparse_f16": ("block-sparse partials+combine fp16 TFLOP/s", "TFLOP/s", True),
+    "block_sparse_causal": ("block-sparse partials+combine fp32 TFLOP/s, right-aligned causal",
+                            "TFLOP/s", True),
+    "append_prompt": ("KV append+RoPE GB/s (prompt)", "GB/s", True),
+    "tiny_decode": ("tiny paged decode latency (2 sequences, scatter + attention), "
+                    "microseconds per call", "us", False),
+}
 
 
 # ----------------------------------------------------------------------------- infra
@@ -47,13 +62,12 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b_decode",
-                    choices=["llama8b_decode", "llama8b_decode_rope", "varlen_mixed",
-                             "block_sparse", "block_sparse_f16", "block_sparse_causal",
-                             "append_prompt"])
+                    choices=WORKLOADS)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer leg")
+    ap.add_argument("--oracle-one-core", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -99,8 +113,11 @@ def measured_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+CLOCK_PAD_S = 0.5
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
+    """nvidia-smi clock / throttle samples every 50 ms while it runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -112,7 +129,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -230,13 +247,74 @@ class Workload:
     pass
 
 
+def paged_config(name, case):
+    """The `config` object of a paged workload (both arms print the same one)."""
+    pool = case.key_cache.nbytes + case.value_cache.nbytes
+    if name == "tiny_decode":
+        kvb, qb, ob = decode_bytes(case)
+        return {"workload": name, "batch": case.batch, "tokens": case.num_tokens,
+                "num_heads": case.num_heads, "kv_num_heads": case.kv_num_heads,
+                "head_size": case.head_size, "block_size": case.block_size,
+                "past": [int(x) for x in case.past_seqlens], "bytes_per_step": kvb + qb + ob,
+                "l2": "no flush: a latency case (%.0f KB of KV pool, L2-resident)" % (pool / 1e3)}
+    if name.startswith("llama8b_decode"):
+        kvb, qb, ob = decode_bytes(case)
+        return {"workload": name, "batch": case.batch, "tokens": case.num_tokens,
+                "num_heads": 32, "kv_num_heads": 8, "head_size": 128, "block_size": 16,
+                "context": "U[512,8192]",
+                "mean_context": float(case.context_lengths().mean()),
+                "kv_bytes_per_step": kvb, "bytes_per_step": kvb + qb + ob,
+                "l2": "no flush: the KV pool (%.2f GB) is larger than L2 (129 MB)"
+                      % (pool / 1e9)}
+    return {"workload": "varlen_mixed", "batch": case.batch, "tokens": case.num_tokens,
+            "num_heads": 32, "kv_num_heads": 8, "head_size": 128, "block_size": 32,
+            "flops_per_step": prefill_flops(case),
+            "l2": "no flush: KV pool %.2f GB > L2" % (pool / 1e9)}
+
+
+def sparse_keys(c, causal):
+    """Keys taking part per edge (block_len clipped; at or before the query if causal)."""
+    bl = np.clip(c.edge_meta[:, 4], 0, c.block_size).astype(np.int64)
+    if causal:
+        qpos = c.query_positions()
+        lim = (qpos[c.edge_meta[:, 0]].astype(np.int64)
+               - c.edge_meta[:, 2].astype(np.int64) * c.block_size + 1)
+        bl = np.clip(np.minimum(bl, lim), 0, None)
+    return bl
+
+
+def sparse_config(name, c):
+    P = c.num_edges * c.qhead
+    flops = 4.0 * c.head_dim * c.qhead * float(sparse_keys(c, name == "block_sparse_causal").sum())
+    compulsory = (c.k_pages.nbytes + c.v_pages.nbytes + c.q.nbytes + P * (c.head_dim + 2) * 4)
+    return {"workload": name, "queries": int(c.q.shape[0]), "edges": c.num_edges,
+            "partials": P, "hq": c.hq, "hkv": c.hkv, "head_dim": c.head_dim,
+            "block": c.block_size, "flops_per_step": flops,
+            "partials_compulsory_bytes": compulsory,
+            "l2": "no flush: K/V pages %.2f GB > L2" % ((c.k_pages.nbytes + c.v_pages.nbytes) / 1e9)}
+
+
+def append_config(c):
+    byts = c.batch * c.seq_len * c.kv_num_heads * c.head_size * 2 * 4 + c.seq_len * c.rotary_dim * 2
+    return {"workload": "append_prompt", "batch": 4, "seq_len": 512, "kv_num_heads": 8,
+            "head_size": 128, "rotary_dim": 128, "bytes_per_step": byts,
+            "l2": "inputs %.1f MB < L2: numbers include L2 hits" % (byts / 1e6)}
+
+
+def workload_config(name, case):
+    if name in ("block_sparse", "block_sparse_f16", "block_sparse_causal"):
+        return sparse_config(name, case)
+    if name == "append_prompt":
+        return append_config(case)
+    return paged_config(name, case)
+
+
 def setup_paged(name, args):
     from paged_kv_cache_231_gb300 import binding as B
     from paged_kv_cache_231_gb300 import workloads as wl
     lib = B.load_library()
     rope = name == "llama8b_decode_rope"
-    case = wl.llama8b_decode(rotary=rope) if name.startswith("llama8b_decode") \
-        else wl.varlen_mixed()
+    case = case_for(name)
     # RoPE variant: new keys and every query head rotated at the token's position
     rot = dict(cos_cache=to_dev(case.cos_cache), sin_cache=to_dev(case.sin_cache),
                rotary_dim=case.rotary_dim, rotary_query=True) if rope else {}
@@ -299,11 +377,18 @@ def setup_paged(name, args):
     w.case, w.step, w.e2e_step, w.h2d, w.d2h = case, step, e2e_step, h2d, d2h
     w.status = status
     w.check = lambda: int(status.item())
-    if name.startswith("llama8b_decode"):
+    w.metric, w.unit, w.higher = METRICS[name]
+    w.config = paged_config(name, case)
+    if name == "tiny_decode":
+        # latency: one call's device time; the whole call is one single-pass launch
         kvb, qb, ob = decode_bytes(case)
-        w.metric, w.unit, w.work, w.dtype = METRIC, "GB/s", (kvb + qb + ob) / 1e9, "f16"
-        if rope:
-            w.metric = METRIC + ", RoPE on new keys and queries"
+        w.work, w.dtype, w.tokens = None, "f16", case.num_tokens
+        w.dominant, w.dom_work, w.bound, w.dom_unit = "single_pass", (kvb + qb + ob) / 1e9, \
+            "hbm", "GB/s"
+        w.traffic_summary, w.traffic_sources = None, []
+    elif name.startswith("llama8b_decode"):
+        kvb, qb, ob = decode_bytes(case)
+        w.work, w.dtype = (kvb + qb + ob) / 1e9, "f16"
         w.tokens = case.num_tokens
         # the persistent attention kernel reads K/V and Q and writes O (fused combine)
         w.dominant, w.dom_work, w.bound = "attention", (kvb + qb + ob) / 1e9, "hbm"
@@ -311,24 +396,13 @@ def setup_paged(name, args):
         w.traffic_summary, w.traffic_sources = "attention_llama8b_decode.md", ATTN_SOURCES
         if rope:   # the summary's counters were taken on the unrotated workload
             w.traffic_summary = None
-        w.config = {"workload": name, "batch": case.batch, "tokens": case.num_tokens,
-                    "num_heads": 32, "kv_num_heads": 8, "head_size": 128, "block_size": 16,
-                    "context": "U[512,8192]", "mean_context": float(case.context_lengths().mean()),
-                    "kv_bytes_per_step": kvb, "bytes_per_step": kvb + qb + ob,
-                    "l2": "no flush: the KV pool (%.2f GB) is larger than L2 (129 MB)"
-                          % ((kc.numel() + vc.numel()) * 2 / 1e9)}
     else:
         fl = prefill_flops(case)
-        w.metric = "varlen prefill+decode attention TFLOP/s (causal pairs)"
-        w.unit, w.work, w.dtype = "TFLOP/s", fl / 1e12, "f16"
+        w.work, w.dtype = fl / 1e12, "f16"
         w.tokens = case.num_tokens
         # prefill tiles run in the tensor-core kernel (decode tokens in the attention one)
         w.dominant, w.dom_work, w.bound, w.dom_unit = "prefill_tc", fl / 1e12, "tensor", "TFLOP/s"
         w.traffic_summary, w.traffic_sources = "prefill_tc_varlen_mixed.md", ATTN_SOURCES
-        w.config = {"workload": "varlen_mixed", "batch": case.batch, "tokens": case.num_tokens,
-                    "num_heads": 32, "kv_num_heads": 8, "head_size": 128, "block_size": 32,
-                    "flops_per_step": fl,
-                    "l2": "no flush: KV pool %.2f GB > L2" % ((kc.numel() + vc.numel()) * 2 / 1e9)}
     w.launches_per_step = None
     return w
 
@@ -338,7 +412,8 @@ def setup_sparse(args, f16=False, causal=False):
     from paged_kv_cache_231_gb300 import workloads as wl
     import ctypes
     lib = B.load_library()
-    c = wl.block_sparse(dtype=np.float16 if f16 else np.float32)
+    name = "block_sparse_causal" if causal else ("block_sparse_f16" if f16 else "block_sparse")
+    c = case_for(name)
     q, kp, vp = to_dev(c.q), to_dev(c.k_pages), to_dev(c.v_pages)
     em, bt, so = to_dev(c.edge_meta), to_dev(c.block_tables), to_dev(c.seg_offsets)
     # right-aligned causal: keys after the query's position take no part
@@ -366,43 +441,30 @@ def setup_sparse(args, f16=False, causal=False):
         if st != 0:
             raise B.PagedKVError("sparse step", st)
 
-    bl = np.clip(c.edge_meta[:, 4], 0, c.block_size).astype(np.int64)
-    if causal:   # keys at or before the query's position
-        lim = qpos[c.edge_meta[:, 0]].astype(np.int64) - c.edge_meta[:, 2].astype(np.int64) * c.block_size + 1
-        bl = np.clip(np.minimum(bl, lim), 0, None)
-    flops = 4.0 * c.head_dim * c.qhead * float(bl.sum())
     w = Workload()
+    w.config = sparse_config(name, c)
+    flops = w.config["flops_per_step"]
     w.case, w.step, w.e2e_step, w.h2d, w.d2h = c, step, None, 0, 0
     w.check = lambda: 0
-    w.metric = "block-sparse partials+combine %s TFLOP/s%s" % (
-        "fp16" if f16 else "fp32", ", right-aligned causal" if causal else "")
-    w.unit, w.work, w.dtype, w.tokens = "TFLOP/s", flops / 1e12, "f16" if f16 else "f32", \
-        c.q.shape[0]
+    w.metric, w.unit, w.higher = METRICS[name]
+    w.work, w.dtype, w.tokens = flops / 1e12, "f16" if f16 else "f32", c.q.shape[0]
     # the partials run on the tensor core (3xTF32 for fp32 inputs: about 0.24 ms of tf32
     # work at this size; kind::f16 for fp16), so their roofline is HBM: K/V pool read once,
     # Q once, partials (fp32) written once
-    compulsory = (c.k_pages.nbytes + c.v_pages.nbytes + c.q.nbytes + P * (c.head_dim + 2) * 4)
+    compulsory = w.config["partials_compulsory_bytes"]
     w.dominant, w.dom_work, w.bound, w.dom_unit = "sparse_partials", compulsory / 1e9, "hbm", "GB/s"
     w.traffic_summary, w.traffic_sources = "sparse_partials_block_sparse.md", SPARSE_SOURCES
     if f16:
         w.traffic_summary, w.traffic_sources = "sparse_tc16_block_sparse_f16.md", SPARSE16_SOURCES
     if causal:   # the committed counters are for the unmasked workload
         w.traffic_summary = None
-    w.config = {"workload": "block_sparse_causal" if causal else
-                ("block_sparse_f16" if f16 else "block_sparse"),
-                "queries": int(c.q.shape[0]), "edges": c.num_edges,
-                "partials": P, "hq": c.hq, "hkv": c.hkv, "head_dim": c.head_dim,
-                "block": c.block_size, "flops_per_step": flops,
-                "partials_compulsory_bytes": compulsory,
-                "l2": "no flush: K/V pages %.2f GB > L2"
-                      % ((kp.numel() + vp.numel()) * kp.element_size() / 1e9)}
     return w
 
 
 def setup_append(args):
     from paged_kv_cache_231_gb300 import binding as B
     from paged_kv_cache_231_gb300 import workloads as wl
-    c = wl.append_rotary(2, mode="prompt", interleaved=False)
+    c = case_for("append_prompt")
     src, pk, pv = to_dev(c.source), to_dev(c.present_key), to_dev(c.present_value)
     ts, kt = to_dev(c.total_sequence_length), to_dev(c.key_total_sequence_lengths)
     cos, sin = to_dev(c.cos_cache), to_dev(c.sin_cache)
@@ -425,13 +487,12 @@ def setup_append(args):
     w = Workload()
     w.case, w.step, w.e2e_step, w.h2d, w.d2h = c, step, None, 0, 0
     w.check = lambda: 0
-    w.metric, w.unit, w.work, w.dtype = "KV append+RoPE GB/s (prompt)", "GB/s", byts / 1e9, "f16"
+    w.metric, w.unit, w.higher = METRICS["append_prompt"]
+    w.work, w.dtype = byts / 1e9, "f16"
     w.tokens = c.batch * c.seq_len
     w.dominant, w.dom_work, w.bound, w.dom_unit = "append", byts / 1e9, "hbm", "GB/s"
     w.traffic_summary, w.traffic_sources = None, []
-    w.config = {"workload": "append_prompt", "batch": 4, "seq_len": 512, "kv_num_heads": 8,
-                "head_size": 128, "rotary_dim": 128, "bytes_per_step": byts,
-                "l2": "inputs %.1f MB < L2: numbers include L2 hits" % (byts / 1e6)}
+    w.config = append_config(c)
     return w
 
 
@@ -439,21 +500,33 @@ def setup_append(args):
 _CASES = {}
 
 
-def oracle_sample(name, seconds):
-    """Time the CPU oracle on whole sequences of the workload until `seconds` of CPU
-    work are spent; returns (units/s in the workload's unit, description)."""
-    from oracle import pagedkv_oracle as orc
+def case_for(name):
+    """The seeded input of a workload, drawn once per process (numpy, host memory)."""
     from paged_kv_cache_231_gb300 import workloads as wl
-    if name not in _CASES:   # inputs are drawn once, outside the timed sample
+    if name not in _CASES:
         _CASES[name] = {"llama8b_decode": wl.llama8b_decode,
                         "llama8b_decode_rope": lambda: wl.llama8b_decode(rotary=True),
                         "varlen_mixed": wl.varlen_mixed,
                         "block_sparse": wl.block_sparse,
                         "block_sparse_f16": lambda: wl.block_sparse(dtype=np.float16),
                         "block_sparse_causal": wl.block_sparse,
-                        "append_prompt": lambda: wl.append_rotary(2, mode="prompt")}[name]()
-    if name in ("llama8b_decode", "llama8b_decode_rope", "varlen_mixed"):
-        case = _CASES[name]
+                        "append_prompt": lambda: wl.append_rotary(2, mode="prompt",
+                                                                  interleaved=False),
+                        "tiny_decode": wl.tiny_decode}[name]()
+    return _CASES[name]
+
+
+def oracle_sample(name, seconds):
+    """Time the CPU oracle on whole sequences (edge batches) of the workload until
+    `seconds` of wall time are spent. Returns (value in the workload's unit, tokens/s or
+    None, description, effective cores = process CPU time / wall time)."""
+    from oracle import pagedkv_oracle as orc
+    case = case_for(name)
+    cpu0, wall0 = time.process_time(), time.perf_counter()
+
+    def busy():   # cores kept busy since the sample began: CPU time / wall time
+        return (time.process_time() - cpu0) / max(time.perf_counter() - wall0, 1e-9)
+    if name in ("llama8b_decode", "llama8b_decode_rope", "varlen_mixed", "tiny_decode"):
         D, Hkv, Hq = case.head_size, case.kv_num_heads, case.num_heads
         done_work, done_tok, spent, seqs = 0.0, 0, 0.0, 0
         for b in range(case.batch):
@@ -468,23 +541,23 @@ def oracle_sample(name, seconds):
             spent += time.perf_counter() - t0
             seqs += 1
             done_tok += sub.num_tokens
-            if name != "varlen_mixed":
+            if name == "varlen_mixed":
+                done_work += prefill_flops(sub) / 1e12
+            else:
                 kvb, qb, ob = decode_bytes(sub)
                 done_work += (kvb + qb + ob) / 1e9
-            else:
-                done_work += prefill_flops(sub) / 1e12
-            if spent >= seconds:
+            if spent >= seconds and name != "tiny_decode":
                 break
+        cores = busy()
+        if name == "tiny_decode":   # the whole call, every sequence: microseconds
+            return spent * 1e6, done_tok / spent, \
+                f"the whole call ({seqs} sequences), {spent * 1e3:.2f} ms", cores
         return done_work / spent, done_tok / spent, \
-            f"{seqs} of {case.batch} sequences, whole (scatter + attention), {spent:.1f} s"
+            f"{seqs} of {case.batch} sequences, whole (scatter + attention), {spent:.1f} s", cores
     if name in ("block_sparse", "block_sparse_f16", "block_sparse_causal"):
-        c = _CASES[name]
+        c = case
         qpos = c.query_positions() if name == "block_sparse_causal" else None
-        keys = np.clip(c.edge_meta[:, 4], 0, c.block_size).astype(np.int64)
-        if qpos is not None:
-            lim = (qpos[c.edge_meta[:, 0]].astype(np.int64)
-                   - c.edge_meta[:, 2].astype(np.int64) * c.block_size + 1)
-            keys = np.clip(np.minimum(keys, lim), 0, None)
+        keys = sparse_keys(c, qpos is not None)
         rng = np.random.default_rng(0)
         order = rng.permutation(c.num_edges)
         spent, n, fl = 0.0, 0, 0.0
@@ -501,8 +574,10 @@ def oracle_sample(name, seconds):
             spent = time.perf_counter() - t0
             if spent >= seconds:
                 break
-        return fl / 1e12 / spent, None, f"{n} random edges of {c.num_edges}, {spent:.1f} s"
-    c = _CASES[name]
+        cores = busy()
+        return fl / 1e12 / spent, None, f"{n} random edges of {c.num_edges}, {spent:.1f} s", \
+            cores
+    c = case
     t0 = time.perf_counter()
     orc.kv_append_rotary(c.source, c.value, packed=True, num_heads=c.num_heads,
                          kv_num_heads=c.kv_num_heads, head_size=128, batch=c.batch,
@@ -512,8 +587,39 @@ def oracle_sample(name, seconds):
                          interleaved=False, present_key=c.present_key,
                          present_value=c.present_value)
     spent = time.perf_counter() - t0
+    cores = busy()
     byts = c.batch * c.seq_len * c.kv_num_heads * 128 * 2 * 4 + c.seq_len * 128 * 2
-    return byts / 1e9 / spent, None, f"whole prompt append, {spent:.1f} s"
+    return byts / 1e9 / spent, None, f"whole prompt append, {spent:.1f} s", cores
+
+
+def oracle_single_core(name, seconds):
+    """The same oracle sample in a child process confined to one CPU with one BLAS
+    thread; None if the child fails."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+
+    def pin():   # before the child starts: every thread it creates inherits one CPU
+        try:
+            os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+        except (AttributeError, OSError):
+            pass
+
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-core",
+                            "--workload", name, "--cpu-seconds", str(seconds)],
+                           env=env, capture_output=True, text=True, timeout=600,
+                           preexec_fn=pin)
+        line = [x for x in r.stdout.splitlines() if x.startswith("{")]
+        return json.loads(line[-1]) if r.returncode == 0 and line else None
+    except (OSError, subprocess.SubprocessError, ValueError):
+        return None
+
+
+def one_core_child(args):
+    """Entry of the single-CPU child (started pinned to one CPU): run the sample, print
+    JSON."""
+    v, tps, desc, cores = oracle_sample(args.workload, args.cpu_seconds)
+    print(json.dumps({"value": v, "unit": METRICS[args.workload][1], "cores": 1,
+                      "cpu_per_wall": cores, "sample": desc, "tokens_per_s": tps}))
 
 
 def _subcase(case, b):
@@ -537,50 +643,58 @@ def _subcase(case, b):
         rotary_interleaved=case.rotary_interleaved)
 
 
-def cpu_cores():
+def cpus_available():
     try:
-        return int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
-    except ValueError:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
         return os.cpu_count() or 1
+
+
+def cpu_baseline(name, seconds, value=None, desc=None, cores=None, tps=None):
+    """cpu_baseline object: the oracle on all host cores (cores = CPU time / wall time of
+    the sample, i.e. the cores it kept busy) plus the same sample on one core."""
+    if value is None:
+        value, tps, desc, cores = oracle_sample(name, seconds)
+    out = {"value": value, "unit": METRICS[name][1], "cores": round(cores, 2),
+           "cpus_available": cpus_available(), "kind": "oracle", "sample": desc}
+    if tps is not None:
+        out["tokens_per_s"] = tps
+    one = oracle_single_core(name, seconds)
+    if one is not None:
+        out["single_core"] = one
+    return out
 
 
 # ----------------------------------------------------------------------------- main
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    unit = {"llama8b_decode": "GB/s", "llama8b_decode_rope": "GB/s", "varlen_mixed": "TFLOP/s",
-            "block_sparse": "TFLOP/s", "block_sparse_f16": "TFLOP/s",
-            "block_sparse_causal": "TFLOP/s",
-            "append_prompt": "GB/s"}[args.workload]
-    metric = {"llama8b_decode": METRIC,
-              "llama8b_decode_rope": METRIC + ", RoPE on new keys and queries",
-              "varlen_mixed": "varlen prefill+decode attention TFLOP/s (causal pairs)",
-              "block_sparse": "block-sparse partials+combine fp32 TFLOP/s",
-              "block_sparse_f16": "block-sparse partials+combine fp16 TFLOP/s",
-              "block_sparse_causal":
-                  "block-sparse partials+combine fp32 TFLOP/s, right-aligned causal",
-              "append_prompt": "KV append+RoPE GB/s (prompt)"}[args.workload]
+    metric, unit, higher = METRICS[args.workload]
     # each step is a bounded sample (at least one whole sequence / edge batch); the
     # whole run is kept to about two minutes of CPU work
     per = min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup))
-    vals, descs, toks, walls = [], [], [], []
+    vals, descs, toks, walls, cores = [], [], [], [], []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        v, tps, desc = oracle_sample(args.workload, per)
+        v, tps, desc, cr = oracle_sample(args.workload, per)
         if i >= args.warmup:
             walls.append(time.perf_counter() - t0)
             vals.append(v)
             descs.append(desc)
             toks.append(tps)
+            cores.append(cr)
     value = statistics.median(vals)
     line = {"impl": "reference", "metric": metric, "value": value, "unit": unit,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * statistics.median(walls), "higher_is_better": True,
+            "ms_per_step": 1e3 * statistics.median(walls), "higher_is_better": higher,
             "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
-            "cpu_baseline": {"value": value, "unit": unit, "cores": cpu_cores(),
-                             "kind": "oracle", "sample": descs[-1]},
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy draws, N(0,1))",
+            "config": dict(workload_config(args.workload, case_for(args.workload)),
+                           parallelism=f"replicas{world}"),
+            "cpu_baseline": {"value": value, "unit": unit,
+                             "cores": round(statistics.median(cores), 2),
+                             "cpus_available": cpus_available(), "kind": "oracle",
+                             "sample": descs[-1]},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     if toks[-1] is not None:
@@ -588,8 +702,20 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_for(fn, seconds):
+    """Untimed steps for about `seconds` of wall time (synchronised every 8 steps)."""
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(8):
+            fn()
+        torch.cuda.synchronize()
+
+
 def main():
     args = parse_args()
+    if args.oracle_one_core:
+        one_core_child(args)
+        return
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank)
@@ -606,7 +732,8 @@ def main():
              "block_sparse": lambda: setup_sparse(args),
              "block_sparse_f16": lambda: setup_sparse(args, f16=True),
              "block_sparse_causal": lambda: setup_sparse(args, causal=True),
-             "append_prompt": lambda: setup_append(args)}[args.workload]
+             "append_prompt": lambda: setup_append(args),
+             "tiny_decode": lambda: setup_paged("tiny_decode", args)}[args.workload]
     w = setup()
     hbm, bf16, bf16_sus, peak_kind = measured_peaks()
 
@@ -615,12 +742,21 @@ def main():
     torch.cuda.synchronize()
     assert w.check() == 0, "device status flagged invalid data"
 
-    # timed region: K steps exactly as a caller runs them (no extra events)
-    launches0 = B.pkv_launch_count()
+    # timed region: K steps exactly as a caller runs them (no extra events). The clock
+    # sampler runs over a window of the same steps around it (half a second before and
+    # after), because a timed region of a few milliseconds is shorter than the sampling
+    # period of nvidia-smi
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    t_win = time.perf_counter()
+    run_for(w.step, CLOCK_PAD_S)
+    launches0 = B.pkv_launch_count()
     ms = timed_loop(w.step, args.steps, world)
-    clk = clocks.stop() if clocks else None
     launches = B.pkv_launch_count() - launches0
+    run_for(w.step, CLOCK_PAD_S)
+    clk = clocks.stop() if clocks else None
+    if clk is not None:
+        clk["window_s"] = round(time.perf_counter() - t_win, 3)
+        clk["window"] = "the same steps, run continuously before, during and after the timed region"
     # second timed pass of the same K steps with a CUDA event pair around every kernel
     # on its launching stream: per-kernel device time for the roofline (events between
     # kernels stop the prefill kernel's early start, so this pass is not the value)
@@ -631,7 +767,7 @@ def main():
     dom_ms, dom_n = B.pkv_profiler_query(w.dominant)
     kernel_ms = {k: B.pkv_profiler_query(k) for k in
                  ("prologue", "attention", "prefill_tc", "decode_split", "combine",
-                  "scatter", "sparse_group", "sparse_partials", "append")}
+                  "single_pass", "scatter", "sparse_group", "sparse_partials", "append")}
     B.pkv_profiler_reset()
 
     e2e = None
@@ -639,17 +775,21 @@ def main():
         for _ in range(3):
             w.e2e_step()
         e2e_ms = timed_loop(w.e2e_step, args.e2e_steps or args.steps, world)
-        e2e = {"value": world * w.work / (e2e_ms / 1e3), "unit": w.unit,
+        e2e_v = e2e_ms * 1e3 if w.work is None else world * w.work / (e2e_ms / 1e3)
+        e2e = {"value": e2e_v, "unit": w.unit,
                "h2d_bytes_per_step": w.h2d, "d2h_bytes_per_step": w.d2h,
                "ms_per_step": e2e_ms}
 
-    value = world * w.work / (ms / 1e3)
+    # w.work None: a latency workload, value = microseconds per call (max over ranks)
+    value = ms * 1e3 if w.work is None else world * w.work / (ms / 1e3)
     dom_avg_ms = dom_ms / max(1, dom_n)
     achieved = w.dom_work / (dom_avg_ms / 1e3) if dom_n else None
     if w.bound == "hbm":
         peak, punit = hbm, "GB/s"
     elif w.bound == "tensor":
-        peak, punit = bf16_sus, "TFLOP/s"
+        # the prefill kernel is timed alone in sub-millisecond steps: the burst rate
+        peak, punit = bf16, "TFLOP/s"
+        peak_kind += " dense bf16 burst rate (fp16 has the same dense rate)"
     else:
         sm_mhz = 2070.0
         peak, punit = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12, "TFLOP/s"
@@ -660,7 +800,7 @@ def main():
         return
     line = {"metric": w.metric, "value": value, "unit": w.unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "higher_is_better": w.higher, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded numpy draws, N(0,1))",
             "config": dict(w.config, parallelism=f"replicas{world}"),
             "tokens_per_s": world * w.tokens / (ms / 1e3)}
@@ -677,11 +817,7 @@ def main():
     line["clocks"] = clk
     line["e2e"] = e2e
     if world == 1 and args.cpu_seconds > 0:
-        v, tps, desc = oracle_sample(args.workload, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": w.unit, "cores": cpu_cores(),
-                                "kind": "oracle", "sample": desc}
-        if tps is not None:
-            line["cpu_baseline"]["tokens_per_s"] = tps
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -72,9 +72,11 @@ typedef enum pkv_status {
                                     unmapped; an edge whose q_idx, head, batch or
                                     block lies outside the tensors gets the empty
                                     partial */
-#define PKV_DEV_TIMEOUT 32u      /* a bounded wait on the tensor core gave up: the
-                                    affected prefill tile's output is not written and
-                                    the kernel freed its resources and returned */
+#define PKV_DEV_TIMEOUT 32u      /* a bounded wait of a tensor-core kernel gave up: the
+                                    outputs that CTA had not yet written (prefill tiles,
+                                    block-sparse partials) are not written; it waited
+                                    (bounded) for what it had issued, freed its tensor
+                                    memory and returned */
 
 typedef enum pkv_dtype { PKV_F16 = 1, PKV_BF16 = 2, PKV_F32 = 3, PKV_I32 = 4 } pkv_dtype;
 
@@ -184,6 +186,12 @@ int pkv_paged_attention_workspace_size(const pkv_paged_attention_args* args,
  *      head hq uses kv head hq / (num_heads / kv_num_heads); tiles write the output
  *      directly, split items write fp32 (o, m, l) partials to the workspace;
  *   4. combine: LSE merge of the partials into output.
+ * When every sequence has one split (the resolved split bound is 1: short caches under
+ * PKV_SPLIT_AUTO, max_splits = 1, fixed_splits = 1, or a manifest numSplits of 1) and
+ * the call is small (ceil(num_tokens * group / 16) * max_blocks * block_size <= 2^18),
+ * the manifest's non-split form (ScatterKV then Attend) runs as ONE launch: each CTA
+ * scatters one (sequence, kv head)'s new rows and attends all of that pair's query rows;
+ * no partials, no combine. Larger one-split calls skip only the combine.
  * workspace: device memory of at least pkv_paged_attention_workspace_size bytes,
  * 256-byte aligned, owned by the caller, contents need not be initialised and are
  * scratch after the call. Supported: head_size in {64, 128}; num_heads/kv_num_heads
@@ -202,7 +210,14 @@ int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
  *     PKV_STATIC_WORKSPACE_BYTES.
  *   - The first call on a device looks up the array's device address (a runtime
  *     call, once per device, with that device current): make that first call before
- *     any stream capture.
+ *     any stream capture. With CUDA's default lazy module loading that first call is
+ *     also when the library's device code is loaded on the device and the array's
+ *     memory is committed: make it before a caller's own pool reserves the device's
+ *     memory (or load modules eagerly, CUDA_MODULE_LOADING=EAGER), else it fails with
+ *     PKV_ERR_LAUNCH.
+ *   - The address is cached per device for the life of the process: a device reset
+ *     (cudaDeviceReset) after the first call is not supported, because the reloaded
+ *     module may place the array elsewhere.
  *   - All calls on a device share the one array and it keeps the last call's contents;
  *     nothing in it needs to start at zero. Calls whose work overlaps on the GPU (other
  *     streams, other threads) race on it: serialise them. */
@@ -397,6 +412,19 @@ int64_t pkv_launch_count(void);
  * time (ms) and launch count of `kernel` ("scatter", "append", "plan", "decode",
  * "prefill", "combine", "sparse_group", "sparse_partials"). Not thread-safe. */
 void pkv_profiler_enable(int on);
+
+/* Testing hook for the give-up path of the tensor-core kernels' bounded waits (the
+ * tcgen05 prefill and the two block-sparse partial kernels). The pages have no
+ * counterpart. max_polls replaces the default poll bound of every such wait (0 restores
+ * the default); with withhold_first_copy != 0 (which needs max_polls > 0) every CTA of
+ * those kernels announces its first bulk copy (the first K box of its first prefill
+ * tile, or its first K/V staging) on the copy's barrier but never issues it, so the wait
+ * for it gives up with no copy or MMA of that data in flight. A CTA whose wait gave up
+ * ORs PKV_DEV_TIMEOUT into device_status, waits (bounded) for what it did issue, frees
+ * its tensor memory and returns; outputs it had not written stay unwritten. Applies to
+ * calls made after it, process-wide; not thread-safe; for tests only. Returns PKV_OK,
+ * or PKV_ERR_SHAPE for withhold_first_copy without a bound. */
+int pkv_testing_wait_limit(uint32_t max_polls, int32_t withhold_first_copy);
 void pkv_profiler_reset(void);
 int pkv_profiler_query(const char* kernel, double* total_ms, int64_t* launches);
 

@@ -8,7 +8,6 @@ raises. Function names match the C entry points.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from typing import Optional
 
@@ -146,7 +145,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
              [ctypes.POINTER(SparseArgs), ctypes.POINTER(ctypes.c_size_t)]),
             ("pkv_sparse_attention_partials", [ctypes.POINTER(SparseArgs), c_vp,
                                                ctypes.c_size_t, c_vp]),
-            ("pkv_combine_partials", [ctypes.POINTER(CombineArgs), c_vp])):
+            ("pkv_combine_partials", [ctypes.POINTER(CombineArgs), c_vp]),
+            ("pkv_testing_wait_limit", [ctypes.c_uint32, c_i32])):
         fn = getattr(lib, name)
         fn.restype = c_i32
         fn.argtypes = args
@@ -540,8 +540,12 @@ def pkv_profiler_query(kernel: str):
     return float(ms.value), int(n.value)
 
 
-def default_scale(head_size: int) -> float:
-    return 1.0 / math.sqrt(head_size)
+def pkv_testing_wait_limit(max_polls: int = 0, withhold_first_copy: bool = False):
+    """Testing hook of the tensor-core kernels' bounded waits (see pagedkv.h): a lower
+    poll bound and, optionally, a withheld first bulk copy per CTA so that a wait gives
+    up. pkv_testing_wait_limit() restores the defaults."""
+    _check("pkv_testing_wait_limit",
+           load_library().pkv_testing_wait_limit(int(max_polls), 1 if withhold_first_copy else 0))
 
 
 def pkv_paged_attention_static_workspace(query, key, value, key_cache, value_cache,

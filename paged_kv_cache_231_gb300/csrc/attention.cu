@@ -18,8 +18,9 @@
 //     same persistent CTAs from an atomic counter, so K/V is read once per tile. For
 //     head size 128 a tile is 128 rows on the 5th-generation tensor core: Q, K and V in
 //     128-byte-swizzled shared memory, the S and O accumulators and P in tensor memory,
-//     tcgen05.mma issued by one thread and completed through mbarriers, one softmax
-//     thread per row reading its TMEM lane and keeping the row sum in a register;
+//     tcgen05.mma issued by two threads (S = Q K^T on one, O += P V on the other) and
+//     completed through mbarriers, one softmax thread per row reading its TMEM lane and
+//     keeping the row sum in a register;
 //   * decode and the head-size-64 tiles run QK^T and PV on mma.sync m16n8k16 (fp16 in,
 //     fp32 accumulate) with the score accumulators reused in registers as the A
 //     operand of PV. Softmax works in base 2 (scores pre-scaled by log2 e).
@@ -703,9 +704,10 @@ enum TcBar {  // mbarrier slots
   kBarSFull0 = 11,   // + buffer, count 1: S_j in TMEM
   kBarPFull = 13,    // count 4 (one per softmax warp): softmax wrote P_j to TMEM
   kBarODone = 14,    // count 1: O += P_j V_j completed
-  kBarDrain = 15,    // count 1: MMAs in flight when a wait gave up
+  kBarDrain = 15,    // count 1: S = Q K^T MMAs in flight when a wait gave up
   kBarSEmpty0 = 16,  // + buffer, count 4: softmax has read S_j out of the buffer
-  kNumBars = 18
+  kBarDrainPv = 18,  // count 1: O += P V MMAs in flight when a wait gave up
+  kNumBars = 19
 };
 static_assert(kNumBars * 8 <= 256, "mbarrier slots");
 // TMEM columns: S_j in buffer j % 2, the O accumulator, and P_j as fp16 pairs (two keys
@@ -713,9 +715,10 @@ static_assert(kNumBars * 8 <= 256, "mbarrier slots");
 constexpr uint32_t kTmS = 0, kTmO = 256, kTmP = 448;
 constexpr int kKStages = 2;        // K ring depth
 constexpr int kVStages = 3;        // V ring depth: V_j streams in once O += P_{j-3} V_{j-3} is done
-constexpr uint32_t kTcWaitTries = 1u << 22;
-constexpr int kTcThreads = 224;
-constexpr int kMmaThread = 128;    // lane 0 of warp 4
+constexpr uint32_t kTcWaitTries = 1u << 22;   // default bound of each wait (polls)
+constexpr int kTcThreads = 256;
+constexpr int kMmaThread = 128;    // lane 0 of warp 4: S = Q K^T
+constexpr int kPvThread = 224;     // lane 0 of warp 7: O += P V
 constexpr int kKLoaderWarp = 5;
 constexpr int kVLoaderWarp = 6;
 constexpr float kTcRescale = 8.f;  // log2 of the largest weight a stale max may give
@@ -728,10 +731,15 @@ __device__ __forceinline__ void mbar_arrive_cp_async(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar))
                : "memory");
 }
+// polls a wait of this kernel may take before it gives up
+__device__ __forceinline__ uint32_t tc_tries(const AttnParams& p) {
+  return p.wait_tries ? p.wait_tries : kTcWaitTries;
+}
 // bounded wait that also gives up when another thread of the CTA already did
-__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                        uint32_t tries) {
   const uint32_t addr = smem_u32(bar);
-  for (uint32_t i = 0; i < kTcWaitTries; ++i) {
+  for (uint32_t i = 0; i < tries; ++i) {
     uint32_t done;
     asm volatile(
         "{\n"
@@ -802,6 +810,9 @@ __device__ void tc_load_k(const AttnParams& p, const TcMaps& maps, unsigned char
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const int lane = threadIdx.x & 31;
   const int R = p.tc_rows;
+  // testing hook: the CTA's first K box is announced but never copied, so the MMA's wait
+  // for it gives up (no copy or MMA of that block is in flight when it does)
+  const bool withhold = p.withhold_copy && k_use[0] == 0;
   if (lane == 0) {
     // rows past the tile's positions hold other tokens (or zeros past the last token)
     // and are never written out
@@ -812,7 +823,7 @@ __device__ void tc_load_k(const AttnParams& p, const TcMaps& maps, unsigned char
   }
   for (int j = 0, s = 0; j < t.nblk; ++j, s = s + 1 == kKStages ? 0 : s + 1) {
     const TcBox x = tc_box(p, t, j, lane, bad);
-    const bool ok = k_use[s] == 0 || tc_wait(bars + kBarKEmpty0 + s, (k_use[s] - 1) & 1u, abort);
+    const bool ok = k_use[s] == 0 || tc_wait(bars + kBarKEmpty0 + s, (k_use[s] - 1) & 1u, abort, tc_tries(p));
     if (!__all_sync(0xffffffffu, ok)) return;
     ++k_use[s];
     const uint32_t bits = __ballot_sync(0xffffffffu, x.mapped);
@@ -820,7 +831,7 @@ __device__ void tc_load_k(const AttnParams& p, const TcMaps& maps, unsigned char
       tc::mbar_arrive_expect_tx(bars + kBarKFull0 + s, (uint32_t)__popc(bits) * R * 256u);
     __syncwarp();
     unsigned char* Ks = sm + TcLayout::kK + s * 32768;
-    if (x.mapped) {
+    if (x.mapped && !(withhold && j == 0)) {
       tc::tma_load_3d(Ks + lane * R * 128, &maps.k, 0, t.h, x.row, bars + kBarKFull0 + s);
       tc::tma_load_3d(Ks + 16384 + lane * R * 128, &maps.k, 64, t.h, x.row,
                       bars + kBarKFull0 + s);
@@ -841,7 +852,7 @@ __device__ void tc_load_v(const AttnParams& p, const TcMaps& maps, unsigned char
   for (int j = 0, s = 0; j < t.nblk; ++j, s = s + 1 == kVStages ? 0 : s + 1) {
     const TcBox x = tc_box(p, t, j, lane, unmapped);
     const bool whole = x.mapped && x.key0 + R <= t.kend;
-    const bool ok = v_use[s] == 0 || tc_wait(bars + kBarVEmpty0 + s, (v_use[s] - 1) & 1u, abort);
+    const bool ok = v_use[s] == 0 || tc_wait(bars + kBarVEmpty0 + s, (v_use[s] - 1) & 1u, abort, tc_tries(p));
     if (!__all_sync(0xffffffffu, ok)) return;
     ++v_use[s];
     const uint32_t bits = __ballot_sync(0xffffffffu, whole);
@@ -886,70 +897,43 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
-// Warp 4, lane 0: the MMA stream of the tile (O += P V checked first: it is on the
-// softmax's critical path, S = Q K^T runs ahead). S_jq = Q K_jq^T may be issued once K_jq
-// landed and the softmax has read S_{jq-2} out of buffer jq % 2 (SEmpty phases are counted
-// per block, across tiles, because the last two of a tile are never waited for); O += P_jp V_jp
-// once P_jp is in TMEM and V_jp landed.
-__device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
-                       uint32_t tmem, uint32_t q_use, uint32_t (&k_use)[kKStages],
-                       uint32_t (&v_use)[kVStages], uint32_t (&s_base)[2], uint32_t& blk_use) {
+// Two MMA issuers, each a thread that does nothing else: the cost of a tcgen05.mma is
+// paid by the issuing thread, so S = Q K^T and O += P V issued from separate threads
+// overlap on the tensor pipe.
+//
+// Warp 4, lane 0: S_jq = Q K_jq^T once K_jq landed and the softmax has read S_{jq-2} out
+// of buffer jq % 2 (SEmpty phases are counted per block, across tiles, because the last
+// two of a tile are never waited for).
+__device__ void tc_mma_s(const AttnParams& p, unsigned char* sm, const TcTile& t,
+                         uint32_t tmem, uint32_t q_use, uint32_t (&k_use)[kKStages],
+                         uint32_t (&s_base)[2]) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const uint32_t idesc_qk = tc::idesc_f16(128, 128, false, false);
-  const uint32_t idesc_pv = tc::idesc_f16(128, 128, false, true);
   const uint32_t qa = smem_u32(sm + TcLayout::kQ);
-  if (!tc_wait(bars + kBarQFull, q_use & 1u, abort)) return;
-  int jq = 0, jp = 0, kq = 0, vq = 0;   // kq = jq % kKStages, vq = jp % kVStages
+  if (!tc_wait(bars + kBarQFull, q_use & 1u, abort, tc_tries(p))) return;
   uint32_t idle = 0;
-  while (jp < t.nblk) {
-    bool progress = false;
-    if (jp < jq) {
-      const int s = vq;
-      if (tc::mbar_test(bars + kBarPFull, (blk_use + jp) & 1u) &&
-          tc::mbar_test(bars + kBarVFull0 + s, v_use[s] & 1u)) {
-        ++v_use[s];
-        tc::fence_async_shared();   // zero-filled value rows were written by cp.async
-        tc::fence_after_sync();
-        const uint32_t va = smem_u32(sm + TcLayout::kV + s * 32768);
+  for (int jq = 0, kq = 0; jq < t.nblk;) {
+    // buffer s was last filled with S_{jq-2}: phase s_base[s] + (jq - 2) / 2 of SEmpty_s
+    const int s = jq & 1;
+    if ((jq < 2 ||
+         tc::mbar_test(bars + kBarSEmpty0 + s, (s_base[s] + (uint32_t)((jq - 2) >> 1)) & 1u)) &&
+        tc::mbar_test(bars + kBarKFull0 + kq, k_use[kq] & 1u)) {
+      ++k_use[kq];
+      tc::fence_after_sync();
+      const uint32_t ka = smem_u32(sm + TcLayout::kK + kq * 32768);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t acc = (jp > 0 || ks > 0) ? 1u : 0u;
-          mma_f16_tmem_a(tmem + kTmO, tmem + kTmP + (uint32_t)ks * 8u,
-                         tc::smem_desc(va + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv, acc);
-        }
-        tc::commit(bars + kBarODone);
-        tc::commit(bars + kBarVEmpty0 + s);
-        ++jp;
-        vq = vq + 1 == kVStages ? 0 : vq + 1;
-        progress = true;
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        tc::mma_f16(tmem + kTmS + s * 128, tc::smem_desc(qa + koff, 16, 1024),
+                    tc::smem_desc(ka + koff, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
       }
-    }
-    if (jq < t.nblk) {
-      // buffer s was last filled with S_{jq-2}: phase s_base[s] + (jq - 2) / 2 of SEmpty_s
-      const int s = jq & 1;
-      if ((jq < 2 ||
-           tc::mbar_test(bars + kBarSEmpty0 + s, (s_base[s] + (uint32_t)((jq - 2) >> 1)) & 1u)) &&
-          tc::mbar_test(bars + kBarKFull0 + kq, k_use[kq] & 1u)) {
-        ++k_use[kq];
-        tc::fence_after_sync();
-        const uint32_t ka = smem_u32(sm + TcLayout::kK + kq * 32768);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-          tc::mma_f16(tmem + kTmS + s * 128, tc::smem_desc(qa + koff, 16, 1024),
-                      tc::smem_desc(ka + koff, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
-        }
-        tc::commit(bars + kBarSFull0 + s);
-        tc::commit(bars + kBarKEmpty0 + kq);
-        ++jq;
-        kq = kq + 1 == kKStages ? 0 : kq + 1;
-        progress = true;
-      }
-    }
-    if (progress) {
+      tc::commit(bars + kBarSFull0 + s);
+      tc::commit(bars + kBarKEmpty0 + kq);
+      ++jq;
+      kq = kq + 1 == kKStages ? 0 : kq + 1;
       idle = 0;
-    } else if (++idle >= kTcWaitTries || ((idle & 255u) == 0 && *abort)) {
+    } else if (++idle >= tc_tries(p) || ((idle & 255u) == 0 && *abort)) {
       *abort = 1;
       return;
     }
@@ -957,6 +941,39 @@ __device__ void tc_mma(const AttnParams& p, unsigned char* sm, const TcTile& t,
   // SEmpty phases of this tile: one per block read from each buffer
   s_base[0] += (uint32_t)((t.nblk + 1) >> 1);
   s_base[1] += (uint32_t)(t.nblk >> 1);
+}
+
+// Warp 7, lane 0: O += P_jp V_jp once the softmax has written P_jp to TMEM and V_jp landed.
+__device__ void tc_mma_pv(const AttnParams& p, unsigned char* sm, const TcTile& t,
+                          uint32_t tmem, uint32_t (&v_use)[kVStages], uint32_t& blk_use) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
+  const uint32_t idesc_pv = tc::idesc_f16(128, 128, false, true);
+  uint32_t idle = 0;
+  for (int jp = 0, vq = 0; jp < t.nblk;) {
+    const int s = vq;
+    if (tc::mbar_test(bars + kBarPFull, (blk_use + jp) & 1u) &&
+        tc::mbar_test(bars + kBarVFull0 + s, v_use[s] & 1u)) {
+      ++v_use[s];
+      tc::fence_async_shared();   // zero-filled value rows were written by cp.async
+      tc::fence_after_sync();
+      const uint32_t va = smem_u32(sm + TcLayout::kV + s * 32768);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t acc = (jp > 0 || ks > 0) ? 1u : 0u;
+        mma_f16_tmem_a(tmem + kTmO, tmem + kTmP + (uint32_t)ks * 8u,
+                       tc::smem_desc(va + (uint32_t)ks * 2048u, 16384, 1024), idesc_pv, acc);
+      }
+      tc::commit(bars + kBarODone);
+      tc::commit(bars + kBarVEmpty0 + s);
+      ++jp;
+      vq = vq + 1 == kVStages ? 0 : vq + 1;
+      idle = 0;
+    } else if (++idle >= tc_tries(p) || ((idle & 255u) == 0 && *abort)) {
+      *abort = 1;
+      return;
+    }
+  }
   blk_use += t.nblk;
 }
 
@@ -1010,7 +1027,7 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
     uint32_t words[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) words[i] = __ballot_sync(0xffffffffu, page && key0 + i < t.kend);
-    ok = tc_wait(bars + kBarSFull0 + s, s_use[s] & 1u, abort);
+    ok = tc_wait(bars + kBarSFull0 + s, s_use[s] & 1u, abort, tc_tries(p));
     ++s_use[s];
     ok = __all_sync(0xffffffffu, ok);   // TMEM loads below are warp-collective
     if (!ok) break;
@@ -1075,7 +1092,7 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
     l_run = l_run * alpha + (((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3])));
     // O and the P columns are free once O += P_{j-1} V_{j-1} has completed
     if (j > 0) {
-      ok = __all_sync(0xffffffffu, tc_wait(bars + kBarODone, (blk_use + j - 1) & 1u, abort));
+      ok = __all_sync(0xffffffffu, tc_wait(bars + kBarODone, (blk_use + j - 1) & 1u, abort, tc_tries(p)));
       if (!ok) break;
       tc::fence_after_sync();
       if (__any_sync(0xffffffffu, alpha != 1.f)) {   // warp-collective TMEM rescale of O
@@ -1102,7 +1119,7 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
   }
   if (ok) {
     ok = __all_sync(0xffffffffu,
-                    tc_wait(bars + kBarODone, (blk_use + t.nblk - 1) & 1u, abort));
+                    tc_wait(bars + kBarODone, (blk_use + t.nblk - 1) & 1u, abort, tc_tries(p)));
     if (ok) {
       tc::fence_after_sync();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -1155,6 +1172,7 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
     tc::mbar_init(bars + kBarPFull, 4);
     tc::mbar_init(bars + kBarODone, 1);
     tc::mbar_init(bars + kBarDrain, 1);
+    tc::mbar_init(bars + kBarDrainPv, 1);
     tc::mbar_init_fence();
     *abort = 0;
   }
@@ -1187,7 +1205,10 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
     if (tid < 128) {
       tc_softmax(p, sm, t, tmem, s_use, blk_use);
     } else if (tid == kMmaThread) {
-      tc_mma(p, sm, t, tmem, q_use, k_use, v_use, s_base, blk_use);
+      tc_mma_s(p, sm, t, tmem, q_use, k_use, s_base);
+      mma_aborted = *abort != 0;
+    } else if (tid == kPvThread) {
+      tc_mma_pv(p, sm, t, tmem, v_use, blk_use);
       mma_aborted = *abort != 0;
     } else if (warp == kKLoaderWarp) {
       tc_load_k(p, maps, sm, t, k_use, bad);
@@ -1205,18 +1226,20 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
   if (*abort) {
     // a wait gave up: let the copies and MMAs this CTA issued land before it exits
     if (tid == 0) flag_status(p.status, PKV_DEV_TIMEOUT);
-    if (tid == kMmaThread && mma_aborted) {
-      tc::commit(bars + kBarDrain);
-      tc::mbar_wait(bars + kBarDrain, 0, kTcWaitTries);
+    if ((tid == kMmaThread || tid == kPvThread) && mma_aborted) {
+      // each issuer drains its own MMAs (a commit tracks the issuing thread's MMAs)
+      uint64_t* drain = bars + (tid == kMmaThread ? kBarDrain : kBarDrainPv);
+      tc::commit(drain);
+      tc::mbar_wait(drain, 0, tc_tries(p));
     }
     if (warp == kKLoaderWarp && lane == 0) {
-      if (q_use > 0) tc::mbar_wait(bars + kBarQFull, (q_use - 1) & 1u, kTcWaitTries);
+      if (q_use > 0) tc::mbar_wait(bars + kBarQFull, (q_use - 1) & 1u, tc_tries(p));
       for (int s = 0; s < kKStages; ++s)
-        if (k_use[s] > 0) tc::mbar_wait(bars + kBarKFull0 + s, (k_use[s] - 1) & 1u, kTcWaitTries);
+        if (k_use[s] > 0) tc::mbar_wait(bars + kBarKFull0 + s, (k_use[s] - 1) & 1u, tc_tries(p));
     }
     if (warp == kVLoaderWarp && lane == 0) {
       for (int s = 0; s < kVStages; ++s)
-        if (v_use[s] > 0) tc::mbar_wait(bars + kBarVFull0 + s, (v_use[s] - 1) & 1u, kTcWaitTries);
+        if (v_use[s] > 0) tc::mbar_wait(bars + kBarVFull0 + s, (v_use[s] - 1) & 1u, tc_tries(p));
     }
   }
   cp_async_wait<0>();
@@ -1226,7 +1249,7 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
-// Persistent tensor-core prefill kernel: one CTA of 7 warps per SM, tiles from the
+// Persistent tensor-core prefill kernel: one CTA of 8 warps per SM, tiles from the
 // planner's counter.
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(AttnParams p, const __grid_constant__ TcMaps maps) {
@@ -1281,30 +1304,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attention_kernel(AttnPar
 }
 
 // ----------------------------------------------------------------------------------
-// Split mode (fixed split counts): CTA = one split of one short sequence for one kv
-// head; the 4 warps take 16 keys each of every 64-key stage and merge at the end. The
-// partials are merged by the combine kernel.
+// Rows of one (sequence, kv head) over one key range, by a CTA of 4 warps: each warp
+// takes 16 keys of every 64-key stage and the four warps' (o, m, l) are merged through
+// shared memory. Serves the split mode (one split of a short sequence per CTA, partials
+// for the combine kernel, or the output itself when every sequence has one split) and the
+// single-pass path (whole sequences, output written directly).
 // ----------------------------------------------------------------------------------
-template <int D, int NSTAGE>
-__global__ void __launch_bounds__(kTileThreads) decode_split_kernel(AttnParams p) {
+// Rows [row0, min(row0 + 16, R)) of (sequence b, kv head h): row r is query head
+// h*G + r % G of token cu0 + r / G at position P + r / G, over keys [kb, ke). kDirect:
+// the normalised fp16 output; else unnormalised partials of split `split` at slot
+// slot_base + r / G.
+template <int D, int NSTAGE, bool kDirect>
+__device__ void split_rows(const AttnParams& p, unsigned char* smem, int b, int h, int cu0,
+                           int P, int row0, int R, int kb, int ke, int slot_base, int split,
+                           bool& bad) {
   constexpr int SK = kStageKeys;
   constexpr int DN = D / 8;
-  extern __shared__ __align__(128) unsigned char smem[];
   __half* sK = reinterpret_cast<__half*>(smem);
   __half* sV = sK + NSTAGE * SK * D;
   uint8_t* sValid = reinterpret_cast<uint8_t*>(sV + NSTAGE * SK * D);
-
-  const int h = blockIdx.x % p.Hkv;
-  const int64_t item_idx = blockIdx.x / p.Hkv;
-  if (item_idx >= p.counts[kCntSplitItems]) return;
-  const DecodeItem it = p.dec_items[item_idx];
-  const int b = it.b;
-  const int cu0 = p.cu[b];
-  const int P = p.past[b];
-  const int n = seq_keys(p, P, it.nq);
-  const int kb = it.split * it.chunk;
-  const int ke = (int)min64(n, (int64_t)kb + it.chunk);
-  const int R = it.nq * p.G;
+  const int nr = min(16, R - row0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
 
@@ -1315,8 +1334,9 @@ __global__ void __launch_bounds__(kTileThreads) decode_split_kernel(AttnParams p
     bool ok[2];
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
-      const int r = g + 8 * hr;
-      ok[hr] = r < R;
+      const int rl = g + 8 * hr;
+      ok[hr] = rl < nr;
+      const int r = row0 + rl;
       const int pos = ok[hr] ? r / p.G : 0;
       const int gg = ok[hr] ? r % p.G : 0;
       rows[hr] = p.q + (int64_t)(cu0 + pos) * p.q_stride + (int64_t)(h * p.G + gg) * D;
@@ -1331,7 +1351,6 @@ __global__ void __launch_bounds__(kTileThreads) decode_split_kernel(AttnParams p
   float o[DN][4];
 #pragma unroll
   for (int i = 0; i < DN; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  bool bad = false;
 
 #pragma unroll
   for (int s = 0; s < NSTAGE - 1; ++s) {
@@ -1400,29 +1419,64 @@ __global__ void __launch_bounds__(kTileThreads) decode_split_kernel(AttnParams p
     sL[warp * 16 + g + 8] = l_run[1];
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < R * D; e += kTileThreads) {
-    const int r = e / D, d = e % D;
+  // two adjacent columns per thread
+  for (int e = threadIdx.x; e < nr * D / 2; e += kTileThreads) {
+    const int rl = e / (D / 2), d = 2 * (e % (D / 2));
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kTileWarps; ++w) M = fmaxf(M, sM[w * 16 + r]);
-    float num = 0.f, L = 0.f;
+    for (int w = 0; w < kTileWarps; ++w) M = fmaxf(M, sM[w * 16 + rl]);
+    float num0 = 0.f, num1 = 0.f, L = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kTileWarps; ++w) {
-        const float wt = ex2(sM[w * 16 + r] - M);
-        num += wt * sO[(w * 16 + r) * D + d];
-        L += wt * sL[w * 16 + r];
+        const float wt = ex2(sM[w * 16 + rl] - M);
+        num0 += wt * sO[(w * 16 + rl) * D + d];
+        num1 += wt * sO[(w * 16 + rl) * D + d + 1];
+        L += wt * sL[w * 16 + rl];
       }
     }
+    const int r = row0 + rl;
     const int pos = r / p.G, gg = r % p.G;
-    const int64_t prow =
-        ((int64_t)(it.slot_base + pos) * p.Hq + h * p.G + gg) * p.max_splits + it.split;
-    p.part_o[prow * D + d] = L > 0.f ? num : 0.f;
-    if (d == 0) {
-      p.part_m[prow] = L > 0.f ? M * kLn2 : kNegLarge;
-      p.part_l[prow] = L;
+    if constexpr (kDirect) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      *reinterpret_cast<__half2*>(p.out + ((int64_t)(cu0 + pos) * p.Hq + h * p.G + gg) * D + d) =
+          __floats2half2_rn(num0 * inv, num1 * inv);
+    } else {
+      const int64_t prow =
+          ((int64_t)(slot_base + pos) * p.Hq + h * p.G + gg) * p.max_splits + split;
+      *reinterpret_cast<float2*>(p.part_o + prow * D + d) =
+          L > 0.f ? make_float2(num0, num1) : make_float2(0.f, 0.f);
+      if (d == 0) {
+        p.part_m[prow] = L > 0.f ? M * kLn2 : kNegLarge;
+        p.part_l[prow] = L;
+      }
     }
   }
+}
+
+// Split mode (fixed split counts): CTA = one split of one short sequence for one kv head.
+// With one split per sequence the output is written here and no combine runs; otherwise
+// the combine kernel merges the partials.
+template <int D, int NSTAGE>
+__global__ void __launch_bounds__(kTileThreads) decode_split_kernel(AttnParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int h = blockIdx.x % p.Hkv;
+  const int64_t item_idx = blockIdx.x / p.Hkv;
+  if (item_idx >= p.counts[kCntSplitItems]) return;
+  const DecodeItem it = p.dec_items[item_idx];
+  const int b = it.b;
+  const int cu0 = p.cu[b];
+  const int P = p.past[b];
+  const int n = seq_keys(p, P, it.nq);
+  const int kb = it.split * it.chunk;
+  const int ke = (int)min64(n, (int64_t)kb + it.chunk);
+  const int R = it.nq * p.G;
+  bool bad = false;
+  if (p.max_splits == 1)
+    split_rows<D, NSTAGE, true>(p, smem, b, h, cu0, P, 0, R, kb, ke, 0, 0, bad);
+  else
+    split_rows<D, NSTAGE, false>(p, smem, b, h, cu0, P, 0, R, kb, ke, it.slot_base, it.split,
+                                 bad);
   if (bad) flag_status(p.status, PKV_DEV_BAD_BLOCK);
 }
 
@@ -1464,6 +1518,32 @@ __device__ int block_scan(int v, int* total) {
   *total = warp_tot[kPrologueThreads / 32 - 1];
   __syncthreads();
   return base + x - v;
+}
+
+// Zero output rows of tokens that no valid sequence covers (nothing to do when
+// all_covered); threads tid, tid + nthr, ... of the caller take the tokens.
+__device__ void zero_uncovered(const AttnParams& p, bool all_covered, int tid, int nthr) {
+  for (int i = tid; !all_covered && i < p.T; i += nthr) {
+    int lo = 0, hi = p.B - 1, b = -1;
+    while (lo <= hi) {
+      const int mid = (lo + hi) >> 1;
+      if (p.cu[mid] <= i) {
+        b = mid;
+        lo = mid + 1;
+      } else {
+        hi = mid - 1;
+      }
+    }
+    bool covered = false;
+    if (b >= 0) {
+      int s0, s1, P;
+      covered = seq_valid(p, b, s0, s1, P) && i >= s0 && i < s1;
+    }
+    if (!covered) {
+      uint4* row = reinterpret_cast<uint4*>(p.out + (int64_t)i * p.Hq * p.D);
+      for (int c = 0; c < p.Hq * p.D / 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
 }
 
 __device__ void plan_block(const AttnParams& p) {
@@ -1595,28 +1675,7 @@ __device__ void plan_block(const AttnParams& p) {
   for (int i = tid; i < ndec * p.Hkv; i += kPrologueThreads) p.seg_done[i] = 0;
   // tokens that no valid sequence covers get zero output; when every sequence is
   // valid and cu runs from 0 to T, cu is monotone and covers every token
-  const bool all_covered = s_bad == 0 && p.cu[0] == 0 && p.cu[p.B] == p.T;
-  for (int i = tid; !all_covered && i < p.T; i += kPrologueThreads) {
-    int lo = 0, hi = p.B - 1, b = -1;
-    while (lo <= hi) {
-      const int mid = (lo + hi) >> 1;
-      if (p.cu[mid] <= i) {
-        b = mid;
-        lo = mid + 1;
-      } else {
-        hi = mid - 1;
-      }
-    }
-    bool covered = false;
-    if (b >= 0) {
-      int s0, s1, P;
-      covered = seq_valid(p, b, s0, s1, P) && i >= s0 && i < s1;
-    }
-    if (!covered) {
-      uint4* row = reinterpret_cast<uint4*>(p.out + (int64_t)i * p.Hq * p.D);
-      for (int c = 0; c < p.Hq * p.D / 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
-    }
-  }
+  zero_uncovered(p, s_bad == 0 && p.cu[0] == 0 && p.cu[p.B] == p.T, tid, kPrologueThreads);
 }
 
 // kQ: the scatter blocks also rotate the query heads into the workspace (the kernel
@@ -1633,6 +1692,65 @@ __global__ void __launch_bounds__(kPrologueThreads) prologue_kernel(AttnParams p
     paged_scatter_row<kQ>(sp, gid >> 4, threadIdx.x & 31);
   else
     paged_scatter_thread<kQ>(sp, gid);
+}
+
+// ----------------------------------------------------------------------------------
+// Single-pass path (the manifest's non-split variants, ScatterKV then Attend, here in one
+// launch): CTA (b, h) writes the new K/V rows of sequence b for kv head h into the cache
+// (rotated when asked, and with kQ the token's query heads of that kv head into the
+// workspace), then attends every query row of (b, h) over all the keys it sees and writes
+// the fp16 output. Only this CTA reads what it scattered, so no plan, partials, combine or
+// second launch are needed. The last CTA zeroes tokens that no valid sequence covers.
+// Taken when every sequence has one split and the call is small (host-side bound).
+// ----------------------------------------------------------------------------------
+template <int D, int NSTAGE, bool kQ>
+__global__ void __launch_bounds__(kTileThreads) single_pass_kernel(AttnParams p,
+                                                                   ScatterParams sp) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int64_t nseq = (int64_t)p.B * p.Hkv;
+  if ((int64_t)blockIdx.x >= nseq) {
+    int any_bad = 0;
+    for (int b = threadIdx.x; b < p.B; b += kTileThreads) {
+      int lo, hi, P;
+      if (!seq_valid(p, b, lo, hi, P)) any_bad = 1;
+    }
+    any_bad = __syncthreads_or(any_bad);
+    zero_uncovered(p, !any_bad && p.cu[0] == 0 && p.cu[p.B] == p.T, threadIdx.x, kTileThreads);
+    return;
+  }
+  const int b = (int)(blockIdx.x / p.Hkv), h = (int)(blockIdx.x % p.Hkv);
+  int lo, hi, P;
+  if (!seq_valid(p, b, lo, hi, P)) {
+    if (h == 0 && threadIdx.x == 0) flag_status(p.status, PKV_DEV_BAD_SEQUENCE);
+    return;
+  }
+  const int N = hi - lo;
+  if (N == 0) return;
+  if (h == 0 && threadIdx.x == 0 && (int64_t)P + N > (int64_t)p.MB * p.BS)
+    flag_status(p.status, PKV_DEV_BAD_BLOCK);
+  if (sp.row_path) {   // half a warp per (token, kv head) row pair
+    for (int t0 = 0; t0 < N; t0 += kTileThreads / 16) {
+      const int t = t0 + (threadIdx.x >> 4);
+      if (t < N) paged_scatter_row<kQ>(sp, (int64_t)(lo + t) * p.Hkv + h, threadIdx.x & 31);
+    }
+  } else {             // one thread per 16-byte chunk
+    const int cpr = p.D / 8;
+    for (int k = threadIdx.x; k < N * cpr; k += kTileThreads)
+      paged_scatter_thread<kQ>(sp, ((int64_t)(lo + k / cpr) * p.Hkv + h) * cpr + k % cpr);
+  }
+  __threadfence_block();
+  __syncthreads();   // the rows written above are read back below by this CTA alone
+  const int n = seq_keys(p, P, N);
+  const int R = N * p.G;
+  bool bad = false;
+  for (int row0 = 0; row0 < R; row0 += 16) {
+    // keys up to the last row's position (causal)
+    const int last_pos = (min(R, row0 + 16) - 1) / p.G;
+    const int ke = (int)min64(n, (int64_t)P + last_pos + 1);
+    split_rows<D, NSTAGE, true>(p, smem, b, h, lo, P, row0, R, 0, ke, 0, 0, bad);
+    __syncthreads();   // the merge buffers alias the next row tile's key stages
+  }
+  if (bad) flag_status(p.status, PKV_DEV_BAD_BLOCK);
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
@@ -1694,12 +1812,27 @@ cudaError_t launch_attention_d(const AttnParams& p, const ScatterParams& sp, cud
     e = cudaFuncSetAttribute(decode_split_kernel<D, NSTAGE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)split_smem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(single_pass_kernel<D, NSTAGE, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)split_smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(single_pass_kernel<D, NSTAGE, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)split_smem);
+    if (e != cudaSuccess) return e;
     if (D == 128) {
       e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kTcSmem);
       if (e != cudaSuccess) return e;
     }
     mark_configured(configured, dev);
+  }
+  if (p.single_pass) {   // one launch: scatter and attention per (sequence, kv head)
+    ProfScope ps("single_pass", s);
+    const unsigned grid = (unsigned)((int64_t)p.B * p.Hkv + 1);
+    if (sp.q_dst)
+      single_pass_kernel<D, NSTAGE, true><<<grid, kTileThreads, split_smem, s>>>(p, sp);
+    else
+      single_pass_kernel<D, NSTAGE, false><<<grid, kTileThreads, split_smem, s>>>(p, sp);
+    return cudaGetLastError();
   }
   const int64_t scatter_threads = pkv::scatter_threads(sp);
   {

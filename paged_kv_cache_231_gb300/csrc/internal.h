@@ -14,6 +14,9 @@ constexpr int kMaxSplitsDefault = 16;    // manifest tunable MAX_SPLITS
 constexpr int kSplitMinKeysDefault = 128;  // manifest tunable SPLIT_MIN_KEYS
 constexpr int kSplitTargetWorkgroups = 1024;  // manifest tunable SPLIT_TARGET_WORKGROUPS
 constexpr int kStageKeys = 64;           // keys per shared-memory stage (attention)
+// Single-pass path bound: row tiles of 16 (if every token were in one sequence) x key
+// ceiling of a sequence, i.e. the most key rows one CTA of that path may have to read.
+constexpr int64_t kSinglePassWork = int64_t(1) << 18;
 
 // ---- paged scatter (ScatterKV) ----------------------------------------------------
 struct ScatterParams {
@@ -126,6 +129,11 @@ struct AttnParams {
   int total_warps;         // warps of the persistent kernel
   int tc_prefill;          // 1: prefill tiles of 128 rows on tcgen05 (head size 128)
   int tc_rows;             // keys per TMA box of the tcgen05 prefill (power of two, >= 8)
+  int single_pass;         // 1: one launch, scatter + attention per (sequence, kv head)
+  // testing hook (pkv_testing_wait_limit): poll bound of the tensor-core kernel's waits
+  // (0 = its default) and 1 = each CTA withholds its first bulk copy
+  uint32_t wait_tries;
+  int withhold_copy;
   // workspace
   int32_t* counts;         // kCnt* words
   DecSeq* dec_seqs;        // stream-K
@@ -189,6 +197,9 @@ struct SparseParams {
   int32_t* group_cursor;   // [ngroups]
   int32_t* perm;           // [E]
   int4* edge_rec;          // [E] (edge, q_idx, block_len clipped to block_size, 0), grouped order
+  // testing hook (pkv_testing_wait_limit), as in AttnParams
+  uint32_t wait_tries;
+  int withhold_copy;
 };
 
 // Kernel attributes (the dynamic shared memory limit) belong to a device's context: each
@@ -229,6 +240,11 @@ __device__ __forceinline__ int edge_keys(const SparseParams& p, int q_idx, int b
 }
 // fp16 partials (sparse16.cu); the runtime has checked the shapes it takes
 cudaError_t launch_sparse_tc16(const SparseParams& p, cudaStream_t s);
+
+// testing hook of the bounded waits (runtime.cpp): current poll bound (0 = default) and
+// whether tensor-core kernels withhold their first bulk copy
+uint32_t testing_wait_tries();
+int testing_withhold_copy();
 
 // profiler hooks (runtime.cpp)
 void prof_begin(const char* name, cudaStream_t s);

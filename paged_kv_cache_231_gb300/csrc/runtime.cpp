@@ -61,6 +61,13 @@ void prof_end(const char* name, cudaStream_t s) {
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+namespace {
+std::atomic<uint32_t> g_wait_tries{0};
+std::atomic<int> g_withhold{0};
+}  // namespace
+uint32_t testing_wait_tries() { return g_wait_tries.load(std::memory_order_relaxed); }
+int testing_withhold_copy() { return g_withhold.load(std::memory_order_relaxed); }
+
 // ---------------------------------------------------------------- helpers
 namespace {
 
@@ -96,6 +103,7 @@ struct PagedLayout {
   int fixed_splits = 1;
   int streamk = 0;
   int tc_rows = 0;   // > 0: prefill tiles on the tensor core, TMA boxes of tc_rows keys
+  int single_pass = 0;   // 1: one launch of the single-pass kernel does the whole call
   int64_t dec_bound = 0, pre_bound = 0, slot_bound = 0;
   size_t off_counts = 0, off_seqs = 0, off_done = 0, off_dec = 0, off_pre = 0,
          off_slot_tok = 0, off_slot_spl = 0, off_po = 0, off_pm = 0, off_pl = 0,
@@ -201,6 +209,10 @@ int check_paged(const pkv_paged_attention_args* a, bool attention, PagedLayout* 
   }
   L->pre_rows = L->tc_rows > 0 ? (int)(128 / G) : 4 * L->dec_rows;
   const int64_t T = a->num_tokens, B = a->batch;
+  // every sequence has one split (no partials, no combine) and the call is small: one
+  // CTA per (sequence, kv head) scatters and attends in a single launch
+  L->single_pass = L->max_splits == 1 && B * a->kv_num_heads < INT32_MAX / 2 &&
+                   ceil_div(T * G, 16) * (a->max_blocks * a->block_size) <= kSinglePassWork;
   L->dec_bound = L->streamk ? 0 : B * L->max_splits;
   L->pre_bound = ceil_div(T, L->pre_rows) + std::min<int64_t>(B, T / (L->dec_rows + 1));
   L->slot_bound = std::min<int64_t>(T, B * L->dec_rows);
@@ -321,6 +333,13 @@ size_t pkv_sizeof_struct(const char* name) {
 
 int64_t pkv_launch_count(void) { return g_launches.load(); }
 
+int pkv_testing_wait_limit(uint32_t max_polls, int32_t withhold_first_copy) {
+  if (withhold_first_copy && max_polls == 0) return PKV_ERR_SHAPE;
+  g_wait_tries.store(max_polls, std::memory_order_relaxed);
+  g_withhold.store(withhold_first_copy ? 1 : 0, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
 void pkv_profiler_enable(int on) { g_prof.store(on != 0, std::memory_order_relaxed); }
 
 void pkv_profiler_reset(void) {
@@ -439,6 +458,9 @@ int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
   ap.total_warps = num_sms_current() * attention_ctas_per_sm() * attention_warps_per_cta();
   ap.tc_prefill = L.tc_rows > 0 ? 1 : 0;
   ap.tc_rows = L.tc_rows;
+  ap.single_pass = L.single_pass;
+  ap.wait_tries = testing_wait_tries();
+  ap.withhold_copy = testing_withhold_copy();
   ap.counts = reinterpret_cast<int32_t*>(ws + L.off_counts);
   ap.dec_seqs = reinterpret_cast<DecSeq*>(ws + L.off_seqs);
   ap.seg_done = reinterpret_cast<int32_t*>(ws + L.off_done);
@@ -463,7 +485,8 @@ int pkv_paged_attention(const pkv_paged_attention_args* args, void* workspace,
   cudaError_t e = launch_attention(ap, sp, s);
   if (e != cudaSuccess) return PKV_ERR_LAUNCH;
 
-  if (!L.streamk && L.slot_bound > 0) {
+  // one split per sequence: the split kernel (or the single-pass one) wrote the output
+  if (!L.streamk && L.slot_bound > 0 && L.max_splits > 1 && !L.single_pass) {
     CombineParams cp{};
     cp.o = ap.part_o;
     cp.m = ap.part_m;
@@ -697,6 +720,8 @@ int pkv_sparse_attention_partials(const pkv_sparse_args* a, void* workspace,
   p.ppb = (int)a->pages_per_block;
   p.scale = a->softmax_scale;
   p.qpos = a->query_positions;
+  p.wait_tries = testing_wait_tries();
+  p.withhold_copy = testing_withhold_copy();
   p.nblk = nb;
   p.ngroups = ng;
   size_t off = 0;

@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kSpThreads, 2) sparse_partials_kernel(SparsePa
 namespace tcs {
 constexpr int kThreads = 256;
 constexpr int kNK = 64;                 // keys per block tile
-constexpr uint32_t kTries = 1u << 24;   // bound of each MMA-completion wait
+constexpr uint32_t kTries = 1u << 24;   // default bound of each wait (polls)
 
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
   return (1u << 4)                      // D format: f32
@@ -393,7 +393,7 @@ struct SpMaps {     // TMA descriptors of the K and V pages (kernel parameters)
 // no copy: the conversion writes zeros for their keys.
 template <int D>
 __device__ void stage_raw(const SparseParams& p, const SpMaps& maps, unsigned char* sm,
-                          int64_t g, uint64_t* rbar) {
+                          int64_t g, uint64_t* rbar, bool withhold = false) {
   using L = Layout<D>;
   const int lane = threadIdx.x & 31;
   uint8_t* rValid = sm + L::kRValid;
@@ -429,7 +429,7 @@ __device__ void stage_raw(const SparseParams& p, const SpMaps& maps, unsigned ch
   if (lane == 0)
     tc::mbar_arrive_expect_tx(rbar, (uint32_t)__popc(bits) * (uint32_t)p.page_size * D * 4u * 2u);
   __syncwarp();
-  if (row0 >= 0) {
+  if (row0 >= 0 && !withhold) {
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) {
       const uint32_t off = (uint32_t)q * (kNK * 128) + (uint32_t)(lane * p.page_size) * 128u;
@@ -463,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, half = warp >> 2;
   const int r = quarter * 32 + lane;   // TMEM lane / tile row of this thread
+  const uint32_t tries = p.wait_tries ? p.wait_tries : kTries;
   if (tid == 0) {
     tc::mbar_init(bar, 1);
     tc::mbar_init(bar + 1, 1);
@@ -487,7 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&maps.k);
       tc::tma_prefetch_desc(&maps.v);
     }
-    stage_raw<D>(p, maps, sm, g, rbar);
+    // testing hook: the first staging is announced but never copied, so the wait for it
+    // gives up with nothing in flight
+    stage_raw<D>(p, maps, sm, g, rbar, p.withhold_copy != 0);
   }
   uint32_t raw_issued = g < p.ngroups ? 1u : 0u, raw_used = 0;
   uint32_t phase = 0;
@@ -548,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   const uint32_t idesc_s = idesc_tf32(128, kNK), idesc_o = idesc_tf32(128, D);
   while (g < p.ngroups && ok) {
-    ok = __syncthreads_and(tc::mbar_wait(rbar, raw_used & 1u, kTries));
+    ok = __syncthreads_and(tc::mbar_wait(rbar, raw_used & 1u, tries));
     ++raw_used;
     if (!ok) break;
     const uint8_t* rValid = sm + L::kRValid;
@@ -635,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // fetched while S is computed: the dependent loads stall here, not on the next tile
       if (c0 + epc < e1) row_edge(c0 + epc, e1, nx_e, nx_q, nx_bl);
       else if (gn < p.ngroups) row_edge(p.group_off[gn], p.group_off[gn + 1], nx_e, nx_q, nx_bl);
-      ok = __syncthreads_and(tc::mbar_wait(bar, phase & 1u, kTries));
+      ok = __syncthreads_and(tc::mbar_wait(bar, phase & 1u, tries));
       ++phase;
       if (!ok) break;
       tc::fence_after_sync();
@@ -715,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::commit(bar);
       }
-      ok = __syncthreads_and(tc::mbar_wait(bar, phase & 1u, kTries));
+      ok = __syncthreads_and(tc::mbar_wait(bar, phase & 1u, tries));
       ++phase;
       if (!ok) break;
       tc::fence_after_sync();
@@ -758,8 +761,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       flag_status(p.status, PKV_DEV_TIMEOUT);
       tc::commit(bar + 1);
-      tc::mbar_wait(bar + 1, 0, kTries);
-      if (raw_issued > raw_used) tc::mbar_wait(rbar, raw_used & 1u, kTries);
+      tc::mbar_wait(bar + 1, 0, tries);
+      if (raw_issued > raw_used) tc::mbar_wait(rbar, raw_used & 1u, tries);
     }
   }
   if (bad) flag_status(p.status, PKV_DEV_BAD_EDGE);

@@ -48,7 +48,9 @@ namespace {
 
 constexpr int kThreads = 448;
 constexpr int kNK = 64;                 // keys per block tile
-constexpr uint32_t kTries = 1u << 22;   // bound of each wait (polls)
+constexpr uint32_t kTries = 1u << 22;   // default bound of each wait (polls)
+// bound of this CTA's waits (kTries unless a test lowered it), set before the first barrier
+__shared__ uint32_t s_tries;
 constexpr uint32_t kTmS = 0, kTmO = 128, kTmP = 384;
 constexpr int kSchedWarp = 8, kMmaWarp = 9, kGatherWarp0 = 10;   // gather: warps 10-13
 constexpr int kRing = 4;                // group ring entries
@@ -129,7 +131,8 @@ __device__ __forceinline__ void bar_arrive_cp_async(uint64_t* bar) {
 // bound runs out or another role raised the flag.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort) {
   const uint32_t addr = smem_u32(bar);
-  for (uint32_t i = 0; i < kTries; ++i) {
+  const uint32_t tries = s_tries;
+  for (uint32_t i = 0; i < tries; ++i) {
     uint32_t done;
     asm volatile(
         "{\n"
@@ -182,7 +185,7 @@ __device__ __forceinline__ int64_t next_group(const SparseParams& p) {
 // kernel starts with, and their weights are exactly 0.
 template <int D>
 __device__ void stage_group(const SparseParams& p, const Maps& maps, unsigned char* sm,
-                            int64_t g, uint32_t st, uint64_t* sbar) {
+                            int64_t g, uint32_t st, uint64_t* sbar, bool withhold = false) {
   using L = Layout<D>;
   const int lane = threadIdx.x & 31;
   uint64_t* masks = reinterpret_cast<uint64_t*>(sm + L::kMasks) + 2 * st;
@@ -224,7 +227,7 @@ __device__ void stage_group(const SparseParams& p, const Maps& maps, unsigned ch
   if (lane == 0)
     tc::mbar_arrive_expect_tx(sbar, (uint32_t)__popc(bits) * (uint32_t)p.page_size * D * 2u * 2u);
   __syncwarp();
-  if (row0 >= 0) {
+  if (row0 >= 0 && !withhold) {
     unsigned char* kdst = sm + L::kK + st * L::kKV;
     unsigned char* vdst = sm + L::kV + st * L::kKV;
 #pragma unroll
@@ -454,7 +457,9 @@ __device__ void sched_role(const SparseParams& p, const Maps& maps, unsigned cha
     if (gi >= kStages &&
         !warp_wait(bars + kKVEmpty + st, ((gi / kStages) - 1) & 1u, abort))
       return;
-    stage_group<D>(p, maps, sm, g, st, bars + kKVFull + st);
+    // testing hook: the CTA's first staging is announced but never copied, so the waits
+    // for it give up with nothing in flight
+    stage_group<D>(p, maps, sm, g, st, bars + kKVFull + st, p.withhold_copy && gi == 0);
     ++issued[st];
   }
 }
@@ -650,6 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(bars + kDrain, 1);
     *abort = 0;
+    s_tries = p.wait_tries ? p.wait_tries : kTries;
     tc::mbar_init_fence();
   }
   if (warp == 0) {
@@ -675,12 +681,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_role<D>(p, sm, tmem);
     // let every MMA this thread issued finish before the CTA leaves
     tc::commit(bars + kDrain);
-    tc::mbar_wait(bars + kDrain, 0, kTries);
+    tc::mbar_wait(bars + kDrain, 0, s_tries);
   }
   if (warp == kSchedWarp && *abort) {
     // a wait gave up: the last staging of each stage must land before the CTA leaves
     for (uint32_t st = 0; st < kStages; ++st)
-      if (issued[st] > 0) tc::mbar_wait(bars + kKVFull + st, (issued[st] - 1) & 1u, kTries);
+      if (issued[st] > 0) tc::mbar_wait(bars + kKVFull + st, (issued[st] - 1) & 1u, s_tries);
   }
   if (bad) flag_status(p.status, PKV_DEV_BAD_EDGE);
   tc::fence_before_sync();

@@ -7,7 +7,10 @@
 // The array's name is a host-side stand-in in host code, not a device address, so the
 // host resolves the real address once per device with cudaGetSymbolAddress (with that
 // device current) and passes it to the unchanged paged attention path. The first call
-// on a device performs that look-up; make it before any stream capture.
+// on a device performs that look-up; make it before any stream capture. Under lazy module
+// loading (CUDA's default) that look-up also loads the module and commits the array, so
+// the first call must come before a caller's pool takes the device's memory. The cached
+// address is not refreshed after a device reset, which is therefore not supported.
 #include <cuda_runtime.h>
 
 #include <mutex>

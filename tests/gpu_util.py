@@ -59,6 +59,26 @@ def assert_f32_close(got, ref, what="", scalars=False, rtol=None):
     return float((err / (np.abs(ref) + row_scale + 1e-30)).max()) if err.size else 0.0
 
 
+def f32_margins(got, ref, what=""):
+    """Achieved fp32 error, reported beside the row-scale tolerance: the largest
+    element-relative error over elements of at least 1 % of their row's largest
+    magnitude, and the largest row-norm relative error ||got - ref|| / ||ref|| (rows are
+    the last axis; all-zero reference rows are skipped). Prints both; returns the
+    row-norm error."""
+    got = np.atleast_2d(np.asarray(got, dtype=np.float64))
+    ref = np.atleast_2d(np.asarray(ref, dtype=np.float64))
+    rmax = np.max(np.abs(ref), axis=-1, keepdims=True)
+    big = (np.abs(ref) >= 0.01 * rmax) & (rmax > 0)
+    elem = float((np.abs(got - ref)[big] / np.abs(ref)[big]).max()) if big.any() else 0.0
+    norm = np.linalg.norm(ref, axis=-1)
+    live = norm > 0
+    row = float((np.linalg.norm(got - ref, axis=-1)[live] / norm[live]).max()) \
+        if live.any() else 0.0
+    print(f"fp32 margin {what}: element-relative (|ref| >= 1% of row max) {elem:.3e}, "
+          f"row-norm relative {row:.3e}")
+    return row
+
+
 class PagedRun:
     def __init__(self, out, kc, vc, status):
         self.out, self.kc, self.vc, self.status = out, kc, vc, status

@@ -24,7 +24,10 @@ def check(case, tokens=None, rotary_query=False, **kw):
 
 
 def test_tiny_decode():
+    # every sequence fits one split: scatter and attention run as one launch
+    before = B.pkv_launch_count()
     check(wl.tiny_decode())
+    assert B.pkv_launch_count() - before == 1
 
 
 CASES = [
@@ -51,6 +54,61 @@ def test_random_shapes(case):
                       past=past, new_tokens=new, packed=packed, use_slot_mapping=slot,
                       extra_blocks=3)
     check(c)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(c[0]) for c in CASES])
+def test_single_pass_shapes(case):
+    """With one split per sequence, small calls take the single-pass kernel (one CTA per
+    (sequence, kv head) scatters, then attends every row of its sequence, prefill rows
+    included) and launch nothing else."""
+    seed, Hq, Hkv, D, BS, past, new, packed, slot = case
+    c = wl.paged_case(seed, num_heads=Hq, kv_num_heads=Hkv, head_size=D, block_size=BS,
+                      past=past, new_tokens=new, packed=packed, use_slot_mapping=slot,
+                      extra_blocks=3)
+    before = B.pkv_launch_count()
+    check(c, max_splits=1)
+    assert B.pkv_launch_count() - before == 1
+
+
+@pytest.mark.parametrize("D,rotary_dim,inter", [(128, 128, False), (64, 12, True)])
+def test_single_pass_rotary_query(D, rotary_dim, inter):
+    c = wl.paged_case(44, num_heads=8, kv_num_heads=2, head_size=D, block_size=16,
+                      past=[5, 300, 0, 1000], new_tokens=[1, 40, 130, 1], packed=True,
+                      rotary_dim=rotary_dim, rotary_interleaved=inter)
+    check(c, rotary_query=True, max_splits=1)
+
+
+def test_single_pass_invalid_sequence_padding_and_slots():
+    c = wl.paged_case(46, num_heads=4, kv_num_heads=2, head_size=64, block_size=16,
+                      past=[10, 20, 30], new_tokens=[3, 2, 2], use_slot_mapping=True)
+    c.past_seqlens[1] = -4                      # invalid sequence: zero output, flagged
+    c.slot_mapping[0] = -1                      # padding: not written
+    c.slot_mapping[6] = c.num_blocks * 16 + 7   # past the pool: flagged, not written
+    check(c, max_splits=1)
+    c2 = wl.paged_case(46, num_heads=4, kv_num_heads=2, head_size=64, block_size=16,
+                       past=[10, 20, 30], new_tokens=[3, 2, 2])
+    c2.cu_seqlens[3] = 5                        # last 2 tokens are padding: zero output
+    g = run_paged_gpu(c2, max_splits=1)
+    r = run_paged_oracle(c2)
+    assert (g.out[5:] == 0).all() and g.status == r.status == 0
+    assert_f16_close(g.out, r.out, "padded batch, single pass")
+
+
+def test_one_split_without_combine():
+    """One split per sequence but too much work for the single-pass kernel: the split
+    kernel writes the output itself and no combine is launched."""
+    c = wl.paged_case(49, num_heads=8, kv_num_heads=2, head_size=128, block_size=16,
+                      past=[0, 63, 5000, 130], new_tokens=[300, 1, 1, 2])
+    B.pkv_profiler_reset()
+    B.pkv_profiler_enable(True)
+    try:
+        check(c, split_policy=B.PKV_SPLIT_FIXED, fixed_splits=1)
+        assert B.pkv_profiler_query("combine")[1] == 0
+        assert B.pkv_profiler_query("single_pass")[1] == 0
+        assert B.pkv_profiler_query("decode_split")[1] == 1
+    finally:
+        B.pkv_profiler_enable(False)
+        B.pkv_profiler_reset()
 
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 5, 7, 16])

@@ -7,7 +7,7 @@ from oracle import pagedkv_oracle as orc
 from paged_kv_cache_231_gb300 import binding as B
 from paged_kv_cache_231_gb300 import workloads as wl
 
-from .gpu_util import DEV, assert_f16_close, assert_f32_close, dev, host
+from .gpu_util import DEV, assert_f16_close, assert_f32_close, dev, f32_margins, host
 
 pytestmark = pytest.mark.gpu
 
@@ -47,6 +47,8 @@ def compare_partials(go, gm, gl, ro, rm, rl, rows, f16=False):
     live = rows[~empty]
     rt = F16_PARTIAL_RTOL if f16 else None
     assert_f32_close(go[live], ro[live], "o partial", rtol=rt)
+    if not f16:   # the 1e-4 relative bar read as a row norm: o rows of the partials
+        assert f32_margins(go[live], ro[live], "o partials") <= 1e-4
     assert_f32_close(gm[live], rm[live], "m partial", scalars=True)
     assert_f32_close(gl[live], rl[live], "l partial", scalars=True, rtol=rt)
 
@@ -65,6 +67,7 @@ def test_small_full_parity(head_dim, pages_per_block, qhead):
     compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]))
     rout, rlse = orc.combine_partials(ro, rm, rl, c.seg_offsets, c.qhead)
     assert_f32_close(gout, rout, "combined output")
+    assert f32_margins(gout, rout, "combined output") <= 1e-4
     fin = np.isfinite(rlse)
     np.testing.assert_array_equal(np.isfinite(glse), fin)
     assert_f32_close(glse[fin], rlse[fin], "lse", scalars=True)
@@ -117,6 +120,7 @@ def test_block_sparse_full_size_sampled():
             pr = [e * c.qhead + qh for e in range(e0, e1)]
             ref, rlse = orc.combine_rows(ro[pr], rm[pr], rl[pr])
             assert_f32_close(gout[s * c.qhead + qh], ref, "combined row")
+            assert f32_margins(gout[s * c.qhead + qh], ref, "combined row") <= 1e-4
 
 
 # fp16 q and pages: tensor-core kind::f16 kernel (blocks of 64 / 32 keys, qhead 3 and 1)
