@@ -316,19 +316,14 @@ __global__ void __launch_bounds__(kSpThreads, 2) sparse_partials_kernel(SparsePa
 // ---- tensor-core partials: 3xTF32 on tcgen05 ----------------------------------------
 // For head size 64/128 and blocks of at most 64 keys. A persistent CTA per SM takes
 // (batch, block, kv head) groups from a counter. The group's raw fp32 K and V rows are
-// staged with cp.async while the previous group computes, then split into tf32 pairs
-// x = hi + lo (hi = x rounded to tf32, lo = x - hi) in 128-byte-swizzled K-major tiles:
-// K [64 keys][D] and V^T [D][64 keys]. For each tile of 128 query rows (edges x query
-// heads) Q (hi, lo) goes to TMEM and S = Q K^T is accumulated from three tf32 products
-// (hi*hi + hi*lo + lo*hi, relative error about 2^-22, i.e. fp32 level); one thread per row
-// forms the partial's max, weights and sum, writes the weights (hi, lo) back to TMEM,
-// and O = P V is accumulated the same way. TMEM: S 0..63, O 64.., Q hi 256.., Q lo 384..,
-// P hi 256..319, P lo 320..383 (P replaces Q once S is complete).
+// staged by TMA, then split into tf32 pairs x = hi + lo (hi = x rounded to tf32,
+// lo = x - hi) in 128-byte-swizzled K-major tiles: K [64 keys][D] and V^T [D][64 keys].
+// For each tile of 128 query rows (edges x query heads) Q (hi, lo) goes to TMEM and
+// S = Q K^T is accumulated from three tf32 products (hi*hi + hi*lo + lo*hi, relative
+// error about 2^-22, i.e. fp32 level); one thread per row forms the partial's max,
+// weights and sum, writes the weights (hi, lo) back to TMEM, and O = P V is accumulated
+// the same way.
 namespace tcs {
-constexpr int kThreads = 256;
-constexpr int kNK = 64;                 // keys per block tile
-constexpr uint32_t kTries = 1u << 24;   // default bound of each wait (polls)
-
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
   return (1u << 4)                      // D format: f32
          | (2u << 7) | (2u << 10)       // A, B format: tf32
@@ -365,79 +360,10 @@ __device__ __forceinline__ float tf32_hi(float x) {
   return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
-template <int D>
-struct Layout {   // byte offsets from a 1024-byte-aligned base
-  static constexpr uint32_t kKhi = 0;                       // [64][D]: D/32 x [64][128 B]
-  static constexpr uint32_t kKlo = kKhi + D * 256;
-  static constexpr uint32_t kVhi = kKlo + D * 256;          // [D][64]: 2 x [D][128 B]
-  static constexpr uint32_t kVlo = kVhi + D * 256;
-  static constexpr uint32_t kRawK = kVlo + D * 256;         // raw K, V as loaded by TMA:
-  static constexpr uint32_t kRawV = kRawK + D * 256;        //   D/32 x [64 keys][128 B], swizzled
-  static constexpr uint32_t kXfer = kRawV + D * 256;        // 8 warps x [32][32] fp32 transpose
-  static constexpr uint32_t kValid = kXfer + 8 * 4096;      // key masks, current group (16 B)
-  static constexpr uint32_t kRValid = kValid + 64;          // [64] key state, staged group
-  static constexpr uint32_t kBar = kRValid + 64;            // MMA completion, drain, raw K/V
-  static constexpr uint32_t kTmem = kBar + 24;
-  static constexpr uint32_t kNext = kTmem + 8;              // int64, 8-byte aligned
-  static constexpr uint32_t kEnd = kNext + 8;
-};
-
 struct SpMaps {     // TMA descriptors of the K and V pages (kernel parameters)
   CUtensorMap k;    // [pages * hkv * page_size rows][D] fp32, box 32 x page_size
   CUtensorMap v;
 };
-
-// One warp: group g's K and V pages by TMA (one box per page and 32-column slice, landing
-// in the 128-byte-swizzled layout of the raw tiles) onto rbar; key states into rValid
-// (0 unmapped or past the block, 1 mapped, 2 invalid table reference). Unmapped pages get
-// no copy: the conversion writes zeros for their keys.
-template <int D>
-__device__ void stage_raw(const SparseParams& p, const SpMaps& maps, unsigned char* sm,
-                          int64_t g, uint64_t* rbar, bool withhold = false) {
-  using L = Layout<D>;
-  const int lane = threadIdx.x & 31;
-  uint8_t* rValid = sm + L::kRValid;
-  const int h = (int)(g % p.hkv);
-  const int64_t bb = g / p.hkv;
-  const int blk = (int)(bb % p.nblk);
-  const int batch = (int)(bb / p.nblk);
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int t = lane + 32 * k;
-    uint8_t state = 0;
-    if (t < p.block_size) {
-      const int64_t slot = (int64_t)blk * p.ppb + t / p.page_size;
-      if (slot < p.max_pages) {
-        const int64_t page = p.bt[(int64_t)batch * p.max_pages + slot];
-        state = page >= p.num_pages ? 2 : page >= 0 ? 1 : 0;
-      } else {
-        state = 2;
-      }
-    }
-    rValid[t] = state;
-  }
-  int row0 = -1;   // first row of page `lane` of the block in the page tensors
-  if (lane < p.ppb) {
-    const int64_t slot = (int64_t)blk * p.ppb + lane;
-    if (slot < p.max_pages) {
-      const int64_t page = p.bt[(int64_t)batch * p.max_pages + slot];
-      if (page >= 0 && page < p.num_pages) row0 = (int)((page * p.hkv + h) * p.page_size);
-    }
-  }
-  const uint32_t bits = __ballot_sync(0xffffffffu, row0 >= 0);
-  __syncwarp();   // the key states are published by lane 0's arrive
-  if (lane == 0)
-    tc::mbar_arrive_expect_tx(rbar, (uint32_t)__popc(bits) * (uint32_t)p.page_size * D * 4u * 2u);
-  __syncwarp();
-  if (row0 >= 0 && !withhold) {
-#pragma unroll
-    for (int q = 0; q < D / 32; ++q) {
-      const uint32_t off = (uint32_t)q * (kNK * 128) + (uint32_t)(lane * p.page_size) * 128u;
-      tc::tma_load_2d(sm + L::kRawK + off, &maps.k, q * 32, row0, rbar);
-      tc::tma_load_2d(sm + L::kRawV + off, &maps.v, q * 32, row0, rbar);
-    }
-  }
-}
 
 // next group (in counter order) that has edges, or ngroups
 __device__ __forceinline__ int64_t next_group(const SparseParams& p) {
@@ -449,6 +375,563 @@ __device__ __forceinline__ int64_t next_group(const SparseParams& p) {
   }
 }
 
+// Warp-specialised form: a persistent CTA of 16 warps per SM, every hand-off on an
+// mbarrier, so that the tensor core runs S = Q K^T of a tile while the previous tile's
+// output is stored and the next tile's Q and the next group's K/V are prepared.
+//   warp 12 (scheduler): takes groups from the counter, publishes each in a 4-entry ring
+//     with its 64-bit key masks (mapped, invalid reference) and stages the group's raw
+//     fp32 K and V pages by TMA (one box per page and 32-column slice) once the
+//     converters have finished the previous group's raw tiles.
+//   warps 8-11 (convert + Q, upper columns): raw K -> tf32 (hi, lo) K-major tiles once
+//     every S of the previous group is done; raw V -> transposed (hi, lo) tiles once every
+//     O = P V of the previous group is done (keys not mapped become zeros); per tile, the
+//     upper half of the Q columns of every row, split into (hi, lo), into TMEM.
+//   warps 4-7 (Q lower columns + store): per tile, the lower half of the Q columns; the O
+//     rows of the previous tile from TMEM to global memory.
+//   warps 13, 14, lane 0 (S issuers): S = Qhi Khi + Qhi Klo + Qlo Khi as two accumulators
+//     (24 tf32 MMAs each; the cost of an MMA is paid by the issuing thread).
+//   warp 15, lane 0 (O issuer): O = Phi Vhi + Phi Vlo + Plo Vhi, P read from TMEM.
+//   warps 0-3 (softmax, one thread per row): m, the weights and l of the row from the sum
+//     of the two S accumulators; P (hi, lo) back into the S columns; m and l to memory.
+// TMEM: S (P hi) 0..63, S' (P lo) 64..127, O 128.., Q hi 256.., Q lo 256 + D.
+// One S/P buffer and one O accumulator: S(t+1) is issued once O(t) = P(t) V is done, so
+// the tensor-core chain per tile is S, softmax, O; everything else overlaps it.
+constexpr int kThreads = 512;
+constexpr int kNK = 64;                 // keys per block tile
+constexpr uint32_t kTries = 1u << 22;   // default bound of each wait (polls)
+constexpr int kRing = 4;                // group ring entries
+constexpr int kSchedWarp = 12, kIssueS0 = 13, kIssueS1 = 14, kIssuePv = 15;
+constexpr uint32_t kTmSa = 0, kTmSb = 64, kTmO = 128, kTmQ = 256;
+// bound of this CTA's waits (kTries unless a test lowered it), set before the first barrier
+__shared__ uint32_t s_tries;
+
+enum : int {
+  kGFull = 0,                   // [kRing] entry published (scheduler, count 1)
+  kGEmpty = kGFull + kRing,     // [kRing] entry released (15 consumer warps / threads)
+  kRawFull = kGEmpty + kRing,   // raw K/V of a group landed (1 arrival + tx)
+  kRawFree,                     // converters done reading the raw tiles (4 warps)
+  kKReady,                      // K (hi, lo) of a group in place (4 warps)
+  kKFree,                       // every S of a group done (2 issuer commits)
+  kVReady,                      // V^T (hi, lo) of a group in place (4 warps)
+  kVFree,                       // every O of a group done (commit)
+  kQReady,                      // Q (hi, lo) of a tile in TMEM (8 warps)
+  kSFull,                       // S of a tile in TMEM (2 issuer commits)
+  kPFull,                       // P of a tile in TMEM (4 softmax warps)
+  kPvDone,                      // O of a tile complete (commit)
+  kOEmpty,                      // O read out of TMEM (4 store warps)
+  kDrainS0, kDrainS1, kDrainPv,
+  kNumBars
+};
+
+struct GroupEntry {   // ring entry: group (ngroups = end of work), edges, key masks
+  long long g;
+  int e0, e1;
+  unsigned long long vmask, imask;
+};
+
+template <int D>
+struct Layout {   // byte offsets from a 1024-byte-aligned base
+  static constexpr uint32_t kTile = D * 256;                // [64][D] fp32
+  static constexpr uint32_t kKhi = 0;                       // D/32 x [64 keys][128 B]
+  static constexpr uint32_t kKlo = kKhi + kTile;
+  static constexpr uint32_t kVhi = kKlo + kTile;            // 2 x [D][128 B] (V^T)
+  static constexpr uint32_t kVlo = kVhi + kTile;
+  static constexpr uint32_t kRawK = kVlo + kTile;           // raw K, V as landed by TMA:
+  static constexpr uint32_t kRawV = kRawK + kTile;          //   D/32 x [64 keys][128 B]
+  static constexpr uint32_t kRingOff = kRawV + kTile;
+  static constexpr uint32_t kBar = kRingOff + kRing * sizeof(GroupEntry);
+  static constexpr uint32_t kAbort = kBar + kNumBars * 8;
+  static constexpr uint32_t kTmem = kAbort + 4;
+  static constexpr uint32_t kEnd = kTmem + 4;
+};
+
+__device__ __forceinline__ void bar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// Bounded wait for the phase of parity `parity`; false (and the abort flag raised) when the
+// bound runs out or another role raised the flag.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const uint32_t addr = smem_u32(bar);
+  const uint32_t tries = s_tries;
+  for (uint32_t i = 0; i < tries; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((i & 255u) == 255u && *abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+// the same for a whole warp (every lane polls; all agree on the outcome)
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort));
+}
+
+// Ring entry gi (waiting for it); false at the end of the work or on abort.
+__device__ __forceinline__ bool read_entry(const SparseParams& p, uint64_t* bars,
+                                           const volatile GroupEntry* ring, uint32_t gi,
+                                           volatile int* abort, bool whole_warp, GroupEntry& e) {
+  const int slot = (int)(gi % kRing);
+  const bool ok = whole_warp ? warp_wait(bars + kGFull + slot, (gi / kRing) & 1u, abort)
+                             : wait_bar(bars + kGFull + slot, (gi / kRing) & 1u, abort);
+  if (!ok) return false;
+  e.g = ring[slot].g;
+  e.e0 = ring[slot].e0;
+  e.e1 = ring[slot].e1;
+  e.vmask = ring[slot].vmask;
+  e.imask = ring[slot].imask;
+  return e.g < p.ngroups;
+}
+
+// Edge record of row `er` of the tile starting at edge c0 of a group ending at e1:
+// (edge, query index, keys taking part, 0); x = -1 for a row past the group.
+__device__ __forceinline__ int4 row_record(const SparseParams& p, int c0, int e1, int er,
+                                           int epc) {
+  if (er < epc && c0 + er < e1) return __ldg(p.edge_rec + c0 + er);
+  return make_int4(-1, 0, 0, 0);
+}
+
+// Warp 12: group scheduling, key masks and raw K/V staging.
+template <int D>
+__device__ void sched_role(const SparseParams& p, const SpMaps& maps, unsigned char* sm,
+                           uint32_t& issued) {
+  using L = Layout<D>;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
+  volatile GroupEntry* ring = reinterpret_cast<volatile GroupEntry*>(sm + L::kRingOff);
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+    tc::tma_prefetch_desc(&maps.k);
+    tc::tma_prefetch_desc(&maps.v);
+  }
+  for (uint32_t gi = 0;; ++gi) {
+    long long g = 0;
+    if (lane == 0) g = next_group(p);
+    g = __shfl_sync(0xffffffffu, g, 0);
+    const int slot = (int)(gi % kRing);
+    if (gi >= kRing && !warp_wait(bars + kGEmpty + slot, ((gi / kRing) - 1) & 1u, abort)) return;
+    uint64_t vmask = 0, imask = 0;
+    int row0 = -1;   // first row of page `lane` of the block in the page tensors
+    int e0 = 0, e1 = 0;
+    if (g < p.ngroups) {
+      const int h = (int)(g % p.hkv);
+      const int64_t bb = g / p.hkv;
+      const int blk = (int)(bb % p.nblk);
+      const int batch = (int)(bb / p.nblk);
+      // key states: 1 mapped, 2 invalid table reference, 0 unmapped or past the block
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int t = lane + 32 * k;
+        int state = 0;
+        if (t < p.block_size) {
+          const int64_t slot_t = (int64_t)blk * p.ppb + t / p.page_size;
+          if (slot_t < p.max_pages) {
+            const int64_t page = p.bt[(int64_t)batch * p.max_pages + slot_t];
+            state = page >= p.num_pages ? 2 : page >= 0 ? 1 : 0;
+          } else {
+            state = 2;
+          }
+        }
+        vmask |= (uint64_t)__ballot_sync(0xffffffffu, state == 1) << (32 * k);
+        imask |= (uint64_t)__ballot_sync(0xffffffffu, state == 2) << (32 * k);
+      }
+      if (lane < p.ppb) {
+        const int64_t slot_t = (int64_t)blk * p.ppb + lane;
+        if (slot_t < p.max_pages) {
+          const int64_t page = p.bt[(int64_t)batch * p.max_pages + slot_t];
+          if (page >= 0 && page < p.num_pages) row0 = (int)((page * p.hkv + h) * p.page_size);
+        }
+      }
+      e0 = p.group_off[g];
+      e1 = p.group_off[g + 1];
+    }
+    if (lane == 0) {
+      ring[slot].g = g;
+      ring[slot].e0 = e0;
+      ring[slot].e1 = e1;
+      ring[slot].vmask = vmask;
+      ring[slot].imask = imask;
+      bar_arrive(bars + kGFull + slot);   // release: the entry is visible to the waiters
+    }
+    if (g >= p.ngroups) return;
+    // the raw tiles are free once the converters finished the previous group's
+    if (gi >= 1 && !warp_wait(bars + kRawFree, (gi - 1) & 1u, abort)) return;
+    const uint32_t bits = __ballot_sync(0xffffffffu, row0 >= 0);
+    if (lane == 0)
+      tc::mbar_arrive_expect_tx(bars + kRawFull,
+                                (uint32_t)__popc(bits) * (uint32_t)p.page_size * D * 4u * 2u);
+    __syncwarp();
+    // testing hook: the first staging is announced but never copied, so the waits for it
+    // give up with nothing in flight
+    const bool withhold = p.withhold_copy && gi == 0;
+    if (row0 >= 0 && !withhold) {
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        const uint32_t off = (uint32_t)q * (kNK * 128) + (uint32_t)(lane * p.page_size) * 128u;
+        tc::tma_load_2d(sm + L::kRawK + off, &maps.k, q * 32, row0, bars + kRawFull);
+        tc::tma_load_2d(sm + L::kRawV + off, &maps.v, q * 32, row0, bars + kRawFull);
+      }
+    }
+    ++issued;
+  }
+}
+
+// Columns [C0, C0 + NC) of this thread's Q row (hi, lo) into its TMEM lane; zeros for a
+// padding row. The row's loads are all issued before any is used (one round trip).
+template <int D, int C0, int NC>
+__device__ __forceinline__ void load_q_cols(uint32_t lane_tm, const float* row, uint64_t pol) {
+  float v[NC];
+#pragma unroll
+  for (int k = 0; k < NC; k += 4) {
+    const float4 x = row ? ldg_hint(row + C0 + k, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[k] = x.x;
+    v[k + 1] = x.y;
+    v[k + 2] = x.z;
+    v[k + 3] = x.w;
+  }
+#pragma unroll
+  for (int c = 0; c < NC; c += 32) {
+    float* h = v + c;
+    float lo[32];
+#pragma unroll
+    for (int k = 0; k < 32; k += 2) {
+      const float x0 = h[k], x1 = h[k + 1];
+      h[k] = tf32_hi(x0);
+      h[k + 1] = tf32_hi(x1);
+      sub2(lo[k], lo[k + 1], x0, x1, h[k], h[k + 1]);
+    }
+    tc::tmem_st32(lane_tm + kTmQ + C0 + c, *reinterpret_cast<const float(*)[32]>(h));
+    tc::tmem_st32(lane_tm + kTmQ + D + C0 + c, lo);
+  }
+  tc::tmem_wait_st();
+}
+
+// Warps 8-11: K/V conversion per group, the upper Q columns per tile.
+template <int D>
+__device__ void convert_role(const SparseParams& p, unsigned char* sm, uint32_t tmem) {
+  using L = Layout<D>;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
+  const volatile GroupEntry* ring = reinterpret_cast<const volatile GroupEntry*>(sm + L::kRingOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp & 3, ct = wq * 32 + lane;   // TMEM quadrant; thread of the 128
+  const int r = ct;                               // tile row of this thread
+  const uint32_t lane_tm = tmem + ((uint32_t)(wq * 32) << 16);
+  const int epc = 128 / p.qhead, my_er = r / p.qhead, my_qh = r - (r / p.qhead) * p.qhead;
+  const uint64_t keep = l2_policy_last();
+  uint32_t t = 0;
+  for (uint32_t gi = 0;; ++gi) {
+    GroupEntry e;
+    if (!read_entry(p, bars, ring, gi, abort, true, e)) return;
+    const int h = (int)(e.g % p.hkv);
+    int4 rec = row_record(p, e.e0, e.e1, my_er, epc);
+    // K of this group: the raw tiles landed and every S of the previous group is done
+    if (!warp_wait(bars + kRawFull, gi & 1u, abort)) return;
+    if (gi > 0 && !warp_wait(bars + kKFree, (gi - 1) & 1u, abort)) return;
+    for (int i = ct; i < kNK * (D / 4); i += 128) {
+      const int tk = i / (D / 4), c = i % (D / 4);
+      const uint32_t off = (uint32_t)(c >> 3) * (kNK * 128) + tc::sw128(tk, c & 7);
+      float4 v = *reinterpret_cast<const float4*>(sm + L::kRawK + off);
+      if (!((e.vmask >> tk) & 1ull)) v = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 hi = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+      float4 lo;
+      sub2(lo.x, lo.y, v.x, v.y, hi.x, hi.y);
+      sub2(lo.z, lo.w, v.z, v.w, hi.z, hi.w);
+      *reinterpret_cast<float4*>(sm + L::kKhi + off) = hi;
+      *reinterpret_cast<float4*>(sm + L::kKlo + off) = lo;
+    }
+    tc::fence_async_shared();
+    __syncwarp();
+    if (lane == 0) bar_arrive(bars + kKReady);
+    bool first = true;
+    for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
+      // the Q columns of every row are free once S of the previous tile is done
+      if (t > 0 && !warp_wait(bars + kSFull, (t - 1) & 1u, abort)) return;
+      tc::fence_after_sync();
+      const float* row = rec.x >= 0 ? p.q + ((int64_t)rec.y * p.hq + h * p.qhead + my_qh) * D
+                                    : nullptr;
+      load_q_cols<D, D / 2, D / 2>(lane_tm, row, keep);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) bar_arrive(bars + kQReady);
+      if (c0 + epc < e.e1) rec = row_record(p, c0 + epc, e.e1, my_er, epc);
+      if (first) {   // V of this group once every O of the previous group is done
+        first = false;
+        if (gi > 0 && !warp_wait(bars + kVFree, (gi - 1) & 1u, abort)) return;
+        const int tk = lane + 32 * (wq & 1);
+        const bool live = (e.vmask >> tk) & 1ull;
+        for (int c = wq >> 1; c < D / 4; c += 2) {
+          float4 v = *reinterpret_cast<const float4*>(sm + L::kRawV + (uint32_t)(c >> 3) * (kNK * 128) +
+                                                      tc::sw128(tk, c & 7));
+          if (!live) v = make_float4(0.f, 0.f, 0.f, 0.f);
+          const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int d = c * 4 + k;
+            const uint32_t off = (uint32_t)(tk >> 5) * (D * 128) + (uint32_t)d * 128u +
+                                 ((uint32_t)(((tk & 31) >> 2) ^ (d & 7)) << 4) + (uint32_t)(tk & 3) * 4u;
+            const float hi = tf32_hi(x[k]);
+            *reinterpret_cast<float*>(sm + L::kVhi + off) = hi;
+            *reinterpret_cast<float*>(sm + L::kVlo + off) = x[k] - hi;
+          }
+        }
+        tc::fence_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          bar_arrive(bars + kVReady);
+          bar_arrive(bars + kRawFree);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) bar_arrive(bars + kGEmpty + (gi % kRing));
+  }
+}
+
+// Warps 4-7: the lower Q columns per tile; the O rows of the previous tile.
+template <int D>
+__device__ void store_role(const SparseParams& p, unsigned char* sm, uint32_t tmem) {
+  using L = Layout<D>;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
+  const volatile GroupEntry* ring = reinterpret_cast<const volatile GroupEntry*>(sm + L::kRingOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp & 3, r = wq * 32 + lane;
+  const uint32_t lane_tm = tmem + ((uint32_t)(wq * 32) << 16);
+  const int epc = 128 / p.qhead, my_er = r / p.qhead, my_qh = r - (r / p.qhead) * p.qhead;
+  const uint64_t keep = l2_policy_last();
+  // O rows of tile tt (partial index pi, -1 = padding row) to memory
+  auto store = [&](uint32_t tt, int pi) -> bool {
+    if (!warp_wait(bars + kPvDone, tt & 1u, abort)) return false;
+    tc::fence_after_sync();
+#pragma unroll 1
+    for (int ch = 0; ch < D / 32; ++ch) {
+      float o[32];
+      tc::tmem_ld32(lane_tm + kTmO + ch * 32, o);
+      tc::tmem_wait_ld();
+      if (pi >= 0) {
+        float4* dst = reinterpret_cast<float4*>(p.o + (int64_t)pi * D + ch * 32);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          __stcs(dst + k, make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]));
+      }
+    }
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) bar_arrive(bars + kOEmpty);
+    return true;
+  };
+  uint32_t t = 0;
+  int prev_pi = -1;
+  for (uint32_t gi = 0;; ++gi) {
+    GroupEntry e;
+    if (!read_entry(p, bars, ring, gi, abort, true, e)) break;
+    const int h = (int)(e.g % p.hkv);
+    int4 rec = row_record(p, e.e0, e.e1, my_er, epc);
+    for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
+      if (t > 0 && !warp_wait(bars + kSFull, (t - 1) & 1u, abort)) return;
+      tc::fence_after_sync();
+      const float* row = rec.x >= 0 ? p.q + ((int64_t)rec.y * p.hq + h * p.qhead + my_qh) * D
+                                    : nullptr;
+      load_q_cols<D, 0, D / 2>(lane_tm, row, keep);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) bar_arrive(bars + kQReady);
+      const int pi = rec.x >= 0 ? rec.x * p.qhead + my_qh : -1;
+      if (c0 + epc < e.e1) rec = row_record(p, c0 + epc, e.e1, my_er, epc);
+      if (t > 0 && !store(t - 1, prev_pi)) return;
+      prev_pi = pi;
+    }
+    __syncwarp();
+    if (lane == 0) bar_arrive(bars + kGEmpty + (gi % kRing));
+  }
+  if (t > 0 && !*abort) store(t - 1, prev_pi);
+}
+
+// Warps 0-3: the softmax of each tile row over the block's keys.
+template <int D>
+__device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t tmem,
+                             bool& bad) {
+  using L = Layout<D>;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
+  const volatile GroupEntry* ring = reinterpret_cast<const volatile GroupEntry*>(sm + L::kRingOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = warp * 32 + lane;
+  const uint32_t lane_tm = tmem + ((uint32_t)(warp * 32) << 16);
+  const int epc = 128 / p.qhead, my_er = r / p.qhead, my_qh = r - (r / p.qhead) * p.qhead;
+  const float sl2 = p.scale * kLog2e;
+  uint32_t t = 0;
+  for (uint32_t gi = 0;; ++gi) {
+    GroupEntry e;
+    if (!read_entry(p, bars, ring, gi, abort, true, e)) return;
+    int4 rec = row_record(p, e.e0, e.e1, my_er, epc);
+    for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
+      const int keys = rec.x >= 0 ? rec.z : 0;
+      const int pi = rec.x >= 0 ? rec.x * p.qhead + my_qh : -1;
+      if (c0 + epc < e.e1) rec = row_record(p, c0 + epc, e.e1, my_er, epc);
+      if (!warp_wait(bars + kSFull, t & 1u, abort)) return;
+      tc::fence_after_sync();
+      float s[64];
+      float (*s32)[32] = reinterpret_cast<float (*)[32]>(s);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {   // S = S_a + S_b, 32 keys at a time
+        float tmp[32];
+        tc::tmem_ld32(lane_tm + kTmSa + hf * 32, s32[hf]);
+        tc::tmem_ld32(lane_tm + kTmSb + hf * 32, tmp);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) add2(s32[hf][k], s32[hf][k + 1], tmp[k], tmp[k + 1]);
+      }
+      const uint64_t used = keys >= 64 ? ~0ull : ((1ull << keys) - 1ull);
+      if (e.imask & used) bad = true;
+      // keys that take part: mapped and inside the block (the rest score -1e30, and keys
+      // past the block never raise m above that sentinel either)
+      const uint64_t live = e.vmask & used;
+      const uint32_t live_lo = (uint32_t)live, live_hi = (uint32_t)(live >> 32);
+      // scores in base-2 units (scale * log2(e) * <q, k>): the weights are 2^(s - max);
+      // four partial maxima and sums keep the dependency chains short
+      float mp[4] = {kNegLarge, kNegLarge, kNegLarge, kNegLarge};
+#pragma unroll
+      for (int k = 0; k < 64; k += 2) {
+        const uint32_t word = k < 32 ? live_lo : live_hi;
+        float x0, x1;
+        fma2(x0, x1, s[k], s[k + 1], sl2, 0.f);
+        s[k] = ((word >> (k & 31)) & 1u) ? x0 : kNegLarge;
+        s[k + 1] = ((word >> ((k + 1) & 31)) & 1u) ? x1 : kNegLarge;
+        mp[k & 3] = fmaxf(mp[k & 3], s[k]);
+        mp[(k + 1) & 3] = fmaxf(mp[(k + 1) & 3], s[k + 1]);
+      }
+      const float m2 = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
+      // 2^(-1e30 - m) is exactly 0 for every finite m; with no key taking part m is the
+      // sentinel itself, and subtracting 0 instead keeps every weight 0
+      const float msub = m2 > 0.5f * kNegLarge ? m2 : 0.f;
+      float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < 64; k += 2) {
+        float d0, d1;
+        fma2(d0, d1, s[k], s[k + 1], 1.f, -msub);   // s - m, exactly as a subtraction
+        s[k] = ex2(d0);
+        s[k + 1] = ex2(d1);
+        add2(la[(k >> 1) & 3], lb[(k >> 1) & 3], s[k], s[k + 1]);
+      }
+      const float lrow = ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
+      // m in natural-log units (the -1e30 sentinel as is when no key takes part)
+      const float mrow = m2 > 0.5f * kNegLarge ? m2 * kLn2 : kNegLarge;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {   // P hi over S_a, P lo over S_b
+        float lo[32];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float w0 = s32[hf][k], w1 = s32[hf][k + 1];
+          s32[hf][k] = tf32_hi(w0);
+          s32[hf][k + 1] = tf32_hi(w1);
+          sub2(lo[k], lo[k + 1], w0, w1, s32[hf][k], s32[hf][k + 1]);
+        }
+        tc::tmem_st32(lane_tm + kTmSa + hf * 32, s32[hf]);
+        tc::tmem_st32(lane_tm + kTmSb + hf * 32, lo);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) bar_arrive(bars + kPFull);
+      if (pi >= 0) {
+        __stcs(p.m + pi, mrow);
+        __stcs(p.l + pi, lrow);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) bar_arrive(bars + kGEmpty + (gi % kRing));
+  }
+}
+
+// Lane 0 of warps 13, 14: S = Q K^T, issuer `which` of two (each its own accumulator).
+template <int D>
+__device__ void s_issue_role(const SparseParams& p, unsigned char* sm, uint32_t tmem, int which) {
+  using L = Layout<D>;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
+  const volatile GroupEntry* ring = reinterpret_cast<const volatile GroupEntry*>(sm + L::kRingOff);
+  const int epc = 128 / p.qhead;
+  constexpr int KS = D / 8;   // tf32 k-steps per product
+  const uint32_t idesc = idesc_tf32(128, kNK);
+  const uint32_t d_tm = tmem + (which == 0 ? kTmSa : kTmSb);
+  const uint32_t khi = smem_u32(sm + L::kKhi), klo = smem_u32(sm + L::kKlo);
+  // issuer 0: Qhi Khi and the first half of Qhi Klo; issuer 1: the second half of
+  // Qhi Klo and Qlo Khi
+  uint32_t t = 0;
+  for (uint32_t gi = 0;; ++gi) {
+    GroupEntry e;
+    if (!read_entry(p, bars, ring, gi, abort, false, e)) return;
+    if (!wait_bar(bars + kKReady, gi & 1u, abort)) return;
+    for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
+      if (!wait_bar(bars + kQReady, t & 1u, abort)) return;
+      // the S columns hold P of the previous tile until its O is done
+      if (t > 0 && !wait_bar(bars + kPvDone, (t - 1) & 1u, abort)) return;
+      tc::fence_after_sync();
+      int n = 0;
+#pragma unroll
+      for (int j = 0; j < 3 * KS / 2; ++j, ++n) {
+        const int g = which * (3 * KS / 2) + j;   // 0 .. 3 KS - 1 over (pass, ks)
+        const int pass = g / KS, ks = g % KS;
+        const uint32_t a = tmem + kTmQ + (pass == 2 ? (uint32_t)D : 0u) + (uint32_t)ks * 8u;
+        const uint32_t b = (pass == 1 ? klo : khi) + (uint32_t)(ks >> 2) * (kNK * 128) +
+                           (uint32_t)(ks & 3) * 32u;
+        mma_tf32(d_tm, a, tc::smem_desc(b, 16, 1024), idesc, n > 0 ? 1u : 0u);
+      }
+      tc::commit(bars + kSFull);
+      if (c0 + epc >= e.e1) tc::commit(bars + kKFree);
+    }
+    bar_arrive(bars + kGEmpty + (gi % kRing));
+  }
+}
+
+// Lane 0 of warp 15: O = P V (P hi from the S_a columns, P lo from the S_b columns).
+template <int D>
+__device__ void pv_issue_role(const SparseParams& p, unsigned char* sm, uint32_t tmem) {
+  using L = Layout<D>;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
+  const volatile GroupEntry* ring = reinterpret_cast<const volatile GroupEntry*>(sm + L::kRingOff);
+  const int epc = 128 / p.qhead;
+  const uint32_t idesc = idesc_tf32(128, D);
+  const uint32_t vhi = smem_u32(sm + L::kVhi), vlo = smem_u32(sm + L::kVlo);
+  uint32_t t = 0;
+  for (uint32_t gi = 0;; ++gi) {
+    GroupEntry e;
+    if (!read_entry(p, bars, ring, gi, abort, false, e)) return;
+    if (!wait_bar(bars + kVReady, gi & 1u, abort)) return;
+    for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
+      if (!wait_bar(bars + kPFull, t & 1u, abort)) return;
+      if (t > 0 && !wait_bar(bars + kOEmpty, (t - 1) & 1u, abort)) return;
+      tc::fence_after_sync();
+      int n = 0;
+#pragma unroll
+      for (int pass = 0; pass < 3; ++pass) {
+        const uint32_t a = tmem + (pass == 2 ? kTmSb : kTmSa);
+        const uint32_t b = pass == 1 ? vlo : vhi;
+#pragma unroll
+        for (int ks = 0; ks < kNK / 8; ++ks, ++n)
+          mma_tf32(tmem + kTmO, a + (uint32_t)ks * 8u,
+                   tc::smem_desc(b + (uint32_t)(ks >> 2) * (D * 128) + (uint32_t)(ks & 3) * 32u,
+                                 16, 1024),
+                   idesc, n > 0 ? 1u : 0u);
+      }
+      tc::commit(bars + kPvDone);
+      if (c0 + epc >= e.e1) tc::commit(bars + kVFree);
+    }
+    bar_arrive(bars + kGEmpty + (gi % kRing));
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_tc_kernel(SparseParams p, const __grid_constant__ SpMaps maps) {
@@ -456,20 +939,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint32_t* sMask = reinterpret_cast<uint32_t*>(sm + L::kValid);   // {mapped, invalid} x 64 bits
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::kTmem);
-  volatile int64_t* snext = reinterpret_cast<volatile int64_t*>(sm + L::kNext);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, half = warp >> 2;
-  const int r = quarter * 32 + lane;   // TMEM lane / tile row of this thread
-  const uint32_t tries = p.wait_tries ? p.wait_tries : kTries;
   if (tid == 0) {
-    tc::mbar_init(bar, 1);
-    tc::mbar_init(bar + 1, 1);
-    tc::mbar_init(bar + 2, 1);   // raw K / V landed (count 1 + tx)
+    for (int i = 0; i < kRing; ++i) {
+      tc::mbar_init(bars + kGFull + i, 1);
+      tc::mbar_init(bars + kGEmpty + i, 15);
+    }
+    tc::mbar_init(bars + kRawFull, 1);
+    tc::mbar_init(bars + kRawFree, 4);
+    tc::mbar_init(bars + kKReady, 4);
+    tc::mbar_init(bars + kKFree, 2);
+    tc::mbar_init(bars + kVReady, 4);
+    tc::mbar_init(bars + kVFree, 1);
+    tc::mbar_init(bars + kQReady, 8);
+    tc::mbar_init(bars + kSFull, 2);
+    tc::mbar_init(bars + kPFull, 4);
+    tc::mbar_init(bars + kPvDone, 1);
+    tc::mbar_init(bars + kOEmpty, 4);
+    tc::mbar_init(bars + kDrainS0, 1);
+    tc::mbar_init(bars + kDrainS1, 1);
+    tc::mbar_init(bars + kDrainPv, 1);
+    *abort = 0;
+    s_tries = p.wait_tries ? p.wait_tries : kTries;
     tc::mbar_init_fence();
-    *snext = next_group(p);
   }
   if (warp == 0) {
     tc::tmem_alloc(tslot, 512);
@@ -479,296 +974,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
-  const uint32_t lane_tm = tmem + ((uint32_t)(quarter * 32) << 16);
-  int64_t g = *snext;
-  uint64_t* rbar = bar + 2;
-  constexpr int kStageWarp = 7;
-  if (warp == kStageWarp && g < p.ngroups) {
-    if (lane == 0) {
-      tc::tma_prefetch_desc(&maps.k);
-      tc::tma_prefetch_desc(&maps.v);
-    }
-    // testing hook: the first staging is announced but never copied, so the wait for it
-    // gives up with nothing in flight
-    stage_raw<D>(p, maps, sm, g, rbar, p.withhold_copy != 0);
-  }
-  uint32_t raw_issued = g < p.ngroups ? 1u : 0u, raw_used = 0;
-  uint32_t phase = 0;
-  bool ok = true, bad = false;
-  const uint64_t keep = l2_policy_last();
-  // edge of this thread's row in a tile starting at edge c0 of a group ending at e1:
-  // (edge, query index, block_len), fetched one tile ahead of its use
-  const int epc = 128 / p.qhead;
-  const int my_er = r / p.qhead, my_qh = r - my_er * p.qhead;
-  auto row_edge = [&](int c0, int e1, int& e, int& qi, int& bl) {
-    e = -1;
-    qi = 0;
-    bl = 0;
-    if (my_er < epc && c0 + my_er < e1) {
-      e = p.perm[c0 + my_er];
-      qi = p.meta[(int64_t)e * 5];
-      bl = edge_keys(p, qi, p.meta[(int64_t)e * 5 + 2], p.meta[(int64_t)e * 5 + 4]);
-    }
-  };
-  int nx_e, nx_q, nx_bl;
-  if (g < p.ngroups) row_edge(p.group_off[g], p.group_off[g + 1], nx_e, nx_q, nx_bl);
-  // Row r of the warp's [32][32] fp32 transpose buffer holds its 16-byte chunk q at chunk
-  // q ^ (r & 7): a lane's own row and a warp-wide 4-row x 128-byte slab both map to
-  // distinct banks. Global rows are read and written whole (128 bytes per 8 lanes)
-  // instead of one row per lane.
-  float* xf = reinterpret_cast<float*>(sm + L::kXfer) + warp * 1024;
-  // columns [col0, col0 + ncols) of the Q rows of this warp's 32 TMEM lanes (hi, lo) into
-  // TMEM; zeros for padding rows
-  auto load_q = [&](int h, int e, int qi, int col0, int ncols) {
-    const float* myrow = e >= 0 ? p.q + ((int64_t)qi * p.hq + h * p.qhead + my_qh) * D : nullptr;
-    const int q4 = lane & 7;
-    for (int ch = 0; ch < ncols / 32; ++ch) {
-      const int cbase = col0 + ch * 32;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {   // 4 rows x 32 floats per instruction
-        const int rr = i * 4 + (lane >> 3);
-        const float* src = reinterpret_cast<const float*>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(myrow), rr));
-        const float4 v = src ? ldg_hint(src + cbase + q4 * 4, keep) : make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(xf + rr * 32 + ((q4 ^ (rr & 7)) << 2)) = v;
-      }
-      __syncwarp();
-      float vh[32], vl[32];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(xf + lane * 32 + ((q ^ (lane & 7)) << 2));
-        const float x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) vh[q * 4 + j] = tf32_hi(x[j]);
-        sub2(vl[q * 4], vl[q * 4 + 1], x[0], x[1], vh[q * 4], vh[q * 4 + 1]);
-        sub2(vl[q * 4 + 2], vl[q * 4 + 3], x[2], x[3], vh[q * 4 + 2], vh[q * 4 + 3]);
-      }
-      __syncwarp();
-      tc::tmem_st32(lane_tm + 256 + cbase, vh);
-      tc::tmem_st32(lane_tm + 384 + cbase, vl);
-    }
-    tc::tmem_wait_st();
-  };
-  const uint32_t idesc_s = idesc_tf32(128, kNK), idesc_o = idesc_tf32(128, D);
-  while (g < p.ngroups && ok) {
-    ok = __syncthreads_and(tc::mbar_wait(rbar, raw_used & 1u, tries));
-    ++raw_used;
-    if (!ok) break;
-    const uint8_t* rValid = sm + L::kRValid;
-    // raw -> tf32 (hi, lo) tiles: K in place (the raw layout is the K-major tile layout),
-    // V transposed (lane = key, conflict-free); keys not mapped become zeros
-    for (int i = tid; i < kNK * (D / 4); i += kThreads) {
-      const int t = i / (D / 4), c = i % (D / 4);
-      const uint32_t off = (uint32_t)(c >> 3) * (kNK * 128) + tc::sw128(t, c & 7);
-      float4 v = *reinterpret_cast<const float4*>(sm + L::kRawK + off);
-      if (rValid[t] != 1) v = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 hi = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
-      float4 lo;
-      sub2(lo.x, lo.y, v.x, v.y, hi.x, hi.y);
-      sub2(lo.z, lo.w, v.z, v.w, hi.z, hi.w);
-      *reinterpret_cast<float4*>(sm + L::kKhi + off) = hi;
-      *reinterpret_cast<float4*>(sm + L::kKlo + off) = lo;
-    }
-    {
-      const int t = lane + 32 * (warp & 1);
-      const bool live = rValid[t] == 1;
-      for (int c = warp >> 1; c < D / 4; c += kThreads / 64) {
-        float4 v = *reinterpret_cast<const float4*>(sm + L::kRawV + (uint32_t)(c >> 3) * (kNK * 128) +
-                                                    tc::sw128(t, c & 7));
-        if (!live) v = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int d = c * 4 + k;
-          const uint32_t off = (uint32_t)(t >> 5) * (D * 128) + (uint32_t)d * 128u +
-                               ((uint32_t)(((t & 31) >> 2) ^ (d & 7)) << 4) + (uint32_t)(t & 3) * 4u;
-          const float hi = tf32_hi(x[k]);
-          *reinterpret_cast<float*>(sm + L::kVhi + off) = hi;
-          *reinterpret_cast<float*>(sm + L::kVlo + off) = x[k] - hi;
-        }
-      }
-    }
-    if (warp < 2) {   // the key masks of this group, 32 keys per warp
-      const uint8_t st = rValid[tid];
-      const uint32_t vb = __ballot_sync(0xffffffffu, st == 1);
-      const uint32_t ib = __ballot_sync(0xffffffffu, st == 2);
-      if (lane == 0) {
-        sMask[warp] = vb;
-        sMask[2 + warp] = ib;
-      }
-    }
-    tc::fence_async_shared();
-    if (tid == 0) *snext = next_group(p);
-    __syncthreads();
-    // the raw buffers are free: stage the next group behind this one's compute
-    const int64_t gn = *snext;
-    if (gn < p.ngroups) {
-      if (warp == kStageWarp) stage_raw<D>(p, maps, sm, gn, rbar);
-      ++raw_issued;
-    }
-    // key masks of this group: bit t of vmask = mapped, of imask = invalid reference
-    const uint64_t vmask = reinterpret_cast<const uint64_t*>(sMask)[0];
-    const uint64_t imask = reinterpret_cast<const uint64_t*>(sMask)[1];
-    const int e0 = p.group_off[g], e1 = p.group_off[g + 1];
-    const int h = (int)(g % p.hkv);
-    for (int c0 = e0; c0 < e1 && ok; c0 += epc) {
-      // this tile's rows (fetched one tile ahead); Q of a group's first tile is loaded here
-      // by all warps (column halves), later tiles' Q during the previous tile's epilogue
-      const int cur_bl = nx_e >= 0 ? nx_bl : 0;
-      const int cur_pi = nx_e >= 0 ? nx_e * p.qhead + my_qh : -1;
-      if (c0 == e0) load_q(h, nx_e, nx_q, half * (D / 2), D / 2);
-      tc::fence_before_sync();
-      __syncthreads();
-      if (tid == 0) {   // S = Qhi Khi + Qhi Klo + Qlo Khi
-        tc::fence_after_sync();
-        int n = 0;
-#pragma unroll
-        for (int pass = 0; pass < 3; ++pass) {
-          const uint32_t a = tmem + (pass == 2 ? 384u : 256u);
-          const uint32_t b = smem_u32(sm + (pass == 1 ? L::kKlo : L::kKhi));
-#pragma unroll
-          for (int ks = 0; ks < D / 8; ++ks, ++n)
-            mma_tf32(tmem, a + ks * 8,
-                     tc::smem_desc(b + (ks >> 2) * (kNK * 128) + (ks & 3) * 32, 16, 1024),
-                     idesc_s, n > 0 ? 1u : 0u);
-        }
-        tc::commit(bar);
-      }
-      // the next tile's rows (later in this group, else the first tile of the next one),
-      // fetched while S is computed: the dependent loads stall here, not on the next tile
-      if (c0 + epc < e1) row_edge(c0 + epc, e1, nx_e, nx_q, nx_bl);
-      else if (gn < p.ngroups) row_edge(p.group_off[gn], p.group_off[gn + 1], nx_e, nx_q, nx_bl);
-      ok = __syncthreads_and(tc::mbar_wait(bar, phase & 1u, tries));
-      ++phase;
-      if (!ok) break;
-      tc::fence_after_sync();
-      float mrow = kNegLarge, lrow = 0.f;
-      if (half == 0) {   // softmax of row r over the block's keys
-        float s[64];
-        float (*s32)[32] = reinterpret_cast<float (*)[32]>(s);
-        tc::tmem_ld32(lane_tm, s32[0]);
-        tc::tmem_ld32(lane_tm + 32, s32[1]);
-        tc::tmem_wait_ld();
-        const int bl = cur_bl;
-        const uint64_t used = bl >= 64 ? ~0ull : ((1ull << bl) - 1ull);
-        if (imask & used) bad = true;
-        // keys that take part: mapped and inside the block (the rest score -1e30, and keys
-        // past the block never raise m above that sentinel either)
-        const uint64_t live = vmask & used;
-        const uint32_t live_lo = (uint32_t)live, live_hi = (uint32_t)(live >> 32);
-        // scores in base-2 units (scale * log2(e) * <q, k>): the weights are 2^(s - max);
-        // four partial maxima and sums keep the dependency chains short
-        // (pairs of keys go through one f32x2 instruction, each rounded as the scalar one)
-        const float sl2 = p.scale * kLog2e;
-        float mp[4] = {kNegLarge, kNegLarge, kNegLarge, kNegLarge};
-#pragma unroll
-        for (int t = 0; t < 64; t += 2) {
-          const uint32_t word = t < 32 ? live_lo : live_hi;
-          float x0, x1;
-          fma2(x0, x1, s[t], s[t + 1], sl2, 0.f);
-          s[t] = ((word >> (t & 31)) & 1u) ? x0 : kNegLarge;
-          s[t + 1] = ((word >> ((t + 1) & 31)) & 1u) ? x1 : kNegLarge;
-          mp[t & 3] = fmaxf(mp[t & 3], s[t]);
-          mp[(t + 1) & 3] = fmaxf(mp[(t + 1) & 3], s[t + 1]);
-        }
-        const float m2 = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
-        // 2^(-1e30 - m) is exactly 0 for every finite m; with no key taking part m is the
-        // sentinel itself, and subtracting 0 instead keeps every weight 0
-        const float msub = m2 > 0.5f * kNegLarge ? m2 : 0.f;
-        float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int t = 0; t < 64; t += 2) {
-          float d0, d1;
-          fma2(d0, d1, s[t], s[t + 1], 1.f, -msub);   // s - m, exactly as a subtraction
-          s[t] = ex2(d0);
-          s[t + 1] = ex2(d1);
-          add2(la[(t >> 1) & 3], lb[(t >> 1) & 3], s[t], s[t + 1]);
-        }
-        lrow = ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
-        // m in natural-log units (the -1e30 sentinel as is when no key takes part)
-        mrow = m2 > 0.5f * kNegLarge ? m2 * 0.6931471805599453f : kNegLarge;
-        float ph[32], pl[32];
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-#pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            ph[k] = tf32_hi(s[ch * 32 + k]);
-            ph[k + 1] = tf32_hi(s[ch * 32 + k + 1]);
-            sub2(pl[k], pl[k + 1], s[ch * 32 + k], s[ch * 32 + k + 1], ph[k], ph[k + 1]);
-          }
-          tc::tmem_st32(lane_tm + 256 + ch * 32, ph);
-          tc::tmem_st32(lane_tm + 320 + ch * 32, pl);
-        }
-        tc::tmem_wait_st();
-      }
-      tc::fence_before_sync();
-      __syncthreads();
-      if (tid == 0) {   // O = Phi Vhi + Phi Vlo + Plo Vhi
-        tc::fence_after_sync();
-        int n = 0;
-#pragma unroll
-        for (int pass = 0; pass < 3; ++pass) {
-          const uint32_t a = tmem + (pass == 2 ? 320u : 256u);
-          const uint32_t b = smem_u32(sm + (pass == 1 ? L::kVlo : L::kVhi));
-#pragma unroll
-          for (int ks = 0; ks < kNK / 8; ++ks, ++n)
-            mma_tf32(tmem + 64, a + ks * 8,
-                     tc::smem_desc(b + (ks >> 2) * (D * 128) + (ks & 3) * 32, 16, 1024),
-                     idesc_o, n > 0 ? 1u : 0u);
-        }
-        tc::commit(bar);
-      }
-      ok = __syncthreads_and(tc::mbar_wait(bar, phase & 1u, tries));
-      ++phase;
-      if (!ok) break;
-      tc::fence_after_sync();
-      if (half == 0) {   // write the partials of this tile (full rows, 128 bytes per 8 lanes)
-        const int q4 = lane & 7;
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          float o[32];
-          tc::tmem_ld32(lane_tm + 64 + ch * 32, o);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(xf + lane * 32 + ((q ^ (lane & 7)) << 2)) =
-                make_float4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]);
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = i * 4 + (lane >> 3);
-            const int pi = __shfl_sync(0xffffffffu, cur_pi, rr);
-            const float4 v = *reinterpret_cast<const float4*>(xf + rr * 32 + ((q4 ^ (rr & 7)) << 2));
-            if (pi >= 0) __stcs(reinterpret_cast<float4*>(p.o + (int64_t)pi * D + ch * 32 + q4 * 4), v);
-          }
-          __syncwarp();
-        }
-        if (cur_pi >= 0) {
-          __stcs(p.m + cur_pi, mrow);
-          __stcs(p.l + cur_pi, lrow);
-        }
-      } else if (c0 + epc < e1) {   // meanwhile the next tile's Q replaces P
-        load_q(h, nx_e, nx_q, 0, D);
-      }
-      tc::fence_before_sync();
-      __syncthreads();   // the next tile's S = Q K^T follows
-      tc::fence_after_sync();
-    }
-    g = gn;
-  }
-  if (!ok) {
-    // a wait gave up: let what this CTA issued finish before leaving
-    if (tid == 0) {
-      flag_status(p.status, PKV_DEV_TIMEOUT);
-      tc::commit(bar + 1);
-      tc::mbar_wait(bar + 1, 0, tries);
-      if (raw_issued > raw_used) tc::mbar_wait(rbar, raw_used & 1u, tries);
-    }
+  bool bad = false;
+  uint32_t issued = 0;
+  if (warp < 4) {
+    softmax_role<D>(p, sm, tmem, bad);
+  } else if (warp < 8) {
+    store_role<D>(p, sm, tmem);
+  } else if (warp < 12) {
+    convert_role<D>(p, sm, tmem);
+  } else if (warp == kSchedWarp) {
+    sched_role<D>(p, maps, sm, issued);
+    // a wait gave up: the last staging must land before the CTA leaves
+    if (*abort && issued > 0)
+      tc::mbar_wait(bars + kRawFull, (issued - 1) & 1u, s_tries);
+  } else if (lane == 0) {
+    const int drain = warp == kIssueS0 ? kDrainS0 : warp == kIssueS1 ? kDrainS1 : kDrainPv;
+    if (warp == kIssuePv)
+      pv_issue_role<D>(p, sm, tmem);
+    else
+      s_issue_role<D>(p, sm, tmem, warp - kIssueS0);
+    // every MMA this thread issued completes before the CTA frees its tensor memory
+    tc::commit(bars + drain);
+    tc::mbar_wait(bars + drain, 0, s_tries);
   }
   if (bad) flag_status(p.status, PKV_DEV_BAD_EDGE);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  if (tid == 0 && *abort) flag_status(p.status, PKV_DEV_TIMEOUT);
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
