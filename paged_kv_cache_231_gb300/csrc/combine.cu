@@ -9,6 +9,8 @@
 // are all in flight together; out = row / L, lse = M + ln L.
 #include <math.h>
 
+#include <atomic>
+
 #include "device_common.cuh"
 #include "internal.h"
 
@@ -18,10 +20,8 @@ namespace {
 constexpr int kCombineWarps = 4;
 
 template <int D, bool PAGED, bool OUT_F16>
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(CombineParams p) {
+__device__ __forceinline__ void combine_row(const CombineParams& p, int64_t row, int lane) {
   constexpr int V = D / 32;  // elements per lane
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   int64_t g0, g1, out_row;
   int64_t lanes = p.lanes, c = 0;
   if (PAGED) {
@@ -109,18 +109,45 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(CombinePara
   if (p.lse && lane == 0) p.lse[out_row] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
+// Persistent: each warp takes rows warp, warp + W, ... (W = the grid's warps), so the
+// whole merge runs in one wave of resident blocks instead of one short block per 4 rows.
+template <int D, bool PAGED, bool OUT_F16>
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(CombineParams p,
+                                                                      int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t W = (int64_t)gridDim.x * kCombineWarps;
+  for (int64_t row = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5); row < rows;
+       row += W)
+    combine_row<D, PAGED, OUT_F16>(p, row, lane);
+}
+
+// resident blocks of the combine kernel per SM (2048 threads / 128)
+constexpr int kCombineBlocksPerSm = 16;
+
 template <int D>
 cudaError_t launch_d(const CombineParams& p, int64_t rows, cudaStream_t s) {
-  const unsigned grid = (unsigned)((rows + kCombineWarps - 1) / kCombineWarps);
+  static std::atomic<int> sms_cache{0};
+  int sms = sms_cache.load(std::memory_order_relaxed);
+  if (sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+      sms = 152;
+    sms_cache.store(sms, std::memory_order_relaxed);
+  }
+  const int64_t need = (rows + kCombineWarps - 1) / kCombineWarps;
+  const int64_t cap = (int64_t)sms * kCombineBlocksPerSm;
+  const unsigned grid = (unsigned)(need < cap ? need : cap);
   if (grid == 0) return cudaSuccess;
   const bool paged = p.slot_token != nullptr;
   ProfScope ps("combine", s);
   if (paged)
-    combine_kernel<D, true, true><<<grid, kCombineWarps * 32, 0, s>>>(p);
+    combine_kernel<D, true, true><<<grid, kCombineWarps * 32, 0, s>>>(p, rows);
   else if (p.out_f16)
-    combine_kernel<D, false, true><<<grid, kCombineWarps * 32, 0, s>>>(p);
+    combine_kernel<D, false, true><<<grid, kCombineWarps * 32, 0, s>>>(p, rows);
   else
-    combine_kernel<D, false, false><<<grid, kCombineWarps * 32, 0, s>>>(p);
+    combine_kernel<D, false, false><<<grid, kCombineWarps * 32, 0, s>>>(p, rows);
   return cudaGetLastError();
 }
 

@@ -68,15 +68,28 @@ __global__ void sparse_count_kernel(SparseParams p) {
 
 // exclusive scan of group_count into group_off (one CTA); clears the fill cursors. Thread i
 // owns the i-th run of ceil(ngroups / 1024) consecutive groups: the run totals are scanned
-// across the block (warp shuffles), then each thread walks its run.
+// across the block (warp shuffles), then each thread walks its run. Runs of 16 groups (the
+// common case) are read and written as four 16-byte vectors, so a thread's run costs one
+// memory round trip instead of sixteen.
 __global__ void __launch_bounds__(1024) sparse_scan_kernel(SparseParams p) {
   __shared__ int warp_tot[32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t per = (p.ngroups + 1023) / 1024;
   const int64_t g0 = (int64_t)threadIdx.x * per;
   const int64_t g1 = g0 + per < p.ngroups ? g0 + per : p.ngroups;
+  // whole vectors: the workspace arrays are 256-byte aligned, g0 is a multiple of 16
+  const bool vec = per == 16 && g1 == g0 + 16;
+  int4 c4[4];
   int run = 0;
-  for (int64_t g = g0; g < g1; ++g) run += p.group_count[g];
+  if (vec) {
+    const int4* src = reinterpret_cast<const int4*>(p.group_count + g0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c4[k] = src[k];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) run += c4[k].x + c4[k].y + c4[k].z + c4[k].w;
+  } else {
+    for (int64_t g = g0; g < g1; ++g) run += p.group_count[g];
+  }
   int x = run;   // inclusive scan of the run totals
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -96,10 +109,26 @@ __global__ void __launch_bounds__(1024) sparse_scan_kernel(SparseParams p) {
   }
   __syncthreads();
   int off = (w > 0 ? warp_tot[w - 1] : 0) + x - run;
-  for (int64_t g = g0; g < g1; ++g) {
-    p.group_off[g] = off;
-    p.group_cursor[g] = 0;
-    off += p.group_count[g];
+  if (vec) {
+    int4* dst = reinterpret_cast<int4*>(p.group_off + g0);
+    int4* cur = reinterpret_cast<int4*>(p.group_cursor + g0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      int4 o4;
+      o4.x = off;
+      o4.y = o4.x + c4[k].x;
+      o4.z = o4.y + c4[k].y;
+      o4.w = o4.z + c4[k].z;
+      off = o4.w + c4[k].w;
+      dst[k] = o4;
+      cur[k] = make_int4(0, 0, 0, 0);
+    }
+  } else {
+    for (int64_t g = g0; g < g1; ++g) {
+      p.group_off[g] = off;
+      p.group_cursor[g] = 0;
+      off += p.group_count[g];
+    }
   }
   if (threadIdx.x == 1023) p.group_off[p.ngroups] = warp_tot[31];
 }
