@@ -385,7 +385,7 @@ def setup_paged(name, args):
         w.work, w.dtype, w.tokens = None, "f16", case.num_tokens
         w.dominant, w.dom_work, w.bound, w.dom_unit = "single_pass", (kvb + qb + ob) / 1e9, \
             "hbm", "GB/s"
-        w.traffic_summary, w.traffic_sources = None, []
+        w.traffic_summary, w.traffic_sources = "single_pass_tiny_decode.md", ATTN_SOURCES
     elif name.startswith("llama8b_decode"):
         kvb, qb, ob = decode_bytes(case)
         w.work, w.dtype = (kvb + qb + ob) / 1e9, "f16"
