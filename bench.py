@@ -767,7 +767,8 @@ def main():
     dom_ms, dom_n = B.pkv_profiler_query(w.dominant)
     kernel_ms = {k: B.pkv_profiler_query(k) for k in
                  ("prologue", "attention", "prefill_tc", "decode_split", "combine",
-                  "single_pass", "scatter", "sparse_group", "sparse_partials", "append")}
+                  "single_pass", "scatter", "sparse_group", "sparse_qsplit", "sparse_partials",
+                  "append")}
     B.pkv_profiler_reset()
 
     e2e = None

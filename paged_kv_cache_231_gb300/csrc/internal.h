@@ -197,6 +197,10 @@ struct SparseParams {
   int32_t* group_cursor;   // [ngroups]
   int32_t* perm;           // [E]
   int4* edge_rec;          // [E] (edge, q_idx, block_len clipped to block_size, 0), grouped order
+  // fp32 tensor-core path: Q rows [Tq * hq] split into fp16 (hi, lo) rows scaled by 2^qshift
+  __half* qhi;
+  __half* qlo;
+  int32_t* qshift;
   // testing hook (pkv_testing_wait_limit), as in AttnParams
   uint32_t wait_tries;
   int withhold_copy;
@@ -240,6 +244,11 @@ __device__ __forceinline__ int edge_keys(const SparseParams& p, int q_idx, int b
 }
 // fp16 partials (sparse16.cu); the runtime has checked the shapes it takes
 cudaError_t launch_sparse_tc16(const SparseParams& p, cudaStream_t s);
+// Whether fp32 partials of this shape run on the tensor core (sparse.cu); such calls need
+// the split Q rows in their workspace. pool_rows = num_pages * hkv * page_size and
+// q_rows = num_queries * hq (callers pass INT64_MAX when a product would overflow).
+bool sparse_tc_shape(int D, int block_size, int qhead, int page_size, int ppb,
+                     int64_t pool_rows, int64_t q_rows);
 
 // testing hook of the bounded waits (runtime.cpp): current poll bound (0 = default) and
 // whether tensor-core kernels withhold their first bulk copy

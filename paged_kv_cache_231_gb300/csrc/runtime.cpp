@@ -635,6 +635,16 @@ int pkv_kv_append_rotary(const pkv_kv_append_args* a, void* stream) {
 
 // ---------------------------------------------------------------- block-sparse
 namespace {
+// fp32 calls whose shape runs on the tensor core take Q as split fp16 rows (workspace)
+bool sparse_split_q(const pkv_sparse_args* a) {
+  // the factors are positive and at most INT32_MAX here (checked before the call)
+  const int64_t hp = a->hkv * a->page_size;
+  const int64_t pool = a->num_pages <= INT32_MAX / hp ? a->num_pages * hp : INT64_MAX;
+  const int64_t qrows = a->num_queries <= INT32_MAX / a->hq ? a->num_queries * a->hq : INT64_MAX;
+  return a->dtype != PKV_F16 && a->num_queries > 0 &&
+         sparse_tc_shape((int)a->head_dim, (int)a->block_size, (int)a->qhead,
+                         (int)a->page_size, (int)a->pages_per_block, pool, qrows);
+}
 int check_sparse(const pkv_sparse_args* a, int64_t* nblk, int64_t* ngroups, size_t* bytes) {
   if (!a) return PKV_ERR_NULL;
   // the sizes below are int64 products of these: bound the factors first
@@ -662,6 +672,10 @@ int check_sparse(const pkv_sparse_args* a, int64_t* nblk, int64_t* ngroups, size
   *ngroups = ng;
   *bytes = 2 * align_up(4 * (size_t)(ng + 1)) + align_up(4 * (size_t)ng) +
            align_up(4 * (size_t)a->num_edges) + align_up(16 * (size_t)a->num_edges);
+  if (sparse_split_q(a)) {   // split Q rows: hi, lo (fp16) and the shift of each row
+    const size_t rows = (size_t)a->num_queries * (size_t)a->hq;
+    *bytes += 2 * align_up(rows * (size_t)a->head_dim * 2) + align_up(rows * 4);
+  }
   return PKV_OK;
 }
 }  // namespace
@@ -734,6 +748,15 @@ int pkv_sparse_attention_partials(const pkv_sparse_args* a, void* workspace,
   p.perm = reinterpret_cast<int32_t*>(ws + off);
   off += align_up(4 * (size_t)a->num_edges);
   p.edge_rec = reinterpret_cast<int4*>(ws + off);
+  off += align_up(16 * (size_t)a->num_edges);
+  if (sparse_split_q(a)) {
+    const size_t rows = (size_t)a->num_queries * (size_t)a->hq;
+    p.qhi = reinterpret_cast<__half*>(ws + off);
+    off += align_up(rows * (size_t)a->head_dim * 2);
+    p.qlo = reinterpret_cast<__half*>(ws + off);
+    off += align_up(rows * (size_t)a->head_dim * 2);
+    p.qshift = reinterpret_cast<int32_t*>(ws + off);
+  }
   return launch_status(launch_sparse(p, static_cast<cudaStream_t>(stream)));
 }
 

@@ -7,7 +7,8 @@
 // rows for every lane and edge. Here the edges are first grouped by (batch, kv head,
 // block) with a device counting sort; the block's K and V are staged in shared memory
 // once for the partials of every edge that names it. Head sizes 64 / 128 with blocks of
-// at most 64 keys run both products on the tensor core in 3xTF32 (sparse_tc_kernel);
+// at most 64 keys run both products on the tensor core from fp16 (hi, lo) splits of the
+// fp32 operands, each block or half row scaled by a power of two (sparse_tc_kernel);
 // other shapes take 64 query rows (edges x lanes) at a time with register-tiled fp32 FMA.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -342,51 +343,80 @@ __global__ void __launch_bounds__(kSpThreads, 2) sparse_partials_kernel(SparsePa
   if (bad) flag_status(p.status, PKV_DEV_BAD_EDGE);
 }
 
-// ---- tensor-core partials: 3xTF32 on tcgen05 ----------------------------------------
+// ---- tensor-core partials from split fp16 operands on tcgen05 -----------------------
 // For head size 64/128 and blocks of at most 64 keys. A persistent CTA per SM takes
 // (batch, block, kv head) groups from a counter. The group's raw fp32 K and V rows are
-// staged by TMA, then split into tf32 pairs x = hi + lo (hi = x rounded to tf32,
-// lo = x - hi) in 128-byte-swizzled K-major tiles: K [64 keys][D] and V^T [D][64 keys].
-// For each tile of 128 query rows (edges x query heads) Q (hi, lo) goes to TMEM and
-// S = Q K^T is accumulated from three tf32 products (hi*hi + hi*lo + lo*hi, relative
-// error about 2^-22, i.e. fp32 level); one thread per row forms the partial's max,
+// staged by TMA and split in place into fp16 pairs x 2^s = hi + lo (s a power-of-two
+// scale per block) in 128-byte-swizzled K-major tiles [64 keys][D]. For each tile of 128
+// query rows (edges x query heads) Q (hi, lo), scaled per half row, goes to TMEM and
+// S = Q K^T is accumulated from three fp16 products (hi*hi + hi*lo + lo*hi, relative
+// error about 2^-21, i.e. fp32 level); one thread per row forms the partial's max,
 // weights and sum, writes the weights (hi, lo) back to TMEM, and O = P V is accumulated
 // the same way.
 namespace tcs {
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-  return (1u << 4)                      // D format: f32
-         | (2u << 7) | (2u << 10)       // A, B format: tf32
-         | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// L2 residency: the partials stream through once (evict first on store); Q rows are
-// re-read by every edge that names their query (evict last).
+// L2 residency: Q rows are re-read by every edge that names their query (evict last).
 __device__ __forceinline__ uint64_t l2_policy_last() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
   return pol;
 }
-__device__ __forceinline__ float4 ldg_hint(const float* gmem, uint64_t pol) {
-  float4 v;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;\n"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "l"(gmem), "l"(pol));
-  return v;
-}
 
-// x rounded to the nearest tf32 (low 13 mantissa bits cleared)
-__device__ __forceinline__ float tf32_hi(float x) {
-  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+// ---- fp32 products from split fp16 operands ------------------------------------------
+// An fp32 operand (a half row of Q, a block of K or V) is scaled by a power of two 2^s,
+// chosen from its largest magnitude so that the scaled values lie below 2^15 and the
+// largest at or above 2^14, and written as two fp16 numbers: hi = fp16(x 2^s) and
+// lo = fp16(x 2^s - hi). Their sum keeps 22 significant bits (as a tf32 pair does), and a
+// product takes three fp16 MMAs with fp32 accumulation (hi*hi + hi*lo + lo*hi); the
+// dropped lo*lo term is below 2^-22 of the product. The result is scaled back by the exact
+// power of two.
+
+// shift s that brings a largest magnitude m into [2^14, 2^15), kept within [-114, 120] so
+// that 2^s and 2^-s are finite fp32 numbers
+__device__ __forceinline__ int scale_shift(float m) {
+  const int e = (int)((__float_as_uint(m) >> 23) & 0xffu);   // biased exponent
+  const int s = 141 - e;                                      // 14 - (e - 127)
+  return s > 120 ? 120 : s;
+}
+// 2^s for s in [-126, 127]
+__device__ __forceinline__ float pow2f(int s) {
+  return __uint_as_float((uint32_t)(s + 127) << 23);
+}
+// (hi, lo) fp16 pairs of two scaled values
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_half2(x0, x1);
+  const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  float r0, r1;
+  sub2(r0, r1, x0, x1, hf.x, hf.y);
+  lo = pack_half2(r0, r1);
+}
+// 16 or 32 consecutive 32-bit columns of this thread's TMEM lane
+template <int N>
+__device__ __forceinline__ void tmem_st_u32(uint32_t taddr, const uint32_t (&v)[N]);
+template <>
+__device__ __forceinline__ void tmem_st_u32<32>(uint32_t taddr, const uint32_t (&v)[32]) {
+  tc::tmem_st32(taddr, *reinterpret_cast<const float(*)[32]>(v));
+}
+template <>
+__device__ __forceinline__ void tmem_st_u32<16>(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16, issued by one thread
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 struct SpMaps {     // TMA descriptors of the K and V pages (kernel parameters)
@@ -404,50 +434,100 @@ __device__ __forceinline__ int64_t next_group(const SparseParams& p) {
   }
 }
 
+// Split pass over Q: one warp per fp32 row (query, head), scaled by 2^s with s from the
+// row's largest magnitude and written as fp16 (hi, lo) rows, with s.
+template <int D>
+__global__ void __launch_bounds__(256) qsplit_kernel(SparseParams p) {
+  constexpr int PER = D / 32;   // values per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = p.Tq * p.hq;
+  const int64_t stride = (int64_t)gridDim.x * 8;
+  for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += stride) {
+    float v[PER];
+    if (PER == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(p.q + row * D + lane * 4);
+      v[0] = x.x; v[1] = x.y; v[PER > 2 ? 2 : 0] = x.z; v[PER > 3 ? 3 : 1] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(p.q + row * D + lane * 2);
+      v[0] = x.x; v[1] = x.y;
+    }
+    float mx = 0.f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) mx = fmaxf(mx, fabsf(v[k]));
+    // non-negative floats order as their bit patterns
+    const int s = scale_shift(__uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx))));
+    const float f = pow2f(s);
+    uint32_t hi[PER / 2], lo[PER / 2];
+#pragma unroll
+    for (int k = 0; k < PER / 2; ++k) {
+      float x0, x1;
+      fma2(x0, x1, v[2 * k], v[2 * k + 1], f, 0.f);
+      split_pair(x0, x1, hi[k], lo[k]);
+    }
+    if (PER == 4) {
+      *reinterpret_cast<uint2*>(p.qhi + row * D + lane * 4) = make_uint2(hi[0], hi[PER / 2 - 1]);
+      *reinterpret_cast<uint2*>(p.qlo + row * D + lane * 4) = make_uint2(lo[0], lo[PER / 2 - 1]);
+    } else {
+      *reinterpret_cast<uint32_t*>(p.qhi + row * D + lane * 2) = hi[0];
+      *reinterpret_cast<uint32_t*>(p.qlo + row * D + lane * 2) = lo[0];
+    }
+    if (lane == 0) p.qshift[row] = s;
+  }
+}
+
+// Q arrives split: a pass before the kernel writes every fp32 Q row as fp16 (hi, lo)
+// rows scaled by the row's own power of two, and that shift.
+//
 // Warp-specialised form: a persistent CTA of 16 warps per SM, every hand-off on an
-// mbarrier, so that the tensor core runs S = Q K^T of a tile while the previous tile's
-// output is stored and the next tile's Q and the next group's K/V are prepared.
+// mbarrier.
 //   warp 12 (scheduler): takes groups from the counter, publishes each in a 4-entry ring
 //     with its 64-bit key masks (mapped, invalid reference) and stages the group's raw
-//     fp32 K and V pages by TMA (one box per page and 32-column slice) once the
-//     converters have finished the previous group's raw tiles.
-//   warps 8-11 (convert + Q, upper columns): raw K -> tf32 (hi, lo) K-major tiles once
-//     every S of the previous group is done; raw V -> transposed (hi, lo) tiles once every
-//     O = P V of the previous group is done (keys not mapped become zeros); per tile, the
-//     upper half of the Q columns of every row, split into (hi, lo), into TMEM.
-//   warps 4-7 (Q lower columns + store): per tile, the lower half of the Q columns; the O
-//     rows of the previous tile from TMEM to global memory.
-//   warps 13, 14, lane 0 (S issuers): S = Qhi Khi + Qhi Klo + Qlo Khi as two accumulators
-//     (24 tf32 MMAs each; the cost of an MMA is paid by the issuing thread).
-//   warp 15, lane 0 (O issuer): O = Phi Vhi + Phi Vlo + Plo Vhi, P read from TMEM.
-//   warps 0-3 (softmax, one thread per row): m, the weights and l of the row from the sum
-//     of the two S accumulators; P (hi, lo) back into the S columns; m and l to memory.
-// TMEM: S (P hi) 0..63, S' (P lo) 64..127, O 128.., Q hi 256.., Q lo 256 + D.
-// One S/P buffer and one O accumulator: S(t+1) is issued once O(t) = P(t) V is done, so
-// the tensor-core chain per tile is S, softmax, O; everything else overlaps it.
+//     fp32 K and V pages by TMA (one box per page and 32-column slice) into one of two
+//     stages, once every product of the group that used the stage last is done.
+//   warps 8-11 (convert + upper Q halves): per tile, the upper half of every split Q row
+//     into TMEM; after the first tile of a group, the raw K, then V, of its stage split in
+//     place into (hi, lo) fp16 tiles (both in the K-major layout: K is the K-major operand
+//     of S = Q K^T and V the MN-major operand of O = P V), each block scaled by its own
+//     power of two; keys not mapped become zeros. The tile's K and V shifts to a ring.
+//   warps 4-7 (lower Q halves + store): per tile, the lower half of every split Q row; the
+//     O rows of the previous tile from TMEM to memory, scaled back.
+//   warps 13, 14, lane 0 (S issuers): S = Q K^T of the even / odd tiles (24 MMAs of
+//     128 x 64 x 16 for head size 128 into the tile parity's accumulator).
+//   warp 15, lane 0 (O issuer): O = P V, P (hi, lo) read from TMEM (12 MMAs).
+//   warps 0-3 (softmax, one thread per row): the row's scores from S and the shifts, m,
+//     the weights and l; P' = 2^14 P (hi, lo) over the S columns; m and l to memory.
+// TMEM: S of tile parity b at 64 b (P' hi at +0 and lo at +32 once the scores are read), O
+// at 128, Q (hi, lo) of tile parity b at 256 + D b (hi D/2 columns, then lo). With two S
+// and two Q buffers the next tile's Q copy and S run while the softmax and O of this one
+// do.
 constexpr int kThreads = 512;
 constexpr int kNK = 64;                 // keys per block tile
 constexpr uint32_t kTries = 1u << 22;   // default bound of each wait (polls)
 constexpr int kRing = 4;                // group ring entries
+constexpr int kStages = 2;              // K/V stages (raw fp32 landed, then split in place)
+constexpr int kScaleRing = 8;           // tile scale entries
 constexpr int kSchedWarp = 12, kIssueS0 = 13, kIssueS1 = 14, kIssuePv = 15;
-constexpr uint32_t kTmSa = 0, kTmSb = 64, kTmO = 128, kTmQ = 256;
+constexpr uint32_t kTmS = 0, kTmO = 128, kTmQ = 256;
+constexpr int kPLog2 = 14;              // P' = 2^14 P keeps the lo parts of the weights normal
 // bound of this CTA's waits (kTries unless a test lowered it), set before the first barrier
 __shared__ uint32_t s_tries;
 
 enum : int {
-  kGFull = 0,                   // [kRing] entry published (scheduler, count 1)
-  kGEmpty = kGFull + kRing,     // [kRing] entry released (15 consumer warps / threads)
-  kRawFull = kGEmpty + kRing,   // raw K/V of a group landed (1 arrival + tx)
-  kRawFree,                     // converters done reading the raw tiles (4 warps)
-  kKReady,                      // K (hi, lo) of a group in place (4 warps)
-  kKFree,                       // every S of a group done (2 issuer commits)
-  kVReady,                      // V^T (hi, lo) of a group in place (4 warps)
-  kVFree,                       // every O of a group done (commit)
-  kQReady,                      // Q (hi, lo) of a tile in TMEM (8 warps)
-  kSFull,                       // S of a tile in TMEM (2 issuer commits)
-  kPFull,                       // P of a tile in TMEM (4 softmax warps)
-  kPvDone,                      // O of a tile complete (commit)
-  kOEmpty,                      // O read out of TMEM (4 store warps)
+  kGFull = 0,                     // [kRing] entry published (scheduler, count 1)
+  kGEmpty = kGFull + kRing,       // [kRing] entry released (15 consumer warps / threads)
+  kRawFull = kGEmpty + kRing,     // [kStages] raw K/V of a group landed (1 arrival + tx)
+  kKReady = kRawFull + kStages,   // [kStages] K (hi, lo) in place (4 converter warps)
+  kVReady = kKReady + kStages,    // [kStages] V (hi, lo) in place (4 converter warps)
+  kKFree = kVReady + kStages,     // [kStages] every S of the stage's group done (2 commits)
+  kVFree = kKFree + kStages,      // [kStages] every O of the stage's group done (commit)
+  kCvtK = kVFree + kStages,       // the converter warps' K block maxima posted (4 warps)
+  kCvtV,                          // the same for V
+  kQReady,                        // [2] Q (hi, lo) of a tile in buffer b (8 warps)
+  kScale = kQReady + 2,           // [kScaleRing] K and V shifts of a tile posted (4 warps)
+  kSFull = kScale + kScaleRing,   // [2] S of a tile in buffer b (issuer b commits)
+  kPFull = kSFull + 2,            // [2] P of a tile in buffer b (4 softmax warps)
+  kPvDone = kPFull + 2,           // [2] O of a tile of parity b complete (commit)
+  kOEmpty = kPvDone + 2,          // O read out of TMEM (4 store warps)
   kDrainS0, kDrainS1, kDrainPv,
   kNumBars
 };
@@ -457,18 +537,20 @@ struct GroupEntry {   // ring entry: group (ngroups = end of work), edges, key m
   int e0, e1;
   unsigned long long vmask, imask;
 };
+struct TileScales {   // scale shifts of one tile: K and V block of the tile's group
+  int32_t sk, sv;
+};
 
 template <int D>
 struct Layout {   // byte offsets from a 1024-byte-aligned base
-  static constexpr uint32_t kTile = D * 256;                // [64][D] fp32
-  static constexpr uint32_t kKhi = 0;                       // D/32 x [64 keys][128 B]
-  static constexpr uint32_t kKlo = kKhi + kTile;
-  static constexpr uint32_t kVhi = kKlo + kTile;            // 2 x [D][128 B] (V^T)
-  static constexpr uint32_t kVlo = kVhi + kTile;
-  static constexpr uint32_t kRawK = kVlo + kTile;           // raw K, V as landed by TMA:
-  static constexpr uint32_t kRawV = kRawK + kTile;          //   D/32 x [64 keys][128 B]
-  static constexpr uint32_t kRingOff = kRawV + kTile;
-  static constexpr uint32_t kBar = kRingOff + kRing * sizeof(GroupEntry);
+  static constexpr uint32_t kHalf = D * 256;     // raw fp32 K (or V) of a block; its (hi, lo)
+  static constexpr uint32_t kStage = 2 * kHalf;  // K, then V
+  static constexpr uint32_t kSub = kNK * 128;    // a 32-column fp32 box or 64-column fp16 tile
+  static constexpr uint32_t kLo = D * 128;       // lo tile after the hi tile
+  static constexpr uint32_t kRingOff = kStages * kStage;
+  static constexpr uint32_t kScaleOff = kRingOff + kRing * sizeof(GroupEntry);
+  static constexpr uint32_t kMaxOff = kScaleOff + kScaleRing * sizeof(TileScales);
+  static constexpr uint32_t kBar = kMaxOff + 8 * sizeof(float);
   static constexpr uint32_t kAbort = kBar + kNumBars * 8;
   static constexpr uint32_t kTmem = kAbort + 4;
   static constexpr uint32_t kEnd = kTmem + 4;
@@ -531,7 +613,7 @@ __device__ __forceinline__ int4 row_record(const SparseParams& p, int c0, int e1
 // Warp 12: group scheduling, key masks and raw K/V staging.
 template <int D>
 __device__ void sched_role(const SparseParams& p, const SpMaps& maps, unsigned char* sm,
-                           uint32_t& issued) {
+                           uint32_t (&issued)[kStages]) {
   using L = Layout<D>;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
@@ -591,65 +673,131 @@ __device__ void sched_role(const SparseParams& p, const SpMaps& maps, unsigned c
       bar_arrive(bars + kGFull + slot);   // release: the entry is visible to the waiters
     }
     if (g >= p.ngroups) return;
-    // the raw tiles are free once the converters finished the previous group's
-    if (gi >= 1 && !warp_wait(bars + kRawFree, (gi - 1) & 1u, abort)) return;
+    // the stage is free once every S and every O of the group that used it last are done
+    const uint32_t st = gi % kStages;
+    if (gi >= kStages) {
+      const uint32_t par = ((gi / kStages) - 1) & 1u;
+      if (!warp_wait(bars + kKFree + st, par, abort)) return;
+      if (!warp_wait(bars + kVFree + st, par, abort)) return;
+    }
     const uint32_t bits = __ballot_sync(0xffffffffu, row0 >= 0);
     if (lane == 0)
-      tc::mbar_arrive_expect_tx(bars + kRawFull,
+      tc::mbar_arrive_expect_tx(bars + kRawFull + st,
                                 (uint32_t)__popc(bits) * (uint32_t)p.page_size * D * 4u * 2u);
     __syncwarp();
     // testing hook: the first staging is announced but never copied, so the waits for it
     // give up with nothing in flight
     const bool withhold = p.withhold_copy && gi == 0;
     if (row0 >= 0 && !withhold) {
+      unsigned char* kb = sm + st * L::kStage;
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
-        const uint32_t off = (uint32_t)q * (kNK * 128) + (uint32_t)(lane * p.page_size) * 128u;
-        tc::tma_load_2d(sm + L::kRawK + off, &maps.k, q * 32, row0, bars + kRawFull);
-        tc::tma_load_2d(sm + L::kRawV + off, &maps.v, q * 32, row0, bars + kRawFull);
+        const uint32_t off = (uint32_t)q * L::kSub + (uint32_t)(lane * p.page_size) * 128u;
+        tc::tma_load_2d(kb + off, &maps.k, q * 32, row0, bars + kRawFull + st);
+        tc::tma_load_2d(kb + L::kHalf + off, &maps.v, q * 32, row0, bars + kRawFull + st);
       }
     }
-    ++issued;
+    ++issued[st];
   }
 }
 
-// Columns [C0, C0 + NC) of this thread's Q row (hi, lo) into its TMEM lane; zeros for a
-// padding row. The row's loads are all issued before any is used (one round trip).
-template <int D, int C0, int NC>
-__device__ __forceinline__ void load_q_cols(uint32_t lane_tm, const float* row, uint64_t pol) {
-  float v[NC];
+// Splits the raw fp32 block at buf (64 keys x D as landed by TMA: D/32 boxes of
+// [64 keys][128 B] in the 128-byte swizzle) in place into an fp16 hi tile at buf and a lo
+// tile at buf + D*128 (64-column sub-tiles [64 keys][128 B] in the 128-byte swizzle), both
+// scaled by 2^s with s from the block's largest magnitude (over the four warps that split it,
+// posted on `bar`); keys not mapped become zeros. Every raw element is read before any
+// warp writes. False on abort.
+template <int D>
+__device__ bool split_block(unsigned char* buf, uint64_t vmask, float* wmax, uint64_t* bar,
+                            uint32_t parity, volatile int* abort, int ct, int& s_out) {
+  using L = Layout<D>;
+  constexpr int kItems = kNK * (D / 8) / 128;   // 8-column chunks per thread
+  const int lane = ct & 31, wq = ct >> 5;
+  float v[kItems][8];
+  float mxs[kItems];
 #pragma unroll
-  for (int k = 0; k < NC; k += 4) {
-    const float4 x = row ? ldg_hint(row + C0 + k, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
-    v[k] = x.x;
-    v[k + 1] = x.y;
-    v[k + 2] = x.z;
-    v[k + 3] = x.w;
+  for (int j = 0; j < kItems; ++j) {
+    const int i = j * 128 + ct;
+    const int tk = i & (kNK - 1), c8 = i >> 6;   // key, 8-column chunk
+    const uint32_t box = (uint32_t)(c8 >> 2) * L::kSub;
+    const uint32_t c16 = (uint32_t)(c8 & 3) * 2u;
+    float4 a = *reinterpret_cast<const float4*>(buf + box + tc::sw128(tk, c16));
+    float4 b = *reinterpret_cast<const float4*>(buf + box + tc::sw128(tk, c16 + 1u));
+    if (!((vmask >> tk) & 1ull)) a = b = make_float4(0.f, 0.f, 0.f, 0.f);
+    v[j][0] = a.x; v[j][1] = a.y; v[j][2] = a.z; v[j][3] = a.w;
+    v[j][4] = b.x; v[j][5] = b.y; v[j][6] = b.z; v[j][7] = b.w;
+    mxs[j] = fmaxf(fmaxf(fmaxf(fabsf(v[j][0]), fabsf(v[j][1])), fmaxf(fabsf(v[j][2]), fabsf(v[j][3]))),
+                   fmaxf(fmaxf(fabsf(v[j][4]), fabsf(v[j][5])), fmaxf(fabsf(v[j][6]), fabsf(v[j][7]))));
   }
+  float mx = mxs[0];
 #pragma unroll
-  for (int c = 0; c < NC; c += 32) {
-    float* h = v + c;
-    float lo[32];
+  for (int j = 1; j < kItems; ++j) mx = fmaxf(mx, mxs[j]);
+  // non-negative floats order as their bit patterns
+  const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+  if (lane == 0) {
+    wmax[wq] = __uint_as_float(wm);
+    bar_arrive(bar);   // release: this warp's maximum, and its reads of the raw block done
+  }
+  if (!warp_wait(bar, parity, abort)) return false;
+  const float bm = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+  const int s = scale_shift(bm);
+  const float f = pow2f(s);
 #pragma unroll
-    for (int k = 0; k < 32; k += 2) {
-      const float x0 = h[k], x1 = h[k + 1];
-      h[k] = tf32_hi(x0);
-      h[k + 1] = tf32_hi(x1);
-      sub2(lo[k], lo[k + 1], x0, x1, h[k], h[k + 1]);
+  for (int j = 0; j < kItems; ++j) {
+    const int i = j * 128 + ct;
+    const int tk = i & (kNK - 1), c8 = i >> 6;
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float x0, x1;
+      fma2(x0, x1, v[j][2 * k], v[j][2 * k + 1], f, 0.f);
+      split_pair(x0, x1, hi[k], lo[k]);
     }
-    tc::tmem_st32(lane_tm + kTmQ + C0 + c, *reinterpret_cast<const float(*)[32]>(h));
-    tc::tmem_st32(lane_tm + kTmQ + D + C0 + c, lo);
+    const uint32_t off = (uint32_t)(c8 >> 3) * L::kSub + tc::sw128(tk, (uint32_t)(c8 & 7));
+    *reinterpret_cast<uint4*>(buf + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(buf + L::kLo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
+  s_out = s;
+  return true;
+}
+
+__device__ __forceinline__ uint4 ldg_hint_u4(const void* gmem, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(gmem), "l"(pol));
+  return v;
+}
+// Half H (0: columns [0, D/2), 1: [D/2, D)) of this thread's split Q row (hi, lo) into its
+// TMEM lane at q_tm (hi at + H*D/4, lo at + D/2 + H*D/4); zeros for a padding row. The
+// row's loads are all issued before any is used (one round trip).
+template <int D, int H>
+__device__ __forceinline__ void copy_q_half(uint32_t q_tm, const __half* hi_row,
+                                            const __half* lo_row, uint64_t pol) {
+  constexpr int NV = D / 16;   // 16-byte vectors in half a row of fp16
+  uint32_t h[NV * 4], l[NV * 4];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const uint4 x = hi_row ? ldg_hint_u4(hi_row + H * (D / 2) + 8 * k, pol) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 y = lo_row ? ldg_hint_u4(lo_row + H * (D / 2) + 8 * k, pol) : make_uint4(0u, 0u, 0u, 0u);
+    h[4 * k] = x.x; h[4 * k + 1] = x.y; h[4 * k + 2] = x.z; h[4 * k + 3] = x.w;
+    l[4 * k] = y.x; l[4 * k + 1] = y.y; l[4 * k + 2] = y.z; l[4 * k + 3] = y.w;
+  }
+  tmem_st_u32<NV * 4>(q_tm + H * (D / 4), h);
+  tmem_st_u32<NV * 4>(q_tm + D / 2 + H * (D / 4), l);
   tc::tmem_wait_st();
 }
 
-// Warps 8-11: K/V conversion per group, the upper Q columns per tile.
+// Warps 8-11: the upper Q half rows per tile; the K and V split of each group once its
+// first tile's Q is in place (S of that tile then waits only for K).
 template <int D>
 __device__ void convert_role(const SparseParams& p, unsigned char* sm, uint32_t tmem) {
   using L = Layout<D>;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
   const volatile GroupEntry* ring = reinterpret_cast<const volatile GroupEntry*>(sm + L::kRingOff);
+  TileScales* scales = reinterpret_cast<TileScales*>(sm + L::kScaleOff);
+  float* wmax = reinterpret_cast<float*>(sm + L::kMaxOff);   // [K: 4][V: 4]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3, ct = wq * 32 + lane;   // TMEM quadrant; thread of the 128
   const int r = ct;                               // tile row of this thread
@@ -661,86 +809,66 @@ __device__ void convert_role(const SparseParams& p, unsigned char* sm, uint32_t 
     GroupEntry e;
     if (!read_entry(p, bars, ring, gi, abort, true, e)) return;
     const int h = (int)(e.g % p.hkv);
+    const uint32_t st = gi % kStages;
+    unsigned char* kb = sm + st * L::kStage;
     int4 rec = row_record(p, e.e0, e.e1, my_er, epc);
-    // K of this group: the raw tiles landed and every S of the previous group is done
-    if (!warp_wait(bars + kRawFull, gi & 1u, abort)) return;
-    if (gi > 0 && !warp_wait(bars + kKFree, (gi - 1) & 1u, abort)) return;
-    for (int i = ct; i < kNK * (D / 4); i += 128) {
-      const int tk = i / (D / 4), c = i % (D / 4);
-      const uint32_t off = (uint32_t)(c >> 3) * (kNK * 128) + tc::sw128(tk, c & 7);
-      float4 v = *reinterpret_cast<const float4*>(sm + L::kRawK + off);
-      if (!((e.vmask >> tk) & 1ull)) v = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 hi = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
-      float4 lo;
-      sub2(lo.x, lo.y, v.x, v.y, hi.x, hi.y);
-      sub2(lo.z, lo.w, v.z, v.w, hi.z, hi.w);
-      *reinterpret_cast<float4*>(sm + L::kKhi + off) = hi;
-      *reinterpret_cast<float4*>(sm + L::kKlo + off) = lo;
-    }
-    tc::fence_async_shared();
-    __syncwarp();
-    if (lane == 0) bar_arrive(bars + kKReady);
-    bool first = true;
+    int sk = 0, sv = 0;
     for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
-      // the Q columns of every row are free once S of the previous tile is done
-      if (t > 0 && !warp_wait(bars + kSFull, (t - 1) & 1u, abort)) return;
+      const uint32_t b = t & 1u;
+      // Q buffer b is free once S of tile t - 2 is done
+      if (t >= 2 && !warp_wait(bars + kSFull + b, ((t >> 1) - 1) & 1u, abort)) return;
       tc::fence_after_sync();
-      const float* row = rec.x >= 0 ? p.q + ((int64_t)rec.y * p.hq + h * p.qhead + my_qh) * D
-                                    : nullptr;
-      load_q_cols<D, D / 2, D / 2>(lane_tm, row, keep);
+      const int64_t qrow = (int64_t)rec.y * p.hq + h * p.qhead + my_qh;
+      copy_q_half<D, 1>(lane_tm + kTmQ + b * (uint32_t)D, rec.x >= 0 ? p.qhi + qrow * D : nullptr,
+                        rec.x >= 0 ? p.qlo + qrow * D : nullptr, keep);
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) bar_arrive(bars + kQReady);
-      if (c0 + epc < e.e1) rec = row_record(p, c0 + epc, e.e1, my_er, epc);
-      if (first) {   // V of this group once every O of the previous group is done
-        first = false;
-        if (gi > 0 && !warp_wait(bars + kVFree, (gi - 1) & 1u, abort)) return;
-        const int tk = lane + 32 * (wq & 1);
-        const bool live = (e.vmask >> tk) & 1ull;
-        for (int c = wq >> 1; c < D / 4; c += 2) {
-          float4 v = *reinterpret_cast<const float4*>(sm + L::kRawV + (uint32_t)(c >> 3) * (kNK * 128) +
-                                                      tc::sw128(tk, c & 7));
-          if (!live) v = make_float4(0.f, 0.f, 0.f, 0.f);
-          const float x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int d = c * 4 + k;
-            const uint32_t off = (uint32_t)(tk >> 5) * (D * 128) + (uint32_t)d * 128u +
-                                 ((uint32_t)(((tk & 31) >> 2) ^ (d & 7)) << 4) + (uint32_t)(tk & 3) * 4u;
-            const float hi = tf32_hi(x[k]);
-            *reinterpret_cast<float*>(sm + L::kVhi + off) = hi;
-            *reinterpret_cast<float*>(sm + L::kVlo + off) = x[k] - hi;
-          }
-        }
+      if (lane == 0) bar_arrive(bars + kQReady + b);
+      if (c0 == e.e0) {   // K, then V, of this group once its raw block landed
+        if (!warp_wait(bars + kRawFull + st, (gi / kStages) & 1u, abort)) return;
+        if (!split_block<D>(kb, e.vmask, wmax, bars + kCvtK, gi & 1u, abort, ct, sk)) return;
         tc::fence_async_shared();
         __syncwarp();
-        if (lane == 0) {
-          bar_arrive(bars + kVReady);
-          bar_arrive(bars + kRawFree);
-        }
+        if (lane == 0) bar_arrive(bars + kKReady + st);
+        if (!split_block<D>(kb + L::kHalf, e.vmask, wmax + 4, bars + kCvtV, gi & 1u, abort, ct,
+                            sv))
+          return;
+        tc::fence_async_shared();
+        __syncwarp();
+        if (lane == 0) bar_arrive(bars + kVReady + st);
       }
+      if (ct == 0) {
+        scales[t % kScaleRing].sk = sk;
+        scales[t % kScaleRing].sv = sv;
+      }
+      __syncwarp();
+      if (lane == 0) bar_arrive(bars + kScale + t % kScaleRing);
+      if (c0 + epc < e.e1) rec = row_record(p, c0 + epc, e.e1, my_er, epc);
     }
     __syncwarp();
     if (lane == 0) bar_arrive(bars + kGEmpty + (gi % kRing));
   }
 }
 
-// Warps 4-7: the lower Q columns per tile; the O rows of the previous tile.
+// Warps 4-7: the lower Q half rows per tile; the O rows of the previous tile.
 template <int D>
 __device__ void store_role(const SparseParams& p, unsigned char* sm, uint32_t tmem) {
   using L = Layout<D>;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
   const volatile GroupEntry* ring = reinterpret_cast<const volatile GroupEntry*>(sm + L::kRingOff);
+  const TileScales* scales = reinterpret_cast<const TileScales*>(sm + L::kScaleOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3, r = wq * 32 + lane;
   const uint32_t lane_tm = tmem + ((uint32_t)(wq * 32) << 16);
   const int epc = 128 / p.qhead, my_er = r / p.qhead, my_qh = r - (r / p.qhead) * p.qhead;
   const uint64_t keep = l2_policy_last();
-  // O rows of tile tt (partial index pi, -1 = padding row) to memory
+  // O rows of tile tt (partial index pi, -1 = padding row) to memory: O' = 2^(14 + sv) O
   auto store = [&](uint32_t tt, int pi) -> bool {
-    if (!warp_wait(bars + kPvDone, tt & 1u, abort)) return false;
+    if (!warp_wait(bars + kPvDone + (tt & 1u), (tt >> 1) & 1u, abort)) return false;
+    if (!warp_wait(bars + kScale + tt % kScaleRing, (tt / kScaleRing) & 1u, abort)) return false;
     tc::fence_after_sync();
+    const float f = ldexpf(1.f, -(kPLog2 + scales[tt % kScaleRing].sv));
 #pragma unroll 1
     for (int ch = 0; ch < D / 32; ++ch) {
       float o[32];
@@ -750,7 +878,8 @@ __device__ void store_role(const SparseParams& p, unsigned char* sm, uint32_t tm
         float4* dst = reinterpret_cast<float4*>(p.o + (int64_t)pi * D + ch * 32);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          __stcs(dst + k, make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]));
+          __stcs(dst + k, make_float4(o[4 * k] * f, o[4 * k + 1] * f, o[4 * k + 2] * f,
+                                      o[4 * k + 3] * f));
       }
     }
     tc::fence_before_sync();
@@ -766,14 +895,15 @@ __device__ void store_role(const SparseParams& p, unsigned char* sm, uint32_t tm
     const int h = (int)(e.g % p.hkv);
     int4 rec = row_record(p, e.e0, e.e1, my_er, epc);
     for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
-      if (t > 0 && !warp_wait(bars + kSFull, (t - 1) & 1u, abort)) return;
+      const uint32_t b = t & 1u;
+      if (t >= 2 && !warp_wait(bars + kSFull + b, ((t >> 1) - 1) & 1u, abort)) return;
       tc::fence_after_sync();
-      const float* row = rec.x >= 0 ? p.q + ((int64_t)rec.y * p.hq + h * p.qhead + my_qh) * D
-                                    : nullptr;
-      load_q_cols<D, 0, D / 2>(lane_tm, row, keep);
+      const int64_t qrow = (int64_t)rec.y * p.hq + h * p.qhead + my_qh;
+      copy_q_half<D, 0>(lane_tm + kTmQ + b * (uint32_t)D, rec.x >= 0 ? p.qhi + qrow * D : nullptr,
+                        rec.x >= 0 ? p.qlo + qrow * D : nullptr, keep);
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) bar_arrive(bars + kQReady);
+      if (lane == 0) bar_arrive(bars + kQReady + b);
       const int pi = rec.x >= 0 ? rec.x * p.qhead + my_qh : -1;
       if (c0 + epc < e.e1) rec = row_record(p, c0 + epc, e.e1, my_er, epc);
       if (t > 0 && !store(t - 1, prev_pi)) return;
@@ -793,51 +923,55 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
   const volatile GroupEntry* ring = reinterpret_cast<const volatile GroupEntry*>(sm + L::kRingOff);
+  const TileScales* scales = reinterpret_cast<const TileScales*>(sm + L::kScaleOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = warp * 32 + lane;
   const uint32_t lane_tm = tmem + ((uint32_t)(warp * 32) << 16);
   const int epc = 128 / p.qhead, my_er = r / p.qhead, my_qh = r - (r / p.qhead) * p.qhead;
   const float sl2 = p.scale * kLog2e;
+  const float p_scale = (float)(1 << kPLog2);
   uint32_t t = 0;
   for (uint32_t gi = 0;; ++gi) {
     GroupEntry e;
     if (!read_entry(p, bars, ring, gi, abort, true, e)) return;
+    const int h = (int)(e.g % p.hkv);
     int4 rec = row_record(p, e.e0, e.e1, my_er, epc);
+    int sq = rec.x >= 0 ? __ldg(p.qshift + (int64_t)rec.y * p.hq + h * p.qhead + my_qh) : 0;
     for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
+      const uint32_t b = t & 1u;
       const int keys = rec.x >= 0 ? rec.z : 0;
       const int pi = rec.x >= 0 ? rec.x * p.qhead + my_qh : -1;
-      if (c0 + epc < e.e1) rec = row_record(p, c0 + epc, e.e1, my_er, epc);
-      if (!warp_wait(bars + kSFull, t & 1u, abort)) return;
+      const int sq_t = sq;
+      if (c0 + epc < e.e1) {
+        rec = row_record(p, c0 + epc, e.e1, my_er, epc);
+        sq = rec.x >= 0 ? __ldg(p.qshift + (int64_t)rec.y * p.hq + h * p.qhead + my_qh) : 0;
+      }
+      // the shifts of this row's Q and of the block's K: S' = 2^(sq + sk) S
+      if (!warp_wait(bars + kScale + t % kScaleRing, (t / kScaleRing) & 1u, abort)) return;
+      const float f = ldexpf(sl2, -(sq_t + scales[t % kScaleRing].sk));
+      if (!warp_wait(bars + kSFull + b, (t >> 1) & 1u, abort)) return;
       tc::fence_after_sync();
+      const uint32_t s_tm = lane_tm + kTmS + b * 64u;
       float s[64];
       float (*s32)[32] = reinterpret_cast<float (*)[32]>(s);
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {   // S = S_a + S_b, 32 keys at a time
-        float tmp[32];
-        tc::tmem_ld32(lane_tm + kTmSa + hf * 32, s32[hf]);
-        tc::tmem_ld32(lane_tm + kTmSb + hf * 32, tmp);
-        tc::tmem_wait_ld();
+      for (int hf = 0; hf < 2; ++hf) tc::tmem_ld32(s_tm + hf * 32, s32[hf]);
+      tc::tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) add2(s32[hf][k], s32[hf][k + 1], tmp[k], tmp[k + 1]);
-      }
+      for (int k = 0; k < 64; k += 2) fma2(s[k], s[k + 1], s[k], s[k + 1], f, 0.f);   // base-2 units
       const uint64_t used = keys >= 64 ? ~0ull : ((1ull << keys) - 1ull);
       if (e.imask & used) bad = true;
       // keys that take part: mapped and inside the block (the rest score -1e30, and keys
       // past the block never raise m above that sentinel either)
       const uint64_t live = e.vmask & used;
       const uint32_t live_lo = (uint32_t)live, live_hi = (uint32_t)(live >> 32);
-      // scores in base-2 units (scale * log2(e) * <q, k>): the weights are 2^(s - max);
-      // four partial maxima and sums keep the dependency chains short
+      // the weights are 2^(s - max); four partial maxima and sums keep the chains short
       float mp[4] = {kNegLarge, kNegLarge, kNegLarge, kNegLarge};
 #pragma unroll
-      for (int k = 0; k < 64; k += 2) {
+      for (int k = 0; k < 64; ++k) {
         const uint32_t word = k < 32 ? live_lo : live_hi;
-        float x0, x1;
-        fma2(x0, x1, s[k], s[k + 1], sl2, 0.f);
-        s[k] = ((word >> (k & 31)) & 1u) ? x0 : kNegLarge;
-        s[k + 1] = ((word >> ((k + 1) & 31)) & 1u) ? x1 : kNegLarge;
+        s[k] = ((word >> (k & 31)) & 1u) ? s[k] : kNegLarge;
         mp[k & 3] = fmaxf(mp[k & 3], s[k]);
-        mp[(k + 1) & 3] = fmaxf(mp[(k + 1) & 3], s[k + 1]);
       }
       const float m2 = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
       // 2^(-1e30 - m) is exactly 0 for every finite m; with no key taking part m is the
@@ -855,23 +989,19 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
       const float lrow = ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
       // m in natural-log units (the -1e30 sentinel as is when no key takes part)
       const float mrow = m2 > 0.5f * kNegLarge ? m2 * kLn2 : kNegLarge;
+      uint32_t ph[32], pl[32];   // P' = 2^14 P as (hi, lo) fp16 pairs of keys
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {   // P hi over S_a, P lo over S_b
-        float lo[32];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float w0 = s32[hf][k], w1 = s32[hf][k + 1];
-          s32[hf][k] = tf32_hi(w0);
-          s32[hf][k + 1] = tf32_hi(w1);
-          sub2(lo[k], lo[k + 1], w0, w1, s32[hf][k], s32[hf][k + 1]);
-        }
-        tc::tmem_st32(lane_tm + kTmSa + hf * 32, s32[hf]);
-        tc::tmem_st32(lane_tm + kTmSb + hf * 32, lo);
+      for (int k = 0; k < 64; k += 2) {
+        float w0, w1;
+        fma2(w0, w1, s[k], s[k + 1], p_scale, 0.f);
+        split_pair(w0, w1, ph[k / 2], pl[k / 2]);
       }
+      tmem_st_u32<32>(s_tm, ph);
+      tmem_st_u32<32>(s_tm + 32, pl);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) bar_arrive(bars + kPFull);
+      if (lane == 0) bar_arrive(bars + kPFull + b);
       if (pi >= 0) {
         __stcs(p.m + pi, mrow);
         __stcs(p.l + pi, lrow);
@@ -882,7 +1012,7 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
   }
 }
 
-// Lane 0 of warps 13, 14: S = Q K^T, issuer `which` of two (each its own accumulator).
+// Lane 0 of warps 13, 14: S = Q K^T of the tiles of parity `which`.
 template <int D>
 __device__ void s_issue_role(const SparseParams& p, unsigned char* sm, uint32_t tmem, int which) {
   using L = Layout<D>;
@@ -890,40 +1020,44 @@ __device__ void s_issue_role(const SparseParams& p, unsigned char* sm, uint32_t 
   volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
   const volatile GroupEntry* ring = reinterpret_cast<const volatile GroupEntry*>(sm + L::kRingOff);
   const int epc = 128 / p.qhead;
-  constexpr int KS = D / 8;   // tf32 k-steps per product
-  const uint32_t idesc = idesc_tf32(128, kNK);
-  const uint32_t d_tm = tmem + (which == 0 ? kTmSa : kTmSb);
-  const uint32_t khi = smem_u32(sm + L::kKhi), klo = smem_u32(sm + L::kKlo);
-  // issuer 0: Qhi Khi and the first half of Qhi Klo; issuer 1: the second half of
-  // Qhi Klo and Qlo Khi
+  constexpr int KS = D / 16;   // k-steps of 16 along the head
+  const uint32_t idesc = tc::idesc_f16(128, kNK, false, false);
   uint32_t t = 0;
   for (uint32_t gi = 0;; ++gi) {
     GroupEntry e;
     if (!read_entry(p, bars, ring, gi, abort, false, e)) return;
-    if (!wait_bar(bars + kKReady, gi & 1u, abort)) return;
+    const uint32_t st = gi % kStages;
+    if (!wait_bar(bars + kKReady + st, (gi / kStages) & 1u, abort)) return;
+    const uint32_t khi = smem_u32(sm + st * L::kStage), klo = khi + L::kLo;
     for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
-      if (!wait_bar(bars + kQReady, t & 1u, abort)) return;
-      // the S columns hold P of the previous tile until its O is done
-      if (t > 0 && !wait_bar(bars + kPvDone, (t - 1) & 1u, abort)) return;
+      const uint32_t b = t & 1u;
+      if (b != (uint32_t)which) continue;
+      if (!wait_bar(bars + kQReady + b, (t >> 1) & 1u, abort)) return;
+      // buffer b holds P of tile t - 2 until its O is done
+      if (t >= 2 && !wait_bar(bars + kPvDone + b, ((t >> 1) - 1) & 1u, abort)) return;
       tc::fence_after_sync();
+      const uint32_t d_tm = tmem + kTmS + b * 64u;
+      const uint32_t q_tm = tmem + kTmQ + b * (uint32_t)D;
       int n = 0;
 #pragma unroll
-      for (int j = 0; j < 3 * KS / 2; ++j, ++n) {
-        const int g = which * (3 * KS / 2) + j;   // 0 .. 3 KS - 1 over (pass, ks)
-        const int pass = g / KS, ks = g % KS;
-        const uint32_t a = tmem + kTmQ + (pass == 2 ? (uint32_t)D : 0u) + (uint32_t)ks * 8u;
-        const uint32_t b = (pass == 1 ? klo : khi) + (uint32_t)(ks >> 2) * (kNK * 128) +
-                           (uint32_t)(ks & 3) * 32u;
-        mma_tf32(d_tm, a, tc::smem_desc(b, 16, 1024), idesc, n > 0 ? 1u : 0u);
+      for (int pass = 0; pass < 3; ++pass) {   // Qhi Khi, Qhi Klo, Qlo Khi
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk, ++n) {
+          const uint32_t a = q_tm + (pass == 2 ? (uint32_t)(D / 2) : 0u) + (uint32_t)kk * 8u;
+          const uint32_t kbase = (pass == 1 ? klo : khi) + (uint32_t)(kk >> 2) * L::kSub +
+                                 (uint32_t)(kk & 3) * 32u;
+          mma_tmem_a(d_tm, a, tc::smem_desc(kbase, 16, 1024), idesc, n > 0 ? 1u : 0u);
+        }
       }
-      tc::commit(bars + kSFull);
-      if (c0 + epc >= e.e1) tc::commit(bars + kKFree);
+      tc::commit(bars + kSFull + b);
     }
+    // both issuers: every S of the group (of either parity) complete frees the K tiles
+    tc::commit(bars + kKFree + st);
     bar_arrive(bars + kGEmpty + (gi % kRing));
   }
 }
 
-// Lane 0 of warp 15: O = P V (P hi from the S_a columns, P lo from the S_b columns).
+// Lane 0 of warp 15: O = P V (P' hi and lo from the first S accumulator's columns).
 template <int D>
 __device__ void pv_issue_role(const SparseParams& p, unsigned char* sm, uint32_t tmem) {
   using L = Layout<D>;
@@ -931,31 +1065,32 @@ __device__ void pv_issue_role(const SparseParams& p, unsigned char* sm, uint32_t
   volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
   const volatile GroupEntry* ring = reinterpret_cast<const volatile GroupEntry*>(sm + L::kRingOff);
   const int epc = 128 / p.qhead;
-  const uint32_t idesc = idesc_tf32(128, D);
-  const uint32_t vhi = smem_u32(sm + L::kVhi), vlo = smem_u32(sm + L::kVlo);
+  const uint32_t idesc = tc::idesc_f16(128, D, false, true);
   uint32_t t = 0;
   for (uint32_t gi = 0;; ++gi) {
     GroupEntry e;
     if (!read_entry(p, bars, ring, gi, abort, false, e)) return;
-    if (!wait_bar(bars + kVReady, gi & 1u, abort)) return;
+    const uint32_t st = gi % kStages;
+    if (!wait_bar(bars + kVReady + st, (gi / kStages) & 1u, abort)) return;
+    const uint32_t vhi = smem_u32(sm + st * L::kStage + L::kHalf), vlo = vhi + L::kLo;
     for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
-      if (!wait_bar(bars + kPFull, t & 1u, abort)) return;
+      const uint32_t b = t & 1u;
+      if (!wait_bar(bars + kPFull + b, (t >> 1) & 1u, abort)) return;
       if (t > 0 && !wait_bar(bars + kOEmpty, (t - 1) & 1u, abort)) return;
       tc::fence_after_sync();
       int n = 0;
 #pragma unroll
-      for (int pass = 0; pass < 3; ++pass) {
-        const uint32_t a = tmem + (pass == 2 ? kTmSb : kTmSa);
-        const uint32_t b = pass == 1 ? vlo : vhi;
+      for (int pass = 0; pass < 3; ++pass) {   // Phi Vhi, Phi Vlo, Plo Vhi
+        const uint32_t a = tmem + kTmS + b * 64u + (pass == 2 ? 32u : 0u);
+        const uint32_t vb = pass == 1 ? vlo : vhi;
 #pragma unroll
-        for (int ks = 0; ks < kNK / 8; ++ks, ++n)
-          mma_tf32(tmem + kTmO, a + (uint32_t)ks * 8u,
-                   tc::smem_desc(b + (uint32_t)(ks >> 2) * (D * 128) + (uint32_t)(ks & 3) * 32u,
-                                 16, 1024),
-                   idesc, n > 0 ? 1u : 0u);
+        for (int ks = 0; ks < kNK / 16; ++ks, ++n)
+          mma_tmem_a(tmem + kTmO, a + (uint32_t)ks * 8u,
+                     tc::smem_desc(vb + (uint32_t)ks * 2048u, L::kSub, 1024), idesc,
+                     n > 0 ? 1u : 0u);
       }
-      tc::commit(bars + kPvDone);
-      if (c0 + epc >= e.e1) tc::commit(bars + kVFree);
+      tc::commit(bars + kPvDone + b);
+      if (c0 + epc >= e.e1) tc::commit(bars + kVFree + st);
     }
     bar_arrive(bars + kGEmpty + (gi % kRing));
   }
@@ -977,16 +1112,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bars + kGFull + i, 1);
       tc::mbar_init(bars + kGEmpty + i, 15);
     }
-    tc::mbar_init(bars + kRawFull, 1);
-    tc::mbar_init(bars + kRawFree, 4);
-    tc::mbar_init(bars + kKReady, 4);
-    tc::mbar_init(bars + kKFree, 2);
-    tc::mbar_init(bars + kVReady, 4);
-    tc::mbar_init(bars + kVFree, 1);
-    tc::mbar_init(bars + kQReady, 8);
-    tc::mbar_init(bars + kSFull, 2);
-    tc::mbar_init(bars + kPFull, 4);
-    tc::mbar_init(bars + kPvDone, 1);
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(bars + kRawFull + s, 1);
+      tc::mbar_init(bars + kKReady + s, 4);
+      tc::mbar_init(bars + kVReady + s, 4);
+      tc::mbar_init(bars + kKFree + s, 2);
+      tc::mbar_init(bars + kVFree + s, 1);
+    }
+    tc::mbar_init(bars + kCvtK, 4);
+    tc::mbar_init(bars + kCvtV, 4);
+    for (int i = 0; i < kScaleRing; ++i) tc::mbar_init(bars + kScale + i, 4);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(bars + kQReady + b, 8);
+      tc::mbar_init(bars + kSFull + b, 1);
+      tc::mbar_init(bars + kPFull + b, 4);
+      tc::mbar_init(bars + kPvDone + b, 1);
+    }
     tc::mbar_init(bars + kOEmpty, 4);
     tc::mbar_init(bars + kDrainS0, 1);
     tc::mbar_init(bars + kDrainS1, 1);
@@ -1004,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
   bool bad = false;
-  uint32_t issued = 0;
+  uint32_t issued[kStages] = {};
   if (warp < 4) {
     softmax_role<D>(p, sm, tmem, bad);
   } else if (warp < 8) {
@@ -1013,9 +1154,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     convert_role<D>(p, sm, tmem);
   } else if (warp == kSchedWarp) {
     sched_role<D>(p, maps, sm, issued);
-    // a wait gave up: the last staging must land before the CTA leaves
-    if (*abort && issued > 0)
-      tc::mbar_wait(bars + kRawFull, (issued - 1) & 1u, s_tries);
+    // a wait gave up: the last staging of each stage must land before the CTA leaves
+    if (*abort) {
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s] > 0) tc::mbar_wait(bars + kRawFull + s, (issued[s] - 1) & 1u, s_tries);
+    }
   } else if (lane == 0) {
     const int drain = warp == kIssueS0 ? kDrainS0 : warp == kIssueS1 ? kDrainS1 : kDrainPv;
     if (warp == kIssuePv)
@@ -1062,12 +1205,9 @@ bool encode_pages(CUtensorMap* m, const void* base, const SparseParams& p) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Shapes the tensor-core kernel takes: head size 64/128, blocks of at most 64 keys made of
-// whole pages of a multiple of 8 rows (each page's box starts on a 1024-byte boundary)
 bool eligible(const SparseParams& p) {
-  return (p.D == 64 || p.D == 128) && p.block_size <= kNK && p.qhead <= 128 &&
-         p.page_size % 8 == 0 && (int64_t)p.ppb * p.page_size <= kNK &&
-         p.num_pages * p.hkv * p.page_size <= INT32_MAX;
+  return sparse_tc_shape(p.D, p.block_size, p.qhead, p.page_size, p.ppb,
+                         p.num_pages * p.hkv * p.page_size, p.Tq * p.hq);
 }
 
 template <int D>
@@ -1089,6 +1229,14 @@ cudaError_t launch_tc(const SparseParams& p, cudaStream_t s) {
   SpMaps maps;
   if (!encode_pages(&maps.k, p.kp, p) || !encode_pages(&maps.v, p.vp, p))
     return cudaErrorInvalidValue;
+  {
+    ProfScope ps("sparse_qsplit", s);
+    const int64_t rows = p.Tq * p.hq;
+    const int64_t want = (rows + 7) / 8, cap = (int64_t)sms * 8;
+    qsplit_kernel<D><<<(unsigned)(want < cap ? want : cap), 256, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const int64_t grid = p.ngroups < sms ? p.ngroups : sms;
   ProfScope ps("sparse_partials", s);
   sparse_tc_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(p, maps);
@@ -1117,6 +1265,15 @@ cudaError_t launch_partials(const SparseParams& p, cudaStream_t s) {
 
 }  // namespace
 
+// Shapes the tensor-core kernel takes: head size 64/128, blocks of at most 64 keys made of
+// whole pages of a multiple of 8 rows (each page's box starts on a 1024-byte boundary)
+bool sparse_tc_shape(int D, int block_size, int qhead, int page_size, int ppb,
+                     int64_t pool_rows, int64_t q_rows) {
+  return (D == 64 || D == 128) && block_size <= tcs::kNK && qhead <= 128 &&
+         page_size % 8 == 0 && (int64_t)ppb * page_size <= tcs::kNK && pool_rows <= INT32_MAX &&
+         q_rows <= INT32_MAX;
+}
+
 cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s) {
   if (p.E == 0) return cudaSuccess;
   const unsigned eg = (unsigned)((p.E + 255) / 256);
@@ -1138,7 +1295,7 @@ cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (p.ngroups == 0) return cudaSuccess;
   if (p.f16) return launch_sparse_tc16(p, s);   // fp16 on the tensor core
-  if (tcs::eligible(p)) {   // 3xTF32 on the tensor core
+  if (tcs::eligible(p)) {   // split fp16 products on the tensor core
     if (p.D == 64) return tcs::launch_tc<64>(p, s);
     if (p.D == 128) return tcs::launch_tc<128>(p, s);
   }

@@ -268,6 +268,24 @@ def test_sparse_and_combine_argument_checks(lib):
     assert lib.pkv_combine_partials(ctypes.byref(c), None) == 1   # NULL pointers
 
 
+def test_sparse_workspace_holds_the_split_q_rows(lib):
+    # fp32 calls that run on the tensor core take Q as split fp16 (hi, lo) rows plus one
+    # shift per row in the workspace; fp16 calls and other shapes do not
+    def size(**kw):
+        a = B.SparseArgs(num_queries=100, num_edges=10, num_seqs=2, max_pages=16, num_pages=32,
+                         qhead=4, hq=32, hkv=8, head_dim=128, block_size=64, page_size=16,
+                         pages_per_block=4, softmax_scale=0.1, dtype=0)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return B.pkv_sparse_attention_partials_workspace_size(a)
+    rows = 100 * 32
+    assert size() - size(num_queries=0) == 2 * rows * 128 * 2 + rows * 4
+    assert size(dtype=B.PKV_F16) == size(dtype=B.PKV_F16, num_queries=0)
+    # 128-key blocks run on fp32 FMA: no split rows
+    assert size(block_size=128, pages_per_block=8) == size(block_size=128, pages_per_block=8,
+                                                           num_queries=0)
+
+
 def test_binding_raises_without_library(tmp_path):
     with pytest.raises(RuntimeError):
         B.load_library(str(tmp_path / "missing.so"))

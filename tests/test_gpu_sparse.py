@@ -53,7 +53,8 @@ def compare_partials(go, gm, gl, ro, rm, rl, rows, f16=False):
     assert_f32_close(gl[live], rl[live], "l partial", scalars=True, rtol=rt)
 
 
-# blocks of 64 and 32 keys run on the tensor core (3xTF32), 128-key blocks on fp32 FMA;
+# blocks of 64 and 32 keys run on the tensor core (split fp16 operands), 128-key blocks on
+# fp32 FMA;
 # qhead 3 leaves two rows of each 128-row tile unused
 @pytest.mark.parametrize("head_dim,pages_per_block,qhead", [(128, 4, 4), (64, 2, 2),
                                                             (128, 8, 1), (128, 4, 3)])
@@ -71,6 +72,27 @@ def test_small_full_parity(head_dim, pages_per_block, qhead):
     fin = np.isfinite(rlse)
     np.testing.assert_array_equal(np.isfinite(glse), fin)
     assert_f32_close(glse[fin], rlse[fin], "lse", scalars=True)
+
+
+# The tensor-core path scales each Q row and each K / V block by a power of two before
+# splitting it into fp16 (hi, lo) pairs. Magnitudes far outside fp16's range (q x 2^eq,
+# k x 2^ek, v x 2^ev, with eq + ek kept small so that the scores stay ordinary) and pages
+# of different magnitude inside one block must give the same partials as the fp64 oracle.
+@pytest.mark.parametrize("eq,ek,ev", [(40, -40, 60), (-50, 45, -70)])
+def test_split_scaling_wide_magnitudes(eq, ek, ev):
+    c = wl.block_sparse(57, n_seqs=2, kv_len=512, queries_per_seq=16, hq=16, hkv=4,
+                        head_dim=128, pages_per_block=4, blocks_per_query=4,
+                        unmapped_frac=0.05)
+    page_f = 2.0 ** np.random.default_rng(7).integers(-3, 4, size=(c.k_pages.shape[0], 1, 1, 1))
+    c.q = (c.q * 2.0 ** eq).astype(np.float32)
+    c.k_pages = (c.k_pages * 2.0 ** ek * page_f).astype(np.float32)
+    c.v_pages = (c.v_pages * 2.0 ** ev * page_f[::-1]).astype(np.float32)
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    ro, rm, rl, rst = oracle_partials(c)
+    assert gst == rst
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]))
+    rout, _ = orc.combine_partials(ro, rm, rl, c.seg_offsets, c.qhead)
+    assert f32_margins(gout, rout, "combined output, wide magnitudes") <= 1e-4
 
 
 def test_groups_spanning_several_row_tiles():
