@@ -348,7 +348,10 @@ typedef struct pkv_sparse_args {
   const int32_t* query_positions;
 } pkv_sparse_args;
 
-/* Host only: workspace bytes for the edge grouping of pkv_sparse_attention_partials. */
+/* Host only: workspace bytes of pkv_sparse_attention_partials: the edge grouping and,
+ * for fp32 calls whose shape runs on the tensor core (head_dim 64/128, block_size <= 64,
+ * page_size a multiple of 8 with pages_per_block * page_size <= 64), the Q rows split
+ * into fp16 (hi, lo) pairs: 4 * head_dim + 4 bytes per (query, head) row. */
 int pkv_sparse_attention_partials_workspace_size(const pkv_sparse_args* args,
                                                  size_t* bytes);
 
@@ -366,6 +369,9 @@ int pkv_sparse_attention_partials_workspace_size(const pkv_sparse_args* args,
  * are fp16 products summed in fp32, the weights are computed in fp32 and summed into l,
  * and rounded once to fp16 for the weighted sum of value rows; the partials are fp32;
  * everything else as above.
+ * fp32 on the tensor core: each Q row and each K / V block is scaled by a power of two
+ * and split into fp16 (hi, lo) pairs, and every product is formed from three fp16 MMAs
+ * with fp32 accumulation (hi*hi + hi*lo + lo*hi), about 2^-21 of |q||k| per score.
  * Supported for fp16: head_dim in {64, 128}, block_size <= 64, page_size a multiple of
  * 8 with pages_per_block * page_size <= 64; else PKV_ERR_UNSUPPORTED.
  * With query_positions the keys after the query's position take no part (they are not
