@@ -316,7 +316,8 @@ int pkv_kv_append_rotary(const pkv_kv_append_args* args, void* stream);
  * Block-sparse partials (sparse_attention_forward.wgsl)
  * ------------------------------------------------------------------------------- */
 typedef struct pkv_sparse_args {
-  const void* q;               /* [num_queries, hq, head_dim], element type `dtype` */
+  const void* q;               /* [num_queries, hq, head_dim], element type `dtype`;
+                                  may be NULL when num_queries is 0 */
   const void* k_pages;         /* [num_pages, hkv, page_size, head_dim], `dtype` */
   const void* v_pages;
   const int32_t* edge_meta;    /* [num_edges, 5]: q_idx, h (kv head), blk, batch, block_len */

@@ -693,8 +693,9 @@ int pkv_sparse_attention_partials(const pkv_sparse_args* a, void* workspace,
   const int st = check_sparse(a, &nb, &ng, &need);
   if (st != PKV_OK) return st;
   if (a->num_edges == 0) return PKV_OK;
-  if (!a->q || !a->k_pages || !a->v_pages || !a->edge_meta || !a->block_tables ||
-      !a->o_partial || !a->m_partial || !a->l_partial)
+  // with no query rows every edge is out of range: q is never read and may be NULL
+  if ((!a->q && a->num_queries > 0) || !a->k_pages || !a->v_pages || !a->edge_meta ||
+      !a->block_tables || !a->o_partial || !a->m_partial || !a->l_partial)
     return PKV_ERR_NULL;
   if (!aligned16(a->q) || !aligned16(a->k_pages) || !aligned16(a->v_pages) ||
       !aligned16(a->o_partial))

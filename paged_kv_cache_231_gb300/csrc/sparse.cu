@@ -1229,9 +1229,9 @@ cudaError_t launch_tc(const SparseParams& p, cudaStream_t s) {
   SpMaps maps;
   if (!encode_pages(&maps.k, p.kp, p) || !encode_pages(&maps.v, p.vp, p))
     return cudaErrorInvalidValue;
-  {
+  const int64_t rows = p.Tq * p.hq;
+  if (rows > 0) {   // no query rows: no edge is valid, so no tile reads the split rows
     ProfScope ps("sparse_qsplit", s);
-    const int64_t rows = p.Tq * p.hq;
     const int64_t want = (rows + 7) / 8, cap = (int64_t)sms * 8;
     qsplit_kernel<D><<<(unsigned)(want < cap ? want : cap), 256, 0, s>>>(p);
     e = cudaGetLastError();

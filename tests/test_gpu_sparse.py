@@ -268,6 +268,14 @@ def test_no_edges_and_all_empty_edges(dtype):
     assert gst == 0
     assert (go == 0).all() and (gm == -1e30).all() and (gl == 0).all()
     assert (gout == 0).all() and np.isneginf(glse).all()
+    # no query rows at all: every edge names a query out of range (flagged, sentinel)
+    c2 = wl.block_sparse(58, n_seqs=2, kv_len=512, queries_per_seq=8, hq=8, hkv=2,
+                         head_dim=128, blocks_per_query=3, dtype=dtype)
+    c2.q = c2.q[:0].copy()
+    go, gm, gl, gout, glse, gst = run_gpu(c2)
+    ro, rm, rl, rst = oracle_partials(c2)
+    assert gst == rst == orc.ST_BAD_EDGE
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]), f16=dtype == np.float16)
 
 
 def _random_partials(rng, n, D, empty_frac=0.2):
