@@ -362,7 +362,7 @@ __device__ __forceinline__ uint64_t l2_policy_last() {
 }
 
 // ---- fp32 products from split fp16 operands ------------------------------------------
-// An fp32 operand (a half row of Q, a block of K or V) is scaled by a power of two 2^s,
+// An fp32 operand (a row of Q, a block of K or V) is scaled by a power of two 2^s,
 // chosen from its largest magnitude so that the scaled values lie below 2^15 and the
 // largest at or above 2^14, and written as two fp16 numbers: hi = fp16(x 2^s) and
 // lo = fp16(x 2^s - hi). Their sum keeps 22 significant bits (as a tf32 pair does), and a
@@ -444,9 +444,9 @@ __global__ void __launch_bounds__(256) qsplit_kernel(SparseParams p) {
   const int64_t stride = (int64_t)gridDim.x * 8;
   for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += stride) {
     float v[PER];
-    if (PER == 4) {
+    if constexpr (PER == 4) {
       const float4 x = *reinterpret_cast<const float4*>(p.q + row * D + lane * 4);
-      v[0] = x.x; v[1] = x.y; v[PER > 2 ? 2 : 0] = x.z; v[PER > 3 ? 3 : 1] = x.w;
+      v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
     } else {
       const float2 x = *reinterpret_cast<const float2*>(p.q + row * D + lane * 2);
       v[0] = x.x; v[1] = x.y;
@@ -464,9 +464,9 @@ __global__ void __launch_bounds__(256) qsplit_kernel(SparseParams p) {
       fma2(x0, x1, v[2 * k], v[2 * k + 1], f, 0.f);
       split_pair(x0, x1, hi[k], lo[k]);
     }
-    if (PER == 4) {
-      *reinterpret_cast<uint2*>(p.qhi + row * D + lane * 4) = make_uint2(hi[0], hi[PER / 2 - 1]);
-      *reinterpret_cast<uint2*>(p.qlo + row * D + lane * 4) = make_uint2(lo[0], lo[PER / 2 - 1]);
+    if constexpr (PER == 4) {
+      *reinterpret_cast<uint2*>(p.qhi + row * D + lane * 4) = make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2*>(p.qlo + row * D + lane * 4) = make_uint2(lo[0], lo[1]);
     } else {
       *reinterpret_cast<uint32_t*>(p.qhi + row * D + lane * 2) = hi[0];
       *reinterpret_cast<uint32_t*>(p.qlo + row * D + lane * 2) = lo[0];
