@@ -448,8 +448,8 @@ def setup_sparse(args, f16=False, causal=False):
     w.check = lambda: 0
     w.metric, w.unit, w.higher = METRICS[name]
     w.work, w.dtype, w.tokens = flops / 1e12, "f16" if f16 else "f32", c.q.shape[0]
-    # the partials run on the tensor core (3xTF32 for fp32 inputs: about 0.24 ms of tf32
-    # work at this size; kind::f16 for fp16), so their roofline is HBM: K/V pool read once,
+    # the partials run on the tensor core (fp32 inputs as three fp16 products of scaled
+    # (hi, lo) splits, fp16 inputs as one), so their roofline is HBM: K/V pool read once,
     # Q once, partials (fp32) written once
     compulsory = w.config["partials_compulsory_bytes"]
     w.dominant, w.dom_work, w.bound, w.dom_unit = "sparse_partials", compulsory / 1e9, "hbm", "GB/s"

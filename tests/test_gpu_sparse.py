@@ -209,7 +209,7 @@ def test_f16_rejects_blocks_past_64_keys():
     assert ei.value.name == "PKV_ERR_UNSUPPORTED"
 
 
-# right-aligned causal mask: 3xTF32 tensor-core (64-key blocks), fp32 FMA (128-key
+# right-aligned causal mask: split-fp16 tensor-core (64-key blocks), fp32 FMA (128-key
 # blocks) and fp16 tensor-core paths
 @pytest.mark.parametrize("head_dim,pages_per_block,qhead,dtype",
                          [(128, 4, 4, np.float32), (64, 8, 2, np.float32),
