@@ -668,17 +668,22 @@ __device__ void prefill_tile(const AttnParams& p, unsigned char* smem, int item_
 //            last visible key are zero-filled with cp.async instead, so that masked
 //            columns meet zeros in P V. K (2 stages) and V (3 stages) are released
 //            separately: K_{j+2} streams in once S_j is computed, V_{j+3} once
-//            O += P_j V_j is.
-//   warp 4 (lane 0):   tcgen05.mma issuer. S_j = Q K_j^T into TMEM buffer j % 2 and
-//            O += P_j V_j are each issued as soon as their operands are ready.
+//            O += P_j V_j is. Warp 5 also claims the tiles from the planner's counter and
+//            publishes them in a 4-entry ring that every other role reads in order; there
+//            is no block-wide barrier between tiles, so a tile's epilogue overlaps the next
+//            tile's loads and S = Q K^T (the Q buffer is released by a commit after the
+//            last S of a tile).
+//   warp 4 (lane 0) and warp 7 (lane 0): the two tcgen05.mma issuers, S_j = Q K_j^T into
+//            TMEM buffer G % 2 (G counts blocks across tiles) and O += P_j V_j, each
+//            issued as soon as its operands are ready.
 //   warps 0-3 (softmax): thread r reads row r of S_j from TMEM, masks it by key
 //            validity (block table entries looked up by the warp itself) and causality,
 //            keeps a running max that is raised only when exceeded by more than 2^8
-//            (then O and l are rescaled), writes P_j (fp16) to shared memory, and
-//            finally normalises O.
-// TMEM: S0 columns 0..127, S1 128..255, O 256..383. Each role waits every phase of the
-// barriers it consumes in order, and no producer can run two phases ahead of a
-// consumer, so parity waits never alias.
+//            (then O and l are rescaled), writes P_j (fp16) to TMEM, and finally
+//            normalises O.
+// TMEM: S0 columns 0..127, S1 128..255, O 256..383, P 448..511. Each role waits every
+// phase of the barriers it consumes in order, and no producer can run two phases ahead of
+// a consumer, so parity waits never alias.
 // ----------------------------------------------------------------------------------
 struct TcMaps {     // TMA descriptors (kernel parameters)
   CUtensorMap q;    // query [tokens][Hq][128], box 64 x G x 128/G
@@ -691,8 +696,8 @@ struct TcLayout {  // byte offsets from a 1024-byte-aligned base
   static constexpr uint32_t kV = kK + 65536;      // kVStages x 32 KB
   static constexpr uint32_t kBars = kV + 98304;   // mbarriers (see TcBar)
   static constexpr uint32_t kTmem = kBars + 256;  // TMEM base address
-  static constexpr uint32_t kTile = kTmem + 4;    // current tile index
-  static constexpr uint32_t kAbort = kTile + 4;   // set when a bounded wait gives up
+  static constexpr uint32_t kTile = kTmem + 4;    // ring of claimed tile indices (4)
+  static constexpr uint32_t kAbort = kTile + 16;  // set when a bounded wait gives up
   static constexpr uint32_t kEnd = kAbort + 8;
 };
 enum TcBar {  // mbarrier slots
@@ -707,7 +712,10 @@ enum TcBar {  // mbarrier slots
   kBarDrain = 15,    // count 1: S = Q K^T MMAs in flight when a wait gave up
   kBarSEmpty0 = 16,  // + buffer, count 4: softmax has read S_j out of the buffer
   kBarDrainPv = 18,  // count 1: O += P V MMAs in flight when a wait gave up
-  kNumBars = 19
+  kBarQEmpty = 19,   // count 1: every S = Q K^T of a tile completed (Q buffer free)
+  kBarTileFull0 = 20,   // + slot (4), count 1: tile ring entry published (key loader)
+  kBarTileEmpty0 = 24,  // + slot (4), count 7: entry read by the other roles
+  kNumBars = 28
 };
 static_assert(kNumBars * 8 <= 256, "mbarrier slots");
 // TMEM columns: S_j in buffer j % 2, the O accumulator, and P_j as fp16 pairs (two keys
@@ -805,7 +813,7 @@ __device__ __forceinline__ TcBox tc_box(const AttnParams& p, const TcTile& t, in
 // Key loader warp: Q tile, then the K boxes of every block (keys past the visible range
 // and unmapped boxes are left as they are: the softmax masks them).
 __device__ void tc_load_k(const AttnParams& p, const TcMaps& maps, unsigned char* sm,
-                          const TcTile& t, uint32_t (&k_use)[kKStages], bool& bad) {
+                          const TcTile& t, uint32_t q_n, uint32_t (&k_use)[kKStages], bool& bad) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const int lane = threadIdx.x & 31;
@@ -813,6 +821,9 @@ __device__ void tc_load_k(const AttnParams& p, const TcMaps& maps, unsigned char
   // testing hook: the CTA's first K box is announced but never copied, so the MMA's wait
   // for it gives up (no copy or MMA of that block is in flight when it does)
   const bool withhold = p.withhold_copy && k_use[0] == 0;
+  if (q_n > 0 && !__all_sync(0xffffffffu, tc_wait(bars + kBarQEmpty, (q_n - 1) & 1u, abort,
+                                                     tc_tries(p))))
+    return;
   if (lane == 0) {
     // rows past the tile's positions hold other tokens (or zeros past the last token)
     // and are never written out
@@ -906,7 +917,7 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
 // two of a tile are never waited for).
 __device__ void tc_mma_s(const AttnParams& p, unsigned char* sm, const TcTile& t,
                          uint32_t tmem, uint32_t q_use, uint32_t (&k_use)[kKStages],
-                         uint32_t (&s_base)[2]) {
+                         uint32_t& g_blk) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const uint32_t idesc_qk = tc::idesc_f16(128, 128, false, false);
@@ -914,10 +925,11 @@ __device__ void tc_mma_s(const AttnParams& p, unsigned char* sm, const TcTile& t
   if (!tc_wait(bars + kBarQFull, q_use & 1u, abort, tc_tries(p))) return;
   uint32_t idle = 0;
   for (int jq = 0, kq = 0; jq < t.nblk;) {
-    // buffer s was last filled with S_{jq-2}: phase s_base[s] + (jq - 2) / 2 of SEmpty_s
-    const int s = jq & 1;
-    if ((jq < 2 ||
-         tc::mbar_test(bars + kBarSEmpty0 + s, (s_base[s] + (uint32_t)((jq - 2) >> 1)) & 1u)) &&
+    // block G = g_blk + jq (counted across tiles) fills buffer G % 2, last filled by
+    // block G - 2: phase (G - 2) / 2 of SEmpty_s
+    const uint32_t G = g_blk + (uint32_t)jq;
+    const int s = (int)(G & 1u);
+    if ((G < 2 || tc::mbar_test(bars + kBarSEmpty0 + s, ((G >> 1) - 1u) & 1u)) &&
         tc::mbar_test(bars + kBarKFull0 + kq, k_use[kq] & 1u)) {
       ++k_use[kq];
       tc::fence_after_sync();
@@ -938,9 +950,9 @@ __device__ void tc_mma_s(const AttnParams& p, unsigned char* sm, const TcTile& t
       return;
     }
   }
-  // SEmpty phases of this tile: one per block read from each buffer
-  s_base[0] += (uint32_t)((t.nblk + 1) >> 1);
-  s_base[1] += (uint32_t)(t.nblk >> 1);
+  g_blk += (uint32_t)t.nblk;
+  // the next tile's Q may land once every S of this one has completed
+  tc::commit(bars + kBarQEmpty);
 }
 
 // Warp 7, lane 0: O += P_jp V_jp once the softmax has written P_jp to TMEM and V_jp landed.
@@ -1016,7 +1028,7 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
   };
   int blk_next = lookup(0);
   for (int j = 0; j < t.nblk && ok; ++j) {
-    const int s = j & 1;
+    const int s = (int)((blk_use + (uint32_t)j) & 1u);
     const int kbase = j * 128;
     // key validity of block j: lane covers keys [kbase + 4 lane, + 4), which lie in one
     // cache block because the block size is a multiple of 8; key c of the block is bit
@@ -1145,14 +1157,15 @@ __device__ void tc_softmax(const AttnParams& p, unsigned char* sm, const TcTile&
   blk_use += t.nblk;
 }
 
-// Tiles from the planner's counter; barriers and 512 TMEM columns held throughout.
+// Tiles from the planner's counter through the tile ring; barriers and 512 TMEM columns
+// held throughout.
 __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsigned char* sm,
                                  bool& bad) {
   const int ntiles = p.counts[kCntTiles];
   if (ntiles == 0) return;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcLayout::kBars);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TcLayout::kTmem);
-  volatile int* tile = reinterpret_cast<volatile int*>(sm + TcLayout::kTile);
+  volatile int* tile = reinterpret_cast<volatile int*>(sm + TcLayout::kTile);   // [4]
   volatile int* abort = reinterpret_cast<volatile int*>(sm + TcLayout::kAbort);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -1173,6 +1186,11 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
     tc::mbar_init(bars + kBarODone, 1);
     tc::mbar_init(bars + kBarDrain, 1);
     tc::mbar_init(bars + kBarDrainPv, 1);
+    tc::mbar_init(bars + kBarQEmpty, 1);
+    for (int i = 0; i < 4; ++i) {
+      tc::mbar_init(bars + kBarTileFull0 + i, 1);
+      tc::mbar_init(bars + kBarTileEmpty0 + i, 7);
+    }
     tc::mbar_init_fence();
     *abort = 0;
   }
@@ -1191,37 +1209,59 @@ __device__ void prefill_phase_tc(const AttnParams& p, const TcMaps& maps, unsign
   const uint32_t tmem = *tslot;
   // per-role phase counters (each role waits every phase it depends on, in order)
   uint32_t k_use[kKStages] = {}, v_use[kVStages] = {}, s_use[2] = {0u, 0u};
-  uint32_t s_base[2] = {0u, 0u};
+  uint32_t g_blk = 0u;   // S issuer: blocks of earlier tiles
   uint32_t q_use = 0u, blk_use = 0u;
   bool mma_aborted = false;
-  while (true) {
-    if (tid == 0) *tile = atomicAdd(&p.counts[kCntTileNext], 1);
-    __syncthreads();
-    const int ti = *tile;
-    const bool stop = ti >= ntiles || *abort;
-    __syncthreads();
-    if (stop) break;
+  // Tiles flow through a 4-entry ring: the key loader claims each from the planner's
+  // counter and publishes it (-1 = no more); every other role reads the entries in order
+  // and releases each at once. No block-wide barrier between tiles: a tile's epilogue and
+  // the next tile's loads and S = Q K^T overlap.
+  const bool producer = warp == kKLoaderWarp;
+  const bool consumer = tid < 128 || tid == kMmaThread || tid == kPvThread || warp == kVLoaderWarp;
+  for (uint32_t n = 0; producer || consumer; ++n) {
+    const uint32_t slot = n & 3u, ph = (n >> 2) & 1u;
+    int ti = -1;
+    if (producer) {
+      if (lane == 0) ti = atomicAdd(&p.counts[kCntTileNext], 1);
+      ti = __shfl_sync(0xffffffffu, ti, 0);
+      if (ti >= ntiles || *abort) ti = -1;
+      if (n >= 4 && !__all_sync(0xffffffffu, tc_wait(bars + kBarTileEmpty0 + slot, ph ^ 1u, abort,
+                                                       tc_tries(p))))
+        break;
+      if (lane == 0) {
+        tile[slot] = ti;
+        mbar_arrive(bars + kBarTileFull0 + slot);
+      }
+    } else {
+      const bool whole_warp = tid < 128 || warp == kVLoaderWarp;
+      bool ok = tc_wait(bars + kBarTileFull0 + slot, ph, abort, tc_tries(p));
+      if (whole_warp) ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ti = tile[slot];
+      if (whole_warp) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + kBarTileEmpty0 + slot);
+      } else {
+        mbar_arrive(bars + kBarTileEmpty0 + slot);
+      }
+    }
+    if (ti < 0) break;
     const TcTile t = tc_tile(p, ti);
     if (tid < 128) {
       tc_softmax(p, sm, t, tmem, s_use, blk_use);
     } else if (tid == kMmaThread) {
-      tc_mma_s(p, sm, t, tmem, q_use, k_use, s_base);
+      tc_mma_s(p, sm, t, tmem, q_use, k_use, g_blk);
       mma_aborted = *abort != 0;
     } else if (tid == kPvThread) {
       tc_mma_pv(p, sm, t, tmem, v_use, blk_use);
       mma_aborted = *abort != 0;
     } else if (warp == kKLoaderWarp) {
-      tc_load_k(p, maps, sm, t, k_use, bad);
+      tc_load_k(p, maps, sm, t, q_use, k_use, bad);
     } else if (warp == kVLoaderWarp) {
       tc_load_v(p, maps, sm, t, v_use);
     }
     ++q_use;
-    // the next tile rewrites Q: every MMA of this tile has completed (the softmax waited
-    // for the last O += P V, and MMAs complete in issue order)
-    cp_async_wait<0>();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
+    if (*abort) break;
   }
   if (*abort) {
     // a wait gave up: let the copies and MMAs this CTA issued land before it exits
