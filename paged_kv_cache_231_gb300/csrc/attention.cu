@@ -370,11 +370,28 @@ __device__ void flush_piece(const AttnParams& p, const Cursor& c, int gw, int W,
   done = __shfl_sync(0xffffffffu, done, 0);
   if (done != pieces - 1) return;
   __threadfence();
+  // every (row, piece) m and l in one round when they fit the warp (lane = row * pieces +
+  // piece); otherwise row by row
+  const bool packed = R * pieces <= 32;
+  float lp_all = 0.f, mp_all = -INFINITY;
+  if (packed && lane < R * pieces) {
+    const int rr = lane / pieces, qq = lane - rr * pieces;
+    const int64_t prow =
+        ((int64_t)(c.d.slot + rr / p.G) * p.Hq + c.h * p.G + rr % p.G) * p.max_splits + qq;
+    lp_all = __ldcg(p.part_l + prow);
+    mp_all = __ldcg(p.part_m + prow);
+  }
   for (int r = 0; r < R; ++r) {
     const int64_t prow0 =
         ((int64_t)(c.d.slot + r / p.G) * p.Hq + c.h * p.G + r % p.G) * p.max_splits;
     float lp = 0.f, mp = -INFINITY;
-    if (lane < pieces) {
+    if (packed) {
+      const int src = r * pieces + (lane < pieces ? lane : 0);
+      lp = __shfl_sync(0xffffffffu, lp_all, src);
+      mp = __shfl_sync(0xffffffffu, mp_all, src);
+      if (lane >= pieces) lp = 0.f;
+      if (!(lp > 0.f)) mp = -INFINITY;
+    } else if (lane < pieces) {
       lp = __ldcg(p.part_l + prow0 + lane);
       if (lp > 0.f) mp = __ldcg(p.part_m + prow0 + lane);
     }
@@ -384,6 +401,7 @@ __device__ void flush_piece(const AttnParams& p, const Cursor& c, int gw, int W,
     float acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = 0.f;
+#pragma unroll 4
     for (int q = 0; q < pieces; ++q) {
       const float wq = __shfl_sync(0xffffffffu, w, q);
       if (wq > 0.f) {
