@@ -481,21 +481,25 @@ __global__ void __launch_bounds__(256) qsplit_kernel(SparseParams p) {
 // Warp-specialised form: a persistent CTA of 16 warps per SM, every hand-off on an
 // mbarrier.
 //   warp 12 (scheduler): takes groups from the counter, publishes each in a 4-entry ring
-//     with its 64-bit key masks (mapped, invalid reference) and stages the group's raw
-//     fp32 K and V pages by TMA (one box per page and 32-column slice) into one of two
-//     stages, once every product of the group that used the stage last is done.
-//   warps 8-11 (convert + upper Q halves): per tile, the upper half of every split Q row
-//     into TMEM; after the first tile of a group, the raw K, then V, of its stage split in
-//     place into (hi, lo) fp16 tiles (both in the K-major layout: K is the K-major operand
-//     of S = Q K^T and V the MN-major operand of O = P V), each block scaled by its own
-//     power of two; keys not mapped become zeros. The tile's K and V shifts to a ring.
+//     with its 64-bit key masks (mapped, invalid reference), a group ahead of its staging,
+//     and stages the group's raw fp32 K and V pages by TMA (one box per page and 32-column
+//     slice) into one of two stages, once every product of the group that used the stage
+//     last is done.
+//   warps 8-11 (convert): at the first tile of a group, the raw K, then V, of its stage
+//     split in place into (hi, lo) fp16 tiles (both in the K-major layout: K is the K-major
+//     operand of S = Q K^T and V the MN-major operand of O = P V), each block scaled by its
+//     own power of two; keys not mapped become zeros. The tile's K and V shifts go to a
+//     ring of slots that the softmax and store warps release.
 //   warps 4-7 (lower Q halves + store): per tile, the lower half of every split Q row; the
-//     O rows of the previous tile from TMEM to memory, scaled back.
+//     O rows of the previous tile from TMEM to memory, scaled back (through a per-warp
+//     staging area, so that each store instruction writes whole 128-byte row segments).
 //   warps 13, 14, lane 0 (S issuers): S = Q K^T of the even / odd tiles (24 MMAs of
 //     128 x 64 x 16 for head size 128 into the tile parity's accumulator).
 //   warp 15, lane 0 (O issuer): O = P V, P (hi, lo) read from TMEM (12 MMAs).
 //   warps 0-3 (softmax, one thread per row): the row's scores from S and the shifts, m,
-//     the weights and l; P' = 2^14 P (hi, lo) over the S columns; m and l to memory.
+//     the weights and l; P' = 2^14 P (hi, lo) over the S columns; m and l to memory; then
+//     the upper half of the split Q row of the tile two ahead into TMEM (its L2 round trip
+//     off the chain of the converter warps).
 // TMEM: S of tile parity b at 64 b (P' hi at +0 and lo at +32 once the scores are read), O
 // at 128, Q (hi, lo) of tile parity b at 256 + D b (hi D/2 columns, then lo). With two S
 // and two Q buffers the next tile's Q copy and S run while the softmax and O of this one
@@ -524,7 +528,8 @@ enum : int {
   kCvtV,                          // the same for V
   kQReady,                        // [2] Q (hi, lo) of a tile in buffer b (8 warps)
   kScale = kQReady + 2,           // [kScaleRing] K and V shifts of a tile posted (4 warps)
-  kSFull = kScale + kScaleRing,   // [2] S of a tile in buffer b (issuer b commits)
+  kScaleFree = kScale + kScaleRing,   // [kScaleRing] a tile's shifts read (8 warps)
+  kSFull = kScaleFree + kScaleRing,   // [2] S of a tile in buffer b (issuer b commits)
   kPFull = kSFull + 2,            // [2] P of a tile in buffer b (4 softmax warps)
   kPvDone = kPFull + 2,           // [2] O of a tile of parity b complete (commit)
   kOEmpty = kPvDone + 2,          // O read out of TMEM (4 store warps)
@@ -547,7 +552,9 @@ struct Layout {   // byte offsets from a 1024-byte-aligned base
   static constexpr uint32_t kStage = 2 * kHalf;  // K, then V
   static constexpr uint32_t kSub = kNK * 128;    // a 32-column fp32 box or 64-column fp16 tile
   static constexpr uint32_t kLo = D * 128;       // lo tile after the hi tile
-  static constexpr uint32_t kRingOff = kStages * kStage;
+  static constexpr uint32_t kStgWarp = 32 * 128;  // a store warp's O staging: 32 rows x 128 B
+  static constexpr uint32_t kStgOff = kStages * kStage;
+  static constexpr uint32_t kRingOff = kStgOff + 4 * kStgWarp;
   static constexpr uint32_t kScaleOff = kRingOff + kRing * sizeof(GroupEntry);
   static constexpr uint32_t kMaxOff = kScaleOff + kScaleRing * sizeof(TileScales);
   static constexpr uint32_t kBar = kMaxOff + 8 * sizeof(float);
@@ -610,7 +617,9 @@ __device__ __forceinline__ int4 row_record(const SparseParams& p, int c0, int e1
   return make_int4(-1, 0, 0, 0);
 }
 
-// Warp 12: group scheduling, key masks and raw K/V staging.
+// Warp 12: group scheduling, key masks and raw K/V staging. Ring entries are published one
+// group ahead of the staging, so that the Q rows of a group's first tile can be fetched
+// while the stage of the group two back is still in use.
 template <int D>
 __device__ void sched_role(const SparseParams& p, const SpMaps& maps, unsigned char* sm,
                            uint32_t (&issued)[kStages]) {
@@ -623,15 +632,18 @@ __device__ void sched_role(const SparseParams& p, const SpMaps& maps, unsigned c
     tc::tma_prefetch_desc(&maps.k);
     tc::tma_prefetch_desc(&maps.v);
   }
-  for (uint32_t gi = 0;; ++gi) {
-    long long g = 0;
+  // ring entry gi: the next group with edges (or the end) with its key masks; row0 = first
+  // row of the group's page `lane` in the page tensors (-1: none)
+  auto publish = [&](uint32_t gi, long long& g, int& row0) -> bool {
+    g = 0;
     if (lane == 0) g = next_group(p);
     g = __shfl_sync(0xffffffffu, g, 0);
     const int slot = (int)(gi % kRing);
-    if (gi >= kRing && !warp_wait(bars + kGEmpty + slot, ((gi / kRing) - 1) & 1u, abort)) return;
+    if (gi >= kRing && !warp_wait(bars + kGEmpty + slot, ((gi / kRing) - 1) & 1u, abort))
+      return false;
     uint64_t vmask = 0, imask = 0;
-    int row0 = -1;   // first row of page `lane` of the block in the page tensors
     int e0 = 0, e1 = 0;
+    row0 = -1;
     if (g < p.ngroups) {
       const int h = (int)(g % p.hkv);
       const int64_t bb = g / p.hkv;
@@ -672,7 +684,15 @@ __device__ void sched_role(const SparseParams& p, const SpMaps& maps, unsigned c
       ring[slot].imask = imask;
       bar_arrive(bars + kGFull + slot);   // release: the entry is visible to the waiters
     }
-    if (g >= p.ngroups) return;
+    return true;
+  };
+  long long g;
+  int row0;
+  if (!publish(0, g, row0)) return;
+  for (uint32_t gi = 0; g < p.ngroups; ++gi) {
+    long long g_next;
+    int row0_next;
+    if (!publish(gi + 1, g_next, row0_next)) return;
     // the stage is free once every S and every O of the group that used it last are done
     const uint32_t st = gi % kStages;
     if (gi >= kStages) {
@@ -698,6 +718,8 @@ __device__ void sched_role(const SparseParams& p, const SpMaps& maps, unsigned c
       }
     }
     ++issued[st];
+    g = g_next;
+    row0 = row0_next;
   }
 }
 
@@ -788,10 +810,82 @@ __device__ __forceinline__ void copy_q_half(uint32_t q_tm, const __half* hi_row,
   tc::tmem_wait_st();
 }
 
-// Warps 8-11: the upper Q half rows per tile; the K and V split of each group once its
-// first tile's Q is in place (S of that tile then waits only for K).
+// Walks the tiles in work order (ring entries read as needed) for this thread's row: the
+// tile's edge record (load left in flight) and kv head; ok = false past the last tile or on
+// abort.
+struct TileCursor {
+  uint32_t gi;
+  int c0, e1;
+  long long g;
+  bool ok;
+};
+__device__ __forceinline__ void cursor_first(const SparseParams& p, uint64_t* bars,
+                                             const volatile GroupEntry* ring,
+                                             volatile int* abort, TileCursor& c) {
+  GroupEntry e;
+  c.ok = read_entry(p, bars, ring, 0, abort, true, e);
+  c.gi = 0;
+  c.c0 = e.e0;
+  c.e1 = e.e1;
+  c.g = e.g;
+}
+__device__ __forceinline__ void cursor_next(const SparseParams& p, uint64_t* bars,
+                                            const volatile GroupEntry* ring, volatile int* abort,
+                                            TileCursor& c) {
+  if (!c.ok) return;
+  const int epc = 128 / p.qhead;
+  if (c.c0 + epc < c.e1) {
+    c.c0 += epc;
+    return;
+  }
+  GroupEntry e;
+  c.ok = read_entry(p, bars, ring, c.gi + 1, abort, true, e);
+  c.gi += 1;
+  c.c0 = e.e0;
+  c.e1 = e.e1;
+  c.g = e.g;
+}
+// split Q row of this thread in the cursor's tile (-1: padding row or no tile)
+__device__ __forceinline__ int64_t cursor_qrow(const SparseParams& p, const TileCursor& c,
+                                               int4 rec, int my_qh) {
+  if (!c.ok || rec.x < 0) return -1;
+  return (int64_t)rec.y * p.hq + (int)(c.g % p.hkv) * p.qhead + my_qh;
+}
+__device__ __forceinline__ int4 cursor_record(const SparseParams& p, const TileCursor& c,
+                                              int my_er) {
+  const int epc = 128 / p.qhead;
+  return c.ok ? row_record(p, c.c0, c.e1, my_er, epc) : make_int4(-1, 0, 0, 0);
+}
+
+// O rows (D columns) of this warp's 32 tile rows, 32 columns from column c, written out
+// through the warp's staging area so that every store instruction writes whole 128-byte row
+// segments: each lane puts its row (o, scaled by f) in place, then lanes copy 4 rows x 128
+// bytes per instruction. `pj` holds, for lane i, the partial index of tile row 4 j + i / 8
+// in slot j (-1: padding row).
 template <int D>
-__device__ void convert_role(const SparseParams& p, unsigned char* sm, uint32_t tmem) {
+__device__ __forceinline__ void store_o_chunk(unsigned char* stg, const float (&o)[32], float f,
+                                              float* out, const int (&pj)[8], int c, int lane) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t off = (uint32_t)lane * 128u + (uint32_t)((k ^ (lane & 7)) * 16);
+    *reinterpret_cast<float4*>(stg + off) =
+        make_float4(o[4 * k] * f, o[4 * k + 1] * f, o[4 * k + 2] * f, o[4 * k + 3] * f);
+  }
+  __syncwarp();
+  const int kk = lane & 7;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int row = 4 * j + (lane >> 3);
+    const float4 v = *reinterpret_cast<const float4*>(
+        stg + (uint32_t)row * 128u + (uint32_t)((kk ^ (row & 7)) * 16));
+    if (pj[j] >= 0) __stcs(reinterpret_cast<float4*>(out + (int64_t)pj[j] * D + c) + kk, v);
+  }
+  __syncwarp();
+}
+
+// Warps 8-11: the K and V split of each group at its first tile; the tile's K and V shifts.
+template <int D>
+__device__ void convert_role(const SparseParams& p, unsigned char* sm) {
   using L = Layout<D>;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
   volatile int* abort = reinterpret_cast<volatile int*>(sm + L::kAbort);
@@ -799,31 +893,20 @@ __device__ void convert_role(const SparseParams& p, unsigned char* sm, uint32_t 
   TileScales* scales = reinterpret_cast<TileScales*>(sm + L::kScaleOff);
   float* wmax = reinterpret_cast<float*>(sm + L::kMaxOff);   // [K: 4][V: 4]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wq = warp & 3, ct = wq * 32 + lane;   // TMEM quadrant; thread of the 128
-  const int r = ct;                               // tile row of this thread
-  const uint32_t lane_tm = tmem + ((uint32_t)(wq * 32) << 16);
-  const int epc = 128 / p.qhead, my_er = r / p.qhead, my_qh = r - (r / p.qhead) * p.qhead;
-  const uint64_t keep = l2_policy_last();
+  const int ct = (warp & 3) * 32 + lane;   // thread of the 128
+  const int epc = 128 / p.qhead;
   uint32_t t = 0;
   for (uint32_t gi = 0;; ++gi) {
     GroupEntry e;
     if (!read_entry(p, bars, ring, gi, abort, true, e)) return;
-    const int h = (int)(e.g % p.hkv);
     const uint32_t st = gi % kStages;
     unsigned char* kb = sm + st * L::kStage;
-    int4 rec = row_record(p, e.e0, e.e1, my_er, epc);
     int sk = 0, sv = 0;
     for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
-      const uint32_t b = t & 1u;
-      // Q buffer b is free once S of tile t - 2 is done
-      if (t >= 2 && !warp_wait(bars + kSFull + b, ((t >> 1) - 1) & 1u, abort)) return;
-      tc::fence_after_sync();
-      const int64_t qrow = (int64_t)rec.y * p.hq + h * p.qhead + my_qh;
-      copy_q_half<D, 1>(lane_tm + kTmQ + b * (uint32_t)D, rec.x >= 0 ? p.qhi + qrow * D : nullptr,
-                        rec.x >= 0 ? p.qlo + qrow * D : nullptr, keep);
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) bar_arrive(bars + kQReady + b);
+      // scale slot t % kScaleRing is free once both readers are done with tile t - kScaleRing
+      if (t >= kScaleRing &&
+          !warp_wait(bars + kScaleFree + t % kScaleRing, ((t / kScaleRing) - 1) & 1u, abort))
+        return;
       if (c0 == e.e0) {   // K, then V, of this group once its raw block landed
         if (!warp_wait(bars + kRawFull + st, (gi / kStages) & 1u, abort)) return;
         if (!split_block<D>(kb, e.vmask, wmax, bars + kCvtK, gi & 1u, abort, ct, sk)) return;
@@ -843,7 +926,6 @@ __device__ void convert_role(const SparseParams& p, unsigned char* sm, uint32_t 
       }
       __syncwarp();
       if (lane == 0) bar_arrive(bars + kScale + t % kScaleRing);
-      if (c0 + epc < e.e1) rec = row_record(p, c0 + epc, e.e1, my_er, epc);
     }
     __syncwarp();
     if (lane == 0) bar_arrive(bars + kGEmpty + (gi % kRing));
@@ -863,24 +945,24 @@ __device__ void store_role(const SparseParams& p, unsigned char* sm, uint32_t tm
   const uint32_t lane_tm = tmem + ((uint32_t)(wq * 32) << 16);
   const int epc = 128 / p.qhead, my_er = r / p.qhead, my_qh = r - (r / p.qhead) * p.qhead;
   const uint64_t keep = l2_policy_last();
+  unsigned char* stg = sm + L::kStgOff + (uint32_t)wq * L::kStgWarp;
   // O rows of tile tt (partial index pi, -1 = padding row) to memory: O' = 2^(14 + sv) O
   auto store = [&](uint32_t tt, int pi) -> bool {
     if (!warp_wait(bars + kPvDone + (tt & 1u), (tt >> 1) & 1u, abort)) return false;
     if (!warp_wait(bars + kScale + tt % kScaleRing, (tt / kScaleRing) & 1u, abort)) return false;
     tc::fence_after_sync();
     const float f = ldexpf(1.f, -(kPLog2 + scales[tt % kScaleRing].sv));
+    __syncwarp();
+    if (lane == 0) bar_arrive(bars + kScaleFree + tt % kScaleRing);
+    int pj[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) pj[j] = __shfl_sync(0xffffffffu, pi, 4 * j + (lane >> 3));
 #pragma unroll 1
     for (int ch = 0; ch < D / 32; ++ch) {
       float o[32];
       tc::tmem_ld32(lane_tm + kTmO + ch * 32, o);
       tc::tmem_wait_ld();
-      if (pi >= 0) {
-        float4* dst = reinterpret_cast<float4*>(p.o + (int64_t)pi * D + ch * 32);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          __stcs(dst + k, make_float4(o[4 * k] * f, o[4 * k + 1] * f, o[4 * k + 2] * f,
-                                      o[4 * k + 3] * f));
-      }
+      store_o_chunk<D>(stg, o, f, p.o, pj, ch * 32, lane);
     }
     tc::fence_before_sync();
     __syncwarp();
@@ -930,25 +1012,50 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
   const int epc = 128 / p.qhead, my_er = r / p.qhead, my_qh = r - (r / p.qhead) * p.qhead;
   const float sl2 = p.scale * kLog2e;
   const float p_scale = (float)(1 << kPLog2);
+  const uint64_t keep = l2_policy_last();
+  // Upper Q half of the cursor's tile (if any) into TMEM buffer b, then QReady of that
+  // buffer; the row's partial index, key count and Q shift join the queue of the tiles
+  // ahead (entry 1 after entry 0; partial index -1: padding row).
+  int pi0 = -1, pi1 = -1, keys0 = 0, keys1 = 0, sq0 = 0, sq1 = 0;
+  auto q_upper = [&](const TileCursor& c, int4 rq, uint32_t b) {
+    const int64_t qr = cursor_qrow(p, c, rq, my_qh);
+    if (c.ok) {
+      copy_q_half<D, 1>(lane_tm + kTmQ + b * (uint32_t)D, qr >= 0 ? p.qhi + qr * D : nullptr,
+                        qr >= 0 ? p.qlo + qr * D : nullptr, keep);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) bar_arrive(bars + kQReady + b);
+    }
+    pi0 = pi1;
+    keys0 = keys1;
+    sq0 = sq1;
+    pi1 = qr >= 0 ? rq.x * p.qhead + my_qh : -1;
+    keys1 = qr >= 0 ? rq.z : 0;
+    sq1 = qr >= 0 ? __ldg(p.qshift + qr) : 0;
+  };
+  // tiles 0 and 1 now; tile t + 2 once the weights of tile t are out (S of tile t, the last
+  // reader of buffer t & 1, is done), from a record loaded a tile before
+  TileCursor cq;
+  cursor_first(p, bars, ring, abort, cq);
+  for (uint32_t k = 0; k < 2; ++k) {
+    q_upper(cq, cursor_record(p, cq, my_er), k);
+    cursor_next(p, bars, ring, abort, cq);
+  }
+  if (*abort) return;
+  int4 rec_q = cursor_record(p, cq, my_er);
   uint32_t t = 0;
   for (uint32_t gi = 0;; ++gi) {
     GroupEntry e;
     if (!read_entry(p, bars, ring, gi, abort, true, e)) return;
-    const int h = (int)(e.g % p.hkv);
-    int4 rec = row_record(p, e.e0, e.e1, my_er, epc);
-    int sq = rec.x >= 0 ? __ldg(p.qshift + (int64_t)rec.y * p.hq + h * p.qhead + my_qh) : 0;
     for (int c0 = e.e0; c0 < e.e1; c0 += epc, ++t) {
       const uint32_t b = t & 1u;
-      const int keys = rec.x >= 0 ? rec.z : 0;
-      const int pi = rec.x >= 0 ? rec.x * p.qhead + my_qh : -1;
-      const int sq_t = sq;
-      if (c0 + epc < e.e1) {
-        rec = row_record(p, c0 + epc, e.e1, my_er, epc);
-        sq = rec.x >= 0 ? __ldg(p.qshift + (int64_t)rec.y * p.hq + h * p.qhead + my_qh) : 0;
-      }
+      // this tile's partial index, key count and Q shift lead the queue
+      const int keys = keys0, pi = pi0, sq_t = sq0;
       // the shifts of this row's Q and of the block's K: S' = 2^(sq + sk) S
       if (!warp_wait(bars + kScale + t % kScaleRing, (t / kScaleRing) & 1u, abort)) return;
       const float f = ldexpf(sl2, -(sq_t + scales[t % kScaleRing].sk));
+      __syncwarp();
+      if (lane == 0) bar_arrive(bars + kScaleFree + t % kScaleRing);
       if (!warp_wait(bars + kSFull + b, (t >> 1) & 1u, abort)) return;
       tc::fence_after_sync();
       const uint32_t s_tm = lane_tm + kTmS + b * 64u;
@@ -989,15 +1096,19 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
       const float lrow = ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
       // m in natural-log units (the -1e30 sentinel as is when no key takes part)
       const float mrow = m2 > 0.5f * kNegLarge ? m2 * kLn2 : kNegLarge;
-      uint32_t ph[32], pl[32];   // P' = 2^14 P as (hi, lo) fp16 pairs of keys
+      // P' = 2^14 P as (hi, lo) fp16 pairs of keys, 32 keys at a time
 #pragma unroll
-      for (int k = 0; k < 64; k += 2) {
-        float w0, w1;
-        fma2(w0, w1, s[k], s[k + 1], p_scale, 0.f);
-        split_pair(w0, w1, ph[k / 2], pl[k / 2]);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          float w0, w1;
+          fma2(w0, w1, s[32 * hf + k], s[32 * hf + k + 1], p_scale, 0.f);
+          split_pair(w0, w1, ph[k / 2], pl[k / 2]);
+        }
+        tmem_st_u32<16>(s_tm + 16 * hf, ph);
+        tmem_st_u32<16>(s_tm + 32 + 16 * hf, pl);
       }
-      tmem_st_u32<32>(s_tm, ph);
-      tmem_st_u32<32>(s_tm + 32, pl);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
@@ -1005,6 +1116,12 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
       if (pi >= 0) {
         __stcs(p.m + pi, mrow);
         __stcs(p.l + pi, lrow);
+      }
+      q_upper(cq, rec_q, b);
+      if (cq.ok) {
+        cursor_next(p, bars, ring, abort, cq);
+        if (*abort) return;
+        rec_q = cursor_record(p, cq, my_er);
       }
     }
     __syncwarp();
@@ -1121,7 +1238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(bars + kCvtK, 4);
     tc::mbar_init(bars + kCvtV, 4);
-    for (int i = 0; i < kScaleRing; ++i) tc::mbar_init(bars + kScale + i, 4);
+    for (int i = 0; i < kScaleRing; ++i) {
+      tc::mbar_init(bars + kScale + i, 4);
+      tc::mbar_init(bars + kScaleFree + i, 8);
+    }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(bars + kQReady + b, 8);
       tc::mbar_init(bars + kSFull + b, 1);
@@ -1151,7 +1271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 8) {
     store_role<D>(p, sm, tmem);
   } else if (warp < 12) {
-    convert_role<D>(p, sm, tmem);
+    convert_role<D>(p, sm);
   } else if (warp == kSchedWarp) {
     sched_role<D>(p, maps, sm, issued);
     // a wait gave up: the last staging of each stage must land before the CTA leaves
