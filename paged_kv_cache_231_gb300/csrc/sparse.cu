@@ -616,6 +616,11 @@ __device__ __forceinline__ int4 row_record(const SparseParams& p, int c0, int e1
   if (er < epc && c0 + er < e1) return __ldg(p.edge_rec + c0 + er);
   return make_int4(-1, 0, 0, 0);
 }
+// Marks the point where a record loaded ahead is first used, so that no arithmetic on it
+// (and no wait for its load) is moved up to the load.
+__device__ __forceinline__ void settle(int4& r) {
+  asm volatile("" : "+r"(r.x), "+r"(r.y), "+r"(r.z), "+r"(r.w));
+}
 
 // Warp 12: group scheduling, key masks and raw K/V staging. Ring entries are published one
 // group ahead of the staging, so that the Q rows of a group's first tile can be fetched
@@ -980,6 +985,7 @@ __device__ void store_role(const SparseParams& p, unsigned char* sm, uint32_t tm
       const uint32_t b = t & 1u;
       if (t >= 2 && !warp_wait(bars + kSFull + b, ((t >> 1) - 1) & 1u, abort)) return;
       tc::fence_after_sync();
+      settle(rec);
       const int64_t qrow = (int64_t)rec.y * p.hq + h * p.qhead + my_qh;
       copy_q_half<D, 0>(lane_tm + kTmQ + b * (uint32_t)D, rec.x >= 0 ? p.qhi + qrow * D : nullptr,
                         rec.x >= 0 ? p.qlo + qrow * D : nullptr, keep);
@@ -1018,6 +1024,7 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
   // ahead (entry 1 after entry 0; partial index -1: padding row).
   int pi0 = -1, pi1 = -1, keys0 = 0, keys1 = 0, sq0 = 0, sq1 = 0;
   auto q_upper = [&](const TileCursor& c, int4 rq, uint32_t b) {
+    settle(rq);
     const int64_t qr = cursor_qrow(p, c, rq, my_qh);
     if (c.ok) {
       copy_q_half<D, 1>(lane_tm + kTmQ + b * (uint32_t)D, qr >= 0 ? p.qhi + qr * D : nullptr,
