@@ -513,6 +513,7 @@ constexpr int kScaleRing = 8;           // tile scale entries
 constexpr int kSchedWarp = 12, kIssueS0 = 13, kIssueS1 = 14, kIssuePv = 15;
 constexpr uint32_t kTmS = 0, kTmO = 128, kTmQ = 256;
 constexpr int kPLog2 = 14;              // P' = 2^14 P keeps the lo parts of the weights normal
+constexpr int kRegsIssue = 72, kRegsData = 144;   // registers per thread after the split
 // bound of this CTA's waits (kTries unless a test lowered it), set before the first barrier
 __shared__ uint32_t s_tries;
 
@@ -615,6 +616,10 @@ __device__ __forceinline__ int4 row_record(const SparseParams& p, int c0, int e1
                                            int epc) {
   if (er < epc && c0 + er < e1) return __ldg(p.edge_rec + c0 + er);
   return make_int4(-1, 0, 0, 0);
+}
+// the 128-byte line holding gmem toward L1
+__device__ __forceinline__ void prefetch_l1(const void* gmem) {
+  asm volatile("prefetch.global.L1 [%0];\n" ::"l"(gmem));
 }
 // Marks the point where a record loaded ahead is first used, so that no arithmetic on it
 // (and no wait for its load) is moved up to the load.
@@ -1091,6 +1096,15 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
       // 2^(-1e30 - m) is exactly 0 for every finite m; with no key taking part m is the
       // sentinel itself, and subtracting 0 instead keeps every weight 0
       const float msub = m2 > 0.5f * kNegLarge ? m2 : 0.f;
+      // the upper Q half rows of the tile two ahead start toward L1 (copied after the weights)
+      if (cq.ok) {
+        settle(rec_q);
+        const int64_t qr = cursor_qrow(p, cq, rec_q, my_qh);
+        if (qr >= 0) {
+          prefetch_l1(p.qhi + qr * D + D / 2);
+          prefetch_l1(p.qlo + qr * D + D / 2);
+        }
+      }
       float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 64; k += 2) {
@@ -1273,6 +1287,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tslot;
   bool bad = false;
   uint32_t issued[kStages] = {};
+  // registers: the scheduling and issuing warpgroup (warps 12-15) gives up part of its share
+  // to the three data warpgroups; the launch holds 128 per thread
+  static_assert(4 * 32 * kRegsIssue + 12 * 32 * kRegsData <= kThreads * 128,
+                "register split over the launch's registers");
+  if (warp >= 12)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegsIssue) : "memory");
+  else
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegsData) : "memory");
   if (warp < 4) {
     softmax_role<D>(p, sm, tmem, bad);
   } else if (warp < 8) {
