@@ -107,6 +107,21 @@ def test_groups_spanning_several_row_tiles():
     compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]))
 
 
+@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+def test_groups_of_many_row_tiles(dtype):
+    # 400 queries naming all 8 blocks of their sequence: 400 edges x 4 query heads per
+    # (block, kv head) group, about 13 row tiles of one group in a row (more than the fp32
+    # kernel's ring of per-tile scale slots, so its slots are reused inside a group)
+    c = wl.block_sparse(59, n_seqs=1, kv_len=512, queries_per_seq=400, hq=16, hkv=4,
+                        head_dim=128, pages_per_block=4, blocks_per_query=8,
+                        unmapped_frac=0.05, dtype=dtype)
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    ro, rm, rl, rst = oracle_partials(c)
+    assert gst == rst
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]),
+                     f16=np.dtype(dtype) == np.float16)
+
+
 def test_bad_edges_and_pages_are_flagged():
     c = wl.block_sparse(52, n_seqs=2, kv_len=512, queries_per_seq=8, hq=8, hkv=2,
                         head_dim=128, blocks_per_query=3, unmapped_frac=0.0)
