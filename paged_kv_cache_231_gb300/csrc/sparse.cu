@@ -143,7 +143,14 @@ __global__ void sparse_fill_kernel(SparseParams p) {
   const int pos = p.group_off[key] + at;
   p.perm[pos] = (int32_t)e;
   const int32_t* m = p.meta + e * 5;
-  p.edge_rec[pos] = make_int4((int)e, m[0], edge_keys(p, m[0], m[2], m[4]), 0);
+  // with split Q rows (already written), the Q shifts of the edge's query heads as signed
+  // bytes (up to four heads), so that the tensor-core kernel reads them with the record
+  int shifts = 0;
+  if (p.qshift != nullptr && p.qhead <= 4) {
+    const int32_t* qs = p.qshift + ((int64_t)m[0] * p.hq + (int64_t)m[1] * p.qhead);
+    for (int j = 0; j < p.qhead; ++j) shifts |= (qs[j] & 0xff) << (8 * j);
+  }
+  p.edge_rec[pos] = make_int4((int)e, m[0], edge_keys(p, m[0], m[2], m[4]), shifts);
 }
 
 // One CTA per (batch, block, kv head) group. Thread (tr, tk) owns rows tr + 16 i and
@@ -1043,7 +1050,8 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
     sq0 = sq1;
     pi1 = qr >= 0 ? rq.x * p.qhead + my_qh : -1;
     keys1 = qr >= 0 ? rq.z : 0;
-    sq1 = qr >= 0 ? __ldg(p.qshift + qr) : 0;
+    sq1 = qr < 0 ? 0 : p.qhead <= 4 ? (int)(signed char)((uint32_t)rq.w >> (8 * my_qh))
+                                    : __ldg(p.qshift + qr);
   };
   // tiles 0 and 1 now; tile t + 2 once the weights of tile t are out (S of tile t, the last
   // reader of buffer t & 1, is done), from a record loaded a tile before
@@ -1354,6 +1362,24 @@ bool encode_pages(CUtensorMap* m, const void* base, const SparseParams& p) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q rows split into fp16 (hi, lo) and their shifts; runs before the edge grouping packs the
+// shifts into the edge records
+cudaError_t launch_qsplit(const SparseParams& p, cudaStream_t s) {
+  const int64_t rows = p.Tq * p.hq;
+  if (rows <= 0) return cudaSuccess;   // no query rows: no edge is valid
+  int dev = -1, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  ProfScope ps("sparse_qsplit", s);
+  const int64_t want = (rows + 7) / 8, cap = (int64_t)sms * 8;
+  if (p.D == 64)
+    qsplit_kernel<64><<<(unsigned)(want < cap ? want : cap), 256, 0, s>>>(p);
+  else
+    qsplit_kernel<128><<<(unsigned)(want < cap ? want : cap), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 bool eligible(const SparseParams& p) {
   return sparse_tc_shape(p.D, p.block_size, p.qhead, p.page_size, p.ppb,
                          p.num_pages * p.hkv * p.page_size, p.Tq * p.hq);
@@ -1378,14 +1404,6 @@ cudaError_t launch_tc(const SparseParams& p, cudaStream_t s) {
   SpMaps maps;
   if (!encode_pages(&maps.k, p.kp, p) || !encode_pages(&maps.v, p.vp, p))
     return cudaErrorInvalidValue;
-  const int64_t rows = p.Tq * p.hq;
-  if (rows > 0) {   // no query rows: no edge is valid, so no tile reads the split rows
-    ProfScope ps("sparse_qsplit", s);
-    const int64_t want = (rows + 7) / 8, cap = (int64_t)sms * 8;
-    qsplit_kernel<D><<<(unsigned)(want < cap ? want : cap), 256, 0, s>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   const int64_t grid = p.ngroups < sms ? p.ngroups : sms;
   ProfScope ps("sparse_partials", s);
   sparse_tc_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(p, maps);
@@ -1435,6 +1453,10 @@ cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s) {
   {
     ProfScope ps("sparse_group", s);
     sparse_scan_kernel<<<1, 1024, 0, s>>>(p);
+  }
+  if (p.qshift != nullptr) {   // split Q rows (tensor-core path): before the fill reads shifts
+    e = tcs::launch_qsplit(p, s);
+    if (e != cudaSuccess) return e;
   }
   {
     ProfScope ps("sparse_group", s);
