@@ -196,7 +196,9 @@ struct SparseParams {
   int32_t* group_off;      // [ngroups + 1]
   int32_t* group_cursor;   // [ngroups]
   int32_t* perm;           // [E]
-  int4* edge_rec;          // [E] (edge, q_idx, block_len clipped to block_size, 0), grouped order
+  int4* edge_rec;          // [E] (edge, q_idx, block_len clipped to block_size, Q shifts of
+                           // the edge's query heads as signed bytes when qshift is set and
+                           // qhead <= 4, else 0), grouped order
   // fp32 tensor-core path: Q rows [Tq * hq] split into fp16 (hi, lo) rows scaled by 2^qshift
   __half* qhi;
   __half* qlo;
