@@ -199,7 +199,8 @@ struct SparseParams {
   int4* edge_rec;          // [E] (edge, q_idx, block_len clipped to block_size, Q shifts of
                            // the edge's query heads as signed bytes when qshift is set and
                            // qhead <= 4, else 0), grouped order
-  // fp32 tensor-core path: Q rows [Tq * hq] split into fp16 (hi, lo) rows scaled by 2^qshift
+  // fp32 tensor-core path: Q rows [Tq * hq] split into fp16 (hi, lo) scaled by 2^qshift, each
+  // array chunk-major: [D / 8][Tq * hq][8]
   __half* qhi;
   __half* qlo;
   int32_t* qshift;

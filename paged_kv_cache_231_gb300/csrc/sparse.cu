@@ -442,7 +442,9 @@ __device__ __forceinline__ int64_t next_group(const SparseParams& p) {
 }
 
 // Split pass over Q: one warp per fp32 row (query, head), scaled by 2^s with s from the
-// row's largest magnitude and written as fp16 (hi, lo) rows, with s.
+// row's largest magnitude and written as fp16 (hi, lo), with s. The split arrays hold each
+// 8-column chunk of all rows together (chunk-major), so that the threads of a tile (one row
+// each) loading the same chunk of an edge's consecutive head rows read one contiguous run.
 template <int D>
 __global__ void __launch_bounds__(256) qsplit_kernel(SparseParams p) {
   constexpr int PER = D / 32;   // values per lane
@@ -471,12 +473,14 @@ __global__ void __launch_bounds__(256) qsplit_kernel(SparseParams p) {
       fma2(x0, x1, v[2 * k], v[2 * k + 1], f, 0.f);
       split_pair(x0, x1, hi[k], lo[k]);
     }
+    // chunk-major: 8-column chunk c of every row together ([D / 8][rows][8])
+    const int64_t at = ((int64_t)(lane * PER / 8) * rows + row) * 8 + (lane * PER) % 8;
     if constexpr (PER == 4) {
-      *reinterpret_cast<uint2*>(p.qhi + row * D + lane * 4) = make_uint2(hi[0], hi[1]);
-      *reinterpret_cast<uint2*>(p.qlo + row * D + lane * 4) = make_uint2(lo[0], lo[1]);
+      *reinterpret_cast<uint2*>(p.qhi + at) = make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2*>(p.qlo + at) = make_uint2(lo[0], lo[1]);
     } else {
-      *reinterpret_cast<uint32_t*>(p.qhi + row * D + lane * 2) = hi[0];
-      *reinterpret_cast<uint32_t*>(p.qlo + row * D + lane * 2) = lo[0];
+      *reinterpret_cast<uint32_t*>(p.qhi + at) = hi[0];
+      *reinterpret_cast<uint32_t*>(p.qlo + at) = lo[0];
     }
     if (lane == 0) p.qshift[row] = s;
   }
@@ -623,10 +627,6 @@ __device__ __forceinline__ int4 row_record(const SparseParams& p, int c0, int e1
                                            int epc) {
   if (er < epc && c0 + er < e1) return __ldg(p.edge_rec + c0 + er);
   return make_int4(-1, 0, 0, 0);
-}
-// the 128-byte line holding gmem toward L1
-__device__ __forceinline__ void prefetch_l1(const void* gmem) {
-  asm volatile("prefetch.global.L1 [%0];\n" ::"l"(gmem));
 }
 // Marks the point where a record loaded ahead is first used, so that no arithmetic on it
 // (and no wait for its load) is moved up to the load.
@@ -807,18 +807,22 @@ __device__ __forceinline__ uint4 ldg_hint_u4(const void* gmem, uint64_t pol) {
                : "l"(gmem), "l"(pol));
   return v;
 }
-// Half H (0: columns [0, D/2), 1: [D/2, D)) of this thread's split Q row (hi, lo) into its
-// TMEM lane at q_tm (hi at + H*D/4, lo at + D/2 + H*D/4); zeros for a padding row. The
-// row's loads are all issued before any is used (one round trip).
+// Half H (0: columns [0, D/2), 1: [D/2, D)) of a split Q row (hi and lo) into this
+// thread's TMEM lane at q_tm (hi at + H*D/4, lo at + D/2 + H*D/4). The split arrays are
+// chunk-major: 8-column chunk c of row r at (c * rows + r) * 8, so that the lanes of an
+// edge's consecutive head rows read one contiguous run per load; hi0 / lo0 point at chunk 0
+// of the row (nullptr: padding row, zeros). The row's loads are all issued before any is
+// used (one round trip).
 template <int D, int H>
-__device__ __forceinline__ void copy_q_half(uint32_t q_tm, const __half* hi_row,
-                                            const __half* lo_row, uint64_t pol) {
-  constexpr int NV = D / 16;   // 16-byte vectors in half a row of fp16
+__device__ __forceinline__ void copy_q_half(uint32_t q_tm, const __half* hi0, const __half* lo0,
+                                            int64_t rows, uint64_t pol) {
+  constexpr int NV = D / 16;   // 8-column chunks in half a row
   uint32_t h[NV * 4], l[NV * 4];
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
-    const uint4 x = hi_row ? ldg_hint_u4(hi_row + H * (D / 2) + 8 * k, pol) : make_uint4(0u, 0u, 0u, 0u);
-    const uint4 y = lo_row ? ldg_hint_u4(lo_row + H * (D / 2) + 8 * k, pol) : make_uint4(0u, 0u, 0u, 0u);
+    const int64_t at = (int64_t)(H * NV + k) * rows * 8;
+    const uint4 x = hi0 ? ldg_hint_u4(hi0 + at, pol) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 y = lo0 ? ldg_hint_u4(lo0 + at, pol) : make_uint4(0u, 0u, 0u, 0u);
     h[4 * k] = x.x; h[4 * k + 1] = x.y; h[4 * k + 2] = x.z; h[4 * k + 3] = x.w;
     l[4 * k] = y.x; l[4 * k + 1] = y.y; l[4 * k + 2] = y.z; l[4 * k + 3] = y.w;
   }
@@ -999,8 +1003,8 @@ __device__ void store_role(const SparseParams& p, unsigned char* sm, uint32_t tm
       tc::fence_after_sync();
       settle(rec);
       const int64_t qrow = (int64_t)rec.y * p.hq + h * p.qhead + my_qh;
-      copy_q_half<D, 0>(lane_tm + kTmQ + b * (uint32_t)D, rec.x >= 0 ? p.qhi + qrow * D : nullptr,
-                        rec.x >= 0 ? p.qlo + qrow * D : nullptr, keep);
+      copy_q_half<D, 0>(lane_tm + kTmQ + b * (uint32_t)D, rec.x >= 0 ? p.qhi + qrow * 8 : nullptr,
+                        rec.x >= 0 ? p.qlo + qrow * 8 : nullptr, p.Tq * p.hq, keep);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) bar_arrive(bars + kQReady + b);
@@ -1039,8 +1043,8 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
     settle(rq);
     const int64_t qr = cursor_qrow(p, c, rq, my_qh);
     if (c.ok) {
-      copy_q_half<D, 1>(lane_tm + kTmQ + b * (uint32_t)D, qr >= 0 ? p.qhi + qr * D : nullptr,
-                        qr >= 0 ? p.qlo + qr * D : nullptr, keep);
+      copy_q_half<D, 1>(lane_tm + kTmQ + b * (uint32_t)D, qr >= 0 ? p.qhi + qr * 8 : nullptr,
+                        qr >= 0 ? p.qlo + qr * 8 : nullptr, p.Tq * p.hq, keep);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) bar_arrive(bars + kQReady + b);
@@ -1104,15 +1108,9 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
       // 2^(-1e30 - m) is exactly 0 for every finite m; with no key taking part m is the
       // sentinel itself, and subtracting 0 instead keeps every weight 0
       const float msub = m2 > 0.5f * kNegLarge ? m2 : 0.f;
-      // the upper Q half rows of the tile two ahead start toward L1 (copied after the weights)
-      if (cq.ok) {
-        settle(rec_q);
-        const int64_t qr = cursor_qrow(p, cq, rec_q, my_qh);
-        if (qr >= 0) {
-          prefetch_l1(p.qhi + qr * D + D / 2);
-          prefetch_l1(p.qlo + qr * D + D / 2);
-        }
-      }
+      // the record of the tile two ahead is taken in hand before the exponentials, so that
+      // the copy after the weights finds it loaded
+      if (cq.ok) settle(rec_q);
       float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 64; k += 2) {
