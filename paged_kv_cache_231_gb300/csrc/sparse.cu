@@ -441,48 +441,56 @@ __device__ __forceinline__ int64_t next_group(const SparseParams& p) {
   }
 }
 
-// Split pass over Q: one warp per fp32 row (query, head), scaled by 2^s with s from the
-// row's largest magnitude and written as fp16 (hi, lo), with s. The split arrays hold each
+// Split pass over Q: every fp32 row (query, head) scaled by 2^s with s from the row's
+// largest magnitude and written as fp16 (hi, lo), with s. The split arrays hold each
 // 8-column chunk of all rows together (chunk-major), so that the threads of a tile (one row
 // each) loading the same chunk of an edge's consecutive head rows read one contiguous run.
+// A warp takes 8 consecutive rows, 4 lanes a row (D/4 columns each): every store then
+// writes one chunk of 8 consecutive rows, 128 contiguous bytes.
 template <int D>
 __global__ void __launch_bounds__(256) qsplit_kernel(SparseParams p) {
-  constexpr int PER = D / 32;   // values per lane
+  constexpr int PER = D / 4;    // values per lane
+  constexpr int NCH = PER / 8;  // 8-column chunks per lane
   const int lane = threadIdx.x & 31;
+  const int r8 = lane >> 2, j = lane & 3;
   const int64_t rows = p.Tq * p.hq;
-  const int64_t stride = (int64_t)gridDim.x * 8;
-  for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += stride) {
+  const int64_t stride = (int64_t)gridDim.x * 64;
+  for (int64_t row0 = (int64_t)blockIdx.x * 64 + (threadIdx.x >> 5) * 8; row0 < rows;
+       row0 += stride) {
+    const int64_t row = row0 + r8;
+    const bool ok = row < rows;
     float v[PER];
-    if constexpr (PER == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(p.q + row * D + lane * 4);
-      v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-    } else {
-      const float2 x = *reinterpret_cast<const float2*>(p.q + row * D + lane * 2);
-      v[0] = x.x; v[1] = x.y;
+#pragma unroll
+    for (int k = 0; k < PER / 4; ++k) {
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok) x = *reinterpret_cast<const float4*>(p.q + row * D + j * PER + 4 * k);
+      v[4 * k] = x.x; v[4 * k + 1] = x.y; v[4 * k + 2] = x.z; v[4 * k + 3] = x.w;
     }
     float mx = 0.f;
 #pragma unroll
     for (int k = 0; k < PER; ++k) mx = fmaxf(mx, fabsf(v[k]));
-    // non-negative floats order as their bit patterns
-    const int s = scale_shift(__uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx))));
+    // the row's maximum over its 4 lanes (non-negative floats order as their bit patterns)
+    uint32_t mb = __float_as_uint(mx);
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    const int s = scale_shift(__uint_as_float(mb));
     const float f = pow2f(s);
-    uint32_t hi[PER / 2], lo[PER / 2];
+    if (!ok) continue;
 #pragma unroll
-    for (int k = 0; k < PER / 2; ++k) {
-      float x0, x1;
-      fma2(x0, x1, v[2 * k], v[2 * k + 1], f, 0.f);
-      split_pair(x0, x1, hi[k], lo[k]);
+    for (int c = 0; c < NCH; ++c) {
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float x0, x1;
+        fma2(x0, x1, v[8 * c + 2 * k], v[8 * c + 2 * k + 1], f, 0.f);
+        split_pair(x0, x1, hi[k], lo[k]);
+      }
+      // chunk-major: 8-column chunk ch of every row together ([D / 8][rows][8])
+      const int64_t at = ((int64_t)(j * NCH + c) * rows + row) * 8;
+      *reinterpret_cast<uint4*>(p.qhi + at) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(p.qlo + at) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    // chunk-major: 8-column chunk c of every row together ([D / 8][rows][8])
-    const int64_t at = ((int64_t)(lane * PER / 8) * rows + row) * 8 + (lane * PER) % 8;
-    if constexpr (PER == 4) {
-      *reinterpret_cast<uint2*>(p.qhi + at) = make_uint2(hi[0], hi[1]);
-      *reinterpret_cast<uint2*>(p.qlo + at) = make_uint2(lo[0], lo[1]);
-    } else {
-      *reinterpret_cast<uint32_t*>(p.qhi + at) = hi[0];
-      *reinterpret_cast<uint32_t*>(p.qlo + at) = lo[0];
-    }
-    if (lane == 0) p.qshift[row] = s;
+    if (j == 0) p.qshift[row] = s;
   }
 }
 
@@ -1370,7 +1378,7 @@ cudaError_t launch_qsplit(const SparseParams& p, cudaStream_t s) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   ProfScope ps("sparse_qsplit", s);
-  const int64_t want = (rows + 7) / 8, cap = (int64_t)sms * 8;
+  const int64_t want = (rows + 63) / 64, cap = (int64_t)sms * 8;
   if (p.D == 64)
     qsplit_kernel<64><<<(unsigned)(want < cap ? want : cap), 256, 0, s>>>(p);
   else

@@ -74,6 +74,20 @@ def test_small_full_parity(head_dim, pages_per_block, qhead):
     assert_f32_close(glse[fin], rlse[fin], "lse", scalars=True)
 
 
+# a query-row count (queries x query heads) that is not a multiple of 8: the split pass
+# takes rows eight at a time
+@pytest.mark.parametrize("head_dim,pages_per_block,qhead", [(128, 4, 3), (64, 2, 1)])
+def test_ragged_query_rows(head_dim, pages_per_block, qhead):
+    c = wl.block_sparse(61, n_seqs=3, kv_len=1024, queries_per_seq=25, hq=4 * qhead,
+                        hkv=4, head_dim=head_dim, pages_per_block=pages_per_block,
+                        blocks_per_query=5, unmapped_frac=0.05)
+    assert (c.q.shape[0] * c.hq) % 8 != 0
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    ro, rm, rl, rst = oracle_partials(c)
+    assert gst == rst
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]))
+
+
 # The tensor-core path scales each Q row and each K / V block by a power of two before
 # splitting it into fp16 (hi, lo) pairs. Magnitudes far outside fp16's range (q x 2^eq,
 # k x 2^ek, v x 2^ev, with eq + ek kept small so that the scores stay ordinary) and pages
