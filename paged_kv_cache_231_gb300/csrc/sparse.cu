@@ -494,8 +494,9 @@ __global__ void __launch_bounds__(256) qsplit_kernel(SparseParams p) {
   }
 }
 
-// Q arrives split: a pass before the kernel writes every fp32 Q row as fp16 (hi, lo)
-// rows scaled by the row's own power of two, and that shift.
+// Q arrives split: a pass before the kernel writes every fp32 Q row as fp16 (hi, lo), in
+// chunk-major arrays, scaled by the row's own power of two, and that shift (which the
+// grouping pass also packs into the edge records).
 //
 // Warp-specialised form: a persistent CTA of 16 warps per SM, every hand-off on an
 // mbarrier.
@@ -522,7 +523,7 @@ __global__ void __launch_bounds__(256) qsplit_kernel(SparseParams p) {
 // TMEM: S of tile parity b at 64 b (P' hi at +0 and lo at +32 once the scores are read), O
 // at 128, Q (hi, lo) of tile parity b at 256 + D b (hi D/2 columns, then lo). With two S
 // and two Q buffers the next tile's Q copy and S run while the softmax and O of this one
-// do.
+// do. Registers: warps 12-15 run on 72 a thread, the other twelve on 144 (setmaxnreg).
 constexpr int kThreads = 512;
 constexpr int kNK = 64;                 // keys per block tile
 constexpr uint32_t kTries = 1u << 22;   // default bound of each wait (polls)
