@@ -1132,19 +1132,15 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
       const float lrow = ((la[0] + lb[0]) + (la[1] + lb[1])) + ((la[2] + lb[2]) + (la[3] + lb[3]));
       // m in natural-log units (the -1e30 sentinel as is when no key takes part)
       const float mrow = m2 > 0.5f * kNegLarge ? m2 * kLn2 : kNegLarge;
-      // P' = 2^14 P as (hi, lo) fp16 pairs of keys, 32 keys at a time
+      uint32_t ph[32], pl[32];   // P' = 2^14 P as (hi, lo) fp16 pairs of keys
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t ph[16], pl[16];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          float w0, w1;
-          fma2(w0, w1, s[32 * hf + k], s[32 * hf + k + 1], p_scale, 0.f);
-          split_pair(w0, w1, ph[k / 2], pl[k / 2]);
-        }
-        tmem_st_u32<16>(s_tm + 16 * hf, ph);
-        tmem_st_u32<16>(s_tm + 32 + 16 * hf, pl);
+      for (int k = 0; k < 64; k += 2) {
+        float w0, w1;
+        fma2(w0, w1, s[k], s[k + 1], p_scale, 0.f);
+        split_pair(w0, w1, ph[k / 2], pl[k / 2]);
       }
+      tmem_st_u32<32>(s_tm, ph);
+      tmem_st_u32<32>(s_tm + 32, pl);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
