@@ -74,6 +74,22 @@ def test_small_full_parity(head_dim, pages_per_block, qhead):
     assert_f32_close(glse[fin], rlse[fin], "lse", scalars=True)
 
 
+# more than four query heads per kv head: the Q shifts do not fit the edge record and the
+# tensor-core kernel reads them per row (and a 128-row tile holds 16 or 8 edges)
+@pytest.mark.parametrize("qhead", [8, 16])
+def test_many_query_heads_per_kv_head(qhead):
+    c = wl.block_sparse(67, n_seqs=2, kv_len=1024, queries_per_seq=40, hq=2 * qhead, hkv=2,
+                        head_dim=128, pages_per_block=4, blocks_per_query=5,
+                        unmapped_frac=0.05)
+    assert c.qhead == qhead
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    ro, rm, rl, rst = oracle_partials(c)
+    assert gst == rst
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]))
+    rout, rlse = orc.combine_partials(ro, rm, rl, c.seg_offsets, c.qhead)
+    assert f32_margins(gout, rout, "combined output, many query heads") <= 1e-4
+
+
 # a query-row count (queries x query heads) that is not a multiple of 8: the split pass
 # takes rows eight at a time
 @pytest.mark.parametrize("head_dim,pages_per_block,qhead", [(128, 4, 3), (64, 2, 1)])
