@@ -30,7 +30,8 @@
 //     four TMEM P buffers) and l of tile t; (m, l) go to an 8-tile shared ring. The
 //     softmax issues no global store, so its barrier arrivals never wait for one.
 //   warps 4-7 (store): the O rows of tile t, through a per-warp shared-memory transpose
-//     (whole 128-byte row segments per store instruction), and the rows' m and l.
+//     (whole 128-byte row segments, 32-byte stores: eight rows per store instruction), and
+//     the rows' m and l.
 // TMEM: S 0 / 64, O 128 / 128 + D, P 384 + 32 k (k < 4). Every wait is bounded; a wait that
 // gives up raises a shared abort flag that ends every role, and the CTA drains what it
 // issued.
@@ -356,6 +357,14 @@ __device__ void softmax_role(const SparseParams& p, unsigned char* sm, uint32_t 
   }
 }
 
+// 32-byte global store (the 256-bit st.global of sm_100 and later) with the streaming hint:
+// half the store instructions of two 16-byte stores. dst must be 32-byte aligned.
+__device__ __forceinline__ void st_cs_v8(float* dst, const float4& a, const float4& b) {
+  asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(dst),
+               "f"(a.x), "f"(a.y), "f"(a.z), "f"(a.w), "f"(b.x), "f"(b.y), "f"(b.z), "f"(b.w)
+               : "memory");
+}
+
 // Warps 4-7: per tile, the O rows of this warp's 32 TMEM lanes to memory.
 template <int D>
 __device__ void store_role(const SparseParams& p, unsigned char* sm, uint32_t tmem) {
@@ -372,6 +381,8 @@ __device__ void store_role(const SparseParams& p, unsigned char* sm, uint32_t tm
   float* xf = reinterpret_cast<float*>(sm + L::kXfer) + quarter * 1024;
   const int epc = 128 / p.qhead;
   const int q4 = lane & 7;
+  // o_partial need only be 16-byte aligned; 32-byte stores when it is 32-byte aligned
+  const bool o32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
   uint32_t t = 0;
   for (uint32_t gi = 0;; ++gi) {
     long long g;
@@ -400,13 +411,28 @@ __device__ void store_role(const SparseParams& p, unsigned char* sm, uint32_t tm
           *reinterpret_cast<float4*>(xf + lane * 32 + ((q ^ (lane & 7)) << 2)) =
               make_float4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]);
         __syncwarp();
+        if (o32) {   // four lanes per 128-byte row segment, eight rows per instruction
+          const int j = lane & 3;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = i * 4 + (lane >> 3);
-          const int rpi = __shfl_sync(0xffffffffu, pi, rr);
-          const float4 v = *reinterpret_cast<const float4*>(xf + rr * 32 + ((q4 ^ (rr & 7)) << 2));
-          if (rpi >= 0)
-            __stcs(reinterpret_cast<float4*>(p.o + (int64_t)rpi * D + ch * 32 + q4 * 4), v);
+          for (int i = 0; i < 4; ++i) {
+            const int rr = i * 8 + (lane >> 2);
+            const int rpi = __shfl_sync(0xffffffffu, pi, rr);
+            const float* row = xf + rr * 32;
+            const float4 v0 = *reinterpret_cast<const float4*>(row + (((2 * j) ^ (rr & 7)) << 2));
+            const float4 v1 =
+                *reinterpret_cast<const float4*>(row + (((2 * j + 1) ^ (rr & 7)) << 2));
+            if (rpi >= 0) st_cs_v8(p.o + (int64_t)rpi * D + ch * 32 + j * 8, v0, v1);
+          }
+        } else {   // eight lanes per row segment, four rows per instruction
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = i * 4 + (lane >> 3);
+            const int rpi = __shfl_sync(0xffffffffu, pi, rr);
+            const float4 v =
+                *reinterpret_cast<const float4*>(xf + rr * 32 + ((q4 ^ (rr & 7)) << 2));
+            if (rpi >= 0)
+              __stcs(reinterpret_cast<float4*>(p.o + (int64_t)rpi * D + ch * 32 + q4 * 4), v);
+          }
         }
         __syncwarp();
       }

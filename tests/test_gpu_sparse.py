@@ -254,6 +254,35 @@ def test_f16_rejects_blocks_past_64_keys():
     assert ei.value.name == "PKV_ERR_UNSUPPORTED"
 
 
+@pytest.mark.parametrize("dtype,head_dim", [(np.float16, 128), (np.float16, 64),
+                                            (np.float32, 128)])
+def test_partials_at_16_byte_aligned_o(dtype, head_dim):
+    """o_partial need only be 16-byte aligned: a 32-byte aligned o takes 32-byte stores, any
+    other the 16-byte ones. Both write the same values (each partial row's arithmetic does
+    not depend on where its row sits in a tile)."""
+    c = wl.block_sparse(57, n_seqs=2, kv_len=1024, queries_per_seq=40, hq=16, hkv=4,
+                        head_dim=head_dim, pages_per_block=4, blocks_per_query=5,
+                        n_empty_edges=3, unmapped_frac=0.05, dtype=dtype)
+    args = (dev(c.q), dev(c.k_pages), dev(c.v_pages), dev(c.edge_meta), dev(c.block_tables))
+    kw = dict(qhead=c.qhead, block_size=c.block_size, page_size=c.page_size,
+              pages_per_block=c.pages_per_block, softmax_scale=c.softmax_scale)
+    P, D = c.num_edges * c.qhead, c.head_dim
+    o32, m32, l32 = B.pkv_sparse_attention_partials(*args, **kw)
+    buf = torch.full((P * D + 8,), 7.0, dtype=torch.float32, device=DEV)
+    o16 = buf[4:4 + P * D].view(P, D)
+    assert o32.data_ptr() % 32 == 0 and o16.data_ptr() % 32 == 16
+    _, m16, l16 = B.pkv_sparse_attention_partials(*args, o=o16, **kw)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(o16), host(o32))
+    np.testing.assert_array_equal(host(m16), host(m32))
+    np.testing.assert_array_equal(host(l16), host(l32))
+    edge = host(buf)   # nothing written outside o
+    assert (edge[:4] == 7.0).all() and (edge[4 + P * D:] == 7.0).all()
+    ro, rm, rl, _ = oracle_partials(c)
+    compare_partials(host(o32), host(m32), host(l32), ro, rm, rl, np.arange(P),
+                     f16=dtype == np.float16)
+
+
 # right-aligned causal mask: split-fp16 tensor-core (64-key blocks), fp32 FMA (128-key
 # blocks) and fp16 tensor-core paths
 @pytest.mark.parametrize("head_dim,pages_per_block,qhead,dtype",
