@@ -13,12 +13,14 @@
 //
 // GB300 form (edges grouped by (batch, block, kv head) by the grouping kernels of the
 // fp32 path): a persistent CTA per SM, warp-specialised, every hand-off on an mbarrier.
-//   warp 8 (scheduler): takes groups from a counter, publishes them in a 4-entry ring and
+//   warp 8 (scheduler): takes groups from a counter, publishes them in an 8-entry ring and
 //     stages each group's K and V pages by TMA (one box per page and 64-column slice,
 //     128-byte swizzle) straight in the operand layouts - K is the K-major B operand of
-//     S = Q K^T, V the MN-major B operand of O = P V - in one of three stages. A group is
-//     published only once the group three back has left its stage, so the Q gathers
-//     never run ahead of the K/V loads the tensor core needs first.
+//     S = Q K^T, V the MN-major B operand of O = P V - in one of three stages. Its global
+//     round trips are pipelined: the counter claim for the next group goes out an
+//     iteration early, the claimed group's offsets and this group's block-table entries
+//     are requested together, and the next group's entry is published before this
+//     group's staging (the gather warps read edge records from it at group boundaries).
 //   warps 10-13 (gather, 32 rows each): for each tile of 128 query rows (edges x query
 //     lanes) read the rows' edge records (one 16-byte load per row, issued a tile ahead),
 //     publish (partial index, block_len) per row in an 8-tile ring, and gather the Q rows
@@ -54,7 +56,7 @@ constexpr uint32_t kTries = 1u << 22;   // default bound of each wait (polls)
 __shared__ uint32_t s_tries;
 constexpr uint32_t kTmS = 0, kTmO = 128, kTmP = 384;
 constexpr int kSchedWarp = 8, kMmaWarp = 9, kGatherWarp0 = 10;   // gather: warps 10-13
-constexpr int kRing = 4;                // group ring entries
+constexpr int kRing = 8;                // group ring entries
 constexpr uint32_t kStages = 3;         // K/V stages
 constexpr uint32_t kQBufs = 3;          // Q buffers
 constexpr uint32_t kRows = 8;           // row-info ring (tiles)
@@ -169,27 +171,19 @@ __device__ __forceinline__ void cp_async_16_hint(void* smem, const void* gmem, i
                : "memory");
 }
 
-// next group (in counter order) that has edges, or ngroups
-__device__ __forceinline__ int64_t next_group(const SparseParams& p) {
-  int* counter = p.group_count + p.ngroups;
-  while (true) {
-    const int64_t g = atomicAdd(counter, 1);
-    if (g >= p.ngroups) return p.ngroups;
-    if (p.group_off[g + 1] > p.group_off[g]) return g;
-  }
-}
-
-// One warp: group g's K and V pages into stage `st` by TMA onto sbar; the key states into
-// masks[st] = {bit t set: key t mapped, bit t set: key t an invalid table reference}
-// (keys past the block and keys of unmapped pages in neither), two ballots per mask.
-// Unmapped pages get no copy: their rows keep earlier (finite) contents or the zeros the
-// kernel starts with, and their weights are exactly 0.
-template <int D>
-__device__ void stage_group(const SparseParams& p, const Maps& maps, unsigned char* sm,
-                            int64_t g, uint32_t st, uint64_t* sbar, bool withhold = false) {
-  using L = Layout<D>;
+// The staging of one group, worked out by one warp from the block table: the key states
+// {bit t set: key t mapped, bit t set: key t an invalid table reference} (keys past the
+// block and keys of unmapped pages in neither), two ballots per mask; for lane j < pages
+// per block the first row of page j in the page tensors (-1: unmapped, no copy), and the
+// ballot of the lanes with a copy.
+struct StagePlan {
+  uint64_t vmask, imask;
+  int row0;
+  uint32_t bits;
+};
+// The staging of group g (block-table reads only: no shared memory is touched).
+__device__ __forceinline__ StagePlan plan_group(const SparseParams& p, int64_t g) {
   const int lane = threadIdx.x & 31;
-  uint64_t* masks = reinterpret_cast<uint64_t*>(sm + L::kMasks) + 2 * st;
   const int h = (int)(g % p.hkv);
   const int64_t bb = g / p.hkv;
   const int blk = (int)(bb % p.nblk);
@@ -211,10 +205,6 @@ __device__ void stage_group(const SparseParams& p, const Maps& maps, unsigned ch
     vmask |= (uint64_t)__ballot_sync(0xffffffffu, state == 1) << (32 * k);
     imask |= (uint64_t)__ballot_sync(0xffffffffu, state == 2) << (32 * k);
   }
-  if (lane == 0) {
-    masks[0] = vmask;
-    masks[1] = imask;
-  }
   int row0 = -1;   // first row of page `lane` of the block in the page tensors
   if (lane < p.ppb) {
     const int64_t slot = (int64_t)blk * p.ppb + lane;
@@ -223,7 +213,28 @@ __device__ void stage_group(const SparseParams& p, const Maps& maps, unsigned ch
       if (page >= 0 && page < p.num_pages) row0 = (int)((page * p.hkv + h) * p.page_size);
     }
   }
-  const uint32_t bits = __ballot_sync(0xffffffffu, row0 >= 0);
+  StagePlan sp;
+  sp.vmask = vmask;
+  sp.imask = imask;
+  sp.row0 = row0;
+  sp.bits = __ballot_sync(0xffffffffu, row0 >= 0);
+  return sp;
+}
+// Stage `st` (free): the key masks of the plan into masks[st], then its K and V pages by
+// TMA onto sbar. Unmapped pages get no copy: their rows keep earlier (finite) contents or
+// the zeros the kernel starts with, and their weights are exactly 0.
+template <int D>
+__device__ void issue_group(const SparseParams& p, const Maps& maps, unsigned char* sm,
+                            const StagePlan& sp, uint32_t st, uint64_t* sbar, bool withhold) {
+  using L = Layout<D>;
+  const int lane = threadIdx.x & 31;
+  uint64_t* masks = reinterpret_cast<uint64_t*>(sm + L::kMasks) + 2 * st;
+  if (lane == 0) {
+    masks[0] = sp.vmask;
+    masks[1] = sp.imask;
+  }
+  const int row0 = sp.row0;
+  const uint32_t bits = sp.bits;
   __syncwarp();   // the key states are published by lane 0's arrive
   if (lane == 0)
     tc::mbar_arrive_expect_tx(sbar, (uint32_t)__popc(bits) * (uint32_t)p.page_size * D * 2u * 2u);
@@ -460,24 +471,63 @@ __device__ void sched_role(const SparseParams& p, const Maps& maps, unsigned cha
     tc::tma_prefetch_desc(&maps.k);
     tc::tma_prefetch_desc(&maps.v);
   }
-  for (uint32_t gi = 0;; ++gi) {
-    long long g = 0;
-    if (lane == 0) g = next_group(p);
-    g = __shfl_sync(0xffffffffu, g, 0);
-    const int slot = (int)(gi % kRing);
-    if (gi >= kRing && !warp_wait(bars + kGEmpty + slot, ((gi / kRing) - 1) & 1u, abort)) return;
+  int* counter = p.group_count + p.ngroups;
+  // the first group in counter order at or after claimed counter value c that has edges
+  auto resolve = [&](int c) -> long long {
+    long long g = p.ngroups;
     if (lane == 0) {
-      int e0 = 0, e1 = 0;
-      if (g < p.ngroups) {
-        e0 = p.group_off[g];
-        e1 = p.group_off[g + 1];
-      }
+      while (c < p.ngroups && p.group_off[c + 1] <= p.group_off[c]) c = atomicAdd(counter, 1);
+      g = c < p.ngroups ? c : p.ngroups;
+    }
+    return __shfl_sync(0xffffffffu, g, 0);
+  };
+  // ring entry gi <- group g (a group past the last one ends the work)
+  auto publish = [&](uint32_t gi, long long g, int e0, int e1) -> bool {
+    const int slot = (int)(gi % kRing);
+    if (gi >= kRing && !warp_wait(bars + kGEmpty + slot, ((gi / kRing) - 1) & 1u, abort))
+      return false;
+    if (lane == 0) {
+      if (g >= p.ngroups) e0 = e1 = 0;
       ring[slot].g = g;
       ring[slot].e0 = e0;
       ring[slot].e1 = e1;
       bar_arrive(bars + kGFull + slot);   // release: the entry is visible to the waiters
     }
-    if (g >= p.ngroups) return;
+    return true;
+  };
+  int c0 = 0;
+  if (lane == 0) c0 = atomicAdd(counter, 1);
+  long long g = resolve(c0);
+  if (!publish(0, g, g < p.ngroups ? p.group_off[g] : 0, g < p.ngroups ? p.group_off[g + 1] : 0))
+    return;
+  // lane 0: the counter value claimed for the next entry, one iteration ahead
+  int cn = 0;
+  if (lane == 0) cn = atomicAdd(counter, 1);
+  for (uint32_t gi = 0; g < p.ngroups; ++gi) {
+    // the claimed group's offsets are requested before this group's block-table reads, so
+    // the two round trips overlap; the claim for the entry after it goes out next
+    int o0 = 0, o1 = 0;
+    if (lane == 0 && cn < p.ngroups) {
+      o0 = p.group_off[cn];
+      o1 = p.group_off[cn + 1];
+    }
+    const StagePlan sp = plan_group(p, g);
+    long long gn = p.ngroups;
+    if (lane == 0) {
+      int c = cn;
+      if (c < p.ngroups && o1 <= o0) {   // empty: the first non-empty group after it
+        c = atomicAdd(counter, 1);
+        while (c < p.ngroups && p.group_off[c + 1] <= p.group_off[c]) c = atomicAdd(counter, 1);
+        if (c < p.ngroups) {
+          o0 = p.group_off[c];
+          o1 = p.group_off[c + 1];
+        }
+      }
+      gn = c < p.ngroups ? c : p.ngroups;
+      cn = gn < p.ngroups ? atomicAdd(counter, 1) : p.ngroups;
+    }
+    gn = __shfl_sync(0xffffffffu, gn, 0);
+    if (!publish(gi + 1, gn, o0, o1)) return;
     const uint32_t st = gi % kStages;
     // the stage is free once every MMA of the group kStages back has completed
     if (gi >= kStages &&
@@ -485,8 +535,9 @@ __device__ void sched_role(const SparseParams& p, const Maps& maps, unsigned cha
       return;
     // testing hook: the CTA's first staging is announced but never copied, so the waits
     // for it give up with nothing in flight
-    stage_group<D>(p, maps, sm, g, st, bars + kKVFull + st, p.withhold_copy && gi == 0);
+    issue_group<D>(p, maps, sm, sp, st, bars + kKVFull + st, p.withhold_copy && gi == 0);
     ++issued[st];
+    g = gn;
   }
 }
 
