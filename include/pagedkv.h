@@ -322,7 +322,9 @@ typedef struct pkv_sparse_args {
   const void* v_pages;
   const int32_t* edge_meta;    /* [num_edges, 5]: q_idx, h (kv head), blk, batch, block_len */
   const int32_t* block_tables; /* [num_seqs, max_pages]: page id or -1 (unmapped) */
-  float* o_partial;            /* [num_edges*qhead, head_dim] */
+  float* o_partial;            /* [num_edges*qhead, head_dim]; 16-byte aligned (the
+                                  fp16 path stores 32 bytes a lane when it is 32-byte
+                                  aligned, which is faster) */
   float* m_partial;            /* [num_edges*qhead] */
   float* l_partial;            /* [num_edges*qhead] */
   int32_t* device_status;      /* optional */
