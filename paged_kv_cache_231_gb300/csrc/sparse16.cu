@@ -24,7 +24,7 @@
 //   warps 10-13 (gather, 32 rows each): for each tile of 128 query rows (edges x query
 //     lanes) read the rows' edge records (one 16-byte load per row, issued a tile ahead),
 //     publish (partial index, block_len) per row in an 8-tile ring, and gather the Q rows
-//     with cp.async into one of three K-major swizzled Q buffers.
+//     with cp.async into one of two K-major swizzled Q buffers.
 //   warp 9, lane 0 (MMA): S(t) = Q(t) K^T into one of two TMEM S buffers, then
 //     O(t-1) = P(t-1) V into one of two TMEM O buffers (tcgen05.mma kind::f16, P read
 //     from TMEM), so the tensor core works on tile t while the softmax finishes t-1.
@@ -58,7 +58,7 @@ constexpr uint32_t kTmS = 0, kTmO = 128, kTmP = 384;
 constexpr int kSchedWarp = 8, kMmaWarp = 9, kGatherWarp0 = 10;   // gather: warps 10-13
 constexpr int kRing = 8;                // group ring entries
 constexpr uint32_t kStages = 3;         // K/V stages
-constexpr uint32_t kQBufs = 3;          // Q buffers
+constexpr uint32_t kQBufs = 2;          // Q buffers
 constexpr uint32_t kRows = 8;           // row-info ring (tiles)
 
 // mbarriers (index into the barrier array)
@@ -583,9 +583,10 @@ __device__ void gather_role(const SparseParams& p, unsigned char* sm) {
     }
     const int4 nrec = more ? lookup(nc0, ne1) : make_int4(-1, 0, 0, 0);
     // row info of this tile. The slot was last read for tile t - 8, whose softmax and
-    // stores are done: this point follows the gather of Q(t-1), which waited for S(t-4)
-    // to finish; the MMA issued S(t-4) after O(t-6) = P V, which waited for the stores of
-    // tile t-8 to read out their O buffer (and P(t-6) came after the softmax of t-8).
+    // stores are done: this point follows the gather of Q(t-1), which waited for S(t-3)
+    // to finish; the MMA issued S(t-3) after O(t-5) = P V, which waited for the stores of
+    // tile t-7 to read out their O buffer (the stores run in tile order) and for P(t-5),
+    // which came after the softmax of t-5.
     const bool live = rec.x >= 0;
     rowinfo[(t % kRows) * 128 + r] =
         live ? make_int2(rec.x * p.qhead + qh, rec.z) : make_int2(-1, 0);
