@@ -141,7 +141,10 @@ __global__ void sparse_fill_kernel(SparseParams p) {
   if (key < 0) return;
   const int at = atomicAdd(&p.group_cursor[key], 1);
   const int pos = p.group_off[key] + at;
-  p.perm[pos] = (int32_t)e;
+  // the fp32 FMA kernel reads perm, the tensor-core kernels the edge records: the launch
+  // passes only the array its partials kernel reads
+  if (p.perm != nullptr) p.perm[pos] = (int32_t)e;
+  if (p.edge_rec == nullptr) return;
   const int32_t* m = p.meta + e * 5;
   // with split Q rows (already written), the Q shifts of the edge's query heads as signed
   // bytes (up to four heads), so that the tensor-core kernel reads them with the record
@@ -1463,7 +1466,12 @@ cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s) {
   }
   {
     ProfScope ps("sparse_group", s);
-    sparse_fill_kernel<<<eg, 256, 0, s>>>(p);
+    SparseParams pf = p;
+    if (p.f16 || tcs::eligible(p))
+      pf.perm = nullptr;
+    else
+      pf.edge_rec = nullptr;
+    sparse_fill_kernel<<<eg, 256, 0, s>>>(pf);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
