@@ -239,15 +239,14 @@ __device__ void issue_group(const SparseParams& p, const Maps& maps, unsigned ch
   if (lane == 0)
     tc::mbar_arrive_expect_tx(sbar, (uint32_t)__popc(bits) * (uint32_t)p.page_size * D * 2u * 2u);
   __syncwarp();
-  if (row0 >= 0 && !withhold) {
-    unsigned char* kdst = sm + L::kK + st * L::kKV;
-    unsigned char* vdst = sm + L::kV + st * L::kKV;
-#pragma unroll
-    for (int q = 0; q < D / 64; ++q) {
-      const uint32_t off = (uint32_t)q * L::kSub + (uint32_t)(lane * p.page_size) * 128u;
-      tc::tma_load_2d(kdst + off, &maps.k, q * 64, row0, sbar);
-      tc::tma_load_2d(vdst + off, &maps.v, q * 64, row0, sbar);
-    }
+  // one box per lane, all issued together: lane = (page j, 64-column slice q, K or V)
+  constexpr int kBoxes = 2 * (D / 64);   // boxes per page
+  const int j = lane / kBoxes, q = (lane % kBoxes) >> 1, isv = lane & 1;
+  const int rj = __shfl_sync(0xffffffffu, row0, j & 31);
+  if (j < p.ppb && rj >= 0 && !withhold) {
+    unsigned char* dst = sm + (isv ? L::kV : L::kK) + st * L::kKV;
+    const uint32_t off = (uint32_t)q * L::kSub + (uint32_t)(j * p.page_size) * 128u;
+    tc::tma_load_2d(dst + off, isv ? &maps.v : &maps.k, q * 64, rj, sbar);
   }
 }
 
