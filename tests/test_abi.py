@@ -268,6 +268,31 @@ def test_sparse_and_combine_argument_checks(lib):
     assert lib.pkv_combine_partials(ctypes.byref(c), None) == 1   # NULL pointers
 
 
+def test_sparse_pointer_checks_come_before_any_launch(lib):
+    """The partials call checks pointers, their alignment (16 bytes; o_partial need not be
+    32-byte aligned) and the workspace before it touches the device, so fake addresses
+    exercise every refusal here; nothing is launched."""
+    base = 1 << 20   # a fake, 256-byte aligned address: never dereferenced on these paths
+
+    def call(ws=base, ws_bytes=1 << 30, num_edges=10, **ptr):
+        a = B.SparseArgs(num_queries=100, num_edges=num_edges, num_seqs=2, max_pages=16,
+                         num_pages=32, qhead=4, hq=32, hkv=8, head_dim=128, block_size=64,
+                         page_size=16, pages_per_block=4, softmax_scale=0.1, dtype=B.PKV_F16)
+        for i, k in enumerate(("q", "k_pages", "v_pages", "edge_meta", "block_tables",
+                               "o_partial", "m_partial", "l_partial")):
+            setattr(a, k, ptr.get(k, base + (i + 1) * (1 << 16)))
+        return lib.pkv_sparse_attention_partials(ctypes.byref(a), ws, ws_bytes, None)
+
+    o = base + 6 * (1 << 16)
+    assert call(o_partial=o + 8) == 8            # PKV_ERR_ALIGN
+    assert call(q=base + 8) == 8
+    assert call(o_partial=o + 16, ws=None) == 7   # 16-byte aligned o passes; no workspace
+    assert call(ws=base + 128) == 7              # workspace not 256-byte aligned
+    assert call(ws_bytes=16) == 7                # workspace too small
+    assert call(o_partial=None) == 1             # PKV_ERR_NULL
+    assert call(num_edges=0, o_partial=None, q=None) == 0   # nothing to do, nothing read
+
+
 def test_sparse_workspace_holds_the_split_q_rows(lib):
     # fp32 calls that run on the tensor core take Q as split fp16 (hi, lo) rows plus one
     # shift per row in the workspace; fp16 calls and other shapes do not
