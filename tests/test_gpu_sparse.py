@@ -256,6 +256,23 @@ def test_f16_rejects_blocks_past_64_keys():
 
 @pytest.mark.parametrize("dtype,head_dim", [(np.float16, 128), (np.float16, 64),
                                             (np.float32, 128)])
+def test_blocks_of_eight_pages_of_eight_keys(dtype, head_dim):
+    """64-key blocks of eight 8-key pages: the tensor-core kernels stage the most boxes per
+    block (with head size 128, one for every lane of the staging warp)."""
+    c = wl.block_sparse(58, n_seqs=2, kv_len=1024, queries_per_seq=24, hq=16, hkv=4,
+                        head_dim=head_dim, page_size=8, pages_per_block=8,
+                        blocks_per_query=5, n_empty_edges=3, unmapped_frac=0.05, dtype=dtype)
+    go, gm, gl, gout, glse, gst = run_gpu(c)
+    ro, rm, rl, rst = oracle_partials(c)
+    assert gst == rst
+    f16 = dtype == np.float16
+    compare_partials(go, gm, gl, ro, rm, rl, np.arange(rl.shape[0]), f16=f16)
+    rout, _ = orc.combine_partials(ro, rm, rl, c.seg_offsets, c.qhead)
+    assert_f32_close(gout, rout, "combined output", rtol=F16_PARTIAL_RTOL if f16 else None)
+
+
+@pytest.mark.parametrize("dtype,head_dim", [(np.float16, 128), (np.float16, 64),
+                                            (np.float32, 128)])
 def test_partials_at_16_byte_aligned_o(dtype, head_dim):
     """o_partial need only be 16-byte aligned: a 32-byte aligned o takes 32-byte stores, any
     other the 16-byte ones. Both write the same values (each partial row's arithmetic does
